@@ -1,0 +1,186 @@
+"""fp64 CPU oracle for the fused Linear + epilogue path (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this package.  The CUDA library never imports it,
+and the two share no code.  The arithmetic lives in ``oracle.c`` (plain C,
+fp64, OpenMP over independent outputs); this module only compiles it and
+marshals numpy arrays.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+against closed forms, library routines (libm / torch fp64 CPU ops / scipy),
+brute force on tiny inputs, or values printed on the pages.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib_handle = None
+
+GELU_ERF, GELU_TANH = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` to ``liboracle.so`` (gcc -O2, OpenMP, no fast-math)."""
+    src = os.path.join(_HERE, "oracle.c")
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", src, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _lib():
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    lib = ctypes.CDLL(build())
+    P, L, D, I = ctypes.c_void_p, ctypes.c_long, ctypes.c_double, ctypes.c_int
+    sig = {
+        "orc_linear": [P, L, P, P, L, P, L, P],
+        "orc_linear_gelu": [P, L, P, P, L, P, L, I, P],
+        "orc_gelu": [P, L, I, P],
+        "orc_qkv_rope": [P, L, P, P, L, L, L, D, P, P, L, P],
+        "orc_swiglu": [P, L, P, P, P, P, L, P, L, P],
+        "orc_rmsnorm_fp8": [P, L, P, P, P, P, L, L, D, P, P, P],
+        "orc_e4m3_encode_array": [P, L, P],
+        "orc_e4m3_decode_array": [P, L, P],
+        "orc_rope_rotate": [D, D, D, P, P],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = None
+    for name in ("orc_gelu_erf", "orc_gelu_tanh", "orc_silu"):
+        getattr(lib, name).argtypes = [D]
+        getattr(lib, name).restype = D
+    lib.orc_rope_angle.argtypes = [D, L, L, D]
+    lib.orc_rope_angle.restype = D
+    lib.orc_e4m3_encode.argtypes = [D]
+    lib.orc_e4m3_encode.restype = I
+    lib.orc_e4m3_decode.argtypes = [I]
+    lib.orc_e4m3_decode.restype = D
+    lib.orc_num_threads.argtypes = []
+    lib.orc_num_threads.restype = I
+    _lib_handle = lib
+    return lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _cols(cols, n):
+    if cols is None:
+        cols = np.arange(n)
+    return np.ascontiguousarray(cols, dtype=np.int64)
+
+
+def num_threads() -> int:
+    return _lib().orc_num_threads()
+
+
+def linear(X, W, b=None, cols=None) -> np.ndarray:
+    """Y = X W^T + b for the rows of X given, at the requested output columns."""
+    X, W, b = _f64(X), _f64(W), _f64(b)
+    K = X.shape[1]
+    c = _cols(cols, W.shape[0])
+    out = np.empty((X.shape[0], len(c)), dtype=np.float64)
+    _lib().orc_linear(_ptr(X), X.shape[0], _ptr(W), _ptr(b), K, _ptr(c), len(c), _ptr(out))
+    return out
+
+
+def linear_gelu(X, W, b=None, mode=GELU_TANH, cols=None) -> np.ndarray:
+    X, W, b = _f64(X), _f64(W), _f64(b)
+    c = _cols(cols, W.shape[0])
+    out = np.empty((X.shape[0], len(c)), dtype=np.float64)
+    _lib().orc_linear_gelu(_ptr(X), X.shape[0], _ptr(W), _ptr(b), X.shape[1], _ptr(c), len(c),
+                           int(mode), _ptr(out))
+    return out
+
+
+def gelu(v, mode) -> np.ndarray:
+    v = _f64(v)
+    out = np.empty_like(v)
+    _lib().orc_gelu(_ptr(v), v.size, int(mode), _ptr(out))
+    return out
+
+
+def gelu_erf(x: float) -> float:
+    return _lib().orc_gelu_erf(float(x))
+
+
+def gelu_tanh(x: float) -> float:
+    return _lib().orc_gelu_tanh(float(x))
+
+
+def silu(x: float) -> float:
+    return _lib().orc_silu(float(x))
+
+
+def rope_angle(pos: float, pair: int, head_dim: int, theta: float) -> float:
+    return _lib().orc_rope_angle(float(pos), int(pair), int(head_dim), float(theta))
+
+
+def rope_rotate(x0: float, x1: float, angle: float):
+    y0, y1 = ctypes.c_double(), ctypes.c_double()
+    _lib().orc_rope_rotate(float(x0), float(x1), float(angle), ctypes.byref(y0), ctypes.byref(y1))
+    return y0.value, y1.value
+
+
+def qkv_rope(X, Wqkv, bqkv, n_heads, head_dim, theta, pos, cols=None) -> np.ndarray:
+    """Columns of [Q|K|V] after RoPE on Q and K; ``pos`` holds each row's position."""
+    X, Wqkv, bqkv = _f64(X), _f64(Wqkv), _f64(bqkv)
+    pos = _f64(np.asarray(pos))
+    c = _cols(cols, Wqkv.shape[0])
+    out = np.empty((X.shape[0], len(c)), dtype=np.float64)
+    _lib().orc_qkv_rope(_ptr(X), X.shape[0], _ptr(Wqkv), _ptr(bqkv), X.shape[1], int(n_heads),
+                        int(head_dim), float(theta), _ptr(pos), _ptr(c), len(c), _ptr(out))
+    return out
+
+
+def swiglu(X, Wg, Wu, bg=None, bu=None, cols=None) -> np.ndarray:
+    X, Wg, Wu, bg, bu = _f64(X), _f64(Wg), _f64(Wu), _f64(bg), _f64(bu)
+    c = _cols(cols, Wg.shape[0])
+    out = np.empty((X.shape[0], len(c)), dtype=np.float64)
+    _lib().orc_swiglu(_ptr(X), X.shape[0], _ptr(Wg), _ptr(Wu), _ptr(bg), _ptr(bu), X.shape[1],
+                      _ptr(c), len(c), _ptr(out))
+    return out
+
+
+def rmsnorm_fp8(X, W, b, Z, gamma, eps):
+    """Returns (codes uint8 [r, N], scale fp64 [r], y fp64 [r, N]) for the rows given."""
+    X, W, b, Z, gamma = _f64(X), _f64(W), _f64(b), _f64(Z), _f64(gamma)
+    r, K = X.shape
+    N = W.shape[0]
+    q = np.empty((r, N), dtype=np.uint8)
+    scale = np.empty(r, dtype=np.float64)
+    y = np.empty((r, N), dtype=np.float64)
+    _lib().orc_rmsnorm_fp8(_ptr(X), r, _ptr(W), _ptr(b), _ptr(Z), _ptr(gamma), N, K, float(eps),
+                           _ptr(q), _ptr(scale), _ptr(y))
+    return q, scale, y
+
+
+def e4m3_encode(y) -> np.ndarray:
+    y = _f64(y)
+    q = np.empty(y.shape, dtype=np.uint8)
+    _lib().orc_e4m3_encode_array(_ptr(y), y.size, _ptr(q))
+    return q
+
+
+def e4m3_decode(q) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    y = np.empty(q.shape, dtype=np.float64)
+    _lib().orc_e4m3_decode_array(_ptr(q), q.size, _ptr(y))
+    return y

@@ -1,0 +1,218 @@
+/* fp64 CPU oracle for the fused Linear + epilogue path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
+ * CPU-baseline leg are the only code that may load this library.  It shares
+ * no source, header, table or helper with the CUDA library and never calls it.
+ *
+ * Each function is the plain definition of what the fused kernels compute,
+ * written out in fp64 with ordinary loops and libm, in the order the pages
+ * state it.  Inputs are the exact fp64 widening of the bf16 / fp32 operands.
+ * Page citations name the page title and its section:
+ *   [T] "Triton 算子融合: Linear 与 Attention" (aiqz.cc, triton-operator-fusion-linear-attention)
+ *   [E] "GEMM Epilogue 完全拆解: 推理内核的最后一公里" (pinghaoyang.com.cn, gemm-epilogue-fusion)
+ *   [L] "什么是算子融合？LayerNorm与GeLU融合如何为深度学习推理提速" (ipipp.com)
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
+
+/* ---- Linear -------------------------------------------------------------
+ * [T] §Linear算子剖析: Y[m,n] = sum_{k=0}^{K-1} X[m,k] * W[n,k] + b[n].
+ * W is stored [N, K] (one row per output feature).  The sum runs in k order.
+ */
+static double linear_at(const double* x_row, const double* W, const double* b, long K, long n) {
+    const double* w = W + (size_t)n * (size_t)K;
+    double s = 0.0;
+    for (long k = 0; k < K; ++k) s += x_row[k] * w[k];
+    if (b) s += b[n];
+    return s;
+}
+
+/* out[i, j] = Linear(X[i, :])[cols[j]] for each of the nrows given rows of X. */
+void orc_linear(const double* X, long nrows, const double* W, const double* b, long K,
+                const long* cols, long ncols, double* out) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (long i = 0; i < nrows; ++i)
+        for (long j = 0; j < ncols; ++j)
+            out[i * ncols + j] = linear_at(X + (size_t)i * (size_t)K, W, b, K, cols[j]);
+}
+
+/* ---- GELU ----------------------------------------------------------------
+ * erf form, [T] §GELU激活融合 (the kernel line 0.5*x*(1+erf(x/sqrt 2))), which
+ * is x * Phi(x) with Phi the standard normal CDF.
+ */
+double orc_gelu_erf(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }
+
+/* tanh form, [T] §GELU激活融合 (formula) and [L] (constant sqrt(2/pi)):
+ * 0.5 x (1 + tanh( sqrt(2/pi) (x + 0.044715 x^3) )).
+ */
+double orc_gelu_tanh(double v) {
+    const double c = sqrt(2.0 / M_PI);
+    return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));
+}
+
+void orc_gelu(const double* v, long n, int mode, double* y) {
+    for (long i = 0; i < n; ++i) y[i] = mode == 0 ? orc_gelu_erf(v[i]) : orc_gelu_tanh(v[i]);
+}
+
+/* Linear followed by GELU (mode 0 = erf, 1 = tanh), [T] §GELU激活融合. */
+void orc_linear_gelu(const double* X, long nrows, const double* W, const double* b, long K,
+                     const long* cols, long ncols, int mode, double* out) {
+    orc_linear(X, nrows, W, b, K, cols, ncols, out);
+    orc_gelu(out, nrows * ncols, mode, out);
+}
+
+/* ---- RoPE ----------------------------------------------------------------
+ * [E] §模式 B and §累加器布局 (逐对运算): each adjacent pair of features
+ * (2i, 2i+1) inside a head is rotated in its plane by the angle
+ * pos * theta^(-2i / head_dim); two values in, two values out.
+ */
+double orc_rope_angle(double pos, long pair, long head_dim, double theta) {
+    return pos * pow(theta, -2.0 * (double)pair / (double)head_dim);
+}
+
+void orc_rope_rotate(double x0, double x1, double angle, double* y0, double* y1) {
+    double c = cos(angle), s = sin(angle);
+    *y0 = x0 * c - x1 * s;
+    *y1 = x0 * s + x1 * c;
+}
+
+/* ---- Fused QKV projection + RoPE ----------------------------------------
+ * [T] §QKV投影融合: [Q|K|V] = X Wqkv^T + bqkv with Q = columns [0, d),
+ * K = [d, 2d), V = [2d, 3d), here d = n_heads * head_dim.
+ * [E] §用形状与步长把约定钉死: rotation happens inside the epilogue, so the
+ * K section is written already rotated; V is not rotated.
+ * out[i, j] is column cols[j] of [Q|K|V] for row i, whose position is pos[i].
+ */
+void orc_qkv_rope(const double* X, long nrows, const double* Wqkv, const double* bqkv, long K,
+                  long n_heads, long head_dim, double theta, const double* pos,
+                  const long* cols, long ncols, double* out) {
+    const long d_model = n_heads * head_dim;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (long i = 0; i < nrows; ++i) {
+        for (long j = 0; j < ncols; ++j) {
+            const double* x = X + (size_t)i * (size_t)K;
+            long c = cols[j];
+            long section = c / d_model;
+            long d = (c % d_model) % head_dim;
+            if (section == 2) {
+                out[i * ncols + j] = linear_at(x, Wqkv, bqkv, K, c);
+                continue;
+            }
+            long c0 = c - (d & 1);
+            double x0 = linear_at(x, Wqkv, bqkv, K, c0);
+            double x1 = linear_at(x, Wqkv, bqkv, K, c0 + 1);
+            double y0, y1;
+            orc_rope_rotate(x0, x1, orc_rope_angle(pos[i], d / 2, head_dim, theta), &y0, &y1);
+            out[i * ncols + j] = (d & 1) ? y1 : y0;
+        }
+    }
+}
+
+/* ---- SwiGLU --------------------------------------------------------------
+ * [E] §模式 B / §末尾布局调整: gate g and value u of the same output feature
+ * give one value, y = SiLU(g) * u with SiLU(g) = g / (1 + e^{-g}); the output
+ * has half the width of the [gate | up] product.
+ */
+double orc_silu(double g) { return g / (1.0 + exp(-g)); }
+
+void orc_swiglu(const double* X, long nrows, const double* Wg, const double* Wu,
+                const double* bg, const double* bu, long K, const long* cols, long ncols,
+                double* out) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (long i = 0; i < nrows; ++i)
+        for (long j = 0; j < ncols; ++j) {
+            const double* x = X + (size_t)i * (size_t)K;
+            double g = linear_at(x, Wg, bg, K, cols[j]);
+            double u = linear_at(x, Wu, bu, K, cols[j]);
+            out[i * ncols + j] = orc_silu(g) * u;
+        }
+}
+
+/* ---- FP8 E4M3 (OCP 8-bit floating point, E4M3FN variant) -----------------
+ * sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no infinities; the
+ * only NaN magnitude is S.1111.111; largest finite 448; subnormals m * 2^-9.
+ */
+double orc_e4m3_decode(int code) {
+    int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double mag = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* [E] §仿射量化与尾声的五步, step 2: round to the nearest representable value
+ * (ties to the even mantissa) and clamp to [-448, 448].  Written as a search
+ * over the 127 non-negative finite codes, nearest first, even code on a tie. */
+int orc_e4m3_encode(double y) {
+    if (isnan(y)) return 0x7F;
+    int s = signbit(y) ? 1 : 0;
+    double a = fabs(y);
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(orc_e4m3_decode(c) - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (s << 7) | best;
+}
+
+void orc_e4m3_encode_array(const double* y, long n, uint8_t* q) {
+    for (long i = 0; i < n; ++i) q[i] = (uint8_t)orc_e4m3_encode(y[i]);
+}
+
+void orc_e4m3_decode_array(const uint8_t* q, long n, double* y) {
+    for (long i = 0; i < n; ++i) y[i] = orc_e4m3_decode(q[i]);
+}
+
+/* ---- Down projection + residual + RMSNorm + FP8 write-back --------------
+ * [E] §模式 A: h = X W^T (+ b) + z; r = 1 / sqrt(mean_n h^2 + eps) is one
+ * scalar per row; y = r * h (.) gamma.
+ * [E] §仿射量化与尾声的五步, steps 1, 2 and 5 with one block per row:
+ * s = max_n |y| / 448; q = e4m3(y / s); s is written beside q.  A row whose
+ * maximum is 0 gets s = 0 and all-zero codes.
+ * Outputs: q [nrows, N] codes, scale [nrows], y [nrows, N] (pre-quantisation).
+ */
+void orc_rmsnorm_fp8(const double* X, long nrows, const double* W, const double* b,
+                     const double* Z, const double* gamma, long N, long K, double eps,
+                     uint8_t* q, double* scale, double* y) {
+    for (long i = 0; i < nrows; ++i) {
+        const double* x = X + (size_t)i * (size_t)K;
+        double* yi = y + (size_t)i * (size_t)N;
+#pragma omp parallel for schedule(static)
+        for (long n = 0; n < N; ++n) yi[n] = linear_at(x, W, b, K, n) + Z[(size_t)i * N + n];
+        double ss = 0.0;
+        for (long n = 0; n < N; ++n) ss += yi[n] * yi[n];
+        double r = 1.0 / sqrt(ss / (double)N + eps);
+        double amax = 0.0;
+        for (long n = 0; n < N; ++n) {
+            yi[n] = yi[n] * gamma[n] * r;
+            if (fabs(yi[n]) > amax) amax = fabs(yi[n]);
+        }
+        scale[i] = amax / 448.0;
+        for (long n = 0; n < N; ++n)
+            q[(size_t)i * N + n] = amax > 0.0 ? (uint8_t)orc_e4m3_encode(yi[n] / scale[i]) : 0;
+    }
+}
+
+/* Number of OpenMP threads the parallel loops above use. */
+int orc_num_threads(void) {
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        {
+#ifdef _OPENMP
+            extern int omp_get_num_threads(void);
+            n = omp_get_num_threads();
+#endif
+        }
+    }
+    return n;
+}

@@ -1,0 +1,286 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+Kinds of pin used here: hand sums and brute force on tiny inputs, closed
+forms and identities of the mathematics, library routines computing the same
+quantity by another route (scipy, torch fp64 CPU ops, torch's float8 type),
+and constants printed on the pages (tests/golden/).  Each is chosen so that a
+plausible slip in the oracle (a dropped term, a wrong sign, a swapped index or
+operand, a wrong exponent) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            vals[parts[0]] = [float(p) for p in parts[1:]]
+    return vals
+
+
+# --------------------------------------------------------------------- Linear
+def test_linear_hand_sum():
+    # Y = X W^T + b, hand-summed: rows of X times rows of W.
+    X = np.array([[1, 2, 3], [4, 5, 6]], float)
+    W = np.array([[1, 0, -1], [2, 1, 0]], float)
+    b = np.array([10, 20], float)
+    Y = oracle.linear(X, W, b)
+    assert Y.tolist() == [[8.0, 24.0], [8.0, 33.0]]
+
+
+def test_linear_brute_force_nonsquare():
+    rng = np.random.default_rng(1)
+    X = rng.integers(-4, 5, size=(4, 8)).astype(float)
+    W = rng.integers(-4, 5, size=(5, 8)).astype(float)   # N=5 != M=4 != K=8
+    b = rng.integers(-4, 5, size=5).astype(float)
+    ref = [[sum(X[m, k] * W[n, k] for k in range(8)) + b[n] for n in range(5)] for m in range(4)]
+    assert oracle.linear(X, W, b).tolist() == ref
+    # column subset selection keeps the requested order
+    assert oracle.linear(X, W, b, cols=[3, 0]).tolist() == [[r[3], r[0]] for r in ref]
+
+
+def test_linear_special_cases():
+    rng = np.random.default_rng(2)
+    X = rng.standard_normal((3, 6))
+    assert np.array_equal(oracle.linear(X, np.eye(6)), X)              # identity W returns X
+    x1, w1 = rng.standard_normal((5, 1)), rng.standard_normal((7, 1))
+    assert np.allclose(oracle.linear(x1, w1), np.outer(x1[:, 0], w1[:, 0]), rtol=0, atol=0)  # K=1
+    assert np.all(oracle.linear(np.ones((2, 9)), np.ones((3, 9))) == 9.0)  # all-ones gives K
+    Xb, Wb = rng.standard_normal((16, 40)), rng.standard_normal((24, 40))
+    assert np.allclose(oracle.linear(Xb, Wb), Xb @ Wb.T, rtol=1e-13, atol=1e-13)  # library matmul
+
+
+# ----------------------------------------------------------------------- GELU
+def test_gelu_closed_forms():
+    for mode in (oracle.GELU_ERF, oracle.GELU_TANH):
+        g = oracle.gelu(np.array([0.0, 10.0, -10.0, 50.0]), mode)
+        assert g[0] == 0.0
+        assert abs(g[1] - 10.0) < 1e-15
+        assert abs(g[2]) < 1e-20
+        assert g[3] == 50.0
+    # erf form equals x * Phi(x); Phi from scipy's normal CDF (independent route)
+    from scipy.special import ndtr
+    x = np.linspace(-8, 8, 2001)
+    assert np.allclose(oracle.gelu(x, oracle.GELU_ERF), x * ndtr(x), rtol=1e-14, atol=1e-14)
+    assert oracle.gelu_erf(1.0) == pytest.approx(0.8413447460685429, rel=1e-15, abs=0)
+
+
+def test_gelu_matches_torch_fp64():
+    x = torch.linspace(-12, 12, 4801, dtype=torch.float64)
+    e = F.gelu(x).numpy()
+    t = F.gelu(x, approximate="tanh").numpy()
+    assert np.allclose(oracle.gelu(x.numpy(), oracle.GELU_ERF), e, rtol=1e-14, atol=1e-15)
+    assert np.allclose(oracle.gelu(x.numpy(), oracle.GELU_TANH), t, rtol=1e-14, atol=1e-15)
+
+
+def test_gelu_printed_constants():
+    g = _golden("gelu_constants.txt")
+    x = np.linspace(-6, 6, 1201)
+    from scipy.special import erf
+    printed_erf = 0.5 * x * (1.0 + erf(x * g["erf_arg_scale"][0]))
+    assert np.max(np.abs(oracle.gelu(x, oracle.GELU_ERF) - printed_erf)) < 1e-8
+    c, a = g["tanh_arg_scale"][0], g["tanh_cubic"][0]
+    printed_tanh = 0.5 * x * (1.0 + np.tanh(c * (x + a * x ** 3)))
+    assert np.max(np.abs(oracle.gelu(x, oracle.GELU_TANH) - printed_tanh)) < 1e-9
+
+
+def test_gelu_erf_tanh_gap():
+    g = _golden("gelu_constants.txt")
+    x = np.linspace(-10, 10, 200001)
+    gap = np.abs(oracle.gelu(x, oracle.GELU_ERF) - oracle.gelu(x, oracle.GELU_TANH))
+    # "about 1e-3": the largest gap lies within one decade below the printed order
+    order = g["erf_tanh_gap_order"][0]
+    assert order / 10 < gap.max() < order
+    assert gap.max() == pytest.approx(4.73e-4, rel=0.01)
+    assert abs(x[np.argmax(gap)] + 2.70) < 0.05
+
+
+def test_gelu_tanh_bracket():
+    # 1 + tanh(z) lies in (0, 2): gelu_tanh(x) / x lies in (0, 1) for x != 0
+    x = np.concatenate([np.linspace(-20, -1e-3, 500), np.linspace(1e-3, 20, 500)])
+    r = oracle.gelu(x, oracle.GELU_TANH) / x
+    assert np.all(r >= 0) and np.all(r <= 1)
+
+
+# ----------------------------------------------------------------------- RoPE
+def test_rope_angle_and_sign():
+    assert oracle.rope_angle(0, 5, 128, 1e4) == 0.0
+    assert oracle.rope_angle(1, 0, 128, 1e4) == 1.0                  # pair 0: 1 rad per position
+    assert oracle.rope_angle(100, 32, 128, 1e4) == pytest.approx(1.0, rel=1e-15)  # 1e4^(-64/128)=0.01
+    assert oracle.rope_angle(1, 63, 128, 1e4) == pytest.approx(1e4 ** (-126 / 128), rel=1e-15)
+    y0, y1 = oracle.rope_rotate(1.0, 0.0, 1.0)
+    assert (y0, y1) == pytest.approx((math.cos(1), math.sin(1)), abs=1e-16)
+    y0, y1 = oracle.rope_rotate(0.0, 1.0, 1.0)
+    assert (y0, y1) == pytest.approx((-math.sin(1), math.cos(1)), abs=1e-16)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        x0, x1, a, b = rng.standard_normal(4) * [1, 1, 50, 50]
+        y0, y1 = oracle.rope_rotate(x0, x1, a)
+        assert math.hypot(y0, y1) == pytest.approx(math.hypot(x0, x1), abs=1e-12)   # norm kept
+        z0, z1 = oracle.rope_rotate(y0, y1, b)
+        w0, w1 = oracle.rope_rotate(x0, x1, a + b)                                 # R(a)R(b)=R(a+b)
+        assert (z0, z1) == pytest.approx((w0, w1), abs=1e-11)
+
+
+def _rope_torch_complex(v, pos, head_dim, theta):
+    """RoPE as complex multiplication (independent formulation): [M, H*D] fp64."""
+    M = v.shape[0]
+    t = torch.from_numpy(v).reshape(M, -1, head_dim // 2, 2)
+    z = torch.view_as_complex(t.contiguous())
+    i = torch.arange(head_dim // 2, dtype=torch.float64)
+    freq = theta ** (-2.0 * i / head_dim)
+    ang = torch.from_numpy(np.asarray(pos, float))[:, None] * freq[None, :]
+    rot = torch.polar(torch.ones_like(ang), ang)[:, None, :]
+    return torch.view_as_real(z * rot).reshape(M, -1).numpy()
+
+
+def test_qkv_rope_composite_against_complex_rotation():
+    rng = np.random.default_rng(4)
+    M, K, H, D = 5, 24, 2, 16
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((3 * H * D, K)) / math.sqrt(K)
+    b = rng.standard_normal(3 * H * D) * 0.02
+    pos = np.array([0, 1, 7, 2047, 300])
+    out = oracle.qkv_rope(X, W, b, H, D, 10000.0, pos)
+    plain = X @ W.T + b
+    d = H * D
+    assert np.allclose(out[:, 2 * d:], plain[:, 2 * d:], rtol=1e-13, atol=1e-13)       # V untouched
+    assert np.allclose(out[0], plain[0], rtol=1e-13, atol=1e-13)                       # pos 0
+    assert np.allclose(out[:, :d], _rope_torch_complex(plain[:, :d], pos, D, 1e4), atol=1e-12)
+    assert np.allclose(out[:, d:2 * d], _rope_torch_complex(plain[:, d:2 * d], pos, D, 1e4), atol=1e-12)
+    # relative position: <RoPE(q, m), RoPE(k, n)> depends only on m - n
+    q, k = plain[1, :D], plain[1, d:d + D]
+    def dot_at(m, n):
+        a = _rope_torch_complex(q[None], [m], D, 1e4)[0]
+        c = _rope_torch_complex(k[None], [n], D, 1e4)[0]
+        return float(a @ c)
+    assert dot_at(10, 3) == pytest.approx(dot_at(107, 100), abs=1e-10)
+
+
+# --------------------------------------------------------------------- SwiGLU
+def test_silu_closed_forms():
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(50.0) == pytest.approx(50.0, abs=1e-18)
+    assert abs(oracle.silu(-50.0)) < 1e-18
+    for x in np.linspace(-9, 9, 37):
+        assert oracle.silu(x) - oracle.silu(-x) == pytest.approx(x, abs=1e-14)   # x*s(x) - (-x)s(-x) = x
+
+
+def test_swiglu_matches_torch_fp64():
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((6, 32))
+    Wg, Wu = rng.standard_normal((10, 32)) / 6, rng.standard_normal((10, 32)) / 6
+    bg, bu = rng.standard_normal(10) * 0.02, rng.standard_normal(10) * 0.02
+    Xt = torch.from_numpy(X)
+    ref = (F.silu(Xt @ torch.from_numpy(Wg).T + torch.from_numpy(bg))
+           * (Xt @ torch.from_numpy(Wu).T + torch.from_numpy(bu))).numpy()
+    assert np.allclose(oracle.swiglu(X, Wg, Wu, bg, bu), ref, rtol=1e-13, atol=1e-14)
+    # u == 1 reduces SwiGLU to SiLU of the gate projection
+    ones = oracle.swiglu(X, Wg, np.zeros_like(Wu), bg, np.ones(10))
+    assert np.allclose(ones, F.silu(Xt @ torch.from_numpy(Wg).T + torch.from_numpy(bg)).numpy(),
+                       rtol=1e-14, atol=1e-15)
+    # gate and up are not interchangeable
+    assert not np.allclose(oracle.swiglu(X, Wu, Wg, bu, bg), oracle.swiglu(X, Wg, Wu, bg, bu))
+
+
+# ------------------------------------------------------------------------ FP8
+def test_e4m3_decode_table():
+    d = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert d[0x00] == 0.0 and d[0x01] == 2.0 ** -9 and d[0x07] == 7 * 2.0 ** -9
+    assert d[0x08] == 2.0 ** -6 and d[0x38] == 1.0 and d[0x7E] == 448.0
+    assert math.isnan(d[0x7F]) and math.isnan(d[0xFF])
+    assert d[0xFE] == -448.0 and d[0x80] == 0.0 and math.copysign(1, d[0x80]) < 0
+    # library decode of the same bytes (torch's float8_e4m3fn type)
+    t = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    fin = ~np.isnan(t)
+    assert np.array_equal(np.isnan(d), ~fin) and np.array_equal(d[fin], t[fin])
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+    enc = lambda v: int(oracle.e4m3_encode(np.array([v]))[0])
+    assert enc(1.0625) == 0x38          # midpoint 1 | 1.125 -> even mantissa (1.0)
+    assert enc(1.1875) == 0x3A          # midpoint 1.125 | 1.25 -> even mantissa (1.25)
+    assert enc(2.0 ** -10) == 0x00      # midpoint 0 | 2^-9 -> 0
+    assert enc(3 * 2.0 ** -10) == 0x02  # midpoint 2^-9 | 2^-8 -> code 2
+    assert enc(449.0) == 0x7E and enc(1e6) == 0x7E and enc(-500.0) == 0xFE
+    assert enc(-1e-6) == 0x80
+
+
+def test_e4m3_encode_matches_torch():
+    rng = np.random.default_rng(6)
+    v = np.concatenate([rng.standard_normal(20000) * 40, rng.uniform(-448, 448, 20000),
+                        rng.standard_normal(5000) * 1e-2]).astype(np.float32)
+    lib = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(v.astype(np.float64)), lib)
+
+
+# -------------------------------------------------------------------- RMSNorm
+def _rms_case(seed, r=4, N=96, K=40, with_b=True):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((r, K))
+    W = rng.standard_normal((N, K)) / math.sqrt(K)
+    b = rng.standard_normal(N) * 0.02 if with_b else None
+    Z = rng.standard_normal((r, N))
+    g = 1.0 + 0.1 * rng.standard_normal(N)
+    return X, W, b, Z, g
+
+
+def test_rmsnorm_matches_torch_fp64():
+    X, W, b, Z, g = _rms_case(7)
+    q, s, y = oracle.rmsnorm_fp8(X, W, b, Z, g, 1e-6)
+    h = torch.from_numpy(X @ W.T + b + Z)
+    ref = F.rms_norm(h, (W.shape[0],), weight=torch.from_numpy(g), eps=1e-6).numpy()
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-14)
+    assert np.allclose(s, np.abs(ref).max(axis=1) / 448.0, rtol=1e-14)
+    lib = torch.from_numpy((ref / s[:, None]).astype(np.float32)).to(torch.float8_e4m3fn)
+    lib = lib.view(torch.uint8).numpy()
+    assert np.mean(lib == q) > 0.999
+
+
+def test_rmsnorm_unit_rms_and_invariance():
+    X, W, b, Z, _ = _rms_case(8, r=3, N=128)
+    ones = np.ones(128)
+    _, _, y = oracle.rmsnorm_fp8(X, W, b, Z, ones, 1e-6)
+    rms = np.sqrt(np.mean(y ** 2, axis=1))
+    assert np.all(np.abs(rms - 1.0) < 1e-6)
+    # with X = 0 the row is the residual alone; scaling it leaves the output unchanged
+    zX = np.zeros_like(X)
+    _, _, y1 = oracle.rmsnorm_fp8(zX, W, None, Z, ones, 1e-12)
+    _, _, y2 = oracle.rmsnorm_fp8(zX, W, None, 7.5 * Z, ones, 1e-12)
+    assert np.allclose(y1, y2, rtol=1e-10, atol=1e-12)
+    # constant row c: every output equals sign(c) / sqrt(1 + eps / c^2)
+    c = -0.3
+    _, _, yc = oracle.rmsnorm_fp8(zX[:1], W, None, np.full((1, 128), c), ones, 1e-6)
+    assert np.allclose(yc, -1.0 / math.sqrt(1 + 1e-6 / c ** 2), rtol=1e-14)
+
+
+def test_rmsnorm_fp8_codes_and_scale():
+    X, W, b, Z, g = _rms_case(9, r=5, N=200)
+    q, s, y = oracle.rmsnorm_fp8(X, W, b, Z, g, 1e-6)
+    for i in range(5):
+        j = int(np.argmax(np.abs(y[i])))
+        assert q[i, j] == (0xFE if y[i, j] < 0 else 0x7E)          # row maximum maps to +-448
+    deq = oracle.e4m3_decode(q) * s[:, None]
+    assert np.all(np.abs(deq - y) <= np.maximum(np.abs(y) * 2.0 ** -4, s[:, None] * 2.0 ** -9) + 1e-15)
+    # a zero row gives scale 0 and zero codes
+    q0, s0, _ = oracle.rmsnorm_fp8(np.zeros((1, 40)), W, None, np.zeros((1, 200)), g, 1e-6)
+    assert s0[0] == 0.0 and not q0.any()
