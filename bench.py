@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of the fused Linear + epilogue library on GB300.
+
+One step = one call of the headline workload, Linear + bias + GELU(tanh) at
+M=8192, N=16384, K=4096 in bf16 (fp32 accumulate), with inputs resident in
+HBM and L2 flushed (a 256 MiB write) before every timed launch.  Each launch
+is timed with CUDA events on the stream it is launched on.  `value` is
+TFLOP/s over all ranks (2*M*N*K per step per rank); `e2e` repeats the
+measurement with the inputs copied from pinned host memory and the output
+copied back inside the timed region.  The other fused workloads of the hot
+path are measured the same way and reported under `rows` (TFLOP/s, or HBM
+GB/s for the decode shape).
+
+`--impl reference` times the fp64 CPU oracle on a bounded row sample of the
+same workload instead (rank 0 only).
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, one rank per GPU; ranks run independent replicas of
+the workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+HEADLINE = "gelu_tanh_8192x16384x4096"
+METRIC = "fused GEMM+epilogue TFLOP/s & % bf16 tensor peak; decode-shape HBM GB/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- environment
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_epilogue_tcgen05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == want and parts[1] == workload:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        with open(self.out.name) as f:
+            rows = [[c.strip() for c in line.split(",")] for line in f if line.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+def dev_bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+class Case:
+    """Device operands of one workload plus the call that runs it through the C ABI."""
+
+    def __init__(self, name: str):
+        import gemm_epilogue_tcgen05_gb300 as fl
+        self.fl = fl
+        self.w = syn.WORKLOADS[name]
+        self.name = name
+        self.host = syn.make_operands(self.w)
+        self.dev = {k: dev_bf16(v) for k, v in self.host.items()}
+        w = self.w
+        d = self.dev
+        if w.kind in ("gelu_tanh", "gelu_erf"):
+            self.out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+            self.flops = 2.0 * w.M * w.N * w.K
+        elif w.kind == "qkv_rope":
+            dm = w.n_heads * w.head_dim
+            self.out = tuple(torch.empty((w.M, dm), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+            self.flops = 2.0 * w.M * w.N * w.K
+        elif w.kind == "swiglu":
+            self.out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+            self.flops = 2.0 * w.M * (2 * w.N) * w.K
+        else:
+            self.out = (torch.empty((w.M, w.N), dtype=torch.uint8, device="cuda"),
+                        torch.empty(w.M, dtype=torch.float32, device="cuda"))
+            self.ws = fl.rmsnorm_fp8_workspace(w.M, w.N, w.K)
+            self.flops = 2.0 * w.M * w.N * w.K
+        self.bytes = self.algorithmic_bytes()
+        self.hbm_bound = w.kind == "rmsnorm_fp8" and w.M <= 32
+
+    def algorithmic_bytes(self) -> float:
+        """Each operand read once and each output written once (bytes)."""
+        w = self.w
+        b = sum(v.nbytes for v in self.host.values())
+        if w.kind == "rmsnorm_fp8":
+            return float(b + w.M * w.N + 4 * w.M)
+        if w.kind == "qkv_rope":
+            return float(b + 2 * w.M * w.N)
+        return float(b + 2 * w.M * w.N)
+
+    def run(self, stream=None):
+        fl, w, d = self.fl, self.w, self.dev
+        if w.kind in ("gelu_tanh", "gelu_erf"):
+            fl.fused_linear_gelu(d["X"], d["W"], d.get("b"), Y=self.out,
+                                 mode="tanh" if w.kind == "gelu_tanh" else "erf", stream=stream)
+        elif w.kind == "qkv_rope":
+            fl.fused_qkv_rope(d["X"], d["W"], d.get("b"), n_heads=w.n_heads, head_dim=w.head_dim,
+                              seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
+        elif w.kind == "swiglu":
+            fl.fused_swiglu(d["X"], d["Wgate"], d["Wup"], d.get("bgate"), d.get("bup"), Y=self.out, stream=stream)
+        else:
+            fl.fused_linear_residual_rmsnorm_fp8(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], w.eps,
+                                                 Yq=self.out[0], row_scale=self.out[1], workspace=self.ws,
+                                                 stream=stream)
+
+    def outputs(self):
+        return self.out if isinstance(self.out, tuple) else (self.out,)
+
+
+def time_device(case: Case, steps: int, warmup: int, flush: torch.Tensor, barrier):
+    """Per-launch CUDA-event times (ms) with an L2 flush before every launch."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        case.run(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        case.run(stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    torch.cuda.synchronize()
+    if case.fl.device_status() != case.fl.FL_OK:
+        raise RuntimeError(f"{case.name}: device-side failure reported")
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
+
+
+def time_e2e(case: Case, steps: int, warmup: int, barrier):
+    """Per-step time (ms) with host->device input copies and device->host output copies inside."""
+    stream = torch.cuda.current_stream()
+    pinned_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).pin_memory()
+                 for k, v in case.host.items()}
+    outs = case.outputs()
+    pinned_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+
+    def step():
+        for k, t in pinned_in.items():
+            case.dev[k].view(torch.int16).copy_(t, non_blocking=True)
+        case.run(stream)
+        for o, p in zip(outs, pinned_out):
+            p.copy_(o, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(w, rows: int):
+    """Oracle on the first `rows` rows of the workload (all output columns); returns seconds."""
+    import oracle
+    ops = syn.make_operands(w, rows=(0, rows))
+    f = {k: syn.to_f64(v, w.dtype) for k, v in ops.items()}
+    t0 = time.perf_counter()
+    if w.kind in ("gelu_tanh", "gelu_erf"):
+        oracle.linear_gelu(f["X"], f["W"], f.get("b"), oracle.GELU_TANH if w.kind == "gelu_tanh"
+                           else oracle.GELU_ERF)
+    elif w.kind == "qkv_rope":
+        oracle.qkv_rope(f["X"], f["W"], f.get("b"), w.n_heads, w.head_dim, w.theta, np.arange(rows) % w.seq_len)
+    elif w.kind == "swiglu":
+        oracle.swiglu(f["X"], f["Wgate"], f["Wup"], f.get("bgate"), f.get("bup"))
+    else:
+        oracle.rmsnorm_fp8(f["X"], f["W"], f.get("b"), f["Z"], f["gamma"], w.eps)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(name: str, target_s: float = 10.0):
+    import oracle
+    w = syn.WORKLOADS[name]
+    t1 = oracle_sample(w, 1)
+    rows = int(max(1, min(w.M, math.floor(target_s / max(t1, 1e-6)))))
+    secs = oracle_sample(w, rows) if rows > 1 else t1
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} of {w.M} rows of {name}, all {w.N} output columns, fp64 ({secs:.2f} s)"}
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--rows", default="all", choices=["all", "none"],
+                    help="also measure the other fused workloads of the hot path")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = dist.barrier
+    else:
+        dist = None
+
+        def barrier():
+            return None
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        barrier()
+        __graft_entry__.build()
+
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    head = Case(HEADLINE)
+    with ClockSampler(local) as clk:
+        times, wall = time_device(head, args.steps, args.warmup, flush, barrier)
+    clocks = clk.summary()
+    ms = statistics.mean(times)
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * head.flops / (ms_max * 1e-3) / 1e12
+    kernel_tflops = head.flops / (ms * 1e-3) / 1e12
+    traffic = recorded_traffic(HEADLINE)
+    roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": kernel_tflops / pk["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"bf16 burst, {'of measured' if pk['source'] == 'measured' else 'of fallback'}",
+                "algorithmic_bytes": head.bytes}
+    e_times, h2d, d2h = time_e2e(head, max(3, args.steps // 2), 2, barrier)
+    e_ms = statistics.mean(e_times)
+    if dist is not None:
+        t = torch.tensor([e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e = {"value": world * head.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+    del head
+
+    rows = []
+    if args.rows == "all":
+        for name in ("qkv_rope_8192x12288x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
+                     "rmsnorm_fp8_decode_32x4096x14336"):
+            c = Case(name)
+            ts, _ = time_device(c, args.steps, args.warmup, flush, barrier)
+            m = statistics.mean(ts)
+            if c.hbm_bound:
+                ach = c.bytes / (m * 1e-3) / 1e9
+                rows.append({"workload": name, "value": ach, "unit": "GB/s", "us_per_launch": m * 1e3,
+                             "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                          "frac": ach / pk["hbm_gbs"], "traffic": recorded_traffic(name),
+                                          "algorithmic_bytes": c.bytes}})
+            else:
+                ach = c.flops / (m * 1e-3) / 1e12
+                rows.append({"workload": name, "value": ach, "unit": "TFLOP/s", "ms_per_launch": m,
+                             "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                                          "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
+                                          "traffic": recorded_traffic(name), "algorithmic_bytes": c.bytes}})
+            del c
+            torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, bf16)",
+        "config": {"workload": HEADLINE, "M": 8192, "N": 16384, "K": 4096, "epilogue": "bias + GELU(tanh)",
+                   "l2": "256 MiB flush before every timed launch; inputs larger than L2",
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+        "rows": rows, "wall_s_timed_region": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(HEADLINE)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def reference_arm(args, world, rank):
+    """The fp64 CPU oracle on bounded samples of the headline workload (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    syn.build()
+    w = syn.WORKLOADS[HEADLINE]
+    t1 = oracle_sample(w, 1)
+    per_step_target = 8.0 if args.steps <= 10 else 80.0 / args.steps
+    rows = int(max(1, min(w.M, math.floor(per_step_target / max(t1, 1e-6)))))
+    for _ in range(args.warmup):
+        oracle_sample(w, 1)
+    secs = [oracle_sample(w, rows) for _ in range(args.steps)]
+    s = statistics.mean(secs)
+    value = 2.0 * rows * w.N * w.K / s / 1e12
+    sample = f"{rows} of {w.M} rows of {HEADLINE} per step, all {w.N} output columns, fp64"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": HEADLINE, "M": 8192, "N": 16384, "K": 4096},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

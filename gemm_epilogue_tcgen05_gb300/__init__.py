@@ -1,0 +1,241 @@
+"""GB300 (sm_103a) fused Linear + epilogue library: Python binding.
+
+This module only marshals arguments: it turns torch CUDA tensors into device
+pointers, leading dimensions and a stream handle, and calls the C ABI of
+``libfusedlinear.so`` (declared in ``include/fused_linear.h``), whose CUDA
+kernels do every step of the computation.  There is no other code path: if
+the library is not built or cannot be loaded, every call raises.
+
+Functions carry the C names: :func:`fused_linear_gelu`,
+:func:`fused_qkv_rope`, :func:`fused_swiglu` and
+:func:`fused_linear_residual_rmsnorm_fp8`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+LIB_PATH = os.path.join(HERE, "libfusedlinear.so")
+HEADER = os.path.join(ROOT, "include", "fused_linear.h")
+
+FL_OK, FL_ERR_INVALID_ARG, FL_ERR_UNSUPPORTED, FL_ERR_ALIGNMENT, FL_ERR_WORKSPACE, FL_ERR_CUDA, \
+    FL_ERR_TIMEOUT, FL_ERR_ARCH = range(8)
+FL_F32, FL_BF16 = 0, 1
+FL_GELU_ERF, FL_GELU_TANH = 0, 1
+
+_lib = None
+
+
+class FusedLinearError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def load() -> ctypes.CDLL:
+    """Loads the in-tree library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run gemm_epilogue_tcgen05_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.fused_linear_gelu.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I, I, P]
+    lib.fused_qkv_rope.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I64, I64, I64, P]
+    lib.fused_swiglu.argtypes = [P, P, P, P, P, P, I, I, I, I64, I64, I64, P]
+    lib.fused_linear_residual_rmsnorm_fp8.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I64, I64, I64, I64,
+                                                      P, SZ, P]
+    for f in (lib.fused_linear_gelu, lib.fused_qkv_rope, lib.fused_swiglu,
+              lib.fused_linear_residual_rmsnorm_fp8):
+        f.restype = I
+    lib.fl_rmsnorm_fp8_workspace_bytes.argtypes = [I, I, I]
+    lib.fl_rmsnorm_fp8_workspace_bytes.restype = SZ
+    lib.fl_device_status.argtypes = [P]
+    lib.fl_device_status.restype = I
+    lib.fl_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.fl_set_wait_timeout_ns.restype = None
+    lib.fl_set_max_ctas.argtypes = [I]
+    lib.fl_set_max_ctas.restype = None
+    lib.fl_status_string.argtypes = [I]
+    lib.fl_status_string.restype = ctypes.c_char_p
+    lib.fl_version.argtypes = []
+    lib.fl_version.restype = I
+    _lib = lib
+    return lib
+
+
+def header_symbols() -> list[str]:
+    """Names of every entry point declared (FL_API) in include/fused_linear.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"^FL_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+
+
+def status_string(status: int) -> str:
+    return load().fl_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return load().fl_version()
+
+
+def _check(fn: str, status: int):
+    if status != FL_OK:
+        raise FusedLinearError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _mat(t, name, dtype):
+    if t.dim() != 2 or t.dtype != dtype or not t.is_cuda or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name}: expected a 2-D {dtype} CUDA tensor with unit column stride")
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def _vec(t, name, dtype, n):
+    if t is None:
+        return None
+    if t.dtype != dtype or not t.is_cuda or t.numel() != n or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous {dtype} CUDA vector of length {n}")
+    return t
+
+
+def _ld(t, width, fallback):
+    # Leading dimension of a [rows, width] row-major matrix.  A one-row matrix
+    # never reads past its first row, so any pitch >= width works; take one
+    # that satisfies the 16-byte pitch rule.
+    if t.shape[0] > 1:
+        return t.stride(0)
+    return max(-(-fallback // 16) * 16, 16)
+
+
+def fused_linear_gelu(X, W, b=None, Y=None, mode: str = "tanh", stream=None):
+    """Y = GELU(X W^T + b); bf16 (tcgen05) or fp32 operands."""
+    dtype = X.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("X must be bf16 or fp32")
+    M, K = X.shape
+    N = W.shape[0]
+    _mat(X, "X", dtype)
+    _mat(W, "W", dtype)
+    _vec(b, "b", dtype, N)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=dtype, device=X.device)
+    _mat(Y, "Y", dtype)
+    m = {"erf": FL_GELU_ERF, "tanh": FL_GELU_TANH}[mode]
+    st = load().fused_linear_gelu(_ptr(X), _ptr(W), _ptr(b), _ptr(Y), M, N, K, _ld(X, K, K), _ld(W, K, K),
+                                  _ld(Y, N, N), FL_BF16 if dtype == torch.bfloat16 else FL_F32, m,
+                                  _stream(stream))
+    _check("fused_linear_gelu", st)
+    return Y
+
+
+def fused_qkv_rope(X, Wqkv, bqkv=None, n_heads: int = 32, head_dim: int = 128, seq_len: int = 2048,
+                   theta: float = 10000.0, positions=None, out=None, stream=None):
+    """Returns (Q, K, V), Q and K already rotated (RoPE on adjacent pairs)."""
+    M, K = X.shape
+    d = n_heads * head_dim
+    _mat(X, "X", torch.bfloat16)
+    _mat(Wqkv, "Wqkv", torch.bfloat16)
+    _vec(bqkv, "bqkv", torch.bfloat16, 3 * d)
+    if positions is not None and (positions.dtype != torch.int32 or positions.numel() != M
+                                  or not positions.is_cuda or not positions.is_contiguous()):
+        raise ValueError("positions must be a contiguous int32 CUDA vector of length M")
+    if out is None:
+        out = tuple(torch.empty((M, d), dtype=torch.bfloat16, device=X.device) for _ in range(3))
+    Q, Ko, V = out
+    lds = {_ld(t, d, d) for t in out}
+    for t, nm in zip(out, "QKV"):
+        _mat(t, nm, torch.bfloat16)
+    if len(lds) != 1:
+        raise ValueError("Q, K and V must share one leading dimension")
+    st = load().fused_qkv_rope(_ptr(X), _ptr(Wqkv), _ptr(bqkv), _ptr(Q), _ptr(Ko), _ptr(V), _ptr(positions),
+                               M, K, n_heads, head_dim, seq_len, float(theta), _ld(X, K, K), _ld(Wqkv, K, K),
+                               lds.pop(), _stream(stream))
+    _check("fused_qkv_rope", st)
+    return Q, Ko, V
+
+
+def fused_swiglu(X, Wgate, Wup, bgate=None, bup=None, Y=None, stream=None):
+    """Y = SiLU(X Wgate^T + bgate) * (X Wup^T + bup)."""
+    M, K = X.shape
+    N = Wgate.shape[0]
+    _mat(X, "X", torch.bfloat16)
+    ldg = _mat(Wgate, "Wgate", torch.bfloat16)
+    ldu = _mat(Wup, "Wup", torch.bfloat16)
+    if Wup.shape != Wgate.shape or (N > 1 and ldg != ldu):
+        raise ValueError("Wgate and Wup must have the same shape and leading dimension")
+    _vec(bgate, "bgate", torch.bfloat16, N)
+    _vec(bup, "bup", torch.bfloat16, N)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _mat(Y, "Y", torch.bfloat16)
+    st = load().fused_swiglu(_ptr(X), _ptr(Wgate), _ptr(Wup), _ptr(bgate), _ptr(bup), _ptr(Y), M, N, K,
+                             _ld(X, K, K), _ld(Wgate, K, K), _ld(Y, N, N), _stream(stream))
+    _check("fused_swiglu", st)
+    return Y
+
+
+def rmsnorm_fp8_workspace_bytes(M: int, N: int, K: int) -> int:
+    return load().fl_rmsnorm_fp8_workspace_bytes(M, N, K)
+
+
+def rmsnorm_fp8_workspace(M: int, N: int, K: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace of the size the library asks for (torch allocation)."""
+    n = max(rmsnorm_fp8_workspace_bytes(M, N, K), 1)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def fused_linear_residual_rmsnorm_fp8(X, W, b, Z, gamma, eps: float = 1e-6, Yq=None, row_scale=None,
+                                      workspace=None, stream=None):
+    """Returns (Yq, row_scale): E4M3 codes as uint8 [M, N] and fp32 scales [M]."""
+    M, K = X.shape
+    N = W.shape[0]
+    _mat(X, "X", torch.bfloat16)
+    _mat(W, "W", torch.bfloat16)
+    _mat(Z, "Z", torch.bfloat16)
+    _vec(b, "b", torch.bfloat16, N)
+    _vec(gamma, "gamma", torch.bfloat16, N)
+    if Yq is None:
+        Yq = torch.empty((M, N), dtype=torch.uint8, device=X.device)
+    if Yq.dtype != torch.uint8:
+        Yq = Yq.view(torch.uint8)
+    _mat(Yq, "Yq", torch.uint8)
+    if row_scale is None:
+        row_scale = torch.empty(M, dtype=torch.float32, device=X.device)
+    _vec(row_scale, "row_scale", torch.float32, M)
+    if workspace is None:
+        workspace = rmsnorm_fp8_workspace(M, N, K, X.device)
+    st = load().fused_linear_residual_rmsnorm_fp8(
+        _ptr(X), _ptr(W), _ptr(b), _ptr(Z), _ptr(gamma), float(eps), _ptr(Yq), _ptr(row_scale), M, N, K,
+        _ld(X, K, K), _ld(W, K, K), _ld(Z, N, N), _ld(Yq, N, N), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check("fused_linear_residual_rmsnorm_fp8", st)
+    return Yq, row_scale
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device-side failure code."""
+    return load().fl_device_status(_stream(stream))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load().fl_set_wait_timeout_ns(int(ns))
+
+
+def set_max_ctas(n: int) -> None:
+    load().fl_set_max_ctas(int(n))

@@ -1,0 +1,151 @@
+// Library-wide host state: device query cache, the per-device status word,
+// wait limits, tensor-map encoding and the small exported utility calls.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "host_common.h"
+
+namespace fl {
+
+// Status word written by kernels that give up a bounded wait (see ptx.cuh).
+__device__ int g_fl_status[ST_WORDS];
+
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_known[kMaxDevices];
+int* g_status_ptr[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_max_ctas{0};
+
+struct SmemAttr {
+  const void* fn;
+  int device;
+  int bytes;
+};
+SmemAttr g_smem_attr[256];
+int g_smem_attr_n = 0;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+int current_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FL_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev_known[dev]) {
+      *out = g_dev[dev];
+      return out->cc == 103 ? FL_OK : FL_ERR_ARCH;
+    }
+  }
+  DeviceInfo d{dev, 0, 0};
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FL_ERR_CUDA;
+  d.cc = major * 10 + minor;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_dev[dev] = d;
+  g_dev_known[dev] = true;
+  *out = d;
+  return d.cc == 103 ? FL_OK : FL_ERR_ARCH;
+}
+
+int* device_status_ptr(int device) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  if (g_status_ptr[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fl_status) != cudaSuccess) return nullptr;
+    g_status_ptr[device] = static_cast<int*>(p);
+  }
+  return g_status_ptr[device];
+}
+
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+int max_ctas_override() { return g_max_ctas.load(); }
+
+bool ensure_smem_attr(const void* kernel, int device, int smem_bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < g_smem_attr_n; ++i)
+    if (g_smem_attr[i].fn == kernel && g_smem_attr[i].device == device && g_smem_attr[i].bytes >= smem_bytes)
+      return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+    return false;
+  if (g_smem_attr_n < 256) g_smem_attr[g_smem_attr_n++] = SmemAttr{kernel, device, smem_bytes};
+  return true;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld_elems * static_cast<uint64_t>(elem_bytes)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fl
+
+extern "C" {
+
+int fl_device_status(void* stream) {
+  using namespace fl;
+  DeviceInfo di;
+  const int st = current_device(&di);
+  if (st == FL_ERR_CUDA) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FL_ERR_CUDA;
+  int* dptr = device_status_ptr(di.device);
+  if (dptr == nullptr) return FL_ERR_CUDA;
+  int words[ST_WORDS];
+  if (cudaMemcpy(words, dptr, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return FL_ERR_CUDA;
+  if (words[ST_CODE] == 0) return FL_OK;
+  if (cudaMemset(dptr, 0, sizeof(words)) != cudaSuccess) return FL_ERR_CUDA;
+  return words[ST_CODE];
+}
+
+void fl_set_wait_timeout_ns(uint64_t ns) { fl::g_timeout_ns.store(ns == 0 ? fl::kDefaultTimeoutNs : ns); }
+
+void fl_set_max_ctas(int n) { fl::g_max_ctas.store(n < 0 ? 0 : n); }
+
+const char* fl_status_string(int status) {
+  switch (status) {
+    case FL_OK: return "ok";
+    case FL_ERR_INVALID_ARG: return "invalid argument";
+    case FL_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case FL_ERR_ALIGNMENT: return "pointer or row pitch not 16-byte aligned";
+    case FL_ERR_WORKSPACE: return "workspace missing or too small";
+    case FL_ERR_CUDA: return "CUDA runtime error";
+    case FL_ERR_TIMEOUT: return "device-side wait timed out";
+    case FL_ERR_ARCH: return "device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+int fl_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,517 @@
+// Persistent, warp-specialised tcgen05 GEMM with the epilogue applied to the
+// accumulator tile while it sits in tensor memory.
+//
+// The two-phase structure (mainloop produces an accumulator tile, the epilogue
+// transforms it before the only write to global memory) and its overlap with
+// the next tile's mainloop follow "GEMM Epilogue 完全拆解: 推理内核的最后一公里"
+// (pinghaoyang.com.cn), §主循环与尾声 and §Blackwell 的张量内存.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: X and W tiles into a ring of shared-memory stages
+//   warp 1      owns tensor memory; one thread issues tcgen05.mma into one of
+//               two accumulator buffers (double-buffered TMEM)
+//   warps 2..5  epilogue: tcgen05.ld -> registers -> tile function -> smem ->
+//               TMA store; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31,
+//               i.e. tile rows 32*(w%4)+lane, one row per thread.
+// Tiles are walked in a static persistent order (tile = blockIdx.x + i*gridDim.x)
+// with grouped rasterisation so that concurrently running CTAs share X and W
+// panels in L2.
+#pragma once
+#include "ptx.cuh"
+
+namespace fl {
+
+constexpr int kBM = 128;          // rows per tile (MMA M)
+constexpr int kBK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kStages = 4;
+constexpr int kStagingBytes = 4096;  // one 32-row x 128-byte TMA store box per buffer
+
+enum EpiKind : int { EPI_GELU_TANH = 0, EPI_GELU_ERF = 1, EPI_QKV_ROPE = 2, EPI_SWIGLU = 3, EPI_RMSNORM_FP8 = 4 };
+
+struct alignas(128) GemmParams {
+  CUtensorMap map_a;       // X [M, K] bf16, box {64, 128}
+  CUtensorMap map_b;       // W [N, K] bf16, box {64, 256}; SwiGLU: W_gate, box {64, 128}
+  CUtensorMap map_b2;      // SwiGLU: W_up, box {64, 128}
+  CUtensorMap map_out[3];  // outputs; box {64 bf16 | 128 fp8 columns, 32 rows}; QKV: Q, K, V
+  int M, N, K;             // N: logical output features (QKV: 3*d_model, SwiGLU: d_ff)
+  int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+  int group_m;             // m-blocks per raster group (1 = row-major tile order)
+  const __nv_bfloat16* bias;
+  const __nv_bfloat16* bias2;  // SwiGLU: b_up
+  // QKV + RoPE
+  const int* positions;
+  int seq_len, head_dim, d_model;
+  float log2_theta;
+  // residual + RMSNorm + FP8
+  const __nv_bfloat16* resid;
+  long long ldz;
+  const __nv_bfloat16* gamma;
+  float eps;
+  float* row_scale;
+  float2* partials;        // [num_m_blocks][num_n_blocks][128] (sum h^2, max |h*gamma|)
+  unsigned* counters;      // [2][num_m_blocks]: arrivals, finished readers
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+template <int EPI>
+struct EpiTraits {
+  static constexpr int kMmaN = 256;                               // accumulator columns per tile
+  static constexpr int kOutN = (EPI == EPI_SWIGLU) ? 128 : 256;   // output columns per tile
+  static constexpr bool kFp8 = (EPI == EPI_RMSNORM_FP8);
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = kMmaN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * kMmaN;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 4 * 2 * kStagingBytes + 1024 /*bars*/ +
+                                    1024 /*alignment slack*/;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
+  const int per_group = p.group_m * p.num_n_blocks;
+  const int g = t / per_group;
+  const int first_m = g * p.group_m;
+  const int gsize = min(p.num_m_blocks - first_m, p.group_m);
+  const int r = t - g * per_group;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+// 32 bf16 values [col0, col0+32) of a vector (bias, gamma) as fp32; zeros past n_limit.
+__device__ __forceinline__ void load_vec32(const __nv_bfloat16* ptr, int col0, int n_limit, float (&v)[32]) {
+  if (ptr == nullptr) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    return;
+  }
+  if (col0 + 32 <= n_limit) {
+    const uint4* q = reinterpret_cast<const uint4*>(ptr + col0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 w = __ldg(q + i);
+      v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+      v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+      v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+      v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = (col0 + j < n_limit) ? __bfloat162float(ptr[col0 + j]) : 0.f;
+  }
+}
+
+// 32 bf16 values of one row of a matrix (the residual): row-pointer based.
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* row, bool row_ok, int col0, int n_limit,
+                                           float (&v)[32]) {
+  if (!row_ok) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    return;
+  }
+  load_vec32(row, col0, n_limit, v);
+}
+
+__device__ __forceinline__ void tmem_load32f(uint32_t taddr, bool zero, float (&v)[32]) {
+  if (zero) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    return;
+  }
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ float gelu_tanh_f(float v) {
+  // 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
+  const float u = v * fmaf(0.0356774081363f, v * v, 0.7978845608028654f);
+  const float hv = 0.5f * v;
+  return fmaf(hv, tanh_approx(u), hv);
+}
+__device__ __forceinline__ float gelu_erf_f(float v) { return 0.5f * v * (1.f + erff(v * 0.70710678118654752f)); }
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
+// Writes 32 bf16 values (one row segment) into a 128B-swizzled staging row:
+// `unit` (0 or 1) selects which half of the 128-byte row they fill.
+__device__ __forceinline__ void stage_bf16_32(uint32_t buf, int lane, int unit, const float (&v)[32]) {
+  const uint32_t row = buf + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int chunk = unit * 4 + c;
+    st_shared_v4(row + ((chunk ^ (lane & 7)) << 4), pack_bf16x2(v[8 * c + 0], v[8 * c + 1]),
+                 pack_bf16x2(v[8 * c + 2], v[8 * c + 3]), pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                 pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+  }
+}
+// Writes 32 E4M3 codes (32 bytes) into a 128B-swizzled staging row; `unit` 0..3.
+__device__ __forceinline__ void stage_fp8_32(uint32_t buf, int lane, int unit, const float (&v)[32]) {
+  const uint32_t row = buf + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 16 * c + 4 * i;
+      w[i] = f32x2_to_e4m3x2(v[j], v[j + 1]) | (f32x2_to_e4m3x2(v[j + 2], v[j + 3]) << 16);
+    }
+    const int chunk = unit * 2 + c;
+    st_shared_v4(row + ((chunk ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Per-warp double-buffered TMA store of 32-row x 128-byte boxes.
+struct StoreRing {
+  uint32_t base;  // this warp's two staging buffers (shared-memory address)
+  int count;
+  // Returns a staging buffer whose previous store has finished reading it.
+  __device__ __forceinline__ uint32_t acquire(int lane) {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    return base + (count & 1) * kStagingBytes;
+  }
+  // Publishes the staged box to the async proxy and stores it at (x, y).
+  __device__ __forceinline__ void commit(const CUtensorMap* map, uint32_t buf, int lane, int x, int y) {
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d_u32(map, buf, x, y);
+      bulk_commit();
+    }
+    ++count;
+  }
+};
+
+// Bounded spin until all `need` tiles of a row block have published their
+// partial row statistics.  Returns false on timeout or if another CTA has
+// already recorded a failure (then the exchange can never complete).
+__device__ __forceinline__ bool wait_row_block(const GemmParams& p, int mb, unsigned need) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (ld_acquire_u32(p.counters + mb) == need) return true;  // exact count: reset to 0 after use
+    if ((i & 15u) == 15u) {
+      if (*reinterpret_cast<volatile int*>(p.status + ST_CODE) != 0) return false;
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        record_failure(p.status, W_ROW_EXCHANGE, mb);
+        return false;
+      }
+    }
+    __nanosleep(100);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using T = EpiTraits<EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_mem = smem;
+  uint8_t* staging = smem + kStages * T::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + 4 * 2 * kStagingBytes);
+  uint64_t* full_bar = bars;                 // [kStages]  TMA landed
+  uint64_t* empty_bar = bars + kStages;      // [kStages]  MMAs reading the stage finished
+  uint64_t* tfull_bar = bars + 2 * kStages;  // [2]        accumulator buffer complete
+  uint64_t* tempty_bar = tfull_bar + 2;      // [2]        epilogue done reading the buffer
+  uint64_t* drain_bar = tempty_bar + 2;      // [1]        all MMAs complete (teardown)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);  // written by the epilogue leader only
+  float* inv_freq = reinterpret_cast<float*>(tmem_slot + 4);  // [64], QKV only
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtx wctx{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0 && p.num_k_blocks > 0) {
+    tma_prefetch_desc(&p.map_a);
+    tma_prefetch_desc(&p.map_b);
+    if (EPI == EPI_SWIGLU) tma_prefetch_desc(&p.map_b2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, T::kTmemCols);
+    tmem_relinquish();
+  }
+  if (EPI == EPI_QKV_ROPE && threadIdx.x >= 64 && threadIdx.x < 128) {
+    const int i = threadIdx.x - 64;  // pair index within a head (head_dim 128 -> 64 pairs)
+    inv_freq[i] = exp2f(-(2.f * static_cast<float>(i) / static_cast<float>(p.head_dim)) * p.log2_theta);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;  // per stage: ever issued / parity of the last issue
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wctx, W_PRODUCER_EMPTY)) { ok = false; break; }
+          uint8_t* a_dst = stage_mem + stage * T::kStageBytes;
+          uint8_t* b_dst = a_dst + T::kABytes;
+          mbar_arrive_expect_tx(&full_bar[stage], T::kStageBytes);
+          tma_load_2d(&p.map_a, &full_bar[stage], a_dst, kb * kBK, mb * kBM);
+          if (EPI == EPI_SWIGLU) {
+            // gate rows and up rows of the same 128 output features, stacked in one B stage
+            tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * 128);
+            tma_load_2d(&p.map_b2, &full_bar[stage], b_dst + 128 * kBK * 2, kb * kBK, nb * 128);
+          } else {
+            tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * T::kMmaN);
+          }
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // Do not leave copies landing in shared memory after the CTA exits.
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_quiet(&full_bar[s], (issued_phase >> s) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, T::kMmaN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+        const int abuf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait(&tempty_bar[abuf], (use & 1u) ^ 1u, wctx, W_MMA_TMEM_EMPTY)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + abuf * T::kMmaN;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, wctx, W_MMA_FULL)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_mem + stage * T::kStageBytes);
+          const uint64_t adesc = sdesc_k_sw128(a_addr);
+          const uint64_t bdesc = sdesc_k_sw128(a_addr + T::kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            // +32 bytes along K per step inside the 128-byte swizzled row (>> 4 in the descriptor)
+            mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty_bar[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&tfull_bar[abuf]);
+      }
+      // Every MMA issued by this thread must be complete before TMEM is freed.
+      mma_commit(drain_bar);
+      mbar_wait_quiet(drain_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int q = warp & 3;  // TMEM lane quarter owned by this warp
+    const int row_in_tile = q * 32 + lane;
+    StoreRing ring{smem_u32(staging) + (warp - 2) * 2 * kStagingBytes, 0};
+    const bool k_empty = p.num_k_blocks == 0;
+    int local = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int abuf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int m = mb * kBM + row_in_tile;
+      const bool row_ok = m < p.M;
+      const int y_box = mb * kBM + q * 32;
+      // warp-uniform: tcgen05.ld below is a warp-collective instruction
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[abuf], use & 1u, wctx, W_EPI_TMEM_FULL));
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * T::kMmaN;
+
+      if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF || EPI == EPI_QKV_ROPE) {
+        if (!ok) break;
+        int n0 = nb * T::kOutN;  // first output column of the tile
+        int sec = 0;
+        float pos = 0.f;
+        if constexpr (EPI == EPI_QKV_ROPE) {
+          sec = n0 / p.d_model;  // 0 = Q, 1 = K, 2 = V (a tile never straddles two sections)
+          n0 -= sec * p.d_model;
+          const int pi = row_ok ? (p.positions ? __ldg(p.positions + m) : m % p.seq_len) : 0;
+          pos = static_cast<float>(pi);
+        }
+        const int n_limit = (EPI == EPI_QKV_ROPE) ? p.d_model : p.N;
+        const __nv_bfloat16* bias =
+            p.bias ? p.bias + (EPI == EPI_QKV_ROPE ? sec * p.d_model : 0) : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < T::kOutN / 64; ++c) {
+          const uint32_t buf = ring.acquire(lane);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col0 = n0 + c * 64 + u * 32;
+            float v[32], b[32];
+            tmem_load32f(tacc + c * 64 + u * 32, k_empty, v);
+            load_vec32(bias, col0, n_limit, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += b[j];
+            if constexpr (EPI == EPI_GELU_TANH) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_f(v[j]);
+            } else if constexpr (EPI == EPI_GELU_ERF) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = gelu_erf_f(v[j]);
+            } else {
+              if (sec < 2) {
+                // adjacent pair (2i, 2i+1) of a head, rotated by pos * theta^(-2i/head_dim)
+                const int pair0 = (col0 % p.head_dim) >> 1;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                  float sn, cs;
+                  sincosf(pos * inv_freq[pair0 + (j >> 1)], &sn, &cs);
+                  const float x0 = v[j], x1 = v[j + 1];
+                  v[j] = x0 * cs - x1 * sn;
+                  v[j + 1] = x0 * sn + x1 * cs;
+                }
+              }
+            }
+            stage_bf16_32(buf, lane, u, v);
+          }
+          ring.commit(&p.map_out[sec], buf, lane, n0 + c * 64, y_box);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[abuf]);
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        if (!ok) break;
+        const int n0 = nb * 128;  // accumulator columns [0,128) = gate, [128,256) = up
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t buf = ring.acquire(lane);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col0 = n0 + c * 64 + u * 32;
+            float g[32], v[32], b[32];
+            tmem_load32f(tacc + c * 64 + u * 32, k_empty, g);
+            load_vec32(p.bias, col0, p.N, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] = silu_f(g[j] + b[j]);
+            tmem_load32f(tacc + 128 + c * 64 + u * 32, k_empty, v);
+            load_vec32(p.bias2, col0, p.N, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = g[j] * (v[j] + b[j]);
+            stage_bf16_32(buf, lane, u, v);
+          }
+          ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[abuf]);
+      } else if constexpr (EPI == EPI_RMSNORM_FP8) {
+        // The 128 epilogue threads take the same named barriers in every
+        // iteration and leave the loop together, right after a barrier.
+        const int n0 = nb * 256;
+        const __nv_bfloat16* zrow = p.resid + static_cast<long long>(row_ok ? m : 0) * p.ldz;
+        // Pass 1: h = acc + b + z; partial sum of h^2 and partial max |h * gamma| over this tile's columns.
+        float ss = 0.f, am = 0.f;
+        if (ok) {
+#pragma unroll 1
+          for (int u = 0; u < 8; ++u) {
+            const int col0 = n0 + u * 32;
+            float v[32], z[32], g[32], b[32];
+            tmem_load32f(tacc + u * 32, k_empty, v);
+            load_row32(zrow, row_ok, col0, p.N, z);
+            load_vec32(p.gamma, col0, p.N, g);
+            load_vec32(p.bias, col0, p.N, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float h = v[j] + b[j] + z[j];
+              ss = fmaf(h, h, ss);
+              am = fmaxf(am, fabsf(h * g[j]));
+            }
+          }
+          p.partials[static_cast<size_t>(mb * p.num_n_blocks + nb) * kBM + row_in_tile] = make_float2(ss, am);
+        }
+        __threadfence();
+        named_bar_sync(1, kEpiThreads);
+        if (threadIdx.x == 64) {
+          int stop = *abort_flag;
+          if (!stop) {
+            __threadfence();
+            atomicAdd(p.counters + mb, 1u);
+            if (!wait_row_block(p, mb, static_cast<unsigned>(p.num_n_blocks))) {
+              stop = 1;
+              *abort_flag = 1;
+            }
+          }
+          *epi_stop = stop;
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (*epi_stop) break;  // uniform: only the leader writes it, between the two barriers
+        // Merge the partials of every tile of this row block (fixed order: deterministic).
+        float SS = 0.f, A = 0.f;
+        const float2* prow = p.partials + static_cast<size_t>(mb) * p.num_n_blocks * kBM + row_in_tile;
+        for (int j = 0; j < p.num_n_blocks; ++j) {
+          const float2 w = __ldcg(prow + static_cast<size_t>(j) * kBM);
+          SS += w.x;
+          A = fmaxf(A, w.y);
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (threadIdx.x == 64) {
+          // The last tile of the row block to finish reading resets the counters for the next call.
+          const unsigned old = atomicAdd(p.counters + p.num_m_blocks + mb, 1u);
+          if (old == static_cast<unsigned>(p.num_n_blocks) - 1u) {
+            p.counters[mb] = 0u;
+            p.counters[p.num_m_blocks + mb] = 0u;
+          }
+        }
+        const float r = rsqrtf(SS / static_cast<float>(p.N) + p.eps);
+        const float qs = A > 0.f ? 448.f / A : 0.f;  // y / scale = h * gamma * 448 / max|h * gamma|
+        if (nb == 0 && row_ok) p.row_scale[m] = r * A * (1.f / 448.f);
+        // Pass 2: codes.
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t buf = ring.acquire(lane);
+#pragma unroll 1
+          for (int u = 0; u < 4; ++u) {
+            const int col0 = n0 + c * 128 + u * 32;
+            float v[32], z[32], g[32], b[32];
+            tmem_load32f(tacc + c * 128 + u * 32, k_empty, v);
+            load_row32(zrow, row_ok, col0, p.N, z);
+            load_vec32(p.gamma, col0, p.N, g);
+            load_vec32(p.bias, col0, p.N, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = (v[j] + b[j] + z[j]) * g[j] * qs;
+            stage_fp8_32(buf, lane, u, v);
+          }
+          ring.commit(&p.map_out[0], buf, lane, n0 + c * 128, y_box);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[abuf]);
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, T::kTmemCols);
+  }
+}
+
+}  // namespace fl

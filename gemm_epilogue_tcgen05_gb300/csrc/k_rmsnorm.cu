@@ -1,0 +1,163 @@
+// fused_linear_residual_rmsnorm_fp8: h = X W^T (+ b) + Z; y = r h (.) gamma with
+// r = 1/sqrt(mean h^2 + eps); Yq = e4m3(y / s), s = max|y| / 448 per row.
+//   "GEMM Epilogue 完全拆解" (pinghaoyang.com.cn), §模式 A and §仿射量化与尾声的五步.
+// M > 32: persistent tcgen05 kernel; the 256-column tiles of one 128-row block
+//         exchange per-row partials through the workspace inside the kernel.
+// M <= 32: split-K swap-AB decode kernel (decode_kernel.cuh).
+#include "decode_kernel.cuh"
+#include "host_common.h"
+
+namespace fl {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct WsLayout {
+  bool decode;
+  size_t counters, partials, hbuf, stats, total;  // byte offsets (total = size)
+  int grid, seg_max;                              // decode only
+};
+
+bool use_decode(int M, int K) { return M <= kDecTokens && K > 0; }
+
+WsLayout layout(int M, int N, int K, int num_sms) {
+  WsLayout w{};
+  if (M <= 0 || N <= 0) return w;
+  if (use_decode(M, K)) {
+    w.decode = true;
+    const int num_f = cdiv(N, 128);
+    const int num_kb = cdiv(K, kBK);
+    const long long units = static_cast<long long>(num_f) * num_kb;
+    w.grid = static_cast<int>(units < num_sms ? units : num_sms);
+    w.seg_max = 1;
+    for (int c = 0; c < w.grid; ++c) {
+      const long long b = dec_unit_begin(c, units, w.grid), e = dec_unit_begin(c + 1, units, w.grid);
+      if (e > b) {
+        const int segs = static_cast<int>((e - 1) / num_kb - b / num_kb + 1);
+        if (segs > w.seg_max) w.seg_max = segs;
+      }
+    }
+    w.counters = 0;
+    w.partials = align_up(static_cast<size_t>(num_f + 2) * sizeof(unsigned));
+    w.hbuf = w.partials + align_up(static_cast<size_t>(w.grid) * w.seg_max * 128 * kDecTokens * sizeof(float));
+    w.stats = w.hbuf + align_up(static_cast<size_t>(num_f) * kDecTokens * 128 * sizeof(float));
+    w.total = w.stats + align_up(static_cast<size_t>(num_f) * kDecTokens * sizeof(float2));
+  } else {
+    const int num_m = cdiv(M, kBM), num_n = cdiv(N, 256);
+    w.counters = 0;
+    w.partials = align_up(static_cast<size_t>(2 * num_m) * sizeof(unsigned));
+    w.total = w.partials + align_up(static_cast<size_t>(num_m) * num_n * kBM * sizeof(float2));
+  }
+  return w;
+}
+
+}  // namespace
+}  // namespace fl
+
+extern "C" size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K) {
+  using namespace fl;
+  DeviceInfo di;
+  if (current_device(&di) == FL_ERR_CUDA) return 0;
+  return layout(M, N, K, di.num_sms).total;
+}
+
+extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const void* b, const void* Z,
+                                                 const void* gamma, float eps, void* Yq, float* row_scale, int M,
+                                                 int N, int K, int64_t ldx, int64_t ldw, int64_t ldz, int64_t ldq,
+                                                 void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace fl;
+  if (M < 0 || N < 0 || K < 0) return FL_ERR_INVALID_ARG;
+  if (!(eps >= 0.f)) return FL_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FL_OK;
+  if (Z == nullptr || gamma == nullptr || Yq == nullptr || row_scale == nullptr ||
+      (K > 0 && (X == nullptr || W == nullptr)))
+    return FL_ERR_INVALID_ARG;
+  if (ldz < N || ldq < N || (K > 0 && (ldx < K || ldw < K))) return FL_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(b) || !aligned16(Z) || !aligned16(gamma) || !aligned16(Yq) ||
+      !aligned16(row_scale))
+    return FL_ERR_ALIGNMENT;
+  if (!pitch_ok(ldz, 2) || !pitch_ok(ldq, 1) || (K > 0 && (!pitch_ok(ldx, 2) || !pitch_ok(ldw, 2))))
+    return FL_ERR_ALIGNMENT;
+  DeviceInfo di;
+  int st = current_device(&di);
+  if (st != FL_OK) return st;
+  const WsLayout wl = layout(M, N, K, di.num_sms);
+  if (workspace == nullptr || workspace_bytes < wl.total) return FL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FL_ERR_ALIGNMENT;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (wl.decode) {
+    if (wl.seg_max > kDecMaxSeg) return FL_ERR_UNSUPPORTED;
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!encode_2d(&p.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, N, ldw, kBK, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&p.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kDecTokens,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return FL_ERR_CUDA;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_f = cdiv(N, 128);
+    p.num_kb = cdiv(K, kBK);
+    p.units = static_cast<long long>(p.num_f) * p.num_kb;
+    p.seg_max = wl.seg_max;
+    p.bias = static_cast<const __nv_bfloat16*>(b);
+    p.resid = static_cast<const __nv_bfloat16*>(Z);
+    p.ldz = ldz;
+    p.gamma = static_cast<const __nv_bfloat16*>(gamma);
+    p.eps = eps;
+    p.yq = static_cast<uint8_t*>(Yq);
+    p.ldq = ldq;
+    p.row_scale = row_scale;
+    p.counters = reinterpret_cast<unsigned*>(ws + wl.counters);
+    p.partials = reinterpret_cast<float*>(ws + wl.partials);
+    p.hbuf = reinterpret_cast<float*>(ws + wl.hbuf);
+    p.stats = reinterpret_cast<float2*>(ws + wl.stats);
+    p.status = device_status_ptr(di.device);
+    p.timeout_ns = wait_timeout_ns();
+    if (p.status == nullptr) return FL_ERR_CUDA;
+    const void* kfn = reinterpret_cast<const void*>(&rmsnorm_fp8_decode_kernel);
+    if (!ensure_smem_attr(kfn, di.device, kDecSmemBytes)) return FL_ERR_CUDA;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(wl.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kDecSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rmsnorm_fp8_decode_kernel, p) == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+  }
+
+  GemmParams p;
+  init_params(p, M, N, K, 256);
+  p.group_m = 1;  // row-major tile order: the tiles of one row block run side by side
+  if (p.num_n_blocks > di.num_sms) return FL_ERR_UNSUPPORTED;
+  if (K > 0) {
+    if (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, N, ldw, kBK, 256,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return FL_ERR_CUDA;
+  }
+  if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Yq, N, M, ldq, 128, 32,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return FL_ERR_CUDA;
+  p.bias = static_cast<const __nv_bfloat16*>(b);
+  p.resid = static_cast<const __nv_bfloat16*>(Z);
+  p.ldz = ldz;
+  p.gamma = static_cast<const __nv_bfloat16*>(gamma);
+  p.eps = eps;
+  p.row_scale = row_scale;
+  p.counters = reinterpret_cast<unsigned*>(ws + wl.counters);
+  p.partials = reinterpret_cast<float2*>(ws + wl.partials);
+  // Every tile of a row block must be resident together: the grid is at least
+  // one row block wide and all CTAs are co-scheduled (cooperative launch).
+  return launch_gemm<EPI_RMSNORM_FP8>(p, di, s, true, p.num_n_blocks);
+}

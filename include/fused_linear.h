@@ -1,0 +1,167 @@
+/* fused_linear.h — C ABI of the GB300 (sm_103a) fused Linear + epilogue library.
+ *
+ * Every entry point computes a Linear layer Y = X W^T (+ b) on the tcgen05
+ * tensor cores, keeps the fp32 accumulator tile in tensor memory, and applies
+ * the memory-bound tail ("epilogue") to that tile before anything is written
+ * to HBM; no intermediate tensor is materialised.
+ *
+ * Conventions shared by all entry points
+ *   - Matrices are row-major.  X is [M, K] with leading dimension ldx (in
+ *     elements), W is [N, K] (one row per output feature, the PyTorch Linear
+ *     layout) with leading dimension ldw, outputs are [M, N_out] with their own
+ *     leading dimension.  All leading dimensions are in elements.
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or retains them.  Except where stated, bf16 means IEEE
+ *     bfloat16 stored as 16-bit words.
+ *   - Calls are asynchronous: they validate the arguments on the host, enqueue
+ *     one kernel on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     return.  Device-side failures (a bounded wait that ran out) are recorded
+ *     in a library status word and reported by fl_device_status().
+ *   - Alignment (a requirement of the tensor-memory-access copies): every base
+ *     pointer must be 16-byte aligned and every leading dimension times the
+ *     element size must be a multiple of 16 bytes.
+ *   - M, N or K equal to 0 is allowed; M == 0 or N == 0 enqueues nothing, and
+ *     K == 0 treats X W^T as zero.
+ *   - Return value: an fl_status code (FL_OK = 0).  No partial work is
+ *     enqueued when a call returns an error.
+ *
+ * Page citations name the page title and its section:
+ *   "Triton 算子融合: Linear 与 Attention" (aiqz.cc, triton-operator-fusion-linear-attention)
+ *   "GEMM Epilogue 完全拆解: 推理内核的最后一公里" (pinghaoyang.com.cn, gemm-epilogue-fusion)
+ */
+#ifndef FUSED_LINEAR_H
+#define FUSED_LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FL_API __attribute__((visibility("default")))
+#else
+#define FL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fl_status {
+    FL_OK = 0,
+    FL_ERR_INVALID_ARG = 1,   /* null pointer, negative size, leading dim below the row width */
+    FL_ERR_UNSUPPORTED = 2,   /* a shape or option this build does not implement */
+    FL_ERR_ALIGNMENT = 3,     /* pointer or row pitch not 16-byte aligned */
+    FL_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+    FL_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    FL_ERR_TIMEOUT = 6,       /* a device-side bounded wait ran out (see fl_device_status) */
+    FL_ERR_ARCH = 7           /* the current device is not sm_103 */
+} fl_status;
+
+enum { FL_F32 = 0, FL_BF16 = 1 };
+enum { FL_GELU_ERF = 0, FL_GELU_TANH = 1 };
+
+/* Linear + bias + GELU.
+ *   "Triton 算子融合: Linear 与 Attention", §Linear算子剖析 (Y[m,n] = sum_k X[m,k] W[n,k] + b[n])
+ *   and §GELU激活融合 (erf form 0.5 v (1 + erf(v / sqrt 2)); tanh form
+ *   0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))).
+ * X [M,K], W [N,K], b [N] (nullable: no bias), Y [M,N].  X, W, b and Y all have
+ * dtype `dtype`: FL_BF16 (tcgen05 bf16 MMA, fp32 accumulate, one bf16 rounding
+ * at the store) or FL_F32 (fp32 operands and output; computed with fp32 FMA).
+ * mode: FL_GELU_ERF or FL_GELU_TANH.  Y must not alias X, W or b.
+ */
+FL_API int fused_linear_gelu(const void* X, const void* W, const void* b, void* Y,
+                      int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldy,
+                      int dtype, int mode, void* stream);
+
+/* Fused QKV projection + RoPE with split write-back.
+ *   "Triton 算子融合: Linear 与 Attention", §QKV投影融合: [Q|K|V] = X Wqkv^T + bqkv with
+ *   Q, K, V the first, middle and last d = n_heads * head_dim output columns.
+ *   "GEMM Epilogue 完全拆解", §模式 B and §累加器布局 (RoPE rotates each adjacent
+ *   feature pair (2i, 2i+1) of a head by pos * theta^(-2i/head_dim)), and
+ *   §用形状与步长把约定钉死 (layout contract).
+ * Layout contract: Q, Kout and V are three separate row-major bf16 [M, d] tensors
+ * with the same leading dimension ldo.  Q and Kout are written ALREADY ROTATED;
+ * downstream code must not rotate them again.  V is not rotated.  Order: bias,
+ * then rotation, then one bf16 rounding.
+ * X [M,K] bf16, Wqkv [3d, K] bf16 (W_q, W_k, W_v stacked by rows), bqkv [3d] bf16
+ * (nullable).  positions: nullable device int32 [M]; when NULL row m has
+ * position m % seq_len (rows are sequences of seq_len tokens laid end to end).
+ * Positions must lie in [0, 2^24).  head_dim must be 128 and d a multiple of 256.
+ */
+FL_API int fused_qkv_rope(const void* X, const void* Wqkv, const void* bqkv,
+                   void* Q, void* Kout, void* V, const int32_t* positions,
+                   int M, int K, int n_heads, int head_dim, int seq_len, float theta,
+                   int64_t ldx, int64_t ldw, int64_t ldo, void* stream);
+
+/* SwiGLU up-projection: Y = SiLU(X Wgate^T + bgate) * (X Wup^T + bup).
+ *   "GEMM Epilogue 完全拆解", §模式 B and §末尾布局调整 (a gate/value pair gives one
+ *   value; the output has half the width of the [gate|up] product).
+ * X [M,K] bf16; Wgate and Wup [N,K] bf16 with the same leading dimension ldw;
+ * bgate, bup [N] bf16 (each nullable); Y [M,N] bf16.  The gate and up rows
+ * that feed the same output columns are loaded side by side into one
+ * shared-memory stage, so no host-side repacking of the weights is needed.
+ */
+FL_API int fused_swiglu(const void* X, const void* Wgate, const void* Wup,
+                 const void* bgate, const void* bup, void* Y,
+                 int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldy, void* stream);
+
+/* Down projection + residual + RMSNorm + per-row FP8 E4M3 quantised write-back.
+ *   "GEMM Epilogue 完全拆解", §模式 A: h = X W^T (+ b) + Z, r = 1/sqrt(mean_n h^2 + eps)
+ *   (one scalar per row), y = r * h (.) gamma; §仿射量化与尾声的五步 steps 1, 2 and 5
+ *   with one block per row: scale = max_n |y| / 448, Yq = e4m3(y / scale) rounded
+ *   to nearest even and saturated to +-448, scale written beside Yq.
+ * The row statistics span all N columns, which several output tiles share: each
+ * tile emits per-row partial sums of squares and partial maxima, which are merged
+ * inside the same kernel through `workspace` (the two-level reduction of §模式 A).
+ * X [M,K] bf16, W [N,K] bf16, b [N] bf16 (nullable), Z [M,N] bf16 residual with
+ * leading dimension ldz, gamma [N] bf16.  Yq [M,N] E4M3 bytes (leading dimension
+ * ldq, a multiple of 16), row_scale [M] fp32 (dequantise with Yq * row_scale).
+ * A row whose maximum is 0 gets scale 0 and zero codes.
+ * workspace: device memory of at least fl_rmsnorm_fp8_workspace_bytes(M, N, K)
+ * bytes, 256-byte aligned and ZERO-FILLED before its first use.  The kernels
+ * reset the counters they keep there before they return, so the same workspace
+ * serves later calls on the same stream without clearing; after FL_ERR_TIMEOUT
+ * it must be zero-filled again.  Calls that may run concurrently must not share
+ * a workspace.  M <= 32 with K > 0 runs the split-K decode kernel (one CTA per
+ * SM, each streaming an equal share of W); larger M runs the persistent
+ * prefill kernel.  Both launch cooperatively (all CTAs resident at once) and
+ * fail with FL_ERR_CUDA if that is impossible.  N must not exceed
+ * 256 * (number of SMs) on the prefill path.
+ */
+FL_API int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const void* b,
+                                      const void* Z, const void* gamma, float eps,
+                                      void* Yq, float* row_scale,
+                                      int M, int N, int K,
+                                      int64_t ldx, int64_t ldw, int64_t ldz, int64_t ldq,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fused_linear_residual_rmsnorm_fp8 needs for this shape
+ * on the current device (0 for an empty problem). */
+FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);
+
+/* Synchronises `stream`, then returns FL_OK if no kernel of this library
+ * recorded a device-side failure on the current device since the previous
+ * call, else the recorded code (FL_ERR_TIMEOUT), and clears the record.
+ * Returns FL_ERR_CUDA if the synchronisation itself fails. */
+FL_API int fl_device_status(void* stream);
+
+/* Upper bound, in nanoseconds, on every device-side wait of later launches
+ * (default 2e9).  A wait that runs out sets the status word, makes the kernel
+ * drain its in-flight copies, free its tensor memory and return.  0 restores
+ * the default.  Process-wide; intended for tests and diagnostics. */
+FL_API void fl_set_wait_timeout_ns(uint64_t ns);
+
+/* Caps the number of CTAs of the persistent kernels (0 = one per SM).  Used by
+ * tests to make each CTA walk many tiles.  Process-wide. */
+FL_API void fl_set_max_ctas(int n);
+
+/* Static text for a status code. */
+FL_API const char* fl_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+FL_API int fl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSED_LINEAR_H */

@@ -1,0 +1,72 @@
+"""The C-ABI library on the host (no GPU needed): it builds, loads, exports
+every entry point the header declares, and rejects bad arguments before it
+touches the device."""
+import ctypes
+
+import pytest
+
+import gemm_epilogue_tcgen05_gb300 as fl
+from gemm_epilogue_tcgen05_gb300 import build as cuda_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return fl.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = fl.header_symbols()
+    assert {"fused_linear_gelu", "fused_qkv_rope", "fused_swiglu",
+            "fused_linear_residual_rmsnorm_fp8"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/fused_linear.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    assert fl.version() == 100
+    assert fl.status_string(fl.FL_OK) == "ok"
+    assert "timed out" in fl.status_string(fl.FL_ERR_TIMEOUT)
+    assert fl.status_string(99) == "unknown status"
+
+
+P = ctypes.c_void_p
+
+
+def test_gelu_rejects_bad_arguments_on_host(lib):
+    a = P(0x10000)
+    # negative sizes, bad dtype / mode, missing pointers, short leading dimension
+    assert lib.fused_linear_gelu(a, a, None, a, -1, 8, 8, 8, 8, 8, 1, 1, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_gelu(a, a, None, a, 8, 8, 8, 8, 8, 8, 7, 1, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_gelu(a, a, None, a, 8, 8, 8, 8, 8, 8, 1, 5, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_gelu(None, a, None, a, 8, 8, 8, 8, 8, 8, 1, 1, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_gelu(a, a, None, a, 8, 8, 16, 8, 16, 8, 1, 1, None) == fl.FL_ERR_INVALID_ARG
+    # misaligned base pointer, row pitch not a multiple of 16 bytes
+    assert lib.fused_linear_gelu(P(0x10002), a, None, a, 8, 8, 8, 8, 8, 8, 1, 1, None) == fl.FL_ERR_ALIGNMENT
+    assert lib.fused_linear_gelu(a, a, None, a, 8, 8, 12, 12, 12, 8, 1, 1, None) == fl.FL_ERR_ALIGNMENT
+    # empty problems succeed without touching the device
+    assert lib.fused_linear_gelu(None, None, None, None, 0, 8, 8, 8, 8, 8, 1, 1, None) == fl.FL_OK
+    assert lib.fused_linear_gelu(None, None, None, None, 8, 0, 8, 8, 8, 8, 1, 1, None) == fl.FL_OK
+
+
+def test_other_entry_points_reject_bad_arguments_on_host(lib):
+    a = P(0x10000)
+    # QKV: head_dim other than 128, or a model width that is not a multiple of 256
+    assert lib.fused_qkv_rope(a, a, None, a, a, a, None, 8, 64, 1, 64, 16, 1e4, 64, 64, 64,
+                              None) == fl.FL_ERR_UNSUPPORTED
+    assert lib.fused_qkv_rope(a, a, None, a, a, a, None, 8, 64, 3, 128, 16, 1e4, 64, 64, 384,
+                              None) == fl.FL_ERR_UNSUPPORTED
+    assert lib.fused_qkv_rope(a, a, None, a, a, a, None, 8, 64, 2, 128, 0, 1e4, 64, 64, 256,
+                              None) == fl.FL_ERR_INVALID_ARG  # no positions and no sequence length
+    assert lib.fused_qkv_rope(a, a, None, a, a, a, None, 8, 64, 2, 128, 16, -1.0, 64, 64, 256,
+                              None) == fl.FL_ERR_INVALID_ARG
+    # SwiGLU: misaligned up-projection weights
+    assert lib.fused_swiglu(a, a, P(0x10008), None, None, a, 8, 8, 8, 8, 8, 8, None) == fl.FL_ERR_ALIGNMENT
+    # RMSNorm: missing gamma, negative eps, FP8 pitch not a multiple of 16
+    f = ctypes.c_float
+    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, None, f(1e-6), a, a, 8, 16, 8, 8, 8, 16, 16,
+                                                 a, 1 << 20, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, a, f(-1.0), a, a, 8, 16, 8, 8, 8, 16, 16,
+                                                 a, 1 << 20, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, a, f(1e-6), a, a, 8, 24, 8, 8, 8, 24, 24,
+                                                 a, 1 << 20, None) == fl.FL_ERR_ALIGNMENT

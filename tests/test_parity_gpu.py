@@ -1,0 +1,264 @@
+"""GPU parity: every entry point, through the C ABI, against the fp64 oracle.
+
+Small cases span several tiles with ragged edges in M, N and K and are
+compared element by element.  The full-size workloads run in the same launch
+configuration the benchmark times and are compared on sampled rows (every
+column of each sampled row, so every N-tile is covered).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_epilogue_tcgen05_gb300 as fl
+import oracle
+import synthetic as syn
+from parity_utils import (assert_bf16_close, assert_f32_close, assert_fp8_close, dev_bf16, dev_f32, f64, host,
+                          sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    fl.set_max_ctas(0)
+    fl.set_wait_timeout_ns(0)
+    yield
+    fl.set_max_ctas(0)
+    fl.set_wait_timeout_ns(0)
+    assert fl.device_status() == fl.FL_OK
+
+
+def _draw(shape, stream, std=1.0, mean=0.0, seed=0, dtype="bf16"):
+    return syn.draw(seed, stream, shape, mean, std, dtype)
+
+
+# ------------------------------------------------------------------ GELU
+@pytest.mark.parametrize("mode", ["tanh", "erf"])
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (130, 264, 72), (300, 520, 200), (256, 256, 1024)])
+def test_gelu_small(mode, M, N, K):
+    X = _draw((M, K), syn.STREAM_X)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5)
+    b = _draw((N,), syn.STREAM_B, 0.02)
+    Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), dev_bf16(b), mode=mode)
+    m = oracle.GELU_TANH if mode == "tanh" else oracle.GELU_ERF
+    assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), f64(b), m), f"gelu {mode} {M}x{N}x{K}")
+
+
+def test_gelu_no_bias_and_k_zero():
+    M, N, K = 70, 296, 96  # 296 bf16 = 592 bytes: a 16-byte row pitch
+    X, W = _draw((M, K), syn.STREAM_X), _draw((N, K), syn.STREAM_W, K ** -0.5)
+    Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), None, mode="tanh")
+    assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), None, oracle.GELU_TANH), "no bias")
+    b = _draw((N,), syn.STREAM_B, 0.5)
+    Xe = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
+    We = torch.empty((N, 0), dtype=torch.bfloat16, device="cuda")
+    Y0 = fl.fused_linear_gelu(Xe, We, dev_bf16(b), mode="erf")
+    ref = oracle.gelu(np.broadcast_to(f64(b), (M, N)).copy(), oracle.GELU_ERF)
+    assert_bf16_close(host(Y0), ref, "K=0")
+
+
+def test_gelu_empty_is_noop():
+    Y = torch.full((0, 16), 7.0, dtype=torch.bfloat16, device="cuda")
+    fl.fused_linear_gelu(torch.empty((0, 8), dtype=torch.bfloat16, device="cuda"),
+                         torch.zeros((16, 8), dtype=torch.bfloat16, device="cuda"), None, Y=Y)
+
+
+def test_gelu_strided_operands_and_few_ctas():
+    # leading dimensions wider than the rows, and 3 CTAs walking 5x5 tiles each
+    M, N, K = 640, 1280, 256
+    X = _draw((M, K + 64), syn.STREAM_X)
+    W = _draw((N, K + 32), syn.STREAM_W, K ** -0.5)
+    b = _draw((N,), syn.STREAM_B, 0.02)
+    Xd, Wd = dev_bf16(X)[:, :K], dev_bf16(W)[:, :K]
+    Yfull = torch.zeros((M, N + 40), dtype=torch.bfloat16, device="cuda")
+    fl.set_max_ctas(3)
+    fl.fused_linear_gelu(Xd, Wd, dev_bf16(b), Y=Yfull[:, :N], mode="tanh")
+    ref = oracle.linear_gelu(f64(X[:, :K]), f64(W[:, :K]), f64(b), oracle.GELU_TANH)
+    assert_bf16_close(host(Yfull[:, :N]), ref, "strided/few CTAs")
+    assert torch.count_nonzero(Yfull[:, N:]) == 0, "wrote outside the output columns"
+
+
+def test_gelu_tiny_fp32_workload():
+    w = syn.WORKLOADS["tiny_gelu_erf_f32"]
+    ops = syn.make_operands(w)
+    Y = fl.fused_linear_gelu(dev_f32(ops["X"]), dev_f32(ops["W"]), dev_f32(ops["b"]), mode="erf")
+    ref = oracle.linear_gelu(ops["X"].astype(np.float64), ops["W"].astype(np.float64),
+                             ops["b"].astype(np.float64), oracle.GELU_ERF)
+    assert_f32_close(host(Y), ref, "tiny fp32 erf")
+
+
+def test_gelu_full_workload_sampled():
+    w = syn.WORKLOADS["gelu_tanh_8192x16384x4096"]
+    ops = syn.make_operands(w)
+    Y = fl.fused_linear_gelu(dev_bf16(ops["X"]), dev_bf16(ops["W"]), dev_bf16(ops["b"]), mode="tanh")
+    rows = sample_rows(w.M)
+    got = host(Y[torch.from_numpy(rows).cuda()])
+    ref = oracle.linear_gelu(f64(ops["X"][rows]), f64(ops["W"]), f64(ops["b"]), oracle.GELU_TANH)
+    assert_bf16_close(got, ref, "gelu full")
+
+
+# ------------------------------------------------------------------ QKV + RoPE
+def _qkv_ref(X, Wq, bq, H, D, pos, theta=10000.0):
+    return oracle.qkv_rope(f64(X), f64(Wq), None if bq is None else f64(bq), H, D, theta, pos)
+
+
+def test_qkv_rope_small_bias_and_positions():
+    M, K, H, D = 300, 192, 2, 128
+    X = _draw((M, K), syn.STREAM_X)
+    Wq = _draw((3 * H * D, K), syn.STREAM_W, K ** -0.5)
+    bq = _draw((3 * H * D,), syn.STREAM_B, 0.02)
+    q, k, v = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), dev_bf16(bq), n_heads=H, head_dim=D, seq_len=100)
+    ref = _qkv_ref(X, Wq, bq, H, D, np.arange(M) % 100)
+    d = H * D
+    assert_bf16_close(host(q), ref[:, :d], "Q")
+    assert_bf16_close(host(k), ref[:, d:2 * d], "K (rotated)")
+    assert_bf16_close(host(v), ref[:, 2 * d:], "V")
+    pos = np.random.default_rng(1).integers(0, 8192, size=M).astype(np.int32)
+    q, k, v = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, head_dim=D,
+                                positions=torch.from_numpy(pos).cuda())
+    ref = _qkv_ref(X, Wq, None, H, D, pos)
+    assert_bf16_close(host(torch.cat([q, k, v], 1)), ref, "explicit positions")
+
+
+def test_qkv_rope_full_workload_sampled():
+    w = syn.WORKLOADS["qkv_rope_8192x12288x4096"]
+    ops = syn.make_operands(w)
+    q, k, v = fl.fused_qkv_rope(dev_bf16(ops["X"]), dev_bf16(ops["W"]), None, n_heads=w.n_heads,
+                                head_dim=w.head_dim, seq_len=w.seq_len, theta=w.theta)
+    rows = sample_rows(w.M)
+    ri = torch.from_numpy(rows).cuda()
+    got = host(torch.cat([q[ri], k[ri], v[ri]], 1))
+    ref = _qkv_ref(ops["X"][rows], ops["W"], None, w.n_heads, w.head_dim, rows % w.seq_len, w.theta)
+    assert_bf16_close(got, ref, "qkv full")
+
+
+# ------------------------------------------------------------------ SwiGLU
+def test_swiglu_small_ragged_with_bias():
+    M, N, K = 300, 200, 136
+    X = _draw((M, K), syn.STREAM_X)
+    Wg, Wu = _draw((N, K), syn.STREAM_W, K ** -0.5), _draw((N, K), syn.STREAM_WUP, K ** -0.5)
+    bg, bu = _draw((N,), syn.STREAM_B, 0.1), _draw((N,), syn.STREAM_BUP, 0.1)
+    Y = fl.fused_swiglu(dev_bf16(X), dev_bf16(Wg), dev_bf16(Wu), dev_bf16(bg), dev_bf16(bu))
+    assert_bf16_close(host(Y), oracle.swiglu(f64(X), f64(Wg), f64(Wu), f64(bg), f64(bu)), "swiglu small")
+
+
+def test_swiglu_full_workload_sampled():
+    w = syn.WORKLOADS["swiglu_8192x14336x4096"]
+    ops = syn.make_operands(w)
+    Y = fl.fused_swiglu(dev_bf16(ops["X"]), dev_bf16(ops["Wgate"]), dev_bf16(ops["Wup"]))
+    rows = sample_rows(w.M)
+    got = host(Y[torch.from_numpy(rows).cuda()])
+    ref = oracle.swiglu(f64(ops["X"][rows]), f64(ops["Wgate"]), f64(ops["Wup"]))
+    assert_bf16_close(got, ref, "swiglu full")
+
+
+# ------------------------------------------------------------------ residual + RMSNorm + FP8
+def _rms_case(M, N, K, bias, seed=0):
+    X = _draw((M, K), syn.STREAM_X, seed=seed)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=seed)
+    b = _draw((N,), syn.STREAM_B, 0.02, seed=seed) if bias else None
+    Z = _draw((M, N), syn.STREAM_Z, seed=seed)
+    g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0, seed=seed)
+    return X, W, b, Z, g
+
+
+def _rms_run(X, W, b, Z, g, ldq=None, workspace=None):
+    M, N = Z.shape
+    Yq = None
+    if ldq is not None:
+        Yq = torch.zeros((M, ldq), dtype=torch.uint8, device="cuda")[:, :N]
+    q, s = fl.fused_linear_residual_rmsnorm_fp8(dev_bf16(X), dev_bf16(W), None if b is None else dev_bf16(b),
+                                                dev_bf16(Z), dev_bf16(g), 1e-6, Yq=Yq, workspace=workspace)
+    return q.cpu().numpy(), s.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M,N,K,bias,ldq", [(300, 1024, 520, True, None), (200, 1000, 256, False, 1008),
+                                             (129, 256, 64, True, None), (64, 4096, 192, False, None)])
+def test_rmsnorm_fp8_prefill_small(M, N, K, bias, ldq):
+    X, W, b, Z, g = _rms_case(M, N, K, bias)
+    q, s = _rms_run(X, W, b, Z, g, ldq=ldq)
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None if b is None else f64(b), f64(Z), f64(g), 1e-6)
+    assert_fp8_close(q, s, q_ref, s_ref, f"prefill {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,bias", [(32, 4096, 1024, False), (1, 512, 200, True), (17, 1000, 320, True),
+                                        (32, 256, 64, False)])
+def test_rmsnorm_fp8_decode_small(M, N, K, bias):
+    X, W, b, Z, g = _rms_case(M, N, K, bias)
+    ldq = -(-N // 16) * 16
+    q, s = _rms_run(X, W, b, Z, g, ldq=ldq if ldq != N else None)
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None if b is None else f64(b), f64(Z), f64(g), 1e-6)
+    assert_fp8_close(q, s, q_ref, s_ref, f"decode {M}x{N}x{K}")
+
+
+def test_rmsnorm_fp8_workspace_reuse_and_few_ctas():
+    # the kernels leave the workspace counters at zero: back-to-back calls agree
+    for M in (300, 24):
+        X, W, b, Z, g = _rms_case(M, 2048, 384, True, seed=3)
+        ws = fl.rmsnorm_fp8_workspace(M, 2048, 384)
+        if M > 32:
+            fl.set_max_ctas(8)  # 2048 / 256 = 8 tiles per row block: the smallest grid allowed
+        q1, s1 = _rms_run(X, W, b, Z, g, workspace=ws)
+        q2, s2 = _rms_run(X, W, b, Z, g, workspace=ws)
+        fl.set_max_ctas(0)
+        assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+        assert torch.count_nonzero(ws[:256]) == 0, "counters not reset"
+        q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), f64(b), f64(Z), f64(g), 1e-6)
+        assert_fp8_close(q1, s1, q_ref, s_ref, f"reuse M={M}")
+
+
+def test_rmsnorm_fp8_prefill_full_workload_sampled():
+    w = syn.WORKLOADS["rmsnorm_fp8_prefill_8192x4096x14336"]
+    ops = syn.make_operands(w)
+    q, s = _rms_run(ops["X"], ops["W"], None, ops["Z"], ops["gamma"])
+    rows = sample_rows(w.M, extra=2)
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(ops["X"][rows]), f64(ops["W"]), None, f64(ops["Z"][rows]),
+                                         f64(ops["gamma"]), w.eps)
+    assert_fp8_close(q[rows], s[rows], q_ref, s_ref, "prefill full")
+
+
+def test_rmsnorm_fp8_decode_full_workload():
+    w = syn.WORKLOADS["rmsnorm_fp8_decode_32x4096x14336"]
+    ops = syn.make_operands(w)
+    q, s = _rms_run(ops["X"], ops["W"], None, ops["Z"], ops["gamma"])
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(ops["X"]), f64(ops["W"]), None, f64(ops["Z"]), f64(ops["gamma"]),
+                                         w.eps)
+    assert_fp8_close(q, s, q_ref, s_ref, "decode full")
+
+
+@pytest.mark.parametrize("M", [256, 16])
+def test_rmsnorm_fp8_wait_timeout_reports_status(M):
+    # A counter that never reaches its target makes the exchange wait run out:
+    # the kernel records FL_ERR_TIMEOUT, drains and returns; the context stays usable.
+    N, K = 1024, 128
+    X, W, b, Z, g = _rms_case(M, N, K, False)
+    ws = fl.rmsnorm_fp8_workspace(M, N, K)
+    ws[:4] = torch.tensor([100, 0, 0, 0], dtype=torch.uint8)  # counters[0] = 100: never equals its target
+    if M <= 32:
+        ws[:] = 0
+        nf = N // 128
+        ws[4 * nf:4 * nf + 4] = torch.tensor([100, 0, 0, 0], dtype=torch.uint8)  # finished-tile counter
+    fl.set_wait_timeout_ns(50_000_000)
+    _rms_run(X, W, b, Z, g, workspace=ws)
+    assert fl.device_status() == fl.FL_ERR_TIMEOUT
+    fl.set_wait_timeout_ns(0)
+    ws.zero_()
+    q, s = _rms_run(X, W, b, Z, g, workspace=ws)
+    assert fl.device_status() == fl.FL_OK
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None, f64(Z), f64(g), 1e-6)
+    assert_fp8_close(q, s, q_ref, s_ref, "after timeout")
+
+
+def test_argument_errors_on_device():
+    X = torch.zeros((16, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((256, 64), dtype=torch.bfloat16, device="cuda")
+    Z = torch.zeros((16, 256), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+    small = torch.zeros(8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fl.FusedLinearError) as e:
+        fl.fused_linear_residual_rmsnorm_fp8(X, W, None, Z, g, workspace=small)
+    assert e.value.status == fl.FL_ERR_WORKSPACE
+    with pytest.raises(fl.FusedLinearError) as e:
+        fl.fused_qkv_rope(X, torch.zeros((3 * 64, 64), dtype=torch.bfloat16, device="cuda"), n_heads=1,
+                          head_dim=64)
+    assert e.value.status == fl.FL_ERR_UNSUPPORTED
