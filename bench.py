@@ -306,6 +306,8 @@ def main():
     ap.add_argument("--rows", default="all", choices=["all", "none"],
                     help="also measure the other fused workloads of the hot path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(syn.WORKLOADS),
+                    help="workload timed as the step (default: the headline); used for profiling runs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -333,6 +335,8 @@ def main():
 
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    if args.workload != HEADLINE:
+        return single_workload(args, world, rank, local, barrier, dist)
     head = Case(HEADLINE)
     with ClockSampler(local) as clk:
         times, wall = time_device(head, args.steps, args.warmup, flush, barrier)
@@ -396,6 +400,30 @@ def main():
         line["cpu_baseline"] = cpu_baseline(HEADLINE)
     if dist is not None:
         dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def single_workload(args, world, rank, local, barrier, dist):
+    """Times one non-headline workload alone (profiling aid); prints one JSON line."""
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    c = Case(args.workload)
+    with ClockSampler(local) as clk:
+        ts, _ = time_device(c, args.steps, args.warmup, flush, barrier)
+    m = statistics.mean(ts)
+    if c.hbm_bound:
+        val, unit, pkv = c.bytes / (m * 1e-3) / 1e9, "GB/s", pk["hbm_gbs"]
+    else:
+        val, unit, pkv = c.flops / (m * 1e-3) / 1e12, "TFLOP/s", pk["bf16_tflops"]
+    line = {"metric": METRIC, "value": world * val, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": m, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": {"workload": args.workload},
+            "roofline": {"bound": "hbm" if c.hbm_bound else "tensor", "achieved": val, "peak": pkv,
+                         "unit": unit, "frac": val / pkv, "traffic": recorded_traffic(args.workload)},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+    if dist is not None:
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))

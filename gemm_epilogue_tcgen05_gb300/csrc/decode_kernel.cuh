@@ -24,7 +24,7 @@
 namespace fl {
 
 constexpr int kDecTokens = 32;
-constexpr int kDecStages = 8;
+constexpr int kDecStages = 10;
 constexpr int kDecABytes = 128 * kBK * 2;  // W tile
 constexpr int kDecBBytes = kDecTokens * kBK * 2;  // X tile
 constexpr int kDecStageBytes = kDecABytes + kDecBBytes;
@@ -37,7 +37,7 @@ struct alignas(128) DecodeParams {
   int M, N, K;
   int num_f;          // feature tiles of 128
   int num_kb;         // k blocks of 64
-  long long units;    // num_f * num_kb
+  int units;          // num_f * num_kb (the host keeps units * (grid + 1) < 2^31)
   int seg_max;        // segment slots per CTA in `partials`
   const __nv_bfloat16* bias;
   const __nv_bfloat16* resid;
@@ -55,12 +55,26 @@ struct alignas(128) DecodeParams {
   unsigned long long timeout_ns;
 };
 
-__host__ __device__ inline long long dec_unit_begin(long long c, long long units, long long grid) {
-  return c * units / grid;
+// First unit of CTA c: units are cut into `grid` contiguous ranges of near-equal size.
+// 32-bit arithmetic on purpose (64-bit division is a long instruction sequence).
+__host__ __device__ inline int dec_unit_begin(int c, int units, int grid) {
+  return static_cast<int>(static_cast<unsigned>(c) * static_cast<unsigned>(units) / static_cast<unsigned>(grid));
 }
 // CTA whose unit range contains unit u.
-__host__ __device__ inline int dec_cta_of(long long u, long long units, long long grid) {
-  return static_cast<int>(((u + 1) * grid - 1) / units);
+__host__ __device__ inline int dec_cta_of(int u, int units, int grid) {
+  return static_cast<int>((static_cast<unsigned>(u + 1) * static_cast<unsigned>(grid) - 1u) /
+                          static_cast<unsigned>(units));
+}
+
+// Four bf16 values [n, n+4) of a vector as fp32 (8-byte load when fully in range); zeros at or past `limit`.
+__device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* base, int n, int limit, float (&v)[4]) {
+  if (n + 4 <= limit) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(base + n));
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = n + j < limit ? __bfloat162float(base[n + j]) : 0.f;
+  }
 }
 
 __device__ __forceinline__ bool spin_until(const unsigned* ctr, unsigned need, const int* status,
@@ -100,10 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtx wctx{abort_flag, p.status, p.timeout_ns};
-  const long long G = gridDim.x;
-  const long long u_begin = dec_unit_begin(blockIdx.x, p.units, G);
-  const long long u_end = dec_unit_begin(blockIdx.x + 1, p.units, G);
-  const int f_first = static_cast<int>(u_begin / p.num_kb);
+  const int G = static_cast<int>(gridDim.x);
+  const int u_begin = dec_unit_begin(blockIdx.x, p.units, G);
+  const int u_end = dec_unit_begin(blockIdx.x + 1, p.units, G);
+  const int f_first = u_begin / p.num_kb;  // the loops below walk units without dividing
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kDecStages; ++s) {
@@ -124,6 +138,22 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
     tma_prefetch_desc(&p.map_w);
     tma_prefetch_desc(&p.map_x);
   }
+  if (warp == 0 && u_end > u_begin) {
+    // Any CTA covering a feature tile may finish it: pull that tile's residual
+    // columns (one 256-byte run per token) and gamma / bias into L2 now.
+    const int f_last = (u_end - 1) / p.num_kb;
+    for (int f = f_first; f <= f_last; ++f) {
+      const int n0 = f * 128;
+      const uint32_t bytes = static_cast<uint32_t>(min(128, p.N - n0) * 2) & ~15u;
+      if (bytes == 0) continue;
+      for (int t = lane; t < p.M + 2; t += 32) {
+        const __nv_bfloat16* src = t < p.M ? p.resid + static_cast<size_t>(t) * p.ldz + n0
+                                           : (t == p.M ? p.gamma + n0 : p.bias + n0);
+        if (t == p.M + 1 && p.bias == nullptr) continue;
+        bulk_prefetch_l2(src, bytes);
+      }
+    }
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 64);
     tmem_relinquish();
@@ -139,13 +169,19 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, issued_phase = 0;
       bool ok = true;
-      for (long long u = u_begin; u < u_end; ++u) {
-        const int f = static_cast<int>(u / p.num_kb);
-        const int kb = static_cast<int>(u - static_cast<long long>(f) * p.num_kb);
+      // W is read exactly once: keep it from evicting the partials, statistics
+      // and residual columns the finishing phases read back from L2.
+      const uint64_t w_policy = l2_policy_evict_first();
+      int f = f_first, kb = u_begin - f_first * p.num_kb;
+      for (int u = u_begin; u < u_end; ++u, ++kb) {
+        if (kb == p.num_kb) {
+          kb = 0;
+          ++f;
+        }
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wctx, W_PRODUCER_EMPTY)) { ok = false; break; }
         uint8_t* a_dst = stage_mem + stage * kDecStageBytes;
         mbar_arrive_expect_tx(&full_bar[stage], kDecStageBytes);
-        tma_load_2d(&p.map_w, &full_bar[stage], a_dst, kb * kBK, f * 128);
+        tma_load_2d_hint(&p.map_w, &full_bar[stage], a_dst, kb * kBK, f * 128, w_policy);
         tma_load_2d(&p.map_x, &full_bar[stage], a_dst + kDecABytes, kb * kBK, 0);
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -163,10 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
       uint32_t phase = 0;
       bool ok = true;
       int ls = 0;
-      for (long long u = u_begin; u < u_end && ok; ++ls) {
-        const int f = static_cast<int>(u / p.num_kb);
-        const long long seg_begin = u;
-        const long long seg_end = min(u_end, static_cast<long long>(f + 1) * p.num_kb);
+      int u = u_begin;
+      for (int f = f_first; u < u_end && ok; ++ls, ++f) {
+        const int seg_begin = u;
+        const int seg_end = min(u_end, (f + 1) * p.num_kb);
         const int abuf = ls & 1;
         const uint32_t use = static_cast<uint32_t>(ls >> 1);
         if (!mbar_wait(&tempty_bar[abuf], (use & 1u) ^ 1u, wctx, W_MMA_TMEM_EMPTY)) { ok = false; break; }
@@ -193,16 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
     }
   } else {
     // ------------------------------------------------------------ epilogue warps
+    // Global traffic of every phase is laid out so that a warp touches
+    // contiguous memory: partial tiles go through shared memory on the way out,
+    // and the finishing passes walk the tile token-major (one warp = one token,
+    // 4 features per lane).
     const int q = warp & 3;
-    const int r = q * 32 + lane;  // feature row of the tile owned by this thread
     const int ti = threadIdx.x - 64;  // 0..127
     const bool leader = ti == 0;
+    const int fq = ti & 31;           // feature quad (features 4*fq .. 4*fq+3 of a tile) in the finishing passes
+    uint8_t* stage_w = reinterpret_cast<uint8_t*>(hT) + q * 4096;  // this warp's 32 x 128-byte staging rows
     // Phase 1: drain each segment's partial accumulator to global scratch and count k blocks.
     int ls = 0;
-    for (long long u = u_begin; u < u_end; ++ls) {
-      const int f = static_cast<int>(u / p.num_kb);
-      const long long seg_begin = u;
-      const long long seg_end = min(u_end, static_cast<long long>(f + 1) * p.num_kb);
+    int f = f_first;
+    for (int u = u_begin; u < u_end; ++ls, ++f) {
+      const int seg_begin = u;
+      const int seg_end = min(u_end, (f + 1) * p.num_kb);
       u = seg_end;
       const int abuf = ls & 1;
       const uint32_t use = static_cast<uint32_t>(ls >> 1);
@@ -214,12 +255,22 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&tempty_bar[abuf]);
-        float4* dst = reinterpret_cast<float4*>(
-            p.partials + ((static_cast<size_t>(blockIdx.x) * p.seg_max + (f - f_first)) * 128 + r) * kDecTokens);
+        // lane = feature row (32 tokens, 128 bytes): stage rows with 16-byte chunks XOR-swizzled by row
+        const uint32_t srow = smem_u32(stage_w) + lane * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          __stcg(dst + i, make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
-                                      __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3])));
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(srow + ((c ^ (lane & 7)) << 4), acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        __syncwarp();
+        // this warp's 32 rows are 4 KB of the slot [128 rows][32 tokens]; write them contiguously
+        float4* dst = reinterpret_cast<float4*>(p.partials) +
+                      (static_cast<size_t>(blockIdx.x) * p.seg_max + (f - f_first)) * 1024 + q * 256;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int idx = lane + 32 * k, row = idx >> 3, chunk = idx & 7;
+          const float4 v = *reinterpret_cast<const float4*>(stage_w + row * 128 + ((chunk ^ (row & 7)) << 4));
+          __stcg(dst + idx, v);
+        }
+        __syncwarp();
       }
       __threadfence();
       named_bar_sync(1, kEpiThreads);
@@ -237,56 +288,78 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
       if (*epi_stop) break;  // uniform: only the leader writes it, between the two barriers
     }
     const int nfin = *epi_stop ? 0 : *fin_count;
-    // Phase 2: finish the feature tiles this CTA completed: h = sum of partials + b + z.
+    // Phase 2: finish the feature tiles this CTA completed: h = sum of partials + b + z,
+    // then per-token partial sum of h^2 and max |h * gamma| over the tile's 128 features.
     for (int i = 0; i < nfin; ++i) {
       const int f = fin_list[i];
-      const int n = f * 128 + r;
-      const bool n_ok = n < p.N;
-      float h[kDecTokens];
+      const int n = f * 128 + fq * 4;  // this lane's 4 features in the token-major pass
+      // residual, bias and gamma of the token-major pass are requested first
+      float z[8][4], b4[4], g4[4];
 #pragma unroll
-      for (int t = 0; t < kDecTokens; ++t) h[t] = 0.f;
-      const int c_lo = dec_cta_of(static_cast<long long>(f) * p.num_kb, p.units, G);
-      const int c_hi = dec_cta_of(static_cast<long long>(f + 1) * p.num_kb - 1, p.units, G);
-      for (int c = c_lo; c <= c_hi; ++c) {
-        const int cf_first = static_cast<int>(dec_unit_begin(c, p.units, G) / p.num_kb);
-        const float4* src = reinterpret_cast<const float4*>(
-            p.partials + ((static_cast<size_t>(c) * p.seg_max + (f - cf_first)) * 128 + r) * kDecTokens);
+      for (int k = 0; k < 8; ++k) {
+        const int t = (ti >> 5) + 4 * k;
+        load_bf16x4(p.resid + static_cast<size_t>(t) * p.ldz, n, t < p.M ? p.N : 0, z[k]);
+      }
+      load_bf16x4(p.bias, n, p.bias ? p.N : 0, b4);
+      load_bf16x4(p.gamma, n, p.N, g4);
+      // contributors' partials, read contiguously: float4 number (ti + 128 k) of each slot is
+      // feature row ti/8 + 16 k, tokens 4*(ti%8) .. 4*(ti%8)+3
+      float4 acc[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 w = __ldcg(src + j);
-          h[4 * j] += w.x; h[4 * j + 1] += w.y; h[4 * j + 2] += w.z; h[4 * j + 3] += w.w;
+      for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int c_lo = dec_cta_of(f * p.num_kb, p.units, G);
+      const int c_hi = dec_cta_of((f + 1) * p.num_kb - 1, p.units, G);
+      for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
+        float4 w[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = c0 + j;
+          if (c <= c_hi) {
+            const int cf_first = dec_unit_begin(c, p.units, G) / p.num_kb;
+            const float4* src = reinterpret_cast<const float4*>(p.partials) +
+                                (static_cast<size_t>(c) * p.seg_max + (f - cf_first)) * 1024 + ti;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[j][k] = __ldcg(src + 128 * k);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
-      }
-      const float bn = (p.bias && n_ok) ? __bfloat162float(p.bias[n]) : 0.f;
 #pragma unroll
-      for (int t = 0; t < kDecTokens; ++t) {
-        const float z = (t < p.M && n_ok) ? __bfloat162float(p.resid[t * p.ldz + n]) : 0.f;
-        hT[t * 129 + r] = h[t] + bn + z;
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            acc[k].x += w[j][k].x; acc[k].y += w[j][k].y; acc[k].z += w[j][k].z; acc[k].w += w[j][k].w;
+          }
       }
-      gs[r] = n_ok ? __bfloat162float(p.gamma[n]) : 0.f;
+      // transpose through shared memory: hT[token][feature row]
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int row = (ti >> 3) + 16 * k, t0 = 4 * (ti & 7);
+        hT[(t0 + 0) * 129 + row] = acc[k].x;
+        hT[(t0 + 1) * 129 + row] = acc[k].y;
+        hT[(t0 + 2) * 129 + row] = acc[k].z;
+        hT[(t0 + 3) * 129 + row] = acc[k].w;
+      }
       named_bar_sync(1, kEpiThreads);
-      {
-        // token t, quarter part of the 128 features
-        const int t = ti >> 2, part = ti & 3;
-        float ss = 0.f, am = 0.f;
-        float* hrow = p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128 + part * 32;
+      // token-major pass: warp w handles tokens w, w+4, ...; each lane 4 features
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 w;
-          w.x = hT[t * 129 + part * 32 + j];
-          w.y = hT[t * 129 + part * 32 + j + 1];
-          w.z = hT[t * 129 + part * 32 + j + 2];
-          w.w = hT[t * 129 + part * 32 + j + 3];
-          ss = fmaf(w.x, w.x, fmaf(w.y, w.y, fmaf(w.z, w.z, fmaf(w.w, w.w, ss))));
-          am = fmaxf(am, fmaxf(fmaxf(fabsf(w.x * gs[part * 32 + j]), fabsf(w.y * gs[part * 32 + j + 1])),
-                               fmaxf(fabsf(w.z * gs[part * 32 + j + 2]), fabsf(w.w * gs[part * 32 + j + 3]))));
-          __stcg(reinterpret_cast<float4*>(hrow + j), w);
+      for (int k = 0; k < 8; ++k) {
+        const int t = (ti >> 5) + 4 * k;
+        float4 hv;
+        hv.x = hT[t * 129 + fq * 4 + 0] + b4[0] + z[k][0];
+        hv.y = hT[t * 129 + fq * 4 + 1] + b4[1] + z[k][1];
+        hv.z = hT[t * 129 + fq * 4 + 2] + b4[2] + z[k][2];
+        hv.w = hT[t * 129 + fq * 4 + 3] + b4[3] + z[k][3];
+        __stcg(reinterpret_cast<float4*>(p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128) + fq, hv);
+        float ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
+        float am = fmaxf(fmaxf(fabsf(hv.x * g4[0]), fabsf(hv.y * g4[1])), fmaxf(fabsf(hv.z * g4[2]), fabsf(hv.w * g4[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
         }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-        if (part == 0) __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + t, make_float2(ss, am));
+        if (lane == 0) __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + t, make_float2(ss, am));
       }
       named_bar_sync(1, kEpiThreads);
       if (leader) p.counters[f] = 0u;  // every contributor has arrived; ready for the next call
@@ -310,38 +383,54 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
     named_bar_sync(1, kEpiThreads);
     const bool finish = !*epi_stop && nfin > 0;
     if (finish) {
-      // Phase 4: merge per-token statistics over all feature tiles, quantise, store.
-      const int t = ti >> 2, part = ti & 3;
-      float SS = 0.f, A = 0.f;
-      for (int f2 = 0; f2 < p.num_f; ++f2) {
-        const float2 w = __ldcg(p.stats + static_cast<size_t>(f2) * kDecTokens + t);
-        SS += w.x;
-        A = fmaxf(A, w.y);
+      // Phase 4: merge per-token statistics over all feature tiles (one lane per token),
+      // then quantise this CTA's finished tiles token-major and store the codes.
+      float* qs_s = gs;  // [32] 448 / max|h * gamma| per token
+      if (ti < 32) {
+        const int t = ti;
+        float SS = 0.f, A = 0.f;
+        for (int f0 = 0; f0 < p.num_f; f0 += 32) {
+          float2 w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            w[j] = f0 + j < p.num_f ? __ldcg(p.stats + static_cast<size_t>(f0 + j) * kDecTokens + t)
+                                    : make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            SS += w[j].x;
+            A = fmaxf(A, w[j].y);
+          }
+        }
+        qs_s[t] = A > 0.f ? 448.f / A : 0.f;
+        bool has_tile0 = false;
+        for (int i = 0; i < nfin; ++i) has_tile0 |= fin_list[i] == 0;
+        if (has_tile0 && t < p.M) p.row_scale[t] = rsqrtf(SS / static_cast<float>(p.N) + p.eps) * A * (1.f / 448.f);
       }
-      const float qs = A > 0.f ? 448.f / A : 0.f;
+      named_bar_sync(1, kEpiThreads);
       for (int i = 0; i < nfin; ++i) {
         const int f = fin_list[i];
-        if (f == 0 && part == 0 && t < p.M) p.row_scale[t] = rsqrtf(SS / static_cast<float>(p.N) + p.eps) * A * (1.f / 448.f);
-        if (t >= p.M) continue;
-        const float* hrow = p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128 + part * 32;
-        const int n0 = f * 128 + part * 32;
-        uint32_t w[8];
+        const int n = f * 128 + fq * 4;
+        float g4[4];
+        load_bf16x4(p.gamma, n, p.N, g4);
+        float4 hv[8];
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 hv = __ldcg(reinterpret_cast<const float4*>(hrow + j));
-          const float g0 = n0 + j < p.N ? __bfloat162float(p.gamma[n0 + j]) : 0.f;
-          const float g1 = n0 + j + 1 < p.N ? __bfloat162float(p.gamma[n0 + j + 1]) : 0.f;
-          const float g2 = n0 + j + 2 < p.N ? __bfloat162float(p.gamma[n0 + j + 2]) : 0.f;
-          const float g3 = n0 + j + 3 < p.N ? __bfloat162float(p.gamma[n0 + j + 3]) : 0.f;
-          w[j / 4] = f32x2_to_e4m3x2(hv.x * g0 * qs, hv.y * g1 * qs) |
-                     (f32x2_to_e4m3x2(hv.z * g2 * qs, hv.w * g3 * qs) << 16);
+        for (int k = 0; k < 8; ++k) {
+          const int t = (ti >> 5) + 4 * k;
+          hv[k] = __ldcg(reinterpret_cast<const float4*>(p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128) + fq);
         }
-        uint8_t* dst = p.yq + static_cast<size_t>(t) * p.ldq + n0;
-        if (n0 + 32 <= p.N) {
-          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        } else {
-          for (int j = 0; j < 32 && n0 + j < p.N; ++j) dst[j] = static_cast<uint8_t>(w[j / 4] >> (8 * (j % 4)));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int t = (ti >> 5) + 4 * k;
+          if (t >= p.M) continue;
+          const float qs = qs_s[t];
+          const uint32_t w = f32x2_to_e4m3x2(hv[k].x * g4[0] * qs, hv[k].y * g4[1] * qs) |
+                             (f32x2_to_e4m3x2(hv[k].z * g4[2] * qs, hv[k].w * g4[3] * qs) << 16);
+          uint8_t* dst = p.yq + static_cast<size_t>(t) * p.ldq + n;
+          if (n + 4 <= p.N) {
+            *reinterpret_cast<uint32_t*>(dst) = w;
+          } else {
+            for (int j = 0; j < 4 && n + j < p.N; ++j) dst[j] = static_cast<uint8_t>(w >> (8 * j));
+          }
         }
       }
     }

@@ -17,6 +17,7 @@ struct WsLayout {
   bool decode;
   size_t counters, partials, hbuf, stats, total;  // byte offsets (total = size)
   int grid, seg_max;                              // decode only
+  bool units_ok;                                  // decode unit indices fit 32-bit arithmetic
 };
 
 bool use_decode(int M, int K) { return M <= kDecTokens && K > 0; }
@@ -28,11 +29,13 @@ WsLayout layout(int M, int N, int K, int num_sms) {
     w.decode = true;
     const int num_f = cdiv(N, 128);
     const int num_kb = cdiv(K, kBK);
-    const long long units = static_cast<long long>(num_f) * num_kb;
-    w.grid = static_cast<int>(units < num_sms ? units : num_sms);
+    const long long units_ll = static_cast<long long>(num_f) * num_kb;
+    w.grid = static_cast<int>(units_ll < num_sms ? units_ll : num_sms);
+    w.units_ok = units_ll * (w.grid + 1) < (1LL << 31);
+    const int units = static_cast<int>(w.units_ok ? units_ll : 0);
     w.seg_max = 1;
-    for (int c = 0; c < w.grid; ++c) {
-      const long long b = dec_unit_begin(c, units, w.grid), e = dec_unit_begin(c + 1, units, w.grid);
+    for (int c = 0; c < w.grid && w.units_ok; ++c) {
+      const int b = dec_unit_begin(c, units, w.grid), e = dec_unit_begin(c + 1, units, w.grid);
       if (e > b) {
         const int segs = static_cast<int>((e - 1) / num_kb - b / num_kb + 1);
         if (segs > w.seg_max) w.seg_max = segs;
@@ -89,7 +92,7 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (wl.decode) {
-    if (wl.seg_max > kDecMaxSeg) return FL_ERR_UNSUPPORTED;
+    if (!wl.units_ok || wl.seg_max > kDecMaxSeg) return FL_ERR_UNSUPPORTED;
     DecodeParams p;
     std::memset(&p, 0, sizeof(p));
     if (!encode_2d(&p.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, N, ldw, kBK, 128,
@@ -102,7 +105,7 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
     p.K = K;
     p.num_f = cdiv(N, 128);
     p.num_kb = cdiv(K, kBK);
-    p.units = static_cast<long long>(p.num_f) * p.num_kb;
+    p.units = p.num_f * p.num_kb;
     p.seg_max = wl.seg_max;
     p.bias = static_cast<const __nv_bfloat16*>(b);
     p.resid = static_cast<const __nv_bfloat16*>(Z);
