@@ -134,6 +134,30 @@ FL_API int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const
                                       int64_t ldx, int64_t ldw, int64_t ldz, int64_t ldq,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Same computation as fused_linear_residual_rmsnorm_fp8, for callers that
+ * cannot allocate device memory and so cannot supply a workspace: a decode
+ * step recorded into a CUDA graph (allocating during capture breaks it), a
+ * serving loop that must not stall in the allocator, or a plugin whose host
+ * framework owns all device memory.  The pages have no counterpart of this
+ * call; it exists only for such callers.
+ * Scratch: one FL_NOALLOC_SCRATCH_BYTES array compiled into the library and
+ * held by every GPU that loads it until the process exits.  A shape whose
+ * fl_rmsnorm_fp8_workspace_bytes(M, N, K) exceeds that size is rejected with
+ * FL_ERR_WORKSPACE.  The array is shared by every call: calls that can overlap
+ * on the GPU (streams with no ordering between them) race and must not be
+ * issued.  Each call clears the counters the kernels wait on with an
+ * asynchronous memset on `stream` before its launch; nothing is allocated.
+ * The first call on a device looks up the array's device address, so make it
+ * before any stream capture that records later calls.  Other arguments,
+ * layouts and errors are those of fused_linear_residual_rmsnorm_fp8. */
+#define FL_NOALLOC_SCRATCH_BYTES (8u << 20)
+FL_API int fused_linear_residual_rmsnorm_fp8_noalloc(const void* X, const void* W, const void* b,
+                                                     const void* Z, const void* gamma, float eps,
+                                                     void* Yq, float* row_scale,
+                                                     int M, int N, int K,
+                                                     int64_t ldx, int64_t ldw, int64_t ldz, int64_t ldq,
+                                                     void* stream);
+
 /* Bytes of workspace fused_linear_residual_rmsnorm_fp8 needs for this shape
  * on the current device (0 for an empty problem). */
 FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);
