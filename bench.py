@@ -92,7 +92,7 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (100 ms) of SM clock and throttle reasons during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -106,7 +106,7 @@ class ClockSampler:
         try:
             self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -142,6 +142,20 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """Largest value of x over all ranks (the slowest rank sets the job time)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank; the job took the slowest rank's time."""
+    return world * units_per_rank / seconds_max
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -234,6 +248,106 @@ def time_device(case: Case, steps: int, warmup: int, flush: torch.Tensor, barrie
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
 
 
+def unfused_fn(case: Case):
+    """The same computation as separate torch / cuBLAS kernels (comparison baseline, not our path)."""
+    import torch.nn.functional as F
+    w, d = case.w, case.dev
+    if w.kind in ("gelu_tanh", "gelu_erf"):
+        approx = "tanh" if w.kind == "gelu_tanh" else "none"
+        return lambda: F.gelu(F.linear(d["X"], d["W"], d.get("b")), approximate=approx)
+    if w.kind == "qkv_rope":
+        dm, hd = w.n_heads * w.head_dim, w.head_dim
+        pos = torch.arange(w.M, device="cuda") % w.seq_len
+        inv = w.theta ** (-torch.arange(0, hd, 2, device="cuda", dtype=torch.float32) / hd)
+        ang = pos[:, None].float() * inv[None, :]
+        cos, sin = ang.cos().repeat(1, w.n_heads), ang.sin().repeat(1, w.n_heads)
+
+        def rope(t):
+            t = t.float()
+            x0, x1 = t[:, 0::2], t[:, 1::2]
+            return torch.stack((x0 * cos - x1 * sin, x0 * sin + x1 * cos), dim=-1).reshape(t.shape).to(torch.bfloat16)
+
+        def fn():
+            h = F.linear(d["X"], d["W"])
+            return rope(h[:, :dm]), rope(h[:, dm:2 * dm]), h[:, 2 * dm:].contiguous()
+        return fn
+    if w.kind == "swiglu":
+        return lambda: F.silu(F.linear(d["X"], d["Wgate"])) * F.linear(d["X"], d["Wup"])
+
+    def rms():
+        h = F.linear(d["X"], d["W"]).float() + d["Z"].float()
+        y = F.rms_norm(h, (w.N,), weight=d["gamma"].float(), eps=w.eps)
+        s = y.abs().amax(dim=1) / 448.0
+        return (y / s[:, None]).to(torch.float8_e4m3fn), s
+    return rms
+
+
+def time_fn(fn, steps: int, warmup: int, flush: torch.Tensor):
+    """CUDA-event time (ms) of a callable with an L2 flush before each timed call."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+
+def time_graph_rotating(case: Case, calls: int = 20, copies: int = 3, replays: int = 20):
+    """Per-call time (ms) of `calls` back-to-back calls captured in one CUDA graph, cycling through
+    `copies` separate copies of every operand (together larger than L2, so each call reads its
+    operands from HBM), as a decode loop would issue them."""
+    import gemm_epilogue_tcgen05_gb300 as fl
+    w = case.w
+    sets = [case.dev] + [{k: v.clone() for k, v in case.dev.items()} for _ in range(copies - 1)]
+    outs = [(torch.empty_like(case.out[0]), torch.empty_like(case.out[1])) for _ in range(copies)]
+    wss = [fl.rmsnorm_fp8_workspace(w.M, w.N, w.K) for _ in range(copies)]
+
+    def seq(stream):
+        for i in range(calls):
+            d, o, ws = sets[i % copies], outs[i % copies], wss[i % copies]
+            fl.fused_linear_residual_rmsnorm_fp8(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], w.eps,
+                                                 Yq=o[0], row_scale=o[1], workspace=ws, stream=stream)
+
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        seq(stream)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    kind = "graph"
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            seq(stream)
+        run = g.replay
+    except Exception:  # noqa: BLE001 - capture unsupported: fall back to plain back-to-back launches
+        kind = "stream"
+        torch.cuda.synchronize()
+
+        def run():
+            with torch.cuda.stream(stream):
+                seq(stream)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(replays):
+        run()
+    e.record()
+    torch.cuda.synchronize()
+    if fl.device_status() != fl.FL_OK:
+        raise RuntimeError("decode graph: device-side failure reported")
+    return s.elapsed_time(e) / (replays * calls), kind
+
+
 def time_e2e(case: Case, steps: int, warmup: int, barrier):
     """Per-step time (ms) with host->device input copies and device->host output copies inside."""
     stream = torch.cuda.current_stream()
@@ -300,8 +414,8 @@ def cpu_baseline(name: str, target_s: float = 10.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default="all", choices=["all", "none"],
                     help="also measure the other fused workloads of the hot path")
@@ -342,25 +456,18 @@ def main():
         times, wall = time_device(head, args.steps, args.warmup, flush, barrier)
     clocks = clk.summary()
     ms = statistics.mean(times)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = world * head.flops / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, dist, "cuda")
+    value = job_rate(head.flops, world, ms_max * 1e-3) / 1e12
     kernel_tflops = head.flops / (ms * 1e-3) / 1e12
     traffic = recorded_traffic(HEADLINE)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": kernel_tflops / pk["bf16_tflops"], "traffic": traffic,
                 "peak_source": f"bf16 burst, {'of measured' if pk['source'] == 'measured' else 'of fallback'}",
                 "algorithmic_bytes": head.bytes}
-    e_times, h2d, d2h = time_e2e(head, max(3, args.steps // 2), 2, barrier)
-    e_ms = statistics.mean(e_times)
-    if dist is not None:
-        t = torch.tensor([e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e = {"value": world * head.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+    head_unfused = time_fn(unfused_fn(head), 20, 3, flush)
+    e_times, h2d, d2h = time_e2e(head, max(3, min(args.steps, 100) // 2), 2, barrier)
+    e_ms = max_over_ranks(statistics.mean(e_times), dist, "cuda")
+    e2e = {"value": job_rate(head.flops, world, e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
     del head
 
@@ -369,20 +476,29 @@ def main():
         for name in ("qkv_rope_8192x12288x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
                      "rmsnorm_fp8_decode_32x4096x14336"):
             c = Case(name)
-            ts, _ = time_device(c, args.steps, args.warmup, flush, barrier)
+            row_steps = min(args.steps, 200)
+            ts, _ = time_device(c, row_steps, args.warmup, flush, barrier)
             m = statistics.mean(ts)
+            unf = time_fn(unfused_fn(c), max(5, row_steps // 10), 3, flush)
             if c.hbm_bound:
                 ach = c.bytes / (m * 1e-3) / 1e9
-                rows.append({"workload": name, "value": ach, "unit": "GB/s", "us_per_launch": m * 1e3,
-                             "roofline": {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                          "frac": ach / pk["hbm_gbs"], "traffic": recorded_traffic(name),
-                                          "algorithmic_bytes": c.bytes}})
+                g_ms, g_kind = time_graph_rotating(c)
+                g_ach = c.bytes / (g_ms * 1e-3) / 1e9
+                rows.append({"workload": name, "value": g_ach, "unit": "GB/s", "us_per_call": g_ms * 1e3,
+                             "timing": f"{g_kind} of 20 back-to-back calls over 3 rotating operand copies (> L2)",
+                             "single_launch": {"us": m * 1e3, "GB/s": ach, "frac": ach / pk["hbm_gbs"],
+                                               "timing": "one launch, L2 flushed before it"},
+                             "roofline": {"bound": "hbm", "achieved": g_ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                          "frac": g_ach / pk["hbm_gbs"], "traffic": recorded_traffic(name),
+                                          "algorithmic_bytes": c.bytes},
+                             "unfused_torch_us": unf * 1e3, "speedup_vs_unfused": unf / m})
             else:
                 ach = c.flops / (m * 1e-3) / 1e12
                 rows.append({"workload": name, "value": ach, "unit": "TFLOP/s", "ms_per_launch": m,
                              "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
                                           "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
-                                          "traffic": recorded_traffic(name), "algorithmic_bytes": c.bytes}})
+                                          "traffic": recorded_traffic(name), "algorithmic_bytes": c.bytes},
+                             "unfused_torch_ms": unf, "speedup_vs_unfused": unf / m})
             del c
             torch.cuda.empty_cache()
 
@@ -394,6 +510,8 @@ def main():
                    "l2": "256 MiB flush before every timed launch; inputs larger than L2",
                    "parallelism": f"replicas x{world} (rows are independent; no collective)"},
         "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+        "unfused_baseline": {"ms_per_step": head_unfused, "speedup": head_unfused / ms,
+                             "what": "torch F.gelu(F.linear(X, W, b), approximate='tanh'): cuBLAS GEMM + separate GELU"},
         "rows": rows, "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -62,6 +62,8 @@ def load() -> ctypes.CDLL:
     lib.fl_set_wait_timeout_ns.restype = None
     lib.fl_set_max_ctas.argtypes = [I]
     lib.fl_set_max_ctas.restype = None
+    lib.fl_set_cta_pairing.argtypes = [I]
+    lib.fl_set_cta_pairing.restype = None
     lib.fl_status_string.argtypes = [I]
     lib.fl_status_string.restype = ctypes.c_char_p
     lib.fl_version.argtypes = []
@@ -239,3 +241,8 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def set_max_ctas(n: int) -> None:
     load().fl_set_max_ctas(int(n))
+
+
+def set_cta_pairing(enable: bool) -> None:
+    """Two-CTA (cta_group::2) prefill tiles on (default) or off; results are the same."""
+    load().fl_set_cta_pairing(1 if enable else 0)

@@ -22,6 +22,7 @@ bool g_dev_known[kMaxDevices];
 int* g_status_ptr[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_max_ctas{0};
+std::atomic<int> g_pairing{1};
 
 struct SmemAttr {
   const void* fn;
@@ -83,6 +84,7 @@ int* device_status_ptr(int device) {
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 int max_ctas_override() { return g_max_ctas.load(); }
+int cta_pairing_mode() { return g_pairing.load(); }
 
 bool ensure_smem_attr(const void* kernel, int device, int smem_bytes) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -131,6 +133,8 @@ int fl_device_status(void* stream) {
 void fl_set_wait_timeout_ns(uint64_t ns) { fl::g_timeout_ns.store(ns == 0 ? fl::kDefaultTimeoutNs : ns); }
 
 void fl_set_max_ctas(int n) { fl::g_max_ctas.store(n < 0 ? 0 : n); }
+
+void fl_set_cta_pairing(int enable) { fl::g_pairing.store(enable != 0 ? 1 : 0); }
 
 const char* fl_status_string(int status) {
   switch (status) {

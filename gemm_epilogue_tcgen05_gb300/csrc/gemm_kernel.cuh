@@ -26,7 +26,6 @@ constexpr int kBK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle
 constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kStages = 4;
 constexpr int kStagingBytes = 4096;  // one 32-row x 128-byte TMA store box per buffer
 
 enum EpiKind : int { EPI_GELU_TANH = 0, EPI_GELU_ERF = 1, EPI_QKV_ROPE = 2, EPI_SWIGLU = 3, EPI_RMSNORM_FP8 = 4 };
@@ -37,8 +36,9 @@ struct alignas(128) GemmParams {
   CUtensorMap map_b2;      // SwiGLU: W_up, box {64, 128}
   CUtensorMap map_out[3];  // outputs; box {64 bf16 | 128 fp8 columns, 32 rows}; QKV: Q, K, V
   int M, N, K;             // N: logical output features (QKV: 3*d_model, SwiGLU: d_ff)
-  int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
-  int group_m;             // m-blocks per raster group (1 = row-major tile order)
+  int num_m_blocks, num_n_blocks, num_k_blocks;
+  int num_m_tiles, num_tiles;  // tiles of (CTAs per cluster) x 128 rows; one tile per cluster
+  int group_m;             // m-tiles per raster group (1 = row-major tile order)
   const __nv_bfloat16* bias;
   const __nv_bfloat16* bias2;  // SwiGLU: b_up
   // QKV + RoPE
@@ -57,13 +57,18 @@ struct alignas(128) GemmParams {
   unsigned long long timeout_ns;
 };
 
-template <int EPI>
+// CG = CTAs per cluster sharing one MMA: 1 (tcgen05 cta_group::1, 128-row tile per CTA) or
+// 2 (cta_group::2: the pair computes a 256-row tile; each CTA loads its 128 rows of X and half
+// of the W tile, so a stage is 32 KB instead of 48 KB and six stages fit).
+template <int EPI, int CG>
 struct EpiTraits {
   static constexpr int kMmaN = 256;                               // accumulator columns per tile
   static constexpr int kOutN = (EPI == EPI_SWIGLU) ? 128 : 256;   // output columns per tile
   static constexpr bool kFp8 = (EPI == EPI_RMSNORM_FP8);
+  static constexpr int kStages = CG == 2 ? 6 : 4;
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = kMmaN * kBK * 2;
+  static constexpr int kBRows = kMmaN / CG;                       // W rows this CTA loads per stage
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * kMmaN;
   static constexpr int kSmemBytes = kStages * kStageBytes + 4 * 2 * kStagingBytes + 1024 /*bars*/ +
@@ -74,7 +79,7 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb,
   const int per_group = p.group_m * p.num_n_blocks;
   const int g = t / per_group;
   const int first_m = g * p.group_m;
-  const int gsize = min(p.num_m_blocks - first_m, p.group_m);
+  const int gsize = min(p.num_m_tiles - first_m, p.group_m);
   const int r = t - g * per_group;
   mb = first_m + r % gsize;
   nb = r / gsize;
@@ -204,9 +209,10 @@ __device__ __forceinline__ bool wait_row_block(const GemmParams& p, int mb, unsi
   }
 }
 
-template <int EPI>
+template <int EPI, int CG>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using T = EpiTraits<EPI>;
+  using T = EpiTraits<EPI, CG>;
+  constexpr int kStages = T::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_mem = smem;
@@ -225,6 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtx wctx{abort_flag, p.status, p.timeout_ns};
+  // Cluster bookkeeping: rank 0 of a pair (the leader) issues the MMAs for both CTAs.
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const bool mma_cta = rank == 0;
+  const int tile0 = static_cast<int>(blockIdx.x) / CG;
+  const int tstride = static_cast<int>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], kEpiThreads);
+      mbar_init(&tempty_bar[a], 4 * CG);  // one arrival per epilogue warp of every CTA in the cluster
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -245,15 +256,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     if (EPI == EPI_SWIGLU) tma_prefetch_desc(&p.map_b2);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, T::kTmemCols);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_slot, T::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, T::kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (EPI == EPI_QKV_ROPE && threadIdx.x >= 64 && threadIdx.x < 128) {
     const int i = threadIdx.x - 64;  // pair index within a head (head_dim 128 -> 64 pairs)
     inv_freq[i] = exp2f(-(2.f * static_cast<float>(i) / static_cast<float>(p.head_dim)) * p.log2_theta);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    cluster_sync_all();  // both CTAs' barriers and tensor memory exist before any cross-CTA use
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -264,49 +284,74 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;  // per stage: ever issued / parity of the last issue
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
+      for (int t = tile0; t < p.num_tiles && ok; t += tstride) {
+        int mt, nb;
+        tile_coords(p, t, mt, nb);
+        const int mb = mt * CG + static_cast<int>(rank);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wctx, W_PRODUCER_EMPTY)) { ok = false; break; }
+          const bool got = CG == 2 ? mbar_wait_cl(&empty_bar[stage], phase ^ 1u, wctx, W_PRODUCER_EMPTY)
+                                   : mbar_wait(&empty_bar[stage], phase ^ 1u, wctx, W_PRODUCER_EMPTY);
+          if (!got) { ok = false; break; }
           uint8_t* a_dst = stage_mem + stage * T::kStageBytes;
           uint8_t* b_dst = a_dst + T::kABytes;
-          mbar_arrive_expect_tx(&full_bar[stage], T::kStageBytes);
-          tma_load_2d(&p.map_a, &full_bar[stage], a_dst, kb * kBK, mb * kBM);
-          if (EPI == EPI_SWIGLU) {
-            // gate rows and up rows of the same 128 output features, stacked in one B stage
-            tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * 128);
-            tma_load_2d(&p.map_b2, &full_bar[stage], b_dst + 128 * kBK * 2, kb * kBK, nb * 128);
+          if constexpr (CG == 2) {
+            // Both CTAs' copies complete on the leader's barrier, which expects the bytes of the pair.
+            if (mma_cta) mbar_arrive_expect_tx(&full_bar[stage], 2 * T::kStageBytes);
+            const uint32_t full_cl = mapa_shared(smem_u32(&full_bar[stage]), 0);
+            tma_load_2d_pair(&p.map_a, full_cl, a_dst, kb * kBK, mb * kBM);
+            if (EPI == EPI_SWIGLU) {
+              // the leader holds the 128 gate rows, the peer the 128 up rows of the same features
+              tma_load_2d_pair(rank == 0 ? &p.map_b : &p.map_b2, full_cl, b_dst, kb * kBK, nb * 128);
+            } else {
+              tma_load_2d_pair(&p.map_b, full_cl, b_dst, kb * kBK, nb * T::kMmaN + static_cast<int>(rank) * 128);
+            }
           } else {
-            tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * T::kMmaN);
+            mbar_arrive_expect_tx(&full_bar[stage], T::kStageBytes);
+            tma_load_2d(&p.map_a, &full_bar[stage], a_dst, kb * kBK, mb * kBM);
+            if (EPI == EPI_SWIGLU) {
+              // gate rows and up rows of the same 128 output features, stacked in one B stage
+              tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * 128);
+              tma_load_2d(&p.map_b2, &full_bar[stage], b_dst + 128 * kBK * 2, kb * kBK, nb * 128);
+            } else {
+              tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * T::kMmaN);
+            }
           }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
-        // Do not leave copies landing in shared memory after the CTA exits.
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) mbar_wait_quiet(&full_bar[s], (issued_phase >> s) & 1u, p.timeout_ns);
+      if (!ok && mma_cta) {
+        // Do not leave copies landing in shared memory after the CTA exits (the leader's barriers
+        // also count the peer's copies; the peer waits for the leader at the final cluster barrier).
+        const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+        for (int s = 0; s < kStages; ++s) {
+          const uint64_t now = global_timer_ns();
+          if (issued_mask & (1u << s))
+            mbar_wait_quiet(&full_bar[s], (issued_phase >> s) & 1u, now < deadline ? deadline - now : 0);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, T::kMmaN);
+    if (lane == 0 && mma_cta) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, T::kMmaN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+      for (int t = tile0; t < p.num_tiles && ok; t += tstride, ++local) {
         const int abuf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
-        if (!mbar_wait(&tempty_bar[abuf], (use & 1u) ^ 1u, wctx, W_MMA_TMEM_EMPTY)) { ok = false; break; }
+        const bool free_acc = CG == 2 ? mbar_wait_cl(&tempty_bar[abuf], (use & 1u) ^ 1u, wctx, W_MMA_TMEM_EMPTY)
+                                      : mbar_wait(&tempty_bar[abuf], (use & 1u) ^ 1u, wctx, W_MMA_TMEM_EMPTY);
+        if (!free_acc) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * T::kMmaN;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, wctx, W_MMA_FULL)) { ok = false; break; }
+          const bool got = CG == 2 ? mbar_wait_cl(&full_bar[stage], phase, wctx, W_MMA_FULL)
+                                   : mbar_wait(&full_bar[stage], phase, wctx, W_MMA_FULL);
+          if (!got) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + stage * T::kStageBytes);
           const uint64_t adesc = sdesc_k_sw128(a_addr);
@@ -314,16 +359,32 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // +32 bytes along K per step inside the 128-byte swizzled row (>> 4 in the descriptor)
-            mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (CG == 2) {
+              mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            } else {
+              mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
-          mma_commit(&empty_bar[stage]);
+          if constexpr (CG == 2) {
+            mma_commit_pair_mc(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
+          } else {
+            mma_commit(&empty_bar[stage]);
+          }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&tfull_bar[abuf]);
+        if constexpr (CG == 2) {
+          mma_commit_pair_mc(&tfull_bar[abuf], 0x3);  // both CTAs' epilogues may read their halves
+        } else {
+          mma_commit(&tfull_bar[abuf]);
+        }
       }
       // Every MMA issued by this thread must be complete before TMEM is freed.
-      mma_commit(drain_bar);
+      if constexpr (CG == 2) {
+        mma_commit_pair(drain_bar);
+      } else {
+        mma_commit(drain_bar);
+      }
       mbar_wait_quiet(drain_bar, 0, p.timeout_ns);
     }
   } else {
@@ -333,16 +394,30 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
     StoreRing ring{smem_u32(staging) + (warp - 2) * 2 * kStagingBytes, 0};
     const bool k_empty = p.num_k_blocks == 0;
     int local = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+    // Releases accumulator buffer `a`: one arrival per warp on the leader's barrier.
+    auto release_acc = [&](int a) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2) {
+          mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[a]), 0));
+        } else {
+          mbar_arrive(&tempty_bar[a]);
+        }
+      }
+    };
+    for (int t = tile0; t < p.num_tiles; t += tstride, ++local) {
+      int mt, nb;
+      tile_coords(p, t, mt, nb);
+      const int mb = mt * CG + static_cast<int>(rank);
       const int abuf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       const int m = mb * kBM + row_in_tile;
       const bool row_ok = m < p.M;
       const int y_box = mb * kBM + q * 32;
       // warp-uniform: tcgen05.ld below is a warp-collective instruction
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[abuf], use & 1u, wctx, W_EPI_TMEM_FULL));
+      const bool ok = __all_sync(0xffffffffu, CG == 2 ? mbar_wait_cl(&tfull_bar[abuf], use & 1u, wctx, W_EPI_TMEM_FULL)
+                                                       : mbar_wait(&tfull_bar[abuf], use & 1u, wctx, W_EPI_TMEM_FULL));
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * T::kMmaN;
 
@@ -395,8 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
           }
           ring.commit(&p.map_out[sec], buf, lane, n0 + c * 64, y_box);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty_bar[abuf]);
+        release_acc(abuf);
       } else if constexpr (EPI == EPI_SWIGLU) {
         if (!ok) break;
         const int n0 = nb * 128;  // accumulator columns [0,128) = gate, [128,256) = up
@@ -419,11 +493,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
           }
           ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty_bar[abuf]);
+        release_acc(abuf);
       } else if constexpr (EPI == EPI_RMSNORM_FP8) {
         // The 128 epilogue threads take the same named barriers in every
         // iteration and leave the loop together, right after a barrier.
+        if (mb >= p.num_m_blocks) {  // the pair's second row block lies past M: no rows, no exchange
+          if (!ok) break;
+          release_acc(abuf);
+          continue;
+        }
         const int n0 = nb * 256;
         const __nv_bfloat16* zrow = p.resid + static_cast<long long>(row_ok ? m : 0) * p.ldz;
         // Pass 1: h = acc + b + z; partial sum of h^2 and partial max |h * gamma| over this tile's columns.
@@ -500,17 +578,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
           }
           ring.commit(&p.map_out[0], buf, lane, n0 + c * 128, y_box);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty_bar[abuf]);
+        release_acc(abuf);
       }
     }
     if (lane == 0) bulk_wait_all();
   }
 
-  __syncthreads();
+  if constexpr (CG == 2) {
+    cluster_sync_all();  // neither CTA leaves while the other may still touch its memory
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, T::kTmemCols);
+    if constexpr (CG == 2) {
+      tmem_dealloc_pair(tmem_base, T::kTmemCols);
+    } else {
+      tmem_dealloc(tmem_base, T::kTmemCols);
+    }
   }
 }
 

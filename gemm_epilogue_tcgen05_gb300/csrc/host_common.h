@@ -36,8 +36,14 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool pitch_ok(int64_t ld, int elem_bytes) { return ((ld * elem_bytes) & 15) == 0; }
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// Fills the launch-independent parts of GemmParams.
-inline void init_params(GemmParams& p, int M, int N, int K, int n_per_tile) {
+// Process-wide switch for the two-CTA (cta_group::2) mainloop: 1 = use it when
+// M spans at least two 128-row blocks (default), 0 = always one CTA per tile.
+int cta_pairing_mode();
+// CTAs per cluster for a problem with M rows.
+inline int choose_cg(int M) { return (cta_pairing_mode() != 0 && M > kBM) ? 2 : 1; }
+
+// Fills the launch-independent parts of GemmParams for tiles of `cg` x 128 rows.
+inline void init_params(GemmParams& p, int M, int N, int K, int n_per_tile, int cg) {
   std::memset(&p, 0, sizeof(p));
   p.M = M;
   p.N = N;
@@ -45,40 +51,88 @@ inline void init_params(GemmParams& p, int M, int N, int K, int n_per_tile) {
   p.num_m_blocks = cdiv(M, kBM);
   p.num_n_blocks = cdiv(N, n_per_tile);
   p.num_k_blocks = cdiv(K, kBK);
-  p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-  p.group_m = 16;
+  p.num_m_tiles = cdiv(p.num_m_blocks, cg);
+  p.num_tiles = p.num_m_tiles * p.num_n_blocks;
+  p.group_m = 32 / cg;  // raster groups of 32 row blocks
   p.timeout_ns = wait_timeout_ns();
 }
 
-// Launches fused_gemm_kernel<EPI> persistently: one CTA per SM (capped by the
-// tile count and the test override, but never below `min_grid`).  With
-// `cooperative` the launch fails instead of starting if not every CTA can be
-// resident at once (needed when CTAs wait on one another).
-template <int EPI>
-int launch_gemm(GemmParams& p, const DeviceInfo& di, cudaStream_t stream, bool cooperative, int min_grid) {
-  using T = EpiTraits<EPI>;
-  const void* kfn = reinterpret_cast<const void*>(&fused_gemm_kernel<EPI>);
-  if (!ensure_smem_attr(kfn, di.device, T::kSmemBytes)) return FL_ERR_CUDA;
+// Internal: the pair (cluster) launch was refused; the caller retries with one CTA per tile.
+constexpr int kRetryUnpaired = -1;
+
+// Launches fused_gemm_kernel<EPI, CG> persistently: as many CTAs (CG = 1) or
+// CTA pairs (CG = 2) as can be resident, capped by the tile count and the test
+// override, but never fewer than `min_units` (tiles that must run at once).
+// With `cooperative` the launch fails instead of starting if not every CTA can
+// be resident at once (needed when CTAs wait on one another).
+template <int EPI, int CG>
+int launch_gemm_cg(GemmParams& p, const DeviceInfo& di, cudaStream_t stream, bool cooperative, int min_units) {
+  using T = EpiTraits<EPI, CG>;
+  const void* kfn = reinterpret_cast<const void*>(&fused_gemm_kernel<EPI, CG>);
+  if (!ensure_smem_attr(kfn, di.device, T::kSmemBytes)) return CG == 2 ? kRetryUnpaired : FL_ERR_CUDA;
   p.status = device_status_ptr(di.device);
   if (p.status == nullptr) return FL_ERR_CUDA;
-  int grid = di.num_sms < p.num_tiles ? di.num_sms : p.num_tiles;
-  const int cap = max_ctas_override();
-  if (cap > 0 && cap < grid) grid = cap;
-  if (grid < min_grid) grid = min_grid;
-  if (grid > di.num_sms) return FL_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = cooperative ? attr : nullptr;
-  cfg.numAttrs = cooperative ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_gemm_kernel<EPI>, p);
-  return e == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
+  int max_units = di.num_sms;
+  if (CG == 2) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = 2;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+    cfg.gridDim = dim3(2 * (di.num_sms / 2));
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, fused_gemm_kernel<EPI, CG>, &cfg) != cudaSuccess || clusters < 1) {
+      cudaGetLastError();
+      return kRetryUnpaired;
+    }
+    max_units = clusters;
+  }
+  int units = max_units < p.num_tiles ? max_units : p.num_tiles;
+  const int cap = max_ctas_override() / CG;
+  if (max_ctas_override() > 0 && cap < units) units = cap > 0 ? cap : 1;
+  if (units < min_units) units = min_units;
+  if (units > max_units) return CG == 2 ? kRetryUnpaired : FL_ERR_UNSUPPORTED;
+  cfg.gridDim = dim3(CG * units);
+  if (cooperative) {
+    attr[nattr].id = cudaLaunchAttributeCooperative;
+    attr[nattr].val.cooperative = 1;
+    ++nattr;
+  }
+  cfg.attrs = nattr ? attr : nullptr;
+  cfg.numAttrs = nattr;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_gemm_kernel<EPI, CG>, p);
+  if (e == cudaSuccess) return FL_OK;
+  if (CG == 2) {
+    cudaGetLastError();
+    return kRetryUnpaired;
+  }
+  return FL_ERR_CUDA;
+}
+
+// Runs `setup(cg, params)` (which fills the tensor maps and epilogue fields for
+// tiles of cg x 128 rows) and launches; a refused pair launch is retried with
+// one CTA per tile.
+template <int EPI, class Setup>
+int run_gemm(int M, Setup&& setup, const DeviceInfo& di, cudaStream_t stream, bool cooperative,
+             int min_units) {
+  GemmParams p;
+  int cg = choose_cg(M);
+  if (cg == 2) {
+    if (!setup(2, p)) return FL_ERR_CUDA;
+    const int st = launch_gemm_cg<EPI, 2>(p, di, stream, cooperative, min_units);
+    if (st != kRetryUnpaired) return st;
+  }
+  if (!setup(1, p)) return FL_ERR_CUDA;
+  return launch_gemm_cg<EPI, 1>(p, di, stream, cooperative, min_units);
 }
 
 }  // namespace fl

@@ -94,19 +94,20 @@ extern "C" int fused_linear_gelu(const void* X, const void* W, const void* b, vo
     return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
   }
 
-  GemmParams p;
-  init_params(p, M, N, K, 256);
-  if (K > 0) {
-    if (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, N, ldw, kBK, 256,
+  auto setup = [&](int cg, GemmParams& p) -> bool {
+    init_params(p, M, N, K, 256, cg);
+    if (K > 0 &&
+        (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, N, ldw, kBK, 256 / cg,
+                    CU_TENSOR_MAP_SWIZZLE_128B)))
+      return false;
+    if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, ldy, 64, 32,
                    CU_TENSOR_MAP_SWIZZLE_128B))
-      return FL_ERR_CUDA;
-  }
-  if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, ldy, 64, 32,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return FL_ERR_CUDA;
-  p.bias = static_cast<const __nv_bfloat16*>(b);
-  return mode == FL_GELU_TANH ? launch_gemm<EPI_GELU_TANH>(p, di, s, false, 1)
-                              : launch_gemm<EPI_GELU_ERF>(p, di, s, false, 1);
+      return false;
+    p.bias = static_cast<const __nv_bfloat16*>(b);
+    return true;
+  };
+  return mode == FL_GELU_TANH ? run_gemm<EPI_GELU_TANH>(M, setup, di, s, false, 1)
+                              : run_gemm<EPI_GELU_ERF>(M, setup, di, s, false, 1);
 }

@@ -30,25 +30,26 @@ extern "C" int fused_qkv_rope(const void* X, const void* Wqkv, const void* bqkv,
   int st = current_device(&di);
   if (st != FL_OK) return st;
 
-  GemmParams p;
-  init_params(p, M, 3 * d_model, K, 256);
-  if (K > 0) {
-    if (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wqkv, K, 3 * d_model, ldw, kBK, 256,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-      return FL_ERR_CUDA;
-  }
   void* outs[3] = {Q, Kout, V};
-  for (int i = 0; i < 3; ++i)
-    if (!encode_2d(&p.map_out[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, outs[i], d_model, M, ldo, 64, 32,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-      return FL_ERR_CUDA;
-  p.bias = static_cast<const __nv_bfloat16*>(bqkv);
-  p.positions = positions;
-  p.seq_len = seq_len > 0 ? seq_len : 1;
-  p.head_dim = head_dim;
-  p.d_model = d_model;
-  p.log2_theta = std::log2(theta);
-  return launch_gemm<EPI_QKV_ROPE>(p, di, static_cast<cudaStream_t>(stream), false, 1);
+  auto setup = [&](int cg, GemmParams& p) -> bool {
+    init_params(p, M, 3 * d_model, K, 256, cg);
+    if (K > 0 &&
+        (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wqkv, K, 3 * d_model, ldw, kBK, 256 / cg,
+                    CU_TENSOR_MAP_SWIZZLE_128B)))
+      return false;
+    for (int i = 0; i < 3; ++i)
+      if (!encode_2d(&p.map_out[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, outs[i], d_model, M, ldo, 64, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    p.bias = static_cast<const __nv_bfloat16*>(bqkv);
+    p.positions = positions;
+    p.seq_len = seq_len > 0 ? seq_len : 1;
+    p.head_dim = head_dim;
+    p.d_model = d_model;
+    p.log2_theta = std::log2(theta);
+    return true;
+  };
+  return run_gemm<EPI_QKV_ROPE>(M, setup, di, static_cast<cudaStream_t>(stream), false, 1);
 }

@@ -138,29 +138,31 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
     return cudaLaunchKernelEx(&cfg, rmsnorm_fp8_decode_kernel, p) == cudaSuccess ? FL_OK : FL_ERR_CUDA;
   }
 
-  GemmParams p;
-  init_params(p, M, N, K, 256);
-  p.group_m = 1;  // row-major tile order: the tiles of one row block run side by side
-  if (p.num_n_blocks > di.num_sms) return FL_ERR_UNSUPPORTED;
-  if (K > 0) {
-    if (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, N, ldw, kBK, 256,
+  const int num_n = cdiv(N, 256);
+  if (num_n > di.num_sms) return FL_ERR_UNSUPPORTED;
+  auto setup = [&](int cg, GemmParams& p) -> bool {
+    init_params(p, M, N, K, 256, cg);
+    p.group_m = 1;  // row-major tile order: the tiles of one row block run side by side
+    if (K > 0 &&
+        (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, K, N, ldw, kBK, 256 / cg,
+                    CU_TENSOR_MAP_SWIZZLE_128B)))
+      return false;
+    if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Yq, N, M, ldq, 128, 32,
                    CU_TENSOR_MAP_SWIZZLE_128B))
-      return FL_ERR_CUDA;
-  }
-  if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Yq, N, M, ldq, 128, 32,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return FL_ERR_CUDA;
-  p.bias = static_cast<const __nv_bfloat16*>(b);
-  p.resid = static_cast<const __nv_bfloat16*>(Z);
-  p.ldz = ldz;
-  p.gamma = static_cast<const __nv_bfloat16*>(gamma);
-  p.eps = eps;
-  p.row_scale = row_scale;
-  p.counters = reinterpret_cast<unsigned*>(ws + wl.counters);
-  p.partials = reinterpret_cast<float2*>(ws + wl.partials);
-  // Every tile of a row block must be resident together: the grid is at least
-  // one row block wide and all CTAs are co-scheduled (cooperative launch).
-  return launch_gemm<EPI_RMSNORM_FP8>(p, di, s, true, p.num_n_blocks);
+      return false;
+    p.bias = static_cast<const __nv_bfloat16*>(b);
+    p.resid = static_cast<const __nv_bfloat16*>(Z);
+    p.ldz = ldz;
+    p.gamma = static_cast<const __nv_bfloat16*>(gamma);
+    p.eps = eps;
+    p.row_scale = row_scale;
+    p.counters = reinterpret_cast<unsigned*>(ws + wl.counters);
+    p.partials = reinterpret_cast<float2*>(ws + wl.partials);
+    return true;
+  };
+  // Every tile of a row block must be resident together: at least one row block's
+  // worth of tiles runs at once and all CTAs are co-scheduled (cooperative launch).
+  return run_gemm<EPI_RMSNORM_FP8>(M, setup, di, s, true, num_n);
 }

@@ -20,21 +20,22 @@ extern "C" int fused_swiglu(const void* X, const void* Wgate, const void* Wup, c
   int st = current_device(&di);
   if (st != FL_OK) return st;
 
-  GemmParams p;
-  init_params(p, M, N, K, 128);
-  if (K > 0) {
-    if (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wgate, K, N, ldw, kBK, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&p.map_b2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wup, K, N, ldw, kBK, 128,
+  auto setup = [&](int cg, GemmParams& p) -> bool {
+    init_params(p, M, N, K, 128, cg);
+    if (K > 0 &&
+        (!encode_2d(&p.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, K, M, ldx, kBK, kBM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !encode_2d(&p.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wgate, K, N, ldw, kBK, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !encode_2d(&p.map_b2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wup, K, N, ldw, kBK, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B)))
+      return false;
+    if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, ldy, 64, 32,
                    CU_TENSOR_MAP_SWIZZLE_128B))
-      return FL_ERR_CUDA;
-  }
-  if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, N, M, ldy, 64, 32,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return FL_ERR_CUDA;
-  p.bias = static_cast<const __nv_bfloat16*>(bgate);
-  p.bias2 = static_cast<const __nv_bfloat16*>(bup);
-  return launch_gemm<EPI_SWIGLU>(p, di, static_cast<cudaStream_t>(stream), false, 1);
+      return false;
+    p.bias = static_cast<const __nv_bfloat16*>(bgate);
+    p.bias2 = static_cast<const __nv_bfloat16*>(bup);
+    return true;
+  };
+  return run_gemm<EPI_SWIGLU>(M, setup, di, static_cast<cudaStream_t>(stream), false, 1);
 }

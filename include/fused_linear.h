@@ -178,6 +178,13 @@ FL_API void fl_set_wait_timeout_ns(uint64_t ns);
  * tests to make each CTA walk many tiles.  Process-wide. */
 FL_API void fl_set_max_ctas(int n);
 
+/* Two-CTA tensor-core mode of the prefill kernels: with 1 (the default) a pair
+ * of CTAs on neighbouring SMs shares each 256-row tile (tcgen05 cta_group::2,
+ * each CTA loading half of the W tile) whenever M spans at least two 128-row
+ * blocks; with 0 every CTA computes its own 128-row tile.  Results are the
+ * same either way.  Process-wide; intended for tests and diagnostics. */
+FL_API void fl_set_cta_pairing(int enable);
+
 /* Static text for a status code. */
 FL_API const char* fl_status_string(int status);
 

@@ -22,9 +22,11 @@ pytestmark = pytest.mark.gpu
 def _defaults():
     fl.set_max_ctas(0)
     fl.set_wait_timeout_ns(0)
+    fl.set_cta_pairing(True)
     yield
     fl.set_max_ctas(0)
     fl.set_wait_timeout_ns(0)
+    fl.set_cta_pairing(True)
     assert fl.device_status() == fl.FL_OK
 
 
@@ -95,6 +97,45 @@ def test_gelu_full_workload_sampled():
     got = host(Y[torch.from_numpy(rows).cuda()])
     ref = oracle.linear_gelu(f64(ops["X"][rows]), f64(ops["W"]), f64(ops["b"]), oracle.GELU_TANH)
     assert_bf16_close(got, ref, "gelu full")
+
+
+@pytest.mark.parametrize("pairing", [True, False])
+def test_every_prefill_epilogue_in_both_cta_modes(pairing):
+    # one CTA per 128-row tile, or a CTA pair per 256-row tile (cta_group::2); 3 row blocks
+    # make the pair's second half run past M on the last tile
+    fl.set_cta_pairing(pairing)
+    M, N, K = 300, 512, 200
+    X = _draw((M, K), syn.STREAM_X)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5)
+    Wu = _draw((N, K), syn.STREAM_WUP, K ** -0.5)
+    b = _draw((N,), syn.STREAM_B, 0.02)
+    Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), dev_bf16(b), mode="tanh")
+    assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), f64(b), oracle.GELU_TANH), "gelu")
+    Ys = fl.fused_swiglu(dev_bf16(X), dev_bf16(W), dev_bf16(Wu), dev_bf16(b), None)
+    assert_bf16_close(host(Ys), oracle.swiglu(f64(X), f64(W), f64(Wu), f64(b), None), "swiglu")
+    H, D = 2, 128
+    Wq = _draw((3 * H * D, K), syn.STREAM_W, K ** -0.5)
+    q, k, v = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, head_dim=D, seq_len=77)
+    ref = oracle.qkv_rope(f64(X), f64(Wq), None, H, D, 1e4, np.arange(M) % 77)
+    assert_bf16_close(host(torch.cat([q, k, v], 1)), ref, "qkv")
+    Z = _draw((M, N), syn.STREAM_Z)
+    g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0)
+    qq, ss = fl.fused_linear_residual_rmsnorm_fp8(dev_bf16(X), dev_bf16(W), dev_bf16(b), dev_bf16(Z),
+                                                  dev_bf16(g), 1e-6)
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), f64(b), f64(Z), f64(g), 1e-6)
+    assert_fp8_close(qq.cpu().numpy(), ss.cpu().numpy().astype(np.float64), q_ref, s_ref, "rmsnorm")
+
+
+@pytest.mark.parametrize("pairing", [True, False])
+def test_gelu_many_tiles_per_cta_both_modes(pairing):
+    # two CTAs (one pair) walk 3 x 6 tiles: accumulator buffers and stage phases wrap many times
+    fl.set_cta_pairing(pairing)
+    fl.set_max_ctas(2)
+    M, N, K = 768, 1536, 320
+    X = _draw((M, K), syn.STREAM_X, seed=5)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=5)
+    Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), None, mode="erf")
+    assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), None, oracle.GELU_ERF), "many tiles")
 
 
 # ------------------------------------------------------------------ QKV + RoPE
