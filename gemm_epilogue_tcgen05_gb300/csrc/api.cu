@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "host_common.h"
@@ -85,6 +86,14 @@ int* device_status_ptr(int device) {
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 int max_ctas_override() { return g_max_ctas.load(); }
 int cta_pairing_mode() { return g_pairing.load(); }
+
+bool launch_tool_attached() {
+  // Nsight tools announce their injection through these variables in the target process.
+  static const bool attached = std::getenv("CUDA_INJECTION64_PATH") != nullptr ||
+                               std::getenv("NV_NSIGHT_INJECTION_TRANSPORT_TYPE") != nullptr ||
+                               std::getenv("NV_TPS_LAUNCH_TOKEN") != nullptr;
+  return attached;
+}
 
 bool ensure_smem_attr(const void* kernel, int device, int smem_bytes) {
   std::lock_guard<std::mutex> lk(g_mu);

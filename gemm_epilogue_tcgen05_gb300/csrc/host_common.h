@@ -24,6 +24,8 @@ int current_device(DeviceInfo* out);
 int* device_status_ptr(int device);
 uint64_t wait_timeout_ns();
 int max_ctas_override();
+// True when a launch-intercepting CUDA tool (e.g. a profiler) is injected into the process.
+bool launch_tool_attached();
 // Makes sure the kernel may use `smem_bytes` of dynamic shared memory on `device`.
 bool ensure_smem_attr(const void* kernel, int device, int smem_bytes);
 
@@ -102,7 +104,10 @@ int launch_gemm_cg(GemmParams& p, const DeviceInfo& di, cudaStream_t stream, boo
   if (units < min_units) units = min_units;
   if (units > max_units) return CG == 2 ? kRetryUnpaired : FL_ERR_UNSUPPORTED;
   cfg.gridDim = dim3(CG * units);
-  if (cooperative) {
+  // Launch-intercepting tools (Nsight Compute) refuse cooperative launches of
+  // clusters; under such a tool the grid stays within the resident-cluster count
+  // computed above, so every pair is still placed at once on the serialised device.
+  if (cooperative && !(CG == 2 && launch_tool_attached())) {
     attr[nattr].id = cudaLaunchAttributeCooperative;
     attr[nattr].val.cooperative = 1;
     ++nattr;
