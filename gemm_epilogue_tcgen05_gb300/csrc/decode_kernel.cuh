@@ -29,6 +29,11 @@ constexpr int kDecABytes = 128 * kBK * 2;  // W tile
 constexpr int kDecBBytes = kDecTokens * kBK * 2;  // X tile
 constexpr int kDecStageBytes = kDecABytes + kDecBBytes;
 constexpr int kDecMaxSeg = 32;
+// After the weight stream the stage ring is idle; finishing reuses it: up to kDecGatherSlots
+// contributors' 16 KB partial tiles are gathered there (cp.async), and the h tiles of the
+// first kDecHoldTiles finished feature tiles wait there for the grid-wide statistics.
+constexpr int kDecGatherSlots = 10;
+constexpr int kDecHoldTiles = 2;
 constexpr int kDecSmemBytes = kDecStages * kDecStageBytes + 32 * 129 * 4 + 128 * 4 + 1024 + 1024;
 
 struct alignas(128) DecodeParams {
@@ -138,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
     tma_prefetch_desc(&p.map_w);
     tma_prefetch_desc(&p.map_x);
   }
-  if (warp == 0 && u_end > u_begin) {
+  if (warp == 2 && u_end > u_begin) {
+    // (An epilogue warp, idle until the first partial, so the weight stream starts at once.)
     // Any CTA covering a feature tile may finish it: pull that tile's residual
     // columns (one 256-byte run per token) and gamma / bias into L2 now.
     const int f_last = (u_end - 1) / p.num_kb;
@@ -238,6 +244,21 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
     const bool leader = ti == 0;
     const int fq = ti & 31;           // feature quad (features 4*fq .. 4*fq+3 of a tile) in the finishing passes
     uint8_t* stage_w = reinterpret_cast<uint8_t*>(hT) + q * 4096;  // this warp's 32 x 128-byte staging rows
+    // Residual, bias and gamma of a feature tile in the layout of the token-major pass
+    // (token (ti/32) + 4k, features 4*fq .. 4*fq+3 of the tile).
+    float z[8][4], b4[4], g4[4];
+    int side_tile = -1;
+    auto load_side = [&](int ft) {
+      const int n = ft * 128 + fq * 4;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int t = (ti >> 5) + 4 * k;
+        load_bf16x4(p.resid + static_cast<size_t>(t) * p.ldz, n, t < p.M ? p.N : 0, z[k]);
+      }
+      load_bf16x4(p.bias, n, p.bias ? p.N : 0, b4);
+      load_bf16x4(p.gamma, n, p.N, g4);
+      side_tile = ft;
+    };
     // Phase 1: drain each segment's partial accumulator to global scratch and count k blocks.
     int ls = 0;
     int f = f_first;
@@ -247,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
       u = seg_end;
       const int abuf = ls & 1;
       const uint32_t use = static_cast<uint32_t>(ls >> 1);
+      // The last segment's tile is the likeliest one for this CTA to finish: fetch its side
+      // operands now, while its last MMAs are still running.
+      if (seg_end == u_end) load_side(f);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[abuf], use & 1u, wctx, W_EPI_TMEM_FULL));
       if (ok) {
         tc_fence_after();
@@ -280,7 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
           __threadfence();
           const unsigned add = static_cast<unsigned>(seg_end - seg_begin);
           const unsigned old = atomicAdd(p.counters + f, add);
-          if (old + add == static_cast<unsigned>(p.num_kb)) fin_list[(*fin_count)++] = f;
+          if (old + add == static_cast<unsigned>(p.num_kb)) {
+            __threadfence();  // acquire: the other contributors' partials are visible from here on
+            fin_list[(*fin_count)++] = f;
+          }
         }
         *epi_stop = stop;
       }
@@ -292,16 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
     // then per-token partial sum of h^2 and max |h * gamma| over the tile's 128 features.
     for (int i = 0; i < nfin; ++i) {
       const int f = fin_list[i];
-      const int n = f * 128 + fq * 4;  // this lane's 4 features in the token-major pass
-      // residual, bias and gamma of the token-major pass are requested first
-      float z[8][4], b4[4], g4[4];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int t = (ti >> 5) + 4 * k;
-        load_bf16x4(p.resid + static_cast<size_t>(t) * p.ldz, n, t < p.M ? p.N : 0, z[k]);
-      }
-      load_bf16x4(p.bias, n, p.bias ? p.N : 0, b4);
-      load_bf16x4(p.gamma, n, p.N, g4);
+      if (side_tile != f) load_side(f);
       // contributors' partials, read contiguously: float4 number (ti + 128 k) of each slot is
       // feature row ti/8 + 16 k, tokens 4*(ti%8) .. 4*(ti%8)+3
       float4 acc[8];
@@ -309,28 +327,52 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
       for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       const int c_lo = dec_cta_of(f * p.num_kb, p.units, G);
       const int c_hi = dec_cta_of((f + 1) * p.num_kb - 1, p.units, G);
-      for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
-        float4 w[4][8];
+      const int ncontrib = c_hi - c_lo + 1;
+      if (ncontrib <= kDecGatherSlots) {
+        // One round trip: every thread copies the 8 float4 it will sum from each contributor's
+        // 16 KB partial tile into the idle stage ring (cp.async, all in flight at once).
+        for (int j = 0; j < ncontrib; ++j) {
+          const int c = c_lo + j;
+          const int cf_first = dec_unit_begin(c, p.units, G) / p.num_kb;
+          const float4* src = reinterpret_cast<const float4*>(p.partials) +
+                              (static_cast<size_t>(c) * p.seg_max + (f - cf_first)) * 1024 + ti;
+          const uint32_t dst = smem_u32(stage_mem + j * 16384) + ti * 16;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = c0 + j;
-          if (c <= c_hi) {
-            const int cf_first = dec_unit_begin(c, p.units, G) / p.num_kb;
-            const float4* src = reinterpret_cast<const float4*>(p.partials) +
-                                (static_cast<size_t>(c) * p.seg_max + (f - cf_first)) * 1024 + ti;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) w[j][k] = __ldcg(src + 128 * k);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) w[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+          for (int k = 0; k < 8; ++k) cp_async_16(dst + k * 2048, src + 128 * k);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
+        cp_async_wait_all();
+        for (int j = 0; j < ncontrib; ++j) {
+          const float4* slot = reinterpret_cast<const float4*>(stage_mem + j * 16384) + ti;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            acc[k].x += w[j][k].x; acc[k].y += w[j][k].y; acc[k].z += w[j][k].z; acc[k].w += w[j][k].w;
+            const float4 w = slot[128 * k];
+            acc[k].x += w.x; acc[k].y += w.y; acc[k].z += w.z; acc[k].w += w.w;
           }
+        }
+      } else {
+        for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
+          float4 w[4][8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = c0 + j;
+            if (c <= c_hi) {
+              const int cf_first = dec_unit_begin(c, p.units, G) / p.num_kb;
+              const float4* src = reinterpret_cast<const float4*>(p.partials) +
+                                  (static_cast<size_t>(c) * p.seg_max + (f - cf_first)) * 1024 + ti;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) w[j][k] = __ldcg(src + 128 * k);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) w[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              acc[k].x += w[j][k].x; acc[k].y += w[j][k].y; acc[k].z += w[j][k].z; acc[k].w += w[j][k].w;
+            }
+        }
       }
       // transpose through shared memory: hT[token][feature row]
 #pragma unroll
@@ -351,7 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
         hv.y = hT[t * 129 + fq * 4 + 1] + b4[1] + z[k][1];
         hv.z = hT[t * 129 + fq * 4 + 2] + b4[2] + z[k][2];
         hv.w = hT[t * 129 + fq * 4 + 3] + b4[3] + z[k][3];
-        __stcg(reinterpret_cast<float4*>(p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128) + fq, hv);
+        if (i < kDecHoldTiles) {
+          reinterpret_cast<float4*>(stage_mem + (kDecGatherSlots + i) * 16384)[t * 32 + fq] = hv;
+        } else {
+          __stcg(reinterpret_cast<float4*>(p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128) + fq, hv);
+        }
         float ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
         float am = fmaxf(fmaxf(fabsf(hv.x * g4[0]), fabsf(hv.y * g4[1])), fmaxf(fabsf(hv.z * g4[2]), fabsf(hv.w * g4[3])));
 #pragma unroll
@@ -416,7 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int t = (ti >> 5) + 4 * k;
-          hv[k] = __ldcg(reinterpret_cast<const float4*>(p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128) + fq);
+          hv[k] = i < kDecHoldTiles
+                      ? reinterpret_cast<const float4*>(stage_mem + (kDecGatherSlots + i) * 16384)[t * 32 + fq]
+                      : __ldcg(reinterpret_cast<const float4*>(p.hbuf + (static_cast<size_t>(f) * kDecTokens + t) * 128) + fq);
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
