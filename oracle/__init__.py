@@ -51,6 +51,7 @@ def _lib():
         "orc_e4m3_encode_array": [P, L, P],
         "orc_e4m3_decode_array": [P, L, P],
         "orc_rope_rotate": [D, D, D, P, P],
+        "orc_residual_rmsnorm_linear": [P, L, P, P, P, P, L, L, D, P, P, L, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -184,3 +185,15 @@ def e4m3_decode(q) -> np.ndarray:
     y = np.empty(q.shape, dtype=np.float64)
     _lib().orc_e4m3_decode_array(_ptr(q), q.size, _ptr(y))
     return y
+
+
+def residual_rmsnorm_linear(X, W0, b0, Z, gamma, eps, W1, b1=None):
+    """(y, h1): y = RMSNorm(X W0^T + b0 + Z, gamma) W1^T + b1 for the rows given; h1 = X W0^T + b0 + Z."""
+    X, W0, b0, Z, gamma, W1, b1 = _f64(X), _f64(W0), _f64(b0), _f64(Z), _f64(gamma), _f64(W1), _f64(b1)
+    r, K = X.shape
+    N, N2 = W0.shape[0], W1.shape[0]
+    y = np.empty((r, N2), dtype=np.float64)
+    h1 = np.empty((r, N), dtype=np.float64)
+    _lib().orc_residual_rmsnorm_linear(_ptr(X), r, _ptr(W0), _ptr(b0), _ptr(Z), _ptr(gamma), N, K, float(eps),
+                                       _ptr(W1), _ptr(b1), N2, _ptr(y), _ptr(h1))
+    return y, h1

@@ -15,6 +15,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #ifndef M_PI
 #define M_PI 3.14159265358979323846
@@ -198,6 +199,33 @@ void orc_rmsnorm_fp8(const double* X, long nrows, const double* W, const double*
         scale[i] = amax / 448.0;
         for (long n = 0; n < N; ++n)
             q[(size_t)i * N + n] = amax > 0.0 ? (uint8_t)orc_e4m3_encode(yi[n] / scale[i]) : 0;
+    }
+}
+
+/* ---- GEMM -> residual -> RMSNorm -> GEMM --------------------------------
+ * [E] §模式 A: y = RMSNorm(x W0^T (+ b0) + z, gamma) W1^T (+ b1), i.e.
+ * h1 = x W0^T + b0 + z,  r = 1 / sqrt(mean_n h1^2 + eps),  v = r * h1 (.) gamma,
+ * y[j] = sum_n v[n] W1[j, n] + b1[j].  Written in that plain order (the
+ * reparameterised order of the kernels is what the tests compare against it).
+ * Also returns h1 (the residual stream after the add).
+ * X [nrows, K], W0 [N, K], Z [nrows, N], gamma [N], W1 [N2, N]; out y [nrows, N2], h1 [nrows, N].
+ */
+void orc_residual_rmsnorm_linear(const double* X, long nrows, const double* W0, const double* b0,
+                                 const double* Z, const double* gamma, long N, long K, double eps,
+                                 const double* W1, const double* b1, long N2, double* y, double* h1) {
+    for (long i = 0; i < nrows; ++i) {
+        const double* x = X + (size_t)i * (size_t)K;
+        double* hi = h1 + (size_t)i * (size_t)N;
+#pragma omp parallel for schedule(static)
+        for (long n = 0; n < N; ++n) hi[n] = linear_at(x, W0, b0, K, n) + Z[(size_t)i * N + n];
+        double ss = 0.0;
+        for (long n = 0; n < N; ++n) ss += hi[n] * hi[n];
+        const double r = 1.0 / sqrt(ss / (double)N + eps);
+        double* v = (double*)malloc((size_t)N * sizeof(double));
+        for (long n = 0; n < N; ++n) v[n] = r * hi[n] * gamma[n];
+#pragma omp parallel for schedule(static)
+        for (long j = 0; j < N2; ++j) y[(size_t)i * N2 + j] = linear_at(v, W1, b1, N, j);
+        free(v);
     }
 }
 

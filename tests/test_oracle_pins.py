@@ -284,3 +284,25 @@ def test_rmsnorm_fp8_codes_and_scale():
     # a zero row gives scale 0 and zero codes
     q0, s0, _ = oracle.rmsnorm_fp8(np.zeros((1, 40)), W, None, np.zeros((1, 200)), g, 1e-6)
     assert s0[0] == 0.0 and not q0.any()
+
+
+# ------------------------------------------------ GEMM -> residual -> RMSNorm -> GEMM
+def test_residual_rmsnorm_linear_matches_torch_fp64():
+    rng = np.random.default_rng(10)
+    r, K, N, N2 = 4, 48, 64, 40
+    X = rng.standard_normal((r, K))
+    W0, W1 = rng.standard_normal((N, K)) / math.sqrt(K), rng.standard_normal((N2, N)) / math.sqrt(N)
+    b0, b1 = rng.standard_normal(N) * 0.02, rng.standard_normal(N2) * 0.02
+    Z, g = rng.standard_normal((r, N)), 1.0 + 0.1 * rng.standard_normal(N)
+    y, h1 = oracle.residual_rmsnorm_linear(X, W0, b0, Z, g, 1e-6, W1, b1)
+    t = lambda a: torch.from_numpy(a)
+    h = F.linear(t(X), t(W0), t(b0)) + t(Z)
+    ref = F.linear(F.rms_norm(h, (N,), weight=t(g), eps=1e-6), t(W1), t(b1)).numpy()
+    assert np.allclose(h1, h.numpy(), rtol=1e-13, atol=1e-13)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-13)
+    # the row scale is one scalar per row: it commutes with the second GEMM (the deferral the kernels use)
+    rr = 1.0 / np.sqrt(np.mean(h1 ** 2, axis=1) + 1e-6)
+    deferred = rr[:, None] * ((h1 * g) @ W1.T) + b1
+    assert np.allclose(y, deferred, rtol=1e-12, atol=1e-13)
+    # a per-column factor does not commute: moving gamma after W1 changes the result
+    assert not np.allclose(y, rr[:, None] * (h1 @ W1.T) * g[:N2] + b1, rtol=1e-3, atol=1e-3)
