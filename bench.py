@@ -185,6 +185,11 @@ class Case:
         elif w.kind == "swiglu":
             self.out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
             self.flops = 2.0 * w.M * (2 * w.N) * w.K
+        elif w.kind == "rms_chain":
+            self.h2 = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+            self.part = torch.empty((fl.rms_partials_per_row(w.N), w.M), dtype=torch.float32, device="cuda")
+            self.out = torch.empty((w.M, w.N2), dtype=torch.bfloat16, device="cuda")
+            self.flops = 2.0 * w.M * w.N * w.K + 2.0 * w.M * w.N2 * w.N
         else:
             self.out = (torch.empty((w.M, w.N), dtype=torch.uint8, device="cuda"),
                         torch.empty(w.M, dtype=torch.float32, device="cuda"))
@@ -201,6 +206,9 @@ class Case:
             return float(b + w.M * w.N + 4 * w.M)
         if w.kind == "qkv_rope":
             return float(b + 2 * w.M * w.N)
+        if w.kind == "rms_chain":
+            # h2 is written by the first GEMM and read by the second; y is written once
+            return float(b + 2 * (2 * w.M * w.N) + 2 * w.M * w.N2)
         return float(b + 2 * w.M * w.N)
 
     def run(self, stream=None):
@@ -213,6 +221,10 @@ class Case:
                               seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
         elif w.kind == "swiglu":
             fl.fused_swiglu(d["X"], d["Wgate"], d["Wup"], d.get("bgate"), d.get("bup"), Y=self.out, stream=stream)
+        elif w.kind == "rms_chain":
+            fl.fused_linear_residual_gamma(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], store_h1=False, H2=self.h2,
+                                           rms_partials=self.part, stream=stream)
+            fl.fused_linear_rms_rowscale(self.h2, d["W2"], None, self.part, w.N, w.eps, Y=self.out, stream=stream)
         else:
             fl.fused_linear_residual_rmsnorm_fp8(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], w.eps,
                                                  Yq=self.out[0], row_scale=self.out[1], workspace=self.ws,
@@ -273,6 +285,9 @@ def unfused_fn(case: Case):
         return fn
     if w.kind == "swiglu":
         return lambda: F.silu(F.linear(d["X"], d["Wgate"])) * F.linear(d["X"], d["Wup"])
+    if w.kind == "rms_chain":
+        return lambda: F.linear(F.rms_norm(F.linear(d["X"], d["W"]) + d["Z"], (w.N,), weight=d["gamma"], eps=w.eps),
+                                d["W2"])
 
     def rms():
         h = F.linear(d["X"], d["W"]).float() + d["Z"].float()
@@ -481,7 +496,7 @@ def main():
     rows = []
     if args.rows == "all":
         for name in ("qkv_rope_8192x12288x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
-                     "rmsnorm_fp8_decode_32x4096x14336"):
+                     "rmsnorm_fp8_decode_32x4096x14336", "rms_chain_8192x4096x4096_to_14336"):
             c = Case(name)
             row_steps = min(args.steps, 200)
             ts, _ = time_device(c, row_steps, args.warmup, flush, barrier)

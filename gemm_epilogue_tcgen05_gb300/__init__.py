@@ -54,6 +54,12 @@ def load() -> ctypes.CDLL:
     for f in (lib.fused_linear_gelu, lib.fused_qkv_rope, lib.fused_swiglu,
               lib.fused_linear_residual_rmsnorm_fp8):
         f.restype = I
+    lib.fused_linear_residual_gamma.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I64, I64, I64, I64, P]
+    lib.fused_linear_rms_rowscale.argtypes = [P, P, P, P, I, F, P, I, I, I, I64, I64, I64, P]
+    lib.fused_linear_residual_gamma.restype = I
+    lib.fused_linear_rms_rowscale.restype = I
+    lib.fl_rms_partials_per_row.argtypes = [I]
+    lib.fl_rms_partials_per_row.restype = I
     lib.fl_rmsnorm_fp8_workspace_bytes.argtypes = [I, I, I]
     lib.fl_rmsnorm_fp8_workspace_bytes.restype = SZ
     lib.fl_device_status.argtypes = [P]
@@ -228,6 +234,56 @@ def fused_linear_residual_rmsnorm_fp8(X, W, b, Z, gamma, eps: float = 1e-6, Yq=N
         _stream(stream))
     _check("fused_linear_residual_rmsnorm_fp8", st)
     return Yq, row_scale
+
+
+def rms_partials_per_row(n_norm: int) -> int:
+    return load().fl_rms_partials_per_row(int(n_norm))
+
+
+def fused_linear_residual_gamma(X, W, b, Z, gamma, store_h1: bool = True, H2=None, H1=None, rms_partials=None,
+                                stream=None):
+    """Step 1 of GEMM -> residual -> RMSNorm -> GEMM: returns (H2 = h1 * gamma, H1 = h1 or None, partials)."""
+    M, K = X.shape
+    N = W.shape[0]
+    _mat(X, "X", torch.bfloat16)
+    _mat(W, "W", torch.bfloat16)
+    _mat(Z, "Z", torch.bfloat16)
+    _vec(b, "b", torch.bfloat16, N)
+    _vec(gamma, "gamma", torch.bfloat16, N)
+    if H2 is None:
+        H2 = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if H1 is None and store_h1:
+        H1 = torch.empty_like(H2)
+    _mat(H2, "H2", torch.bfloat16)
+    if H1 is not None and (_mat(H1, "H1", torch.bfloat16) != _mat(H2, "H2", torch.bfloat16) and M > 1):
+        raise ValueError("H1 and H2 must share one leading dimension")
+    npart = rms_partials_per_row(N)
+    if rms_partials is None:
+        rms_partials = torch.empty((npart, M), dtype=torch.float32, device=X.device)
+    if rms_partials.dtype != torch.float32 or rms_partials.numel() < npart * M or not rms_partials.is_contiguous():
+        raise ValueError("rms_partials must be a contiguous fp32 tensor of [ceil(N/256), M] entries")
+    st = load().fused_linear_residual_gamma(_ptr(X), _ptr(W), _ptr(b), _ptr(Z), _ptr(gamma), _ptr(H2), _ptr(H1),
+                                            _ptr(rms_partials), M, N, K, _ld(X, K, K), _ld(W, K, K), _ld(Z, N, N),
+                                            _ld(H2, N, N), _stream(stream))
+    _check("fused_linear_residual_gamma", st)
+    return H2, H1, rms_partials
+
+
+def fused_linear_rms_rowscale(H2, W1, b1, rms_partials, n_norm: int, eps: float = 1e-6, Y=None, stream=None):
+    """Step 2: Y = r * (H2 W1^T) + b1, r = 1/sqrt(sum of the row's partials / n_norm + eps)."""
+    M, K = H2.shape
+    N = W1.shape[0]
+    _mat(H2, "H2", torch.bfloat16)
+    _mat(W1, "W1", torch.bfloat16)
+    _vec(b1, "b1", torch.bfloat16, N)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=H2.device)
+    _mat(Y, "Y", torch.bfloat16)
+    st = load().fused_linear_rms_rowscale(_ptr(H2), _ptr(W1), _ptr(b1), _ptr(rms_partials), int(n_norm), float(eps),
+                                          _ptr(Y), M, N, K, _ld(H2, K, K), _ld(W1, K, K), _ld(Y, N, N),
+                                          _stream(stream))
+    _check("fused_linear_rms_rowscale", st)
+    return Y
 
 
 def device_status(stream=None) -> int:

@@ -28,7 +28,11 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kStagingBytes = 4096;  // one 32-row x 128-byte TMA store box per buffer
 
-enum EpiKind : int { EPI_GELU_TANH = 0, EPI_GELU_ERF = 1, EPI_QKV_ROPE = 2, EPI_SWIGLU = 3, EPI_RMSNORM_FP8 = 4 };
+enum EpiKind : int {
+  EPI_GELU_TANH = 0, EPI_GELU_ERF = 1, EPI_QKV_ROPE = 2, EPI_SWIGLU = 3, EPI_RMSNORM_FP8 = 4,
+  EPI_RESID_GAMMA = 5,  // h1 = acc + b + z; stores h1 (optional) and h1 * gamma; per-row partial sum h1^2
+  EPI_ROWSCALE = 6      // y = r * acc + b with r = 1/sqrt(sum of the row's partials / n + eps)
+};
 
 struct alignas(128) GemmParams {
   CUtensorMap map_a;       // X [M, K] bf16, box {64, 128}
@@ -52,6 +56,8 @@ struct alignas(128) GemmParams {
   float eps;
   float* row_scale;
   float2* partials;        // [num_m_blocks][num_n_blocks][128] (sum h^2, max |h*gamma|)
+  float* rms_partials;     // [ceil(n/256)][M] per-row partial sums of squares (GEMM -> RMSNorm -> GEMM chain)
+  int n_partials, n_norm, store_h1;
   unsigned* counters;      // [2][num_m_blocks]: arrivals, finished readers
   int* status;
   unsigned long long timeout_ns;
@@ -489,6 +495,73 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             load_vec32(p.bias2, col0, p.N, b);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = g[j] * (v[j] + b[j]);
+            stage_bf16_32(buf, lane, u, v);
+          }
+          ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);
+        }
+        release_acc(abuf);
+      } else if constexpr (EPI == EPI_RESID_GAMMA) {
+        // Epilogue 1 of the chain: h1 = acc + b + z (the residual stream), h2 = h1 (.) gamma feeds the
+        // next GEMM unscaled, and the tile's partial sum of h1^2 per row goes to the partials array.
+        if (!ok) break;
+        const int n0 = nb * 256;
+        const __nv_bfloat16* zrow = p.resid + static_cast<long long>(row_ok ? m : 0) * p.ldz;
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float h[2][32];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col0 = n0 + c * 64 + u * 32;
+            float z[32], b[32];
+            tmem_load32f(tacc + c * 64 + u * 32, k_empty, h[u]);
+            load_row32(zrow, row_ok, col0, p.N, z);
+            load_vec32(p.bias, col0, p.N, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              h[u][j] += b[j] + z[j];
+              ss = fmaf(h[u][j], h[u][j], ss);
+            }
+          }
+          if (p.store_h1) {
+            const uint32_t buf = ring.acquire(lane);
+            stage_bf16_32(buf, lane, 0, h[0]);
+            stage_bf16_32(buf, lane, 1, h[1]);
+            ring.commit(&p.map_out[1], buf, lane, n0 + c * 64, y_box);
+          }
+          const uint32_t buf = ring.acquire(lane);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float g[32];
+            load_vec32(p.gamma, n0 + c * 64 + u * 32, p.N, g);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] *= h[u][j];
+            stage_bf16_32(buf, lane, u, g);
+          }
+          ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);
+        }
+        if (row_ok) p.rms_partials[static_cast<size_t>(nb) * p.M + m] = ss;
+        release_acc(abuf);
+      } else if constexpr (EPI == EPI_ROWSCALE) {
+        // Epilogue 2 of the chain: the row scale r, deferred past this GEMM (it is one scalar per
+        // row, so (r v) W = r (v W)), is merged from the row's partials and applied here.
+        if (!ok) break;
+        float ssum = 0.f;
+        if (row_ok)
+          for (int j = 0; j < p.n_partials; ++j) ssum += __ldg(p.rms_partials + static_cast<size_t>(j) * p.M + m);
+        const float r = rsqrtf(ssum / static_cast<float>(p.n_norm) + p.eps);
+        const int n0 = nb * 256;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t buf = ring.acquire(lane);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col0 = n0 + c * 64 + u * 32;
+            float v[32], b[32];
+            tmem_load32f(tacc + c * 64 + u * 32, k_empty, v);
+            load_vec32(p.bias, col0, p.N, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaf(r, v[j], b[j]);
             stage_bf16_32(buf, lane, u, v);
           }
           ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);

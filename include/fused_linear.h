@@ -158,6 +158,34 @@ FL_API int fused_linear_residual_rmsnorm_fp8_noalloc(const void* X, const void* 
                                                      int64_t ldx, int64_t ldw, int64_t ldz, int64_t ldq,
                                                      void* stream);
 
+/* GEMM -> residual -> RMSNorm -> GEMM, with the RMSNorm row scale deferred into
+ * the second GEMM ("GEMM Epilogue 完全拆解", §模式 A: y = RMSNorm(x W0 + z, gamma) W1
+ * = r (.) (((x W0 + z) (.) gamma) W1), since r is one scalar per row and commutes
+ * with a matrix product; a per-column factor such as gamma does not).
+ *
+ * Step 1, fused_linear_residual_gamma: h1 = X W^T (+ b) + Z; writes H2 = h1 (.) gamma
+ * (bf16, the unscaled input of the second GEMM), optionally H1 = h1 (bf16, the
+ * residual stream after the add; NULL to skip), and rms_partials: fp32
+ * [fl_rms_partials_per_row(N)][M] (tile-major), entry [j][m] = sum of h1[m, n]^2 over
+ * columns n of the j-th 256-column tile.  X [M,K], W [N,K], b [N] (nullable),
+ * Z [M,N] (ldz), gamma [N]; H1 and H2 share the leading dimension ldh.
+ *
+ * Step 2, fused_linear_rms_rowscale: Y = r (.) (H2 W1^T) (+ b1) with
+ * r[m] = 1 / sqrt((sum_j rms_partials[j][m]) / n_norm + eps), the partials merged in a
+ * fixed order inside the epilogue (no separate reduction launch).  H2 [M,K] with
+ * K = n_norm normally, W1 [N,K], b1 [N] (nullable), Y [M,N] bf16.  Run step 2 on the
+ * same stream after step 1 (or after an event) so the partials are complete. */
+FL_API int fused_linear_residual_gamma(const void* X, const void* W, const void* b, const void* Z,
+                                       const void* gamma, void* H2, void* H1, float* rms_partials,
+                                       int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldz,
+                                       int64_t ldh, void* stream);
+FL_API int fused_linear_rms_rowscale(const void* H2, const void* W1, const void* b1,
+                                     const float* rms_partials, int n_norm, float eps, void* Y,
+                                     int M, int N, int K, int64_t ldh, int64_t ldw, int64_t ldy,
+                                     void* stream);
+/* Number of rms_partials entries per row for a normalised width of n_norm (ceil(n_norm / 256)). */
+FL_API int fl_rms_partials_per_row(int n_norm);
+
 /* Bytes of workspace fused_linear_residual_rmsnorm_fp8 needs for this shape
  * on the current device (0 for an empty problem). */
 FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);

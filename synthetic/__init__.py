@@ -22,7 +22,7 @@ Recipe (one element):
    bf16 (round to nearest even).
 
 Streams within a workload: X = 0, W = 1, b = 2, Z = 3, gamma = 4,
-W_up = 5, b_up = 6.
+W_up = 5, b_up = 6, W2 (second GEMM of a chain) = 7.
 """
 from __future__ import annotations
 
@@ -40,7 +40,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 21  # elements per vectorised chunk (bounds host memory)
 
-STREAM_X, STREAM_W, STREAM_B, STREAM_Z, STREAM_GAMMA, STREAM_WUP, STREAM_BUP = range(7)
+STREAM_X, STREAM_W, STREAM_B, STREAM_Z, STREAM_GAMMA, STREAM_WUP, STREAM_BUP, STREAM_W2 = range(8)
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -198,7 +198,7 @@ def draw_numpy(seed: int, stream: int, shape, mean: float, std: float, dtype: st
 class Workload:
     """One synthetic workload: shapes, dtype and the distribution of each operand."""
     name: str
-    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8"
+    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain"
     M: int
     N: int               # output features (QKV: 3*H*D; SwiGLU: d_ff)
     K: int
@@ -210,6 +210,7 @@ class Workload:
     theta: float = 10000.0
     eps: float = 1e-6
     seed: int = 0
+    N2: int = 0          # rms_chain: output features of the second GEMM (its K is N)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
 
@@ -225,6 +226,9 @@ WORKLOADS = {
                                                     8192, 4096, 14336, has_bias=False),
     "rmsnorm_fp8_decode_32x4096x14336": Workload("rmsnorm_fp8_decode_32x4096x14336", "rmsnorm_fp8",
                                                  32, 4096, 14336, has_bias=False),
+    # attention output projection -> residual -> RMSNorm -> gate (or up) projection, d 4096, d_ff 14336
+    "rms_chain_8192x4096x4096_to_14336": Workload("rms_chain_8192x4096x4096_to_14336", "rms_chain",
+                                                  8192, 4096, 4096, has_bias=False, N2=14336),
 }
 
 
@@ -243,9 +247,11 @@ def operand_specs(w: Workload):
     specs.append(("W", STREAM_W, (w.N, w.K), 0.0, w_std, dt))
     if w.has_bias:
         specs.append(("b", STREAM_B, (w.N,), 0.0, 0.02, dt))
-    if w.kind == "rmsnorm_fp8":
+    if w.kind in ("rmsnorm_fp8", "rms_chain"):
         specs += [("Z", STREAM_Z, (w.M, w.N), 0.0, 1.0, dt),
                   ("gamma", STREAM_GAMMA, (w.N,), 1.0, 0.1, dt)]
+    if w.kind == "rms_chain":
+        specs.append(("W2", STREAM_W2, (w.N2, w.N), 0.0, 1.0 / math.sqrt(w.N), dt))
     return specs
 
 

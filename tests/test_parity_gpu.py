@@ -303,3 +303,37 @@ def test_argument_errors_on_device():
         fl.fused_qkv_rope(X, torch.zeros((3 * 64, 64), dtype=torch.bfloat16, device="cuda"), n_heads=1,
                           head_dim=64)
     assert e.value.status == fl.FL_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ GEMM -> residual -> RMSNorm -> GEMM
+@pytest.mark.parametrize("pairing", [True, False])
+def test_rms_chain_small(pairing):
+    fl.set_cta_pairing(pairing)
+    M, N, K, N2 = 300, 512, 200, 384
+    X = _draw((M, K), syn.STREAM_X)
+    W0 = _draw((N, K), syn.STREAM_W, K ** -0.5)
+    b0 = _draw((N,), syn.STREAM_B, 0.02)
+    Z = _draw((M, N), syn.STREAM_Z)
+    g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0)
+    W1 = _draw((N2, N), syn.STREAM_W2, N ** -0.5)
+    b1 = _draw((N2,), syn.STREAM_BUP, 0.02)
+    H2, H1, part = fl.fused_linear_residual_gamma(dev_bf16(X), dev_bf16(W0), dev_bf16(b0), dev_bf16(Z), dev_bf16(g))
+    Y = fl.fused_linear_rms_rowscale(H2, dev_bf16(W1), dev_bf16(b1), part, N, 1e-6)
+    y_ref, h1_ref = oracle.residual_rmsnorm_linear(f64(X), f64(W0), f64(b0), f64(Z), f64(g), 1e-6, f64(W1), f64(b1))
+    assert_bf16_close(host(H1), h1_ref, "h1 (residual stream)")
+    assert_bf16_close(host(H2), h1_ref * f64(g), "h2 = h1 * gamma")
+    tiles = np.stack([np.sum(h1_ref[:, j * 256:(j + 1) * 256] ** 2, axis=1) for j in range(2)])
+    assert np.allclose(part.cpu().numpy(), tiles, rtol=1e-4, atol=1e-3), "per-tile sums of squares"
+    assert_bf16_close(host(Y), y_ref, "y = RMSNorm(h1) W1 + b1")
+
+
+def test_rms_chain_full_workload_sampled():
+    w = syn.WORKLOADS["rms_chain_8192x4096x4096_to_14336"]
+    ops = syn.make_operands(w)
+    H2, _, part = fl.fused_linear_residual_gamma(dev_bf16(ops["X"]), dev_bf16(ops["W"]), None, dev_bf16(ops["Z"]),
+                                                 dev_bf16(ops["gamma"]), store_h1=False)
+    Y = fl.fused_linear_rms_rowscale(H2, dev_bf16(ops["W2"]), None, part, w.N, w.eps)
+    rows = sample_rows(w.M, extra=2)
+    y_ref, _ = oracle.residual_rmsnorm_linear(f64(ops["X"][rows]), f64(ops["W"]), None, f64(ops["Z"][rows]),
+                                              f64(ops["gamma"]), w.eps, f64(ops["W2"]))
+    assert_bf16_close(host(Y[torch.from_numpy(rows).cuda()]), y_ref, "rms chain full")
