@@ -52,6 +52,7 @@ def _lib():
         "orc_e4m3_decode_array": [P, L, P],
         "orc_rope_rotate": [D, D, D, P, P],
         "orc_residual_rmsnorm_linear": [P, L, P, P, P, P, L, L, D, P, P, L, P, P],
+        "orc_linear_cross_entropy": [P, L, P, P, L, L, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -197,3 +198,13 @@ def residual_rmsnorm_linear(X, W0, b0, Z, gamma, eps, W1, b1=None):
     _lib().orc_residual_rmsnorm_linear(_ptr(X), r, _ptr(W0), _ptr(b0), _ptr(Z), _ptr(gamma), N, K, float(eps),
                                        _ptr(W1), _ptr(b1), N2, _ptr(y), _ptr(h1))
     return y, h1
+
+
+def linear_cross_entropy(X, W, b, labels) -> np.ndarray:
+    """Per-row loss -h[y] + logsumexp(h) with h = X W^T + b; label < 0 gives 0, label >= V gives NaN."""
+    X, W, b = _f64(X), _f64(W), _f64(b)
+    lab = np.ascontiguousarray(labels, dtype=np.int64)
+    out = np.empty(X.shape[0], dtype=np.float64)
+    _lib().orc_linear_cross_entropy(_ptr(X), X.shape[0], _ptr(W), _ptr(b), W.shape[0], X.shape[1], _ptr(lab),
+                                    _ptr(out))
+    return out

@@ -229,6 +229,34 @@ void orc_residual_rmsnorm_linear(const double* X, long nrows, const double* W0, 
     }
 }
 
+/* ---- LM-head cross-entropy ----------------------------------------------
+ * [E] §模式 C: logits h_i = x_i W^T (+ b) over the vocabulary, and
+ * loss_i = -h_{i, y_i} + log sum_k exp(h_{i, k}); the log-sum-exp is evaluated in
+ * the usual shifted form m + log sum_k exp(h_k - m) with m = max_k h_k.
+ * A negative label marks an ignored row (loss 0).  X [nrows, K], W [V, K].
+ */
+void orc_linear_cross_entropy(const double* X, long nrows, const double* W, const double* b, long V, long K,
+                              const long* labels, double* loss) {
+    for (long i = 0; i < nrows; ++i) {
+        const double* x = X + (size_t)i * (size_t)K;
+        double* h = (double*)malloc((size_t)V * sizeof(double));
+#pragma omp parallel for schedule(static)
+        for (long v = 0; v < V; ++v) h[v] = linear_at(x, W, b, K, v);
+        if (labels[i] < 0) {
+            loss[i] = 0.0;
+        } else if (labels[i] >= V) {
+            loss[i] = NAN;
+        } else {
+            double m = -INFINITY;
+            for (long v = 0; v < V; ++v) m = h[v] > m ? h[v] : m;
+            double s = 0.0;
+            for (long v = 0; v < V; ++v) s += exp(h[v] - m);
+            loss[i] = m + log(s) - h[labels[i]];
+        }
+        free(h);
+    }
+}
+
 /* Number of OpenMP threads the parallel loops above use. */
 int orc_num_threads(void) {
     int n = 1;

@@ -306,3 +306,40 @@ def test_residual_rmsnorm_linear_matches_torch_fp64():
     assert np.allclose(y, deferred, rtol=1e-12, atol=1e-13)
     # a per-column factor does not commute: moving gamma after W1 changes the result
     assert not np.allclose(y, rr[:, None] * (h1 @ W1.T) * g[:N2] + b1, rtol=1e-3, atol=1e-3)
+
+
+# ------------------------------------------------------------- LM-head cross-entropy
+def test_cross_entropy_matches_torch_and_closed_forms():
+    rng = np.random.default_rng(11)
+    r, K, V = 6, 32, 300
+    X = rng.standard_normal((r, K))
+    W = rng.standard_normal((V, K)) / math.sqrt(K)
+    b = rng.standard_normal(V) * 0.1
+    y = rng.integers(0, V, size=r)
+    loss = oracle.linear_cross_entropy(X, W, b, y)
+    logits = F.linear(torch.from_numpy(X), torch.from_numpy(W), torch.from_numpy(b))
+    ref = F.cross_entropy(logits, torch.from_numpy(y), reduction="none").numpy()
+    assert np.allclose(loss, ref, rtol=1e-13, atol=1e-13)
+    # uniform logits: loss = log V exactly; a dominant label logit: loss -> 0
+    assert np.allclose(oracle.linear_cross_entropy(X, np.zeros((V, K)), None, y), math.log(V), rtol=0, atol=1e-13)
+    bb = np.zeros(V)
+    bb[7] = 60.0
+    assert oracle.linear_cross_entropy(X[:1], np.zeros((V, K)), bb, [7])[0] < 1e-20
+    # large logits do not overflow (shifted form), ignored and out-of-range labels
+    big = oracle.linear_cross_entropy(X[:1], W * 1e3, None, [3])[0]
+    assert np.isfinite(big) and big >= 0
+    assert oracle.linear_cross_entropy(X[:2], W, b, [-100, V])[0] == 0.0
+    assert math.isnan(oracle.linear_cross_entropy(X[:2], W, b, [-100, V])[1])
+
+
+def test_online_lse_merge_matches_library():
+    # the per-tile (m, s) merge the kernel uses reproduces torch.logsumexp over the whole row
+    rng = np.random.default_rng(12)
+    h = rng.standard_normal(1000) * 5
+    m, s = -np.inf, 0.0
+    for tile in np.array_split(h, 7):
+        mt, st = tile.max(), np.exp(tile - tile.max()).sum()
+        mn = max(m, mt)
+        s = s * math.exp(m - mn) + st * math.exp(mt - mn)
+        m = mn
+    assert m + math.log(s) == pytest.approx(torch.logsumexp(torch.from_numpy(h), 0).item(), rel=1e-14)
