@@ -185,6 +185,11 @@ class Case:
         elif w.kind == "swiglu":
             self.out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
             self.flops = 2.0 * w.M * (2 * w.N) * w.K
+        elif w.kind == "cross_entropy":
+            self.labels = torch.from_numpy(syn.make_labels(w)).cuda()
+            self.out = torch.empty(w.M, dtype=torch.float32, device="cuda")
+            self.ws = fl.cross_entropy_workspace(w.M, w.N)
+            self.flops = 2.0 * w.M * w.N * w.K
         elif w.kind == "rms_chain":
             self.h2 = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
             self.part = torch.empty((fl.rms_partials_per_row(w.N), w.M), dtype=torch.float32, device="cuda")
@@ -206,6 +211,8 @@ class Case:
             return float(b + w.M * w.N + 4 * w.M)
         if w.kind == "qkv_rope":
             return float(b + 2 * w.M * w.N)
+        if w.kind == "cross_entropy":
+            return float(b + 4 * w.M + 4 * w.M)  # + labels in, loss out
         if w.kind == "rms_chain":
             # h2 is written by the first GEMM and read by the second; y is written once
             return float(b + 2 * (2 * w.M * w.N) + 2 * w.M * w.N2)
@@ -221,6 +228,9 @@ class Case:
                               seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
         elif w.kind == "swiglu":
             fl.fused_swiglu(d["X"], d["Wgate"], d["Wup"], d.get("bgate"), d.get("bup"), Y=self.out, stream=stream)
+        elif w.kind == "cross_entropy":
+            fl.fused_linear_cross_entropy(d["X"], d["W"], d.get("b"), self.labels, loss=self.out, workspace=self.ws,
+                                          stream=stream)
         elif w.kind == "rms_chain":
             fl.fused_linear_residual_gamma(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], store_h1=False, H2=self.h2,
                                            rms_partials=self.part, stream=stream)
@@ -285,6 +295,8 @@ def unfused_fn(case: Case):
         return fn
     if w.kind == "swiglu":
         return lambda: F.silu(F.linear(d["X"], d["Wgate"])) * F.linear(d["X"], d["Wup"])
+    if w.kind == "cross_entropy":
+        return lambda: F.cross_entropy(F.linear(d["X"], d["W"]).float(), case.labels.long(), reduction="none")
     if w.kind == "rms_chain":
         return lambda: F.linear(F.rms_norm(F.linear(d["X"], d["W"]) + d["Z"], (w.N,), weight=d["gamma"], eps=w.eps),
                                 d["W2"])
@@ -496,7 +508,8 @@ def main():
     rows = []
     if args.rows == "all":
         for name in ("qkv_rope_8192x12288x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
-                     "rmsnorm_fp8_decode_32x4096x14336", "rms_chain_8192x4096x4096_to_14336"):
+                     "rmsnorm_fp8_decode_32x4096x14336", "rms_chain_8192x4096x4096_to_14336",
+                     "lm_head_ce_8192x32768x4096"):
             c = Case(name)
             row_steps = min(args.steps, 200)
             ts, _ = time_device(c, row_steps, args.warmup, flush, barrier)

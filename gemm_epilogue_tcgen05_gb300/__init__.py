@@ -58,6 +58,10 @@ def load() -> ctypes.CDLL:
     lib.fused_linear_rms_rowscale.argtypes = [P, P, P, P, I, F, P, I, I, I, I64, I64, I64, P]
     lib.fused_linear_residual_gamma.restype = I
     lib.fused_linear_rms_rowscale.restype = I
+    lib.fused_linear_cross_entropy.argtypes = [P, P, P, P, P, P, I, I, I, I64, I64, I64, P, SZ, P]
+    lib.fused_linear_cross_entropy.restype = I
+    lib.fl_cross_entropy_workspace_bytes.argtypes = [I, I]
+    lib.fl_cross_entropy_workspace_bytes.restype = SZ
     lib.fl_rms_partials_per_row.argtypes = [I]
     lib.fl_rms_partials_per_row.restype = I
     lib.fl_rmsnorm_fp8_workspace_bytes.argtypes = [I, I, I]
@@ -284,6 +288,39 @@ def fused_linear_rms_rowscale(H2, W1, b1, rms_partials, n_norm: int, eps: float 
                                           _stream(stream))
     _check("fused_linear_rms_rowscale", st)
     return Y
+
+
+def cross_entropy_workspace(M: int, V: int, device=None) -> torch.Tensor:
+    n = max(load().fl_cross_entropy_workspace_bytes(int(M), int(V)), 1)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def fused_linear_cross_entropy(X, W, b, labels, loss=None, logits=None, store_logits: bool = False,
+                               workspace=None, stream=None):
+    """Per-row loss logsumexp(X W^T + b) - (X W^T + b)[label]; returns (loss, logits or None)."""
+    M, K = X.shape
+    V = W.shape[0]
+    _mat(X, "X", torch.bfloat16)
+    _mat(W, "W", torch.bfloat16)
+    _vec(b, "b", torch.bfloat16, V)
+    if labels.dtype != torch.int32 or labels.numel() != M or not labels.is_cuda or not labels.is_contiguous():
+        raise ValueError("labels must be a contiguous int32 CUDA vector of length M")
+    if loss is None:
+        loss = torch.empty(M, dtype=torch.float32, device=X.device)
+    _vec(loss, "loss", torch.float32, M)
+    if logits is None and store_logits:
+        logits = torch.empty((M, V), dtype=torch.bfloat16, device=X.device)
+    ldl = 0
+    if logits is not None:
+        _mat(logits, "logits", torch.bfloat16)
+        ldl = _ld(logits, V, V)
+    if workspace is None:
+        workspace = cross_entropy_workspace(M, V, X.device)
+    st = load().fused_linear_cross_entropy(_ptr(X), _ptr(W), _ptr(b), _ptr(labels), _ptr(loss), _ptr(logits), M, V, K,
+                                           _ld(X, K, K), _ld(W, K, K), ldl, _ptr(workspace), workspace.numel(),
+                                           _stream(stream))
+    _check("fused_linear_cross_entropy", st)
+    return loss, logits
 
 
 def device_status(stream=None) -> int:

@@ -31,7 +31,8 @@ constexpr int kStagingBytes = 4096;  // one 32-row x 128-byte TMA store box per 
 enum EpiKind : int {
   EPI_GELU_TANH = 0, EPI_GELU_ERF = 1, EPI_QKV_ROPE = 2, EPI_SWIGLU = 3, EPI_RMSNORM_FP8 = 4,
   EPI_RESID_GAMMA = 5,  // h1 = acc + b + z; stores h1 (optional) and h1 * gamma; per-row partial sum h1^2
-  EPI_ROWSCALE = 6      // y = r * acc + b with r = 1/sqrt(sum of the row's partials / n + eps)
+  EPI_ROWSCALE = 6,     // y = r * acc + b with r = 1/sqrt(sum of the row's partials / n + eps)
+  EPI_CE = 7            // per-row online log-sum-exp state + label logit; last tile of a row block merges
 };
 
 struct alignas(128) GemmParams {
@@ -58,6 +59,12 @@ struct alignas(128) GemmParams {
   float2* partials;        // [num_m_blocks][num_n_blocks][128] (sum h^2, max |h*gamma|)
   float* rms_partials;     // [ceil(n/256)][M] per-row partial sums of squares (GEMM -> RMSNorm -> GEMM chain)
   int n_partials, n_norm, store_h1;
+  // LM-head cross-entropy
+  const int* labels;       // [M]; negative = ignored row
+  float* loss;             // [M]
+  float2* ce_partials;     // [num_n_blocks][M] (running max, sum of exp(h - max)) per tile
+  float* label_logit;      // [M]
+  int store_logits;
   unsigned* counters;      // [2][num_m_blocks]: arrivals, finished readers
   int* status;
   unsigned long long timeout_ns;
@@ -232,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);  // written by the epilogue leader only
+  volatile int* ce_last = reinterpret_cast<volatile int*>(tmem_slot + 3);   // idem: this tile merges its row block
   float* inv_freq = reinterpret_cast<float*>(tmem_slot + 4);  // [64], QKV only
 
   const int warp = threadIdx.x >> 5;
@@ -565,6 +573,105 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             stage_bf16_32(buf, lane, u, v);
           }
           ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);
+        }
+        release_acc(abuf);
+      } else if constexpr (EPI == EPI_CE) {
+        // Stateful epilogue ("GEMM Epilogue 完全拆解", §模式 C): each tile keeps, per row, the running
+        // maximum m and s = sum exp(h - m) over its columns and picks the label's logit; the last
+        // tile of a 128-row block to finish (an atomic count, no waiting) merges the row's states in
+        // column-tile order into loss = m + log s - h[label].  Like the RMSNorm exchange, the
+        // 128 threads take the same named barriers and leave together right after one.
+        if (mb >= p.num_m_blocks) {
+          if (!ok) break;
+          release_acc(abuf);
+          continue;
+        }
+        const int n0 = nb * 256;
+        const int label = row_ok ? __ldg(p.labels + m) : -1;
+        if (ok) {
+          float mx = -INFINITY, se = 0.f, hl = 0.f;
+          bool has_label = false;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t buf = 0;
+            if (p.store_logits) buf = ring.acquire(lane);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int col0 = n0 + c * 64 + u * 32;
+              float v[32], b[32];
+              tmem_load32f(tacc + c * 64 + u * 32, k_empty, v);
+              load_vec32(p.bias, col0, p.N, b);
+              float um = -INFINITY;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                v[j] = col0 + j < p.N ? v[j] + b[j] : -INFINITY;  // columns past the vocabulary count for nothing
+                um = fmaxf(um, v[j]);
+                if (col0 + j == label) {
+                  hl = v[j];
+                  has_label = true;
+                }
+              }
+              const float nm = fmaxf(mx, um);
+              if (nm > -INFINITY) {
+                float add = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) add += __expf(v[j] - nm);
+                se = (mx > -INFINITY ? se * __expf(mx - nm) : 0.f) + add;
+                mx = nm;
+              }
+              if (p.store_logits) stage_bf16_32(buf, lane, u, v);
+            }
+            if (p.store_logits) ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);
+          }
+          if (row_ok) {
+            p.ce_partials[static_cast<size_t>(nb) * p.M + m] = make_float2(mx, se);
+            if (has_label) p.label_logit[m] = hl;
+          }
+        }
+        __threadfence();
+        named_bar_sync(1, kEpiThreads);
+        if (threadIdx.x == 64) {
+          const int stop = *abort_flag;
+          int last = 0;
+          if (!stop) {
+            __threadfence();
+            last = atomicAdd(p.counters + mb, 1u) == static_cast<unsigned>(p.num_n_blocks) - 1u;
+            if (last) __threadfence();  // acquire: every tile's state for this row block is visible
+          }
+          *epi_stop = stop;
+          *ce_last = last;
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (*epi_stop) break;  // uniform: only the leader writes it, between the two barriers
+        if (*ce_last) {
+          if (row_ok) {
+            float M_ = -INFINITY, S_ = 0.f;
+            for (int j0 = 0; j0 < p.num_n_blocks; j0 += 16) {
+              float2 w[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                w[j] = j0 + j < p.num_n_blocks ? __ldcg(p.ce_partials + static_cast<size_t>(j0 + j) * p.M + m)
+                                               : make_float2(-INFINITY, 0.f);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float nm = fmaxf(M_, w[j].x);
+                if (nm > -INFINITY) {
+                  S_ = (M_ > -INFINITY ? S_ * __expf(M_ - nm) : 0.f) + (w[j].x > -INFINITY ? w[j].y * __expf(w[j].x - nm) : 0.f);
+                  M_ = nm;
+                }
+              }
+            }
+            float l;
+            if (label < 0) {
+              l = 0.f;
+            } else if (label >= p.N) {
+              l = __int_as_float(0x7fc00000);  // NaN: label outside the vocabulary
+            } else {
+              l = M_ + __logf(S_) - __ldcg(p.label_logit + m);
+            }
+            p.loss[m] = l;
+          }
+          if (threadIdx.x == 64) p.counters[mb] = 0u;  // every tile of this row block has arrived
         }
         release_acc(abuf);
       } else if constexpr (EPI == EPI_RMSNORM_FP8) {

@@ -186,6 +186,25 @@ FL_API int fused_linear_rms_rowscale(const void* H2, const void* W1, const void*
 /* Number of rms_partials entries per row for a normalised width of n_norm (ceil(n_norm / 256)). */
 FL_API int fl_rms_partials_per_row(int n_norm);
 
+/* LM-head cross-entropy: logits h = X W^T (+ b) over a vocabulary of V and
+ * loss[m] = logsumexp_v(h[m, v]) - h[m, labels[m]], without writing the logits.
+ *   "GEMM Epilogue 完全拆解", §模式 C: every 256-column tile keeps, per row, the running
+ *   maximum m and s = sum exp(h - m) (a stateful epilogue) and the tile holding the
+ *   label keeps that logit; the last tile of each 128-row block to finish merges the
+ *   row's states in column order (m = max(m1, m2), s = s1 e^{m1-m} + s2 e^{m2-m}), so the
+ *   result is deterministic and needs no waiting between CTAs.
+ * X [M,K] bf16, W [V,K] bf16, b [V] bf16 (nullable), labels [M] int32 (negative: ignored
+ * row, loss 0; >= V: loss NaN), loss [M] fp32 out.  logits: nullable bf16 [M,V] copy of
+ * the logits (leading dimension ldl), e.g. kept for a backward pass.
+ * workspace: fl_cross_entropy_workspace_bytes(M, V) bytes, 256-byte aligned and
+ * zero-filled before first use; the kernel resets its counters, so it can be reused
+ * by later calls on the same stream (re-zero it after FL_ERR_TIMEOUT). */
+FL_API int fused_linear_cross_entropy(const void* X, const void* W, const void* b, const int32_t* labels,
+                                      float* loss, void* logits, int M, int V, int K,
+                                      int64_t ldx, int64_t ldw, int64_t ldl,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+FL_API size_t fl_cross_entropy_workspace_bytes(int M, int V);
+
 /* Bytes of workspace fused_linear_residual_rmsnorm_fp8 needs for this shape
  * on the current device (0 for an empty problem). */
 FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);

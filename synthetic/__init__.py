@@ -22,7 +22,8 @@ Recipe (one element):
    bf16 (round to nearest even).
 
 Streams within a workload: X = 0, W = 1, b = 2, Z = 3, gamma = 4,
-W_up = 5, b_up = 6, W2 (second GEMM of a chain) = 7.
+W_up = 5, b_up = 6, W2 (second GEMM of a chain) = 7, labels = 8.
+Labels are uniform integers: (top 53 bits of counter i) mod V.
 """
 from __future__ import annotations
 
@@ -40,7 +41,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 21  # elements per vectorised chunk (bounds host memory)
 
-STREAM_X, STREAM_W, STREAM_B, STREAM_Z, STREAM_GAMMA, STREAM_WUP, STREAM_BUP, STREAM_W2 = range(8)
+STREAM_X, STREAM_W, STREAM_B, STREAM_Z, STREAM_GAMMA, STREAM_WUP, STREAM_BUP, STREAM_W2, STREAM_LABEL = range(9)
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -134,6 +135,15 @@ def normal_f64(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     return out
 
 
+def draw_labels(seed: int, stream: int, count: int, vocab: int) -> np.ndarray:
+    """Uniform int32 labels in [0, vocab): (mix64(key + (i + 1) * golden) >> 11) mod vocab."""
+    key = stream_key(seed, stream)
+    i = np.arange(count, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = _mix64(key + (i + np.uint64(1)) * GOLDEN_GAMMA)
+    return ((z >> np.uint64(11)) % np.uint64(vocab)).astype(np.int32)
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (nearest even); returns uint16 bit patterns."""
     bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
@@ -198,7 +208,7 @@ def draw_numpy(seed: int, stream: int, shape, mean: float, std: float, dtype: st
 class Workload:
     """One synthetic workload: shapes, dtype and the distribution of each operand."""
     name: str
-    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain"
+    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain" | "cross_entropy"
     M: int
     N: int               # output features (QKV: 3*H*D; SwiGLU: d_ff)
     K: int
@@ -229,6 +239,9 @@ WORKLOADS = {
     # attention output projection -> residual -> RMSNorm -> gate (or up) projection, d 4096, d_ff 14336
     "rms_chain_8192x4096x4096_to_14336": Workload("rms_chain_8192x4096x4096_to_14336", "rms_chain",
                                                   8192, 4096, 4096, has_bias=False, N2=14336),
+    # LM head over a 32K vocabulary with the cross-entropy in the epilogue
+    "lm_head_ce_8192x32768x4096": Workload("lm_head_ce_8192x32768x4096", "cross_entropy", 8192, 32768, 4096,
+                                           has_bias=False),
 }
 
 
@@ -253,6 +266,10 @@ def operand_specs(w: Workload):
     if w.kind == "rms_chain":
         specs.append(("W2", STREAM_W2, (w.N2, w.N), 0.0, 1.0 / math.sqrt(w.N), dt))
     return specs
+
+
+def make_labels(w: Workload) -> np.ndarray:
+    return draw_labels(w.seed, STREAM_LABEL, w.M, w.N)
 
 
 def make_operands(w: Workload, rows: tuple[int, int] | None = None) -> dict:

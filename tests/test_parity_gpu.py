@@ -337,3 +337,44 @@ def test_rms_chain_full_workload_sampled():
     y_ref, _ = oracle.residual_rmsnorm_linear(f64(ops["X"][rows]), f64(ops["W"]), None, f64(ops["Z"][rows]),
                                               f64(ops["gamma"]), w.eps, f64(ops["W2"]))
     assert_bf16_close(host(Y[torch.from_numpy(rows).cuda()]), y_ref, "rms chain full")
+
+
+# ------------------------------------------------------------------ LM-head cross-entropy
+CE_ATOL, CE_RTOL = 2e-3, 1e-4  # fp32 logits from bf16 operands, fp32 online log-sum-exp
+
+
+def _assert_loss_close(got, ref, what):
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan), f"{what}: NaN pattern differs"
+    err = np.abs(got[~nan] - ref[~nan])
+    assert np.all(err <= CE_ATOL + CE_RTOL * np.abs(ref[~nan])), f"{what}: max err {err.max():.3g}"
+
+
+@pytest.mark.parametrize("pairing", [True, False])
+def test_cross_entropy_small_with_logits(pairing):
+    fl.set_cta_pairing(pairing)
+    M, V, K = 300, 1000, 200
+    X = _draw((M, K), syn.STREAM_X)
+    W = _draw((V, K), syn.STREAM_W, K ** -0.5)
+    b = _draw((V,), syn.STREAM_B, 0.5)
+    lab = syn.draw_labels(0, syn.STREAM_LABEL, M, V)
+    lab[5], lab[17] = -100, V  # ignored row, label outside the vocabulary
+    ws = fl.cross_entropy_workspace(M, V)
+    for _ in range(2):  # the workspace counters are reset by the kernel
+        loss, logits = fl.fused_linear_cross_entropy(dev_bf16(X), dev_bf16(W), dev_bf16(b),
+                                                     torch.from_numpy(lab).cuda(), store_logits=True, workspace=ws)
+        ref = oracle.linear_cross_entropy(f64(X), f64(W), f64(b), lab)
+        _assert_loss_close(loss.cpu().numpy().astype(np.float64), ref, "ce small")
+        assert_bf16_close(host(logits), oracle.linear(f64(X), f64(W), f64(b)), "logits")
+    assert torch.count_nonzero(ws[:256]) == 0
+
+
+def test_cross_entropy_full_workload_sampled():
+    w = syn.WORKLOADS["lm_head_ce_8192x32768x4096"]
+    ops = syn.make_operands(w)
+    lab = syn.make_labels(w)
+    loss, _ = fl.fused_linear_cross_entropy(dev_bf16(ops["X"]), dev_bf16(ops["W"]), None,
+                                            torch.from_numpy(lab).cuda())
+    rows = sample_rows(w.M, extra=2)
+    ref = oracle.linear_cross_entropy(f64(ops["X"][rows]), f64(ops["W"]), None, lab[rows])
+    _assert_loss_close(loss.cpu().numpy()[rows].astype(np.float64), ref, "ce full")
