@@ -53,6 +53,7 @@ def _lib():
         "orc_rope_rotate": [D, D, D, P, P],
         "orc_residual_rmsnorm_linear": [P, L, P, P, P, P, L, L, D, P, P, L, P, P],
         "orc_linear_cross_entropy": [P, L, P, P, L, L, P, P],
+        "orc_linear_quant": [P, L, P, P, L, L, I, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -67,6 +68,10 @@ def _lib():
     lib.orc_e4m3_encode.restype = I
     lib.orc_e4m3_decode.argtypes = [I]
     lib.orc_e4m3_decode.restype = D
+    lib.orc_e2m1_decode.argtypes = [I]
+    lib.orc_e2m1_decode.restype = D
+    lib.orc_e2m1_encode.argtypes = [D]
+    lib.orc_e2m1_encode.restype = I
     lib.orc_num_threads.argtypes = []
     lib.orc_num_threads.restype = I
     _lib_handle = lib
@@ -208,3 +213,30 @@ def linear_cross_entropy(X, W, b, labels) -> np.ndarray:
     _lib().orc_linear_cross_entropy(_ptr(X), X.shape[0], _ptr(W), _ptr(b), W.shape[0], X.shape[1], _ptr(lab),
                                     _ptr(out))
     return out
+
+
+QUANT_FP8_1X128, QUANT_INT4_G32, QUANT_NVFP4_G16 = 0, 1, 2
+QUANT_BLOCK = {QUANT_FP8_1X128: 128, QUANT_INT4_G32: 32, QUANT_NVFP4_G16: 16}
+
+
+def e2m1_decode(code: int) -> float:
+    return _lib().orc_e2m1_decode(int(code))
+
+
+def e2m1_encode(y: float) -> int:
+    return _lib().orc_e2m1_encode(float(y))
+
+
+def linear_quant(X, W, b, fmt):
+    """(codes uint8 [r, qbytes], scales [r, nblocks], y fp64 [r, N]) of the block-scaled Linear output."""
+    X, W, b = _f64(X), _f64(W), _f64(b)
+    r, K = X.shape
+    N = W.shape[0]
+    bs = QUANT_BLOCK[fmt]
+    nb = -(-N // bs)
+    qbytes = N if fmt == QUANT_FP8_1X128 else -(-N // 2)
+    q = np.empty((r, qbytes), dtype=np.uint8)
+    sc = np.empty((r, nb), dtype=np.float64)
+    y = np.empty((r, N), dtype=np.float64)
+    _lib().orc_linear_quant(_ptr(X), r, _ptr(W), _ptr(b), N, K, int(fmt), _ptr(q), _ptr(sc), _ptr(y))
+    return q, sc, y

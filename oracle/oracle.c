@@ -257,6 +257,87 @@ void orc_linear_cross_entropy(const double* X, long nrows, const double* W, cons
     }
 }
 
+/* ---- Block-scaled quantised write-back ------------------------------------
+ * [E] §仿射量化与尾声的五步: per block, (1) s = max|x| / qmax, (2) q = round(x / s)
+ * clamped to [-qmax, qmax], (4) compact layout, (5) the scale written beside the codes.
+ * A block whose maximum is 0 gets s = 0 and zero codes.
+ *
+ * FP4 E2M1 (OCP microscaling formats): sign, 2 exponent bits (bias 1), 1 mantissa
+ * bit; exponent 0 is subnormal (m * 0.5); largest finite 6; no inf / NaN.
+ */
+double orc_e2m1_decode(int code) {
+    int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
+}
+
+/* Nearest of the 8 non-negative codes (even code on a tie), saturating at 6. */
+int orc_e2m1_encode(double y) {
+    int s = signbit(y) ? 1 : 0;
+    double a = fabs(y);
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c <= 7; ++c) {
+        double d = fabs(orc_e2m1_decode(c) - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (s << 3) | best;
+}
+
+/* Linear followed by block-scaled quantisation of every row.
+ * fmt 0: FP8 E4M3, blocks of 128 columns, fp32 scale = amax / 448, codes 1 byte each.
+ * fmt 1: INT4 symmetric, groups of 32, fp32 scale = amax / 7, code = round-half-even(y / s)
+ *        clamped to [-7, 7], two's-complement nibble; column 2j in the low nibble of byte j.
+ * fmt 2: NVFP4, groups of 16, scale = E4M3 code of amax / 6 (the stored scale is what the
+ *        codes are divided by), values E2M1, column 2j in the low nibble of byte j.
+ * Outputs: q [nrows, qbytes_per_row] (qbytes = N for fmt 0, N/2 otherwise),
+ *          scale [nrows, nblocks] as fp64 (fmt 0, 1) or as E4M3 codes widened to fp64 (fmt 2),
+ *          y [nrows, N] the unquantised Linear output. */
+void orc_linear_quant(const double* X, long nrows, const double* W, const double* b, long N, long K, int fmt,
+                      uint8_t* q, double* scale, double* y) {
+    const long bs = fmt == 0 ? 128 : (fmt == 1 ? 32 : 16);
+    const long nblocks = (N + bs - 1) / bs;
+    const long qbytes = fmt == 0 ? N : (N + 1) / 2;
+    for (long i = 0; i < nrows; ++i) {
+        const double* x = X + (size_t)i * (size_t)K;
+        double* yi = y + (size_t)i * (size_t)N;
+#pragma omp parallel for schedule(static)
+        for (long n = 0; n < N; ++n) yi[n] = linear_at(x, W, b, K, n);
+        uint8_t* qi = q + (size_t)i * (size_t)qbytes;
+        for (long n = 0; n < qbytes; ++n) qi[n] = 0;
+        for (long blk = 0; blk < nblocks; ++blk) {
+            const long c0 = blk * bs, c1 = c0 + bs < N ? c0 + bs : N;
+            double amax = 0.0;
+            for (long n = c0; n < c1; ++n) amax = fabs(yi[n]) > amax ? fabs(yi[n]) : amax;
+            double s;
+            if (fmt == 0) s = amax / 448.0;
+            else if (fmt == 1) s = amax / 7.0;
+            else s = orc_e4m3_decode(orc_e4m3_encode(amax / 6.0));
+            scale[i * nblocks + blk] = fmt == 2 ? (double)orc_e4m3_encode(amax / 6.0) : s;
+            for (long n = c0; n < c1; ++n) {
+                const double v = s > 0.0 ? yi[n] / s : 0.0;
+                if (fmt == 0) {
+                    qi[n] = s > 0.0 ? (uint8_t)orc_e4m3_encode(v) : 0;
+                } else {
+                    int nib;
+                    if (fmt == 1) {
+                        double r = nearbyint(v);  /* default rounding mode: to nearest, ties to even */
+                        if (r > 7.0) r = 7.0;
+                        if (r < -7.0) r = -7.0;
+                        nib = ((int)r) & 15;
+                    } else {
+                        nib = s > 0.0 ? orc_e2m1_encode(v) : 0;
+                    }
+                    qi[n / 2] |= (uint8_t)(nib << (4 * (n & 1)));
+                }
+            }
+        }
+    }
+}
+
 /* Number of OpenMP threads the parallel loops above use. */
 int orc_num_threads(void) {
     int n = 1;

@@ -343,3 +343,55 @@ def test_online_lse_merge_matches_library():
         s = s * math.exp(m - mn) + st * math.exp(mt - mn)
         m = mn
     assert m + math.log(s) == pytest.approx(torch.logsumexp(torch.from_numpy(h), 0).item(), rel=1e-14)
+
+
+# ------------------------------------------------------- block-scaled quantised write-back
+def test_e2m1_table_and_rounding():
+    # OCP FP4 E2M1 magnitudes, listed from the format definition
+    assert [oracle.e2m1_decode(c) for c in range(8)] == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert [oracle.e2m1_decode(c | 8) for c in range(1, 8)] == [-0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    assert [oracle.e2m1_encode(oracle.e2m1_decode(c)) for c in range(16) if c != 8] == [c for c in range(16) if c != 8]
+    assert oracle.e2m1_encode(2.5) == 4 and oracle.e2m1_encode(3.5) == 6   # ties to the even code (2.0, 4.0)
+    assert oracle.e2m1_encode(0.25) == 0 and oracle.e2m1_encode(5.0) == 6  # 0 | 0.5 -> 0; 4 | 6 -> 6 (even)
+    assert oracle.e2m1_encode(100.0) == 7 and oracle.e2m1_encode(-7.0) == 15
+
+
+def _unpack_nibbles(q, n):
+    lo, hi = q & 15, q >> 4
+    out = np.empty((q.shape[0], 2 * q.shape[1]), dtype=np.int64)
+    out[:, 0::2], out[:, 1::2] = lo, hi
+    return out[:, :n]
+
+
+def test_quant_formats_round_trip_and_layout():
+    rng = np.random.default_rng(13)
+    r, K, N = 3, 24, 256
+    X = rng.standard_normal((r, K))
+    W = rng.standard_normal((N, K)) / math.sqrt(K)
+    y = X @ W.T
+    # FP8 1x128: scale = blockwise amax / 448 and the block maximum encodes to +-448
+    q, s, yy = oracle.linear_quant(X, W, None, oracle.QUANT_FP8_1X128)
+    assert np.allclose(yy, y, rtol=1e-13, atol=1e-13)
+    for blk in range(2):
+        seg = y[:, blk * 128:(blk + 1) * 128]
+        assert np.allclose(s[:, blk], np.abs(seg).max(axis=1) / 448, rtol=1e-14)
+        dq = oracle.e4m3_decode(q[:, blk * 128:(blk + 1) * 128]) * s[:, blk:blk + 1]
+        assert np.all(np.abs(dq - seg) <= np.abs(seg) * 2.0 ** -4 + s[:, blk:blk + 1] * 2.0 ** -9)
+    # INT4 g32: nibble two's complement, low nibble first, values = numpy rint (half to even) clamp 7
+    q, s, _ = oracle.linear_quant(X, W, None, oracle.QUANT_INT4_G32)
+    nib = _unpack_nibbles(q, N)
+    vals = np.where(nib >= 8, nib - 16, nib)
+    sref = np.abs(y.reshape(r, -1, 32)).max(axis=2) / 7
+    assert np.allclose(s, sref, rtol=1e-14)
+    expect = np.clip(np.rint(y / np.repeat(sref, 32, axis=1)), -7, 7)
+    assert np.array_equal(vals, expect)
+    # NVFP4 g16: the stored E4M3 scale divides the values; decoded values stay within half an ulp
+    q, s, _ = oracle.linear_quant(X, W, None, oracle.QUANT_NVFP4_G16)
+    sc = oracle.e4m3_decode(s.astype(np.uint8))
+    assert np.array_equal(s.astype(np.uint8), oracle.e4m3_encode(np.abs(y.reshape(r, -1, 16)).max(axis=2) / 6))
+    dec = np.vectorize(oracle.e2m1_decode)(_unpack_nibbles(q, N)) * np.repeat(sc, 16, axis=1)
+    rel = np.abs(dec - y) / np.repeat(sc, 16, axis=1)
+    assert rel.max() <= 1.0 + 1e-12  # at most one E2M1 step (1.0 at the top of the range, 2 -> 3 -> 4 -> 6)
+    # a zero block gives scale 0 and zero codes
+    q0, s0, _ = oracle.linear_quant(np.zeros((1, K)), W, None, oracle.QUANT_INT4_G32)
+    assert not q0.any() and not s0.any()
