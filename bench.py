@@ -190,6 +190,14 @@ class Case:
             self.out = torch.empty(w.M, dtype=torch.float32, device="cuda")
             self.ws = fl.cross_entropy_workspace(w.M, w.N)
             self.flops = 2.0 * w.M * w.N * w.K
+        elif w.kind == "quant":
+            self.fmt = QUANT_FMT[w.quant]
+            bs = fl.QUANT_BLOCK[self.fmt]
+            qbytes = w.N if self.fmt == fl.QUANT_FP8_1X128 else w.N // 2
+            sdt = torch.uint8 if self.fmt == fl.QUANT_NVFP4_G16 else torch.float32
+            self.out = (torch.empty((w.M, qbytes), dtype=torch.uint8, device="cuda"),
+                        torch.empty((w.M, -(-w.N // bs)), dtype=sdt, device="cuda"))
+            self.flops = 2.0 * w.M * w.N * w.K
         elif w.kind == "rms_chain":
             self.h2 = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
             self.part = torch.empty((fl.rms_partials_per_row(w.N), w.M), dtype=torch.float32, device="cuda")
@@ -213,6 +221,8 @@ class Case:
             return float(b + 2 * w.M * w.N)
         if w.kind == "cross_entropy":
             return float(b + 4 * w.M + 4 * w.M)  # + labels in, loss out
+        if w.kind == "quant":
+            return float(b + sum(t.numel() * t.element_size() for t in self.out))
         if w.kind == "rms_chain":
             # h2 is written by the first GEMM and read by the second; y is written once
             return float(b + 2 * (2 * w.M * w.N) + 2 * w.M * w.N2)
@@ -231,6 +241,9 @@ class Case:
         elif w.kind == "cross_entropy":
             fl.fused_linear_cross_entropy(d["X"], d["W"], d.get("b"), self.labels, loss=self.out, workspace=self.ws,
                                           stream=stream)
+        elif w.kind == "quant":
+            fl.fused_linear_quant(d["X"], d["W"], d.get("b"), self.fmt, Yq=self.out[0], scales=self.out[1],
+                                  stream=stream)
         elif w.kind == "rms_chain":
             fl.fused_linear_residual_gamma(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], store_h1=False, H2=self.h2,
                                            rms_partials=self.part, stream=stream)
@@ -297,6 +310,8 @@ def unfused_fn(case: Case):
         return lambda: F.silu(F.linear(d["X"], d["Wgate"])) * F.linear(d["X"], d["Wup"])
     if w.kind == "cross_entropy":
         return lambda: F.cross_entropy(F.linear(d["X"], d["W"]).float(), case.labels.long(), reduction="none")
+    if w.kind == "quant":
+        return lambda: unfused_quant(F.linear(d["X"], d["W"], d.get("b")).float(), case.fmt)
     if w.kind == "rms_chain":
         return lambda: F.linear(F.rms_norm(F.linear(d["X"], d["W"]) + d["Z"], (w.N,), weight=d["gamma"], eps=w.eps),
                                 d["W2"])
@@ -307,6 +322,31 @@ def unfused_fn(case: Case):
         s = y.abs().amax(dim=1) / 448.0
         return (y / s[:, None]).to(torch.float8_e4m3fn), s
     return rms
+
+
+QUANT_FMT = {"fp8_1x128": 0, "int4_g32": 1, "nvfp4_g16": 2}
+_E2M1_MIDPOINTS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def unfused_quant(y: torch.Tensor, fmt: int):
+    """Block-scaled quantisation as separate torch kernels after the GEMM (comparison baseline only)."""
+    M, N = y.shape
+    bs = {0: 128, 1: 32, 2: 16}[fmt]
+    g = y.view(M, N // bs, bs)
+    amax = g.abs().amax(dim=2, keepdim=True)
+    if fmt == 0:
+        s = amax / 448.0
+        return (g / torch.where(s > 0, s, 1.0)).to(torch.float8_e4m3fn).view(M, N), s.view(M, -1)
+    if fmt == 1:
+        s = amax / 7.0
+        q = torch.clamp(torch.round(g / torch.where(s > 0, s, 1.0)), -7, 7).to(torch.int8).view(M, N)
+        packed = (q[:, 0::2] & 15) | ((q[:, 1::2] & 15) << 4)
+        return packed.to(torch.uint8), s.view(M, -1)
+    sc = (amax / 6.0).to(torch.float8_e4m3fn)
+    v = g / torch.where(sc.float() > 0, sc.float(), 1.0)
+    mag = torch.bucketize(v.abs(), torch.tensor(_E2M1_MIDPOINTS, device=y.device)).to(torch.uint8)
+    code = (mag | ((v < 0).to(torch.uint8) << 3)).view(M, N)
+    return code[:, 0::2] | (code[:, 1::2] << 4), sc.view(M, -1)
 
 
 def time_fn(fn, steps: int, warmup: int, flush: torch.Tensor):
@@ -421,6 +461,12 @@ def oracle_sample(w, rows: int):
         oracle.qkv_rope(f["X"], f["W"], f.get("b"), w.n_heads, w.head_dim, w.theta, np.arange(rows) % w.seq_len)
     elif w.kind == "swiglu":
         oracle.swiglu(f["X"], f["Wgate"], f["Wup"], f.get("bgate"), f.get("bup"))
+    elif w.kind == "quant":
+        oracle.linear_quant(f["X"], f["W"], f.get("b"), QUANT_FMT[w.quant])
+    elif w.kind == "cross_entropy":
+        oracle.linear_cross_entropy(f["X"], f["W"], f.get("b"), syn.make_labels(w)[:rows])
+    elif w.kind == "rms_chain":
+        oracle.residual_rmsnorm_linear(f["X"], f["W"], f.get("b"), f["Z"], f["gamma"], w.eps, f["W2"])
     else:
         oracle.rmsnorm_fp8(f["X"], f["W"], f.get("b"), f["Z"], f["gamma"], w.eps)
     return time.perf_counter() - t0
@@ -509,7 +555,8 @@ def main():
     if args.rows == "all":
         for name in ("qkv_rope_8192x12288x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
                      "rmsnorm_fp8_decode_32x4096x14336", "rms_chain_8192x4096x4096_to_14336",
-                     "lm_head_ce_8192x32768x4096"):
+                     "lm_head_ce_8192x32768x4096", "quant_fp8_1x128_8192x16384x4096",
+                     "quant_int4_g32_8192x16384x4096", "quant_nvfp4_g16_8192x16384x4096"):
             c = Case(name)
             row_steps = min(args.steps, 200)
             ts, _ = time_device(c, row_steps, args.warmup, flush, barrier)

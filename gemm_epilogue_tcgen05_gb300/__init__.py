@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
     lib.fused_linear_rms_rowscale.restype = I
     lib.fused_linear_cross_entropy.argtypes = [P, P, P, P, P, P, I, I, I, I64, I64, I64, P, SZ, P]
     lib.fused_linear_cross_entropy.restype = I
+    lib.fused_linear_quant.argtypes = [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, P]
+    lib.fused_linear_quant.restype = I
     lib.fl_cross_entropy_workspace_bytes.argtypes = [I, I]
     lib.fl_cross_entropy_workspace_bytes.restype = SZ
     lib.fl_rms_partials_per_row.argtypes = [I]
@@ -321,6 +323,40 @@ def fused_linear_cross_entropy(X, W, b, labels, loss=None, logits=None, store_lo
                                            _stream(stream))
     _check("fused_linear_cross_entropy", st)
     return loss, logits
+
+
+QUANT_FP8_1X128, QUANT_INT4_G32, QUANT_NVFP4_G16 = 0, 1, 2
+QUANT_BLOCK = {QUANT_FP8_1X128: 128, QUANT_INT4_G32: 32, QUANT_NVFP4_G16: 16}
+
+
+def fused_linear_quant(X, W, b=None, fmt: int = QUANT_FP8_1X128, Yq=None, scales=None, stream=None):
+    """Block-scaled quantised Linear output; returns (codes uint8, scales).
+
+    FP8 1x128: codes [M, N] E4M3, scales fp32 [M, ceil(N/128)].
+    INT4 g32:  codes [M, N/2] (column 2j in the low nibble of byte j), scales fp32 [M, ceil(N/32)].
+    NVFP4 g16: codes [M, N/2] E2M1 pairs, scales E4M3 bytes (uint8) [M, ceil(N/16)].
+    """
+    if fmt not in QUANT_BLOCK:
+        raise ValueError(f"unknown quantisation format {fmt}")
+    M, K = X.shape
+    N = W.shape[0]
+    _mat(X, "X", torch.bfloat16)
+    _mat(W, "W", torch.bfloat16)
+    _vec(b, "b", torch.bfloat16, N)
+    qbytes = N if fmt == QUANT_FP8_1X128 else N // 2
+    nblocks = -(-N // QUANT_BLOCK[fmt])
+    sdt = torch.uint8 if fmt == QUANT_NVFP4_G16 else torch.float32
+    if Yq is None:  # row pitch rounded up to 16 bytes, as the TMA store needs
+        Yq = torch.empty((M, -(-qbytes // 16) * 16), dtype=torch.uint8, device=X.device)[:, :qbytes]
+    if scales is None:
+        scales = torch.empty((M, nblocks), dtype=sdt, device=X.device)
+    _mat(Yq, "Yq", torch.uint8)
+    _mat(scales, "scales", sdt)
+    st = load().fused_linear_quant(_ptr(X), _ptr(W), _ptr(b), _ptr(Yq), _ptr(scales), M, N, K, _ld(X, K, K),
+                                   _ld(W, K, K), _ld(Yq, qbytes, qbytes), _ld(scales, nblocks, nblocks), int(fmt),
+                                   _stream(stream))
+    _check("fused_linear_quant", st)
+    return Yq, scales
 
 
 def device_status(stream=None) -> int:

@@ -32,8 +32,10 @@ enum EpiKind : int {
   EPI_GELU_TANH = 0, EPI_GELU_ERF = 1, EPI_QKV_ROPE = 2, EPI_SWIGLU = 3, EPI_RMSNORM_FP8 = 4,
   EPI_RESID_GAMMA = 5,  // h1 = acc + b + z; stores h1 (optional) and h1 * gamma; per-row partial sum h1^2
   EPI_ROWSCALE = 6,     // y = r * acc + b with r = 1/sqrt(sum of the row's partials / n + eps)
-  EPI_CE = 7            // per-row online log-sum-exp state + label logit; last tile of a row block merges
+  EPI_CE = 7,           // per-row online log-sum-exp state + label logit; last tile of a row block merges
+  EPI_QUANT = 8         // block-scaled quantised write-back: FP8 1x128, INT4 g32 or NVFP4 g16 + scales
 };
+enum QuantFmt : int { QF_FP8_1X128 = 0, QF_INT4_G32 = 1, QF_NVFP4_G16 = 2 };
 
 struct alignas(128) GemmParams {
   CUtensorMap map_a;       // X [M, K] bf16, box {64, 128}
@@ -65,6 +67,10 @@ struct alignas(128) GemmParams {
   float2* ce_partials;     // [num_n_blocks][M] (running max, sum of exp(h - max)) per tile
   float* label_logit;      // [M]
   int store_logits;
+  // block-scaled quantised write-back
+  int quant_fmt;
+  void* qscale;            // fp32 [M][lds] (FP8, INT4) or E4M3 bytes [M][lds] (NVFP4)
+  long long lds;
   unsigned* counters;      // [2][num_m_blocks]: arrivals, finished readers
   int* status;
   unsigned long long timeout_ns;
@@ -672,6 +678,103 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             p.loss[m] = l;
           }
           if (threadIdx.x == 64) p.counters[mb] = 0u;  // every tile of this row block has arrived
+        }
+        release_acc(abuf);
+      } else if constexpr (EPI == EPI_QUANT) {
+        // "GEMM Epilogue 完全拆解", §仿射量化与尾声的五步: block maximum -> scale -> codes -> compact
+        // layout, scales written beside the codes in the same epilogue.  Blocks are row segments
+        // of one thread, so no cross-thread reduction is needed.
+        if (!ok) break;
+        const int n0 = nb * 256;
+        if (p.quant_fmt == QF_FP8_1X128) {
+#pragma unroll 1
+          for (int blk = 0; blk < 2; ++blk) {
+            float amax = 0.f;
+#pragma unroll 1
+            for (int u = 0; u < 4; ++u) {
+              float v[32], b[32];
+              tmem_load32f(tacc + blk * 128 + u * 32, k_empty, v);
+              load_vec32(p.bias, n0 + blk * 128 + u * 32, p.N, b);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j] + b[j]));
+            }
+            const float qs = amax > 0.f ? 448.f / amax : 0.f;
+            if (row_ok && n0 + blk * 128 < p.N)
+              static_cast<float*>(p.qscale)[static_cast<long long>(m) * p.lds + nb * 2 + blk] = amax * (1.f / 448.f);
+            const uint32_t buf = ring.acquire(lane);
+#pragma unroll 1
+            for (int u = 0; u < 4; ++u) {
+              float v[32], b[32];
+              tmem_load32f(tacc + blk * 128 + u * 32, k_empty, v);
+              load_vec32(p.bias, n0 + blk * 128 + u * 32, p.N, b);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = (v[j] + b[j]) * qs;
+              stage_fp8_32(buf, lane, u, v);
+            }
+            ring.commit(&p.map_out[0], buf, lane, n0 + blk * 128, y_box);
+          }
+        } else {
+          // INT4 / NVFP4: 4 bits per value, a 256-column tile is one 128-byte row of codes
+          const uint32_t buf = ring.acquire(lane);
+          const uint32_t srow = buf + lane * 128;
+#pragma unroll 1
+          for (int u = 0; u < 8; ++u) {
+            const int col0 = n0 + u * 32;
+            float v[32], b[32];
+            tmem_load32f(tacc + u * 32, k_empty, v);
+            load_vec32(p.bias, col0, p.N, b);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += b[j];
+            uint32_t w[4];
+            if (p.quant_fmt == QF_INT4_G32) {
+              float amax = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+              const float inv = amax > 0.f ? 7.f / amax : 0.f;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  int qv = __float2int_rn(v[8 * i + e] * inv);  // round half to even
+                  qv = max(-7, min(7, qv));
+                  word |= (static_cast<uint32_t>(qv) & 15u) << (4 * e);
+                }
+                w[i] = word;
+              }
+              if (row_ok && col0 < p.N)
+                static_cast<float*>(p.qscale)[static_cast<long long>(m) * p.lds + nb * 8 + u] = amax * (1.f / 7.f);
+            } else {
+              uint32_t codes[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                float amax = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[16 * h + j]));
+                uint32_t sc;
+                const float s = round_to_e4m3(amax * (1.f / 6.f), sc);
+                codes[h] = sc;
+                const float inv = s > 0.f ? 1.f / s : 0.f;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  uint32_t word = 0;
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int j = 16 * h + 8 * i + 2 * e;
+                    word |= f32x2_to_e2m1x2(v[j] * inv, v[j + 1] * inv) << (8 * e);
+                  }
+                  w[2 * h + i] = word;
+                }
+              }
+              if (row_ok && col0 < p.N) {
+                uint8_t* sp = static_cast<uint8_t*>(p.qscale) + static_cast<long long>(m) * p.lds + nb * 16 + u * 2;
+                sp[0] = static_cast<uint8_t>(codes[0]);
+                if (col0 + 16 < p.N) sp[1] = static_cast<uint8_t>(codes[1]);
+              }
+            }
+            st_shared_v4(srow + ((u ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+          ring.commit(&p.map_out[0], buf, lane, n0 / 2, y_box);
         }
         release_acc(abuf);
       } else if constexpr (EPI == EPI_RMSNORM_FP8) {

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace fl {
 
@@ -358,6 +359,24 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Two fp32 values -> two FP4 E2M1 codes in one byte (round to nearest even, saturate to +-6);
+// the first argument lands in the low nibble.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+// fp32 -> nearest E4M3 value (round to nearest even, saturate), returned as fp32 and as its code.
+__device__ __forceinline__ float round_to_e4m3(float v, uint32_t& code) {
+  code = f32x2_to_e4m3x2(v, 0.f) & 0xFFu;
+  uint32_t h;
+  asm("{\n\t.reg .b32 t;\n\tcvt.rn.f16x2.e4m3x2 t, %1;\n\tmov.b32 %0, t;\n\t}"
+      : "=r"(h)
+      : "h"(static_cast<uint16_t>(code)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -205,6 +205,26 @@ FL_API int fused_linear_cross_entropy(const void* X, const void* W, const void* 
                                       void* workspace, size_t workspace_bytes, void* stream);
 FL_API size_t fl_cross_entropy_workspace_bytes(int M, int V);
 
+/* Linear (+ bias) with a block-scaled quantised write-back.
+ *   "GEMM Epilogue 完全拆解", §仿射量化与尾声的五步: for every block of consecutive columns
+ *   of a row, scale = max|y| / qmax, codes = y / scale rounded to the format (nearest
+ *   even, saturating), packed compactly, and the scale array written beside them.
+ *   A block whose maximum is 0 gets scale 0 and zero codes.
+ * fmt FL_QUANT_FP8_1X128: E4M3 codes, one byte per value (Yq [M,N], ldq >= N bytes);
+ *     blocks of 128 columns, fp32 scales [M][lds] = max / 448.
+ * fmt FL_QUANT_INT4_G32: signed 4-bit codes in [-7, 7] (two's complement), two per byte
+ *     with column 2j in the low nibble of byte j (Yq [M,N/2] bytes); groups of 32,
+ *     fp32 scales = max / 7.  N must be even.
+ * fmt FL_QUANT_NVFP4_G16: FP4 E2M1 codes, two per byte as above; groups of 16, scales
+ *     stored as E4M3 bytes [M][lds] = e4m3(max / 6), the values divided by that stored
+ *     scale.  N must be even.
+ * X [M,K] bf16, W [N,K] bf16, b [N] bf16 (nullable); ldq in bytes (multiple of 16),
+ * lds in scale elements (>= number of blocks per row). */
+enum { FL_QUANT_FP8_1X128 = 0, FL_QUANT_INT4_G32 = 1, FL_QUANT_NVFP4_G16 = 2 };
+FL_API int fused_linear_quant(const void* X, const void* W, const void* b, void* Yq, void* scales,
+                              int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldq, int64_t lds,
+                              int fmt, void* stream);
+
 /* Bytes of workspace fused_linear_residual_rmsnorm_fp8 needs for this shape
  * on the current device (0 for an empty problem). */
 FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);

@@ -208,7 +208,7 @@ def draw_numpy(seed: int, stream: int, shape, mean: float, std: float, dtype: st
 class Workload:
     """One synthetic workload: shapes, dtype and the distribution of each operand."""
     name: str
-    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain" | "cross_entropy"
+    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain" | "cross_entropy" | "quant"
     M: int
     N: int               # output features (QKV: 3*H*D; SwiGLU: d_ff)
     K: int
@@ -221,6 +221,7 @@ class Workload:
     eps: float = 1e-6
     seed: int = 0
     N2: int = 0          # rms_chain: output features of the second GEMM (its K is N)
+    quant: str = ""      # quant: "fp8_1x128" | "int4_g32" | "nvfp4_g16"
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
 
@@ -242,6 +243,13 @@ WORKLOADS = {
     # LM head over a 32K vocabulary with the cross-entropy in the epilogue
     "lm_head_ce_8192x32768x4096": Workload("lm_head_ce_8192x32768x4096", "cross_entropy", 8192, 32768, 4096,
                                            has_bias=False),
+    # up-projection whose output is written block-scaled for a low-precision consumer
+    "quant_fp8_1x128_8192x16384x4096": Workload("quant_fp8_1x128_8192x16384x4096", "quant", 8192, 16384, 4096,
+                                                quant="fp8_1x128"),
+    "quant_int4_g32_8192x16384x4096": Workload("quant_int4_g32_8192x16384x4096", "quant", 8192, 16384, 4096,
+                                               quant="int4_g32"),
+    "quant_nvfp4_g16_8192x16384x4096": Workload("quant_nvfp4_g16_8192x16384x4096", "quant", 8192, 16384, 4096,
+                                                quant="nvfp4_g16"),
 }
 
 

@@ -1,7 +1,8 @@
 """Shared helpers for the GPU parity tests: moving generator output to the
 device, reading results back, and the tolerance checks (bf16 outputs:
 |gpu - ref| <= 2e-2 + 1e-2 |ref|; fp32 outputs: |gpu - ref| <= 1e-4; FP8
-codes: ordered-code distance <= 1; per-row scales: relative error <= 1e-3)."""
+codes: ordered-code distance <= 1; per-row scales: relative error <= 1e-3;
+block-scaled codes: see ``assert_quant_close``)."""
 import numpy as np
 import torch
 
@@ -61,3 +62,66 @@ def sample_rows(M: int, extra: int = 4, seed: int = 0) -> np.ndarray:
     rows = {0, 1, 127, 128, M - 1, M // 2, min(M - 1, 129)}
     rows |= set(rng.integers(0, M, size=extra).tolist())
     return np.array(sorted(r for r in rows if 0 <= r < M), dtype=np.int64)
+
+
+def ordered_nibble(codes: np.ndarray, fmt: int) -> np.ndarray:
+    """4-bit codes (already unpacked) as integers ordered like the values they encode."""
+    c = codes.astype(np.int32) & 15
+    if fmt == 1:  # two's complement INT4
+        return np.where(c & 8, c - 16, c)
+    return np.where(c & 8, -(c & 7), c & 7)  # E2M1: sign bit, then a monotone magnitude index
+
+
+def unpack_nibbles(packed: np.ndarray, n: int) -> np.ndarray:
+    """[rows, ceil(n/2)] bytes -> [rows, n] nibbles; column 2j is the low nibble of byte j."""
+    out = np.empty((packed.shape[0], 2 * packed.shape[1]), dtype=np.uint8)
+    out[:, 0::2] = packed & 15
+    out[:, 1::2] = packed >> 4
+    return out[:, :n]
+
+
+def assert_quant_close(fmt: int, codes, scales, q_ref, s_ref, y_ref, decode, what=""):
+    """Block-scaled output against the oracle.
+
+    Scales: fp32 scales within 1e-3 relative; NVFP4's E4M3 scale codes within one
+    code step and equal for at least 98% of the blocks.  Codes: in blocks whose
+    scale code agrees, within one code step of the oracle's, and equal for at
+    least 98% of all values.  Every value, dequantised with the kernel's own
+    scale, lies within half the format's largest gap of the exact output
+    (``decode`` maps codes to the values they stand for).
+    """
+    n = y_ref.shape[1]
+    bs = {0: 128, 1: 32, 2: 16}[fmt]
+    blk = np.arange(n) // bs
+    if fmt == 0:
+        oc, orf = ordered_e4m3(codes), ordered_e4m3(q_ref)
+        same_scale = np.ones(scales.shape, dtype=bool)
+        s_val = scales.astype(np.float64)
+    else:
+        oc = ordered_nibble(unpack_nibbles(codes, n), fmt)
+        orf = ordered_nibble(unpack_nibbles(q_ref, n), fmt)
+        if fmt == 2:
+            ds = np.abs(ordered_e4m3(scales) - ordered_e4m3(s_ref.astype(np.uint8)))
+            assert ds.max() <= 1, f"{what}: scale code distance {ds.max()}"
+            assert np.mean(ds != 0) < 0.02, f"{what}: {np.mean(ds != 0):.3%} of scale codes differ"
+            same_scale = ds == 0
+            s_val = decode["scale"](scales)
+        else:
+            same_scale = np.ones(scales.shape, dtype=bool)
+            s_val = scales.astype(np.float64)
+    if fmt != 2:
+        rel = np.abs(s_val - s_ref) / np.maximum(np.abs(s_ref), 1e-30)
+        assert rel.max() <= SCALE_RTOL, f"{what}: scale rel err {rel.max():.3g}"
+    d = np.abs(oc - orf)
+    mask = same_scale[:, blk]
+    assert d[mask].max(initial=0) <= 1, f"{what}: code distance {d[mask].max()}"
+    assert np.mean(d != 0) < 0.02, f"{what}: {np.mean(d != 0):.3%} of codes differ"
+    deq = decode["value"](codes if fmt == 0 else unpack_nibbles(codes, n)) * s_val[:, blk]
+    half_gap = {0: None, 1: 0.5, 2: 1.0}[fmt]
+    if fmt == 0:  # E4M3: relative half-step 2^-4, subnormal half-step 2^-10 (times the scale)
+        bound = 2.0 ** -4 * np.abs(y_ref) + 2.0 ** -10 * s_val[:, blk]
+    else:
+        bound = half_gap * s_val[:, blk]
+    err = np.abs(deq - y_ref)
+    slack = 1e-5 * np.abs(y_ref).max(initial=0) + 1e-12
+    assert np.all(err <= bound + slack), f"{what}: dequantised error {np.max(err - bound):.3g} over the bound"

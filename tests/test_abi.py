@@ -70,3 +70,14 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
                                                  a, 1 << 20, None) == fl.FL_ERR_INVALID_ARG
     assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, a, f(1e-6), a, a, 8, 24, 8, 8, 8, 24, 24,
                                                  a, 1 << 20, None) == fl.FL_ERR_ALIGNMENT
+
+
+def test_quant_rejects_bad_arguments_on_host(lib):
+    a = P(0x10000)
+    # unknown format, odd N for a 4-bit format, short scale pitch, code pitch not a multiple of 16
+    assert lib.fused_linear_quant(a, a, None, a, a, 8, 32, 16, 16, 16, 32, 4, 3, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_quant(a, a, None, a, a, 8, 33, 16, 16, 16, 32, 4, 1, None) == fl.FL_ERR_UNSUPPORTED
+    assert lib.fused_linear_quant(a, a, None, a, a, 8, 256, 16, 16, 16, 128, 7, 1, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_quant(a, a, None, a, a, 8, 264, 16, 16, 16, 264, 3, 0, None) == fl.FL_ERR_ALIGNMENT
+    assert lib.fused_linear_quant(a, a, None, a, None, 8, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_quant(None, None, None, None, None, 0, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_OK

@@ -12,8 +12,8 @@ import torch
 import gemm_epilogue_tcgen05_gb300 as fl
 import oracle
 import synthetic as syn
-from parity_utils import (assert_bf16_close, assert_f32_close, assert_fp8_close, dev_bf16, dev_f32, f64, host,
-                          sample_rows)
+from parity_utils import (assert_bf16_close, assert_f32_close, assert_fp8_close, assert_quant_close, dev_bf16,
+                          dev_f32, f64, host, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -378,3 +378,63 @@ def test_cross_entropy_full_workload_sampled():
     rows = sample_rows(w.M, extra=2)
     ref = oracle.linear_cross_entropy(f64(ops["X"][rows]), f64(ops["W"]), None, lab[rows])
     _assert_loss_close(loss.cpu().numpy()[rows].astype(np.float64), ref, "ce full")
+
+
+# ------------------------------------------------------------------ block-scaled quantised write-back
+def _quant_decoders():
+    e2m1 = np.array([oracle.e2m1_decode(c) for c in range(16)])
+    return {"value_fp8": lambda c: oracle.e4m3_decode(c),
+            "value_4bit": lambda c: e2m1[c],
+            "scale": lambda c: oracle.e4m3_decode(c)}
+
+
+def _check_quant(fmt, Yq, S, X, W, b, what):
+    q_ref, s_ref, y_ref = oracle.linear_quant(f64(X), f64(W), None if b is None else f64(b), fmt)
+    d = _quant_decoders()
+    dec = {"scale": d["scale"]}
+    if fmt == fl.QUANT_FP8_1X128:
+        dec["value"] = d["value_fp8"]
+    elif fmt == fl.QUANT_INT4_G32:
+        dec["value"] = lambda c: np.where(c & 8, c.astype(np.int32) - 16, c).astype(np.float64)
+    else:
+        dec["value"] = d["value_4bit"]
+    assert_quant_close(fmt, Yq.cpu().numpy(), S.cpu().numpy(), q_ref, s_ref, y_ref, dec, what)
+
+
+@pytest.mark.parametrize("pairing", [True, False])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (1, 64, 40), (257, 1024, 136)])
+def test_quant_small(fmt, pairing, M, N, K):
+    fl.set_cta_pairing(pairing)
+    X = _draw((M, K), syn.STREAM_X)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5)
+    b = _draw((N,), syn.STREAM_B, 0.5)
+    X[M // 2] = 0  # with no bias below, an all-zero row: scale 0, codes 0
+    for bias in (b, None):
+        Yq, S = fl.fused_linear_quant(dev_bf16(X), dev_bf16(W), None if bias is None else dev_bf16(bias), fmt)
+        _check_quant(fmt, Yq, S, X, W, bias, f"quant fmt {fmt} {M}x{N}x{K} bias={bias is not None}")
+    if M > 2:
+        assert torch.count_nonzero(Yq[M // 2]) == 0 and torch.count_nonzero(S[M // 2]) == 0
+
+
+def test_quant_rejects_odd_n_for_4bit_and_bad_format():
+    X = dev_bf16(_draw((8, 16), syn.STREAM_X))
+    W = dev_bf16(_draw((33, 16), syn.STREAM_W))
+    Yq = torch.empty((8, 32), dtype=torch.uint8, device="cuda")
+    S = torch.empty((8, 4), dtype=torch.float32, device="cuda")
+    with pytest.raises(fl.FusedLinearError) as e:
+        fl.fused_linear_quant(X, W, None, fl.QUANT_INT4_G32, Yq=Yq[:, :16], scales=S)
+    assert e.value.status == fl.FL_ERR_UNSUPPORTED
+    st = fl.load().fused_linear_quant(None, None, None, None, None, 8, 32, 16, 16, 16, 32, 4, 7, None)
+    assert st == fl.FL_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["quant_fp8_1x128_8192x16384x4096", "quant_int4_g32_8192x16384x4096",
+                                  "quant_nvfp4_g16_8192x16384x4096"])
+def test_quant_full_workload_sampled(name):
+    w = syn.WORKLOADS[name]
+    fmt = {"fp8_1x128": 0, "int4_g32": 1, "nvfp4_g16": 2}[w.quant]
+    ops = syn.make_operands(w)
+    Yq, S = fl.fused_linear_quant(dev_bf16(ops["X"]), dev_bf16(ops["W"]), dev_bf16(ops["b"]), fmt)
+    rows = sample_rows(w.M, extra=2)
+    _check_quant(fmt, Yq[rows], S[rows], ops["X"][rows], ops["W"], ops["b"], name)
