@@ -54,6 +54,7 @@ def _lib():
         "orc_residual_rmsnorm_linear": [P, L, P, P, P, P, L, L, D, P, P, L, P, P],
         "orc_linear_cross_entropy": [P, L, P, P, L, L, P, P],
         "orc_linear_quant": [P, L, P, P, L, L, I, P, P, P],
+        "orc_qkv_rope_kv_fp8": [P, L, P, P, L, L, L, L, D, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -240,3 +241,22 @@ def linear_quant(X, W, b, fmt):
     y = np.empty((r, N), dtype=np.float64)
     _lib().orc_linear_quant(_ptr(X), r, _ptr(W), _ptr(b), N, K, int(fmt), _ptr(q), _ptr(sc), _ptr(y))
     return q, sc, y
+
+
+def qkv_rope_kv_fp8(X, Wqkv, bqkv, n_heads, n_kv_heads, head_dim, theta, pos):
+    """QKV + RoPE with K and V quantised to E4M3 per (row, kv head).
+
+    Returns dict with q (fp64 [r, H*D]), kq / vq (uint8 [r, Hkv*D]), ks / vs (fp64 [r, Hkv])
+    and kv (fp64 [r, 2*Hkv*D], the unquantised rotated K then V).
+    """
+    X, Wqkv, bqkv = _f64(X), _f64(Wqkv), _f64(bqkv)
+    pos = _f64(np.asarray(pos))
+    r, K = X.shape
+    qw, kvw = n_heads * head_dim, n_kv_heads * head_dim
+    assert Wqkv.shape[0] == qw + 2 * kvw
+    out = {"q": np.empty((r, qw)), "kq": np.empty((r, kvw), dtype=np.uint8), "ks": np.empty((r, n_kv_heads)),
+           "vq": np.empty((r, kvw), dtype=np.uint8), "vs": np.empty((r, n_kv_heads)), "kv": np.empty((r, 2 * kvw))}
+    _lib().orc_qkv_rope_kv_fp8(_ptr(X), r, _ptr(Wqkv), _ptr(bqkv), K, int(n_heads), int(n_kv_heads), int(head_dim),
+                               float(theta), _ptr(pos), _ptr(out["q"]), _ptr(out["kq"]), _ptr(out["ks"]),
+                               _ptr(out["vq"]), _ptr(out["vs"]), _ptr(out["kv"]))
+    return out

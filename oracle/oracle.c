@@ -338,6 +338,60 @@ void orc_linear_quant(const double* X, long nrows, const double* W, const double
     }
 }
 
+/* ---- QKV projection + RoPE with the K/V cache written in FP8 -------------
+ * [E] §一个瓦片的字节账 (the decode K/V write-back quantised to FP8 in the epilogue,
+ * halving its bytes) with the scale of [E] §仿射量化与尾声的五步 taken over one
+ * head's head_dim values of one token (a 1 x head_dim block; head_dim 128 gives
+ * the 1 x 128 blocks of fine-grained FP8 scaling).
+ * Widths: Q = n_heads * head_dim, K = V = n_kv_heads * head_dim (grouped-query
+ * attention when n_kv_heads < n_heads); the rows of Wqkv are [Q | K | V].
+ * Q and K are rotated as in orc_qkv_rope ([T] §QKV投影融合, adjacent pairs);
+ * V is not.  Q stays unquantised (fp64 out).  For K and V, per (row, kv head):
+ * s = max|y| / 448 over the head, codes e4m3(y / s); a head whose maximum is 0
+ * gets s = 0 and zero codes.
+ * Outputs: q [nrows, n_heads*head_dim] fp64; kq, vq [nrows, n_kv_heads*head_dim]
+ * E4M3 codes; ks, vs [nrows, n_kv_heads] scales; kv [nrows, 2*n_kv_heads*head_dim]
+ * the unquantised rotated K then V (for error bounds in the tests). */
+void orc_qkv_rope_kv_fp8(const double* X, long nrows, const double* Wqkv, const double* bqkv, long K,
+                         long n_heads, long n_kv_heads, long head_dim, double theta, const double* pos,
+                         double* q, uint8_t* kq, double* ks, uint8_t* vq, double* vs, double* kv) {
+    const long qw = n_heads * head_dim, kvw = n_kv_heads * head_dim;
+    const long width = qw + 2 * kvw;
+    double* row = (double*)malloc((size_t)width * sizeof(double));
+    for (long i = 0; i < nrows; ++i) {
+        const double* x = X + (size_t)i * (size_t)K;
+#pragma omp parallel for schedule(static)
+        for (long c = 0; c < width; ++c) row[c] = linear_at(x, Wqkv, bqkv, K, c);
+        /* rotate every adjacent pair of the Q and K sections */
+        for (long c = 0; c < qw + kvw; c += 2) {
+            const long d = (c < qw ? c : c - qw) % head_dim;
+            double y0, y1;
+            orc_rope_rotate(row[c], row[c + 1], orc_rope_angle(pos[i], d / 2, head_dim, theta), &y0, &y1);
+            row[c] = y0;
+            row[c + 1] = y1;
+        }
+        for (long c = 0; c < qw; ++c) q[(size_t)i * (size_t)qw + (size_t)c] = row[c];
+        for (long c = 0; c < 2 * kvw; ++c) kv[(size_t)i * (size_t)(2 * kvw) + (size_t)c] = row[qw + c];
+        for (long sec = 0; sec < 2; ++sec) {
+            const double* y = row + qw + sec * kvw;
+            uint8_t* codes = (sec == 0 ? kq : vq) + (size_t)i * (size_t)kvw;
+            double* scale = (sec == 0 ? ks : vs) + (size_t)i * (size_t)n_kv_heads;
+            for (long h = 0; h < n_kv_heads; ++h) {
+                double amax = 0.0;
+                for (long d = 0; d < head_dim; ++d) {
+                    const double a = fabs(y[h * head_dim + d]);
+                    amax = a > amax ? a : amax;
+                }
+                const double sc = amax / 448.0;
+                scale[h] = sc;
+                for (long d = 0; d < head_dim; ++d)
+                    codes[h * head_dim + d] = sc > 0.0 ? (uint8_t)orc_e4m3_encode(y[h * head_dim + d] / sc) : 0;
+            }
+        }
+    }
+    free(row);
+}
+
 /* Number of OpenMP threads the parallel loops above use. */
 int orc_num_threads(void) {
     int n = 1;

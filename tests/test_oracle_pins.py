@@ -395,3 +395,43 @@ def test_quant_formats_round_trip_and_layout():
     # a zero block gives scale 0 and zero codes
     q0, s0, _ = oracle.linear_quant(np.zeros((1, K)), W, None, oracle.QUANT_INT4_G32)
     assert not q0.any() and not s0.any()
+
+
+def test_qkv_rope_kv_fp8_against_complex_rotation_and_e4m3_bounds():
+    """GQA widths (4 query heads, 2 kv heads): Q and K against RoPE as complex
+    multiplication of a numpy projection, V against the projection alone; each
+    (row, kv head) block's maximum encodes to +-448 and its dequantised values
+    lie within half an E4M3 step; an all-zero head gets scale 0 and zero codes."""
+    rng = np.random.default_rng(11)
+    M, K, H, Hkv, D = 6, 40, 4, 2, 16
+    X = rng.standard_normal((M, K))
+    X[3] = 0.0
+    W = rng.standard_normal(((H + 2 * Hkv) * D, K)) / math.sqrt(K)
+    b = rng.standard_normal((H + 2 * Hkv) * D) * 0.02
+    b[H * D + Hkv * D:H * D + Hkv * D + D] = 0.0  # V head 0 of the zero row stays exactly 0
+    pos = np.array([0, 1, 7, 2047, 300, 5])
+    o = oracle.qkv_rope_kv_fp8(X, W, b, H, Hkv, D, 10000.0, pos)
+    P = X @ W.T + b
+    qw, kvw = H * D, Hkv * D
+    np.testing.assert_allclose(o["q"], _rope_torch_complex(P[:, :qw], pos, D, 1e4), rtol=0, atol=1e-12)
+    k_ref = _rope_torch_complex(P[:, qw:qw + kvw], pos, D, 1e4)
+    v_ref = P[:, qw + kvw:]
+    np.testing.assert_allclose(o["kv"], np.concatenate([k_ref, v_ref], axis=1), rtol=0, atol=1e-12)
+    for codes, scale, ref in ((o["kq"], o["ks"], k_ref), (o["vq"], o["vs"], v_ref)):
+        blocks = ref.reshape(M, Hkv, D)
+        amax = np.abs(blocks).max(axis=2)
+        np.testing.assert_allclose(scale, amax / 448.0, rtol=1e-15, atol=0)
+        deq = oracle.e4m3_decode(codes).reshape(M, Hkv, D) * scale[:, :, None]
+        bound = 2.0 ** -4 * np.abs(blocks) + 2.0 ** -10 * scale[:, :, None]
+        assert np.all(np.abs(deq - blocks) <= bound * (1 + 1e-12))
+        c = codes.reshape(M, Hkv, D)
+        for i in range(M):
+            for h in range(Hkv):
+                if amax[i, h] > 0:
+                    j = int(np.argmax(np.abs(blocks[i, h])))
+                    assert c[i, h, j] == (0x7E if blocks[i, h, j] > 0 else 0xFE)
+    assert o["vs"][3, 0] == 0.0 and not o["vq"][3, :D].any()
+    # the pages' K/V byte ledger for one token of an 8-kv-head, head_dim-128 model:
+    # 4096 bytes per layer in bf16, 2048 in FP8; 64 KiB over 32 layers
+    kv_bytes_fp8 = 2 * 8 * 128 * np.dtype(np.uint8).itemsize
+    assert (kv_bytes_fp8, 2 * kv_bytes_fp8, 32 * kv_bytes_fp8) == (2048, 4096, 64 * 1024)
