@@ -182,6 +182,14 @@ class Case:
             dm = w.n_heads * w.head_dim
             self.out = tuple(torch.empty((w.M, dm), dtype=torch.bfloat16, device="cuda") for _ in range(3))
             self.flops = 2.0 * w.M * w.N * w.K
+        elif w.kind == "qkv_fp8kv":
+            dq, dkv = w.n_heads * w.head_dim, w.n_kv_heads * w.head_dim
+            self.out = (torch.empty((w.M, dq), dtype=torch.bfloat16, device="cuda"),
+                        torch.empty((w.M, dkv), dtype=torch.uint8, device="cuda"),
+                        torch.empty((w.M, dkv), dtype=torch.uint8, device="cuda"),
+                        torch.empty((w.M, w.n_kv_heads), dtype=torch.float32, device="cuda"),
+                        torch.empty((w.M, w.n_kv_heads), dtype=torch.float32, device="cuda"))
+            self.flops = 2.0 * w.M * w.N * w.K
         elif w.kind == "swiglu":
             self.out = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
             self.flops = 2.0 * w.M * (2 * w.N) * w.K
@@ -221,7 +229,7 @@ class Case:
             return float(b + 2 * w.M * w.N)
         if w.kind == "cross_entropy":
             return float(b + 4 * w.M + 4 * w.M)  # + labels in, loss out
-        if w.kind == "quant":
+        if w.kind in ("quant", "qkv_fp8kv"):
             return float(b + sum(t.numel() * t.element_size() for t in self.out))
         if w.kind == "rms_chain":
             # h2 is written by the first GEMM and read by the second; y is written once
@@ -236,6 +244,9 @@ class Case:
         elif w.kind == "qkv_rope":
             fl.fused_qkv_rope(d["X"], d["W"], d.get("b"), n_heads=w.n_heads, head_dim=w.head_dim,
                               seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
+        elif w.kind == "qkv_fp8kv":
+            fl.fused_qkv_rope_fp8kv(d["X"], d["W"], d.get("b"), n_heads=w.n_heads, n_kv_heads=w.n_kv_heads,
+                                    head_dim=w.head_dim, seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
         elif w.kind == "swiglu":
             fl.fused_swiglu(d["X"], d["Wgate"], d["Wup"], d.get("bgate"), d.get("bup"), Y=self.out, stream=stream)
         elif w.kind == "cross_entropy":
@@ -306,6 +317,28 @@ def unfused_fn(case: Case):
             h = F.linear(d["X"], d["W"])
             return rope(h[:, :dm]), rope(h[:, dm:2 * dm]), h[:, 2 * dm:].contiguous()
         return fn
+    if w.kind == "qkv_fp8kv":
+        dq, dkv, hd = w.n_heads * w.head_dim, w.n_kv_heads * w.head_dim, w.head_dim
+        pos = torch.arange(w.M, device="cuda") % w.seq_len
+        inv = w.theta ** (-torch.arange(0, hd, 2, device="cuda", dtype=torch.float32) / hd)
+        ang = pos[:, None].float() * inv[None, :]
+        cos_q, sin_q = ang.cos().repeat(1, w.n_heads), ang.sin().repeat(1, w.n_heads)
+        cos_k, sin_k = ang.cos().repeat(1, w.n_kv_heads), ang.sin().repeat(1, w.n_kv_heads)
+
+        def rot(t, c, s):
+            x0, x1 = t[:, 0::2], t[:, 1::2]
+            return torch.stack((x0 * c - x1 * s, x0 * s + x1 * c), dim=-1).reshape(t.shape)
+
+        def fp8_heads(t):
+            g = t.view(w.M, -1, hd)
+            sc = g.abs().amax(dim=2, keepdim=True) / 448.0
+            return (g / torch.where(sc > 0, sc, 1.0)).to(torch.float8_e4m3fn).view(w.M, -1), sc.view(w.M, -1)
+
+        def fn_kv():
+            h = F.linear(d["X"], d["W"]).float()
+            q = rot(h[:, :dq], cos_q, sin_q).to(torch.bfloat16)
+            return (q,) + fp8_heads(rot(h[:, dq:dq + dkv], cos_k, sin_k)) + fp8_heads(h[:, dq + dkv:])
+        return fn_kv
     if w.kind == "swiglu":
         return lambda: F.silu(F.linear(d["X"], d["Wgate"])) * F.linear(d["X"], d["Wup"])
     if w.kind == "cross_entropy":
@@ -461,6 +494,9 @@ def oracle_sample(w, rows: int):
         oracle.qkv_rope(f["X"], f["W"], f.get("b"), w.n_heads, w.head_dim, w.theta, np.arange(rows) % w.seq_len)
     elif w.kind == "swiglu":
         oracle.swiglu(f["X"], f["Wgate"], f["Wup"], f.get("bgate"), f.get("bup"))
+    elif w.kind == "qkv_fp8kv":
+        oracle.qkv_rope_kv_fp8(f["X"], f["W"], f.get("b"), w.n_heads, w.n_kv_heads, w.head_dim, w.theta,
+                               np.arange(rows) % w.seq_len)
     elif w.kind == "quant":
         oracle.linear_quant(f["X"], f["W"], f.get("b"), QUANT_FMT[w.quant])
     elif w.kind == "cross_entropy":
@@ -553,7 +589,7 @@ def main():
 
     rows = []
     if args.rows == "all":
-        for name in ("qkv_rope_8192x12288x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
+        for name in ("qkv_rope_8192x12288x4096", "qkv_fp8kv_8192x6144x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
                      "rmsnorm_fp8_decode_32x4096x14336", "rms_chain_8192x4096x4096_to_14336",
                      "lm_head_ce_8192x32768x4096", "quant_fp8_1x128_8192x16384x4096",
                      "quant_int4_g32_8192x16384x4096", "quant_nvfp4_g16_8192x16384x4096"):

@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
     lib.fused_linear_rms_rowscale.restype = I
     lib.fused_linear_cross_entropy.argtypes = [P, P, P, P, P, P, I, I, I, I64, I64, I64, P, SZ, P]
     lib.fused_linear_cross_entropy.restype = I
+    lib.fused_qkv_rope_fp8kv.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I64, I64, I64, I64, I64, P]
+    lib.fused_qkv_rope_fp8kv.restype = I
     lib.fused_linear_quant.argtypes = [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, P]
     lib.fused_linear_quant.restype = I
     lib.fl_cross_entropy_workspace_bytes.argtypes = [I, I]
@@ -182,6 +184,45 @@ def fused_qkv_rope(X, Wqkv, bqkv=None, n_heads: int = 32, head_dim: int = 128, s
                                lds.pop(), _stream(stream))
     _check("fused_qkv_rope", st)
     return Q, Ko, V
+
+
+def fused_qkv_rope_fp8kv(X, Wqkv, bqkv=None, n_heads: int = 32, n_kv_heads: int = 8, head_dim: int = 128,
+                         seq_len: int = 2048, theta: float = 10000.0, positions=None, out=None, stream=None):
+    """QKV + RoPE with the K/V cache entry in FP8; returns (Q, Kq, Vq, k_scale, v_scale).
+
+    Q bf16 [M, n_heads*head_dim] (rotated); Kq (rotated) and Vq E4M3 bytes
+    [M, n_kv_heads*head_dim]; k_scale, v_scale fp32 [M, n_kv_heads].
+    """
+    M, K = X.shape
+    dq, dkv = n_heads * head_dim, n_kv_heads * head_dim
+    _mat(X, "X", torch.bfloat16)
+    _mat(Wqkv, "Wqkv", torch.bfloat16)
+    _vec(bqkv, "bqkv", torch.bfloat16, dq + 2 * dkv)
+    if positions is not None and (positions.dtype != torch.int32 or positions.numel() != M
+                                  or not positions.is_cuda or not positions.is_contiguous()):
+        raise ValueError("positions must be a contiguous int32 CUDA vector of length M")
+    if out is None:
+        out = (torch.empty((M, dq), dtype=torch.bfloat16, device=X.device),
+               torch.empty((M, dkv), dtype=torch.uint8, device=X.device),
+               torch.empty((M, dkv), dtype=torch.uint8, device=X.device),
+               torch.empty((M, n_kv_heads), dtype=torch.float32, device=X.device),
+               torch.empty((M, n_kv_heads), dtype=torch.float32, device=X.device))
+    Q, Kq, Vq, ks, vs = out
+    _mat(Q, "Q", torch.bfloat16)
+    for t, nm in ((Kq, "Kq"), (Vq, "Vq")):
+        _mat(t, nm, torch.uint8)
+    for t, nm in ((ks, "k_scale"), (vs, "v_scale")):
+        _mat(t, nm, torch.float32)
+    ldkv = {_ld(Kq, dkv, dkv), _ld(Vq, dkv, dkv)}
+    lds = {_ld(ks, n_kv_heads, n_kv_heads), _ld(vs, n_kv_heads, n_kv_heads)}
+    if len(ldkv) != 1 or len(lds) != 1:
+        raise ValueError("Kq and Vq (and their scales) must share one leading dimension")
+    st = load().fused_qkv_rope_fp8kv(_ptr(X), _ptr(Wqkv), _ptr(bqkv), _ptr(Q), _ptr(Kq), _ptr(Vq), _ptr(ks),
+                                     _ptr(vs), _ptr(positions), M, K, n_heads, n_kv_heads, head_dim, seq_len,
+                                     float(theta), _ld(X, K, K), _ld(Wqkv, K, K), _ld(Q, dq, dq), ldkv.pop(),
+                                     lds.pop(), _stream(stream))
+    _check("fused_qkv_rope_fp8kv", st)
+    return Q, Kq, Vq, ks, vs
 
 
 def fused_swiglu(X, Wgate, Wup, bgate=None, bup=None, Y=None, stream=None):

@@ -33,7 +33,8 @@ enum EpiKind : int {
   EPI_RESID_GAMMA = 5,  // h1 = acc + b + z; stores h1 (optional) and h1 * gamma; per-row partial sum h1^2
   EPI_ROWSCALE = 6,     // y = r * acc + b with r = 1/sqrt(sum of the row's partials / n + eps)
   EPI_CE = 7,           // per-row online log-sum-exp state + label logit; last tile of a row block merges
-  EPI_QUANT = 8         // block-scaled quantised write-back: FP8 1x128, INT4 g32 or NVFP4 g16 + scales
+  EPI_QUANT = 8,        // block-scaled quantised write-back: FP8 1x128, INT4 g32 or NVFP4 g16 + scales
+  EPI_QKV_FP8KV = 9     // QKV + RoPE, Q in bf16, K and V as E4M3 with one scale per token and kv head
 };
 enum QuantFmt : int { QF_FP8_1X128 = 0, QF_INT4_G32 = 1, QF_NVFP4_G16 = 2 };
 
@@ -51,7 +52,7 @@ struct alignas(128) GemmParams {
   // QKV + RoPE
   const int* positions;
   int seq_len, head_dim, d_model;
-  float log2_theta;
+  double log2_theta;
   // residual + RMSNorm + FP8
   const __nv_bfloat16* resid;
   long long ldz;
@@ -71,6 +72,10 @@ struct alignas(128) GemmParams {
   int quant_fmt;
   void* qscale;            // fp32 [M][lds] (FP8, INT4) or E4M3 bytes [M][lds] (NVFP4)
   long long lds;
+  // QKV with an FP8 K/V cache: K/V section width (n_kv_heads * head_dim) and their scales [M][lds]
+  int kv_width;
+  float* kscale;
+  float* vscale;
   unsigned* counters;      // [2][num_m_blocks]: arrivals, finished readers
   int* status;
   unsigned long long timeout_ns;
@@ -151,6 +156,21 @@ __device__ __forceinline__ void tmem_load32f(uint32_t taddr, bool zero, float (&
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// sin and cos of the RoPE angle pos * f for an integer-valued position (exact in fp32) and a
+// frequency held as two floats f = hi + lo.  The product is carried exactly (FMA residual),
+// reduced modulo 2 pi by Cody and Waite's method (2 pi split into two floats, one FMA per
+// part) and only the reduced angle is rounded, so large positions keep the angle accurate
+// to a few fp32 ulps instead of pos * 2^-24.
+__device__ __forceinline__ void rope_sincos(float pos, float hi, float lo, float& sn, float& cs) {
+  const float p = pos * hi;
+  const float e = fmaf(pos, hi, -p);     // pos * hi - p, exactly
+  const float t = fmaf(pos, lo, e);      // the small part of the angle
+  const float k = rintf(p * 0.159154943091895336f);  // nearest multiple of 2 pi
+  float r = fmaf(-k, 6.28318548202514648f, p);         // 2 pi rounded to fp32 ...
+  r = fmaf(-k, -1.74845553146951657e-07f, r);          // ... and the remainder 2 pi - that
+  sincosf(r + t, &sn, &cs);
+}
+
 __device__ __forceinline__ float gelu_tanh_f(float v) {
   // 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
   const float u = v * fmaf(0.0356774081363f, v * v, 0.7978845608028654f);
@@ -197,6 +217,14 @@ struct StoreRing {
     if (lane == 0) bulk_wait_read<1>();
     __syncwarp();
     return base + (count & 1) * kStagingBytes;
+  }
+  // Both staging buffers at once (every earlier store has finished reading them); the
+  // caller commits the first, then the second.
+  __device__ __forceinline__ void acquire_pair(int lane, uint32_t& first, uint32_t& second) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+    first = base + (count & 1) * kStagingBytes;
+    second = base + ((count + 1) & 1) * kStagingBytes;
   }
   // Publishes the staged box to the async proxy and stores it at (x, y).
   __device__ __forceinline__ void commit(const CUtensorMap* map, uint32_t buf, int lane, int x, int y) {
@@ -246,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);  // written by the epilogue leader only
   volatile int* ce_last = reinterpret_cast<volatile int*>(tmem_slot + 3);   // idem: this tile merges its row block
-  float* inv_freq = reinterpret_cast<float*>(tmem_slot + 4);  // [64], QKV only
+  // QKV only: RoPE frequency of pair i as two floats, inv_freq[i] + inv_freq[64 + i]
+  float* inv_freq = reinterpret_cast<float*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -284,9 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
       tmem_relinquish();
     }
   }
-  if (EPI == EPI_QKV_ROPE && threadIdx.x >= 64 && threadIdx.x < 128) {
+  if ((EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV) && threadIdx.x >= 64 && threadIdx.x < 128) {
     const int i = threadIdx.x - 64;  // pair index within a head (head_dim 128 -> 64 pairs)
-    inv_freq[i] = exp2f(-(2.f * static_cast<float>(i) / static_cast<float>(p.head_dim)) * p.log2_theta);
+    const double f = exp2(-(2.0 * i / p.head_dim) * p.log2_theta);  // theta^(-2i/head_dim)
+    const float hi = static_cast<float>(f);
+    inv_freq[i] = hi;
+    inv_freq[64 + i] = static_cast<float>(f - static_cast<double>(hi));
   }
   tc_fence_before();
   if constexpr (CG == 2) {
@@ -441,20 +473,146 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * T::kMmaN;
 
-      if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF || EPI == EPI_QKV_ROPE) {
+      if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF || EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV) {
         if (!ok) break;
+        constexpr bool kQkv = EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV;
         int n0 = nb * T::kOutN;  // first output column of the tile
-        int sec = 0;
+        int sec = 0, base = 0;
         float pos = 0.f;
-        if constexpr (EPI == EPI_QKV_ROPE) {
-          sec = n0 / p.d_model;  // 0 = Q, 1 = K, 2 = V (a tile never straddles two sections)
-          n0 -= sec * p.d_model;
+        if constexpr (kQkv) {
+          // 0 = Q, 1 = K, 2 = V (a tile never straddles two sections)
+          if (n0 >= p.d_model) {
+            sec = 1;
+            base = p.d_model;
+            if (n0 >= p.d_model + p.kv_width) {
+              sec = 2;
+              base += p.kv_width;
+            }
+          }
+          n0 -= base;
           const int pi = row_ok ? (p.positions ? __ldg(p.positions + m) : m % p.seq_len) : 0;
           pos = static_cast<float>(pi);
         }
-        const int n_limit = (EPI == EPI_QKV_ROPE) ? p.d_model : p.N;
-        const __nv_bfloat16* bias =
-            p.bias ? p.bias + (EPI == EPI_QKV_ROPE ? sec * p.d_model : 0) : nullptr;
+        const int n_limit = kQkv ? (sec == 0 ? p.d_model : p.kv_width) : p.N;
+        const __nv_bfloat16* bias = p.bias ? p.bias + base : nullptr;
+        if constexpr (kQkv) {
+          if (sec == 0 || (EPI == EPI_QKV_ROPE && sec == 1)) {
+            // Rotated bf16 section: the tile's two heads share their angles (same row, same pair
+            // index), so each group of 16 angles is computed once and applied to both heads,
+            // which are staged side by side in the two buffers of the ring.
+#pragma unroll 1
+            for (int c2 = 0; c2 < 2; ++c2) {
+              uint32_t buf0, buf1;
+              ring.acquire_pair(lane, buf0, buf1);
+#pragma unroll 1
+              for (int gg = 0; gg < 2; ++gg) {
+                const int g = c2 * 2 + gg;  // 16-pair group within a head
+                float sn[16], cs[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  rope_sincos(pos, inv_freq[g * 16 + i], inv_freq[64 + g * 16 + i], sn[i], cs[i]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  float v[32], b[32];
+                  tmem_load32f(tacc + h * 128 + g * 32, k_empty, v);
+                  load_vec32(bias, n0 + h * 128 + g * 32, n_limit, b);
+#pragma unroll
+                  for (int j = 0; j < 32; j += 2) {
+                    const float x0 = v[j] + b[j], x1 = v[j + 1] + b[j + 1];
+                    v[j] = x0 * cs[j >> 1] - x1 * sn[j >> 1];
+                    v[j + 1] = x0 * sn[j >> 1] + x1 * cs[j >> 1];
+                  }
+                  stage_bf16_32(h == 0 ? buf0 : buf1, lane, gg, v);
+                }
+              }
+              ring.commit(&p.map_out[sec], buf0, lane, n0 + c2 * 64, y_box);
+              ring.commit(&p.map_out[sec], buf1, lane, n0 + 128 + c2 * 64, y_box);
+            }
+            release_acc(abuf);
+            continue;
+          }
+        }
+        if constexpr (EPI == EPI_QKV_FP8KV) {
+          if (sec > 0) {
+            // K/V cache entry in FP8 ("GEMM Epilogue 完全拆解", §一个瓦片的字节账): per head of
+            // head_dim (= 128) values of this row, K is rotated, scale = max|.|/448 over the
+            // head, and the codes are stored with it.  The two heads of a tile share their
+            // rotation angles (same row, same pair index), so each group of 16 angles serves
+            // both heads: pass 1 takes the heads' maxima, pass 2 reloads the accumulator from
+            // TMEM, rotates again and quantises into one staging buffer per head.  The group
+            // loops stay rolled to keep the kernel's code small.
+            float amax0 = 0.f, amax1 = 0.f;
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+              float sn[16], cs[16];
+              if (sec == 1) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  rope_sincos(pos, inv_freq[g * 16 + i], inv_freq[64 + g * 16 + i], sn[i], cs[i]);
+              }
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                float v[32], b[32];
+                tmem_load32f(tacc + h * 128 + g * 32, k_empty, v);
+                load_vec32(bias, n0 + h * 128 + g * 32, n_limit, b);
+                float am = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                  float x0 = v[j] + b[j], x1 = v[j + 1] + b[j + 1];
+                  if (sec == 1) {
+                    const float r0 = x0 * cs[j >> 1] - x1 * sn[j >> 1];
+                    x1 = x0 * sn[j >> 1] + x1 * cs[j >> 1];
+                    x0 = r0;
+                  }
+                  am = fmaxf(am, fmaxf(fabsf(x0), fabsf(x1)));
+                }
+                if (h == 0) amax0 = fmaxf(amax0, am);
+                else amax1 = fmaxf(amax1, am);
+              }
+            }
+            const float qs0 = amax0 > 0.f ? 448.f / amax0 : 0.f;
+            const float qs1 = amax1 > 0.f ? 448.f / amax1 : 0.f;
+            if (row_ok) {
+              float* sp = (sec == 1 ? p.kscale : p.vscale) + static_cast<long long>(m) * p.lds + (n0 >> 7);
+              if (n0 < n_limit) sp[0] = amax0 * (1.f / 448.f);
+              if (n0 + 128 < n_limit) sp[1] = amax1 * (1.f / 448.f);
+            }
+            uint32_t buf0, buf1;
+            ring.acquire_pair(lane, buf0, buf1);
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+              float sn[16], cs[16];
+              if (sec == 1) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  rope_sincos(pos, inv_freq[g * 16 + i], inv_freq[64 + g * 16 + i], sn[i], cs[i]);
+              }
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                float v[32], b[32];
+                tmem_load32f(tacc + h * 128 + g * 32, k_empty, v);
+                load_vec32(bias, n0 + h * 128 + g * 32, n_limit, b);
+                const float qs = h == 0 ? qs0 : qs1;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                  float x0 = v[j] + b[j], x1 = v[j + 1] + b[j + 1];
+                  if (sec == 1) {
+                    const float r0 = x0 * cs[j >> 1] - x1 * sn[j >> 1];
+                    x1 = x0 * sn[j >> 1] + x1 * cs[j >> 1];
+                    x0 = r0;
+                  }
+                  v[j] = fmaf(x0, qs, 0.f);  // + 0: a rotated -0 codes as 0
+                  v[j + 1] = fmaf(x1, qs, 0.f);
+                }
+                stage_fp8_32(h == 0 ? buf0 : buf1, lane, g, v);
+              }
+            }
+            ring.commit(&p.map_out[sec], buf0, lane, n0, y_box);
+            ring.commit(&p.map_out[sec], buf1, lane, n0 + 128, y_box);
+            release_acc(abuf);
+            continue;
+          }
+        }
 #pragma unroll 1
         for (int c = 0; c < T::kOutN / 64; ++c) {
           const uint32_t buf = ring.acquire(lane);
@@ -472,20 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             } else if constexpr (EPI == EPI_GELU_ERF) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = gelu_erf_f(v[j]);
-            } else {
-              if (sec < 2) {
-                // adjacent pair (2i, 2i+1) of a head, rotated by pos * theta^(-2i/head_dim)
-                const int pair0 = (col0 % p.head_dim) >> 1;
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                  float sn, cs;
-                  sincosf(pos * inv_freq[pair0 + (j >> 1)], &sn, &cs);
-                  const float x0 = v[j], x1 = v[j + 1];
-                  v[j] = x0 * cs - x1 * sn;
-                  v[j + 1] = x0 * sn + x1 * cs;
-                }
-              }
-            }
+            }  // QKV: only the unrotated V section reaches this loop
             stage_bf16_32(buf, lane, u, v);
           }
           ring.commit(&p.map_out[sec], buf, lane, n0 + c * 64, y_box);

@@ -92,6 +92,23 @@ FL_API int fused_qkv_rope(const void* X, const void* Wqkv, const void* bqkv,
                    int M, int K, int n_heads, int head_dim, int seq_len, float theta,
                    int64_t ldx, int64_t ldw, int64_t ldo, void* stream);
 
+/* QKV projection + RoPE whose epilogue writes the K/V cache entry in FP8.
+ *   "GEMM Epilogue 完全拆解", §一个瓦片的字节账 (the K/V write-back quantised to FP8 in
+ *   the epilogue, half the bytes of bf16) with the scale of §仿射量化与尾声的五步 taken
+ *   over one head of one token: s = max|y| / 448 over its head_dim values, codes
+ *   E4M3(y / s) (round to nearest even, saturating); a head whose maximum is 0 gets
+ *   s = 0 and zero codes.
+ * Grouped-query widths: Wqkv [(n_heads + 2 n_kv_heads) * head_dim, K] bf16 with rows
+ * [Q | K | V]; bqkv nullable.  Q [M, n_heads*head_dim] bf16 (rotated, pitch ldq elements);
+ * Kq, Vq [M, n_kv_heads*head_dim] E4M3 bytes (K rotated, V not; pitch ldkv bytes, a
+ * multiple of 16); k_scale, v_scale [M, lds] fp32, one per (token, kv head).
+ * Positions as in fused_qkv_rope.  head_dim must be 128 and n_heads, n_kv_heads even
+ * and non-zero (FL_ERR_UNSUPPORTED otherwise). */
+FL_API int fused_qkv_rope_fp8kv(const void* X, const void* Wqkv, const void* bqkv, void* Q, void* Kq, void* Vq,
+                                float* k_scale, float* v_scale, const int32_t* positions, int M, int K,
+                                int n_heads, int n_kv_heads, int head_dim, int seq_len, float theta,
+                                int64_t ldx, int64_t ldw, int64_t ldq, int64_t ldkv, int64_t lds, void* stream);
+
 /* SwiGLU up-projection: Y = SiLU(X Wgate^T + bgate) * (X Wup^T + bup).
  *   "GEMM Epilogue 完全拆解", §模式 B and §末尾布局调整 (a gate/value pair gives one
  *   value; the output has half the width of the [gate|up] product).

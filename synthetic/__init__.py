@@ -208,7 +208,7 @@ def draw_numpy(seed: int, stream: int, shape, mean: float, std: float, dtype: st
 class Workload:
     """One synthetic workload: shapes, dtype and the distribution of each operand."""
     name: str
-    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain" | "cross_entropy" | "quant"
+    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain" | "cross_entropy" | "quant" | "qkv_fp8kv"
     M: int
     N: int               # output features (QKV: 3*H*D; SwiGLU: d_ff)
     K: int
@@ -222,6 +222,7 @@ class Workload:
     seed: int = 0
     N2: int = 0          # rms_chain: output features of the second GEMM (its K is N)
     quant: str = ""      # quant: "fp8_1x128" | "int4_g32" | "nvfp4_g16"
+    n_kv_heads: int = 0  # qkv_fp8kv: key/value heads (grouped-query attention)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
 
@@ -231,6 +232,9 @@ WORKLOADS = {
     "gelu_tanh_8192x16384x4096": Workload("gelu_tanh_8192x16384x4096", "gelu_tanh", 8192, 16384, 4096),
     "qkv_rope_8192x12288x4096": Workload("qkv_rope_8192x12288x4096", "qkv_rope", 8192, 12288, 4096,
                                          has_bias=False, n_heads=32, head_dim=128, seq_len=2048),
+    # grouped-query QKV (32 query heads, 8 kv heads of 128) writing the K/V cache entry in FP8
+    "qkv_fp8kv_8192x6144x4096": Workload("qkv_fp8kv_8192x6144x4096", "qkv_fp8kv", 8192, 6144, 4096,
+                                         has_bias=False, n_heads=32, n_kv_heads=8, head_dim=128, seq_len=2048),
     "swiglu_8192x14336x4096": Workload("swiglu_8192x14336x4096", "swiglu", 8192, 14336, 4096,
                                        has_bias=False),
     "rmsnorm_fp8_prefill_8192x4096x14336": Workload("rmsnorm_fp8_prefill_8192x4096x14336", "rmsnorm_fp8",

@@ -81,3 +81,19 @@ def test_quant_rejects_bad_arguments_on_host(lib):
     assert lib.fused_linear_quant(a, a, None, a, a, 8, 264, 16, 16, 16, 264, 3, 0, None) == fl.FL_ERR_ALIGNMENT
     assert lib.fused_linear_quant(a, a, None, a, None, 8, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_ERR_INVALID_ARG
     assert lib.fused_linear_quant(None, None, None, None, None, 0, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_OK
+
+
+def test_qkv_fp8kv_rejects_bad_arguments_on_host(lib):
+    a = P(0x10000)
+    f = ctypes.c_float
+    # odd kv head count, head_dim other than 128, short scale pitch, KV pitch not a multiple of 16
+    assert lib.fused_qkv_rope_fp8kv(a, a, None, a, a, a, a, a, None, 8, 64, 2, 1, 128, 16, f(1e4), 64, 64, 256, 128,
+                                    1, None) == fl.FL_ERR_UNSUPPORTED
+    assert lib.fused_qkv_rope_fp8kv(a, a, None, a, a, a, a, a, None, 8, 64, 4, 4, 64, 16, f(1e4), 64, 64, 256, 256,
+                                    4, None) == fl.FL_ERR_UNSUPPORTED
+    assert lib.fused_qkv_rope_fp8kv(a, a, None, a, a, a, a, a, None, 8, 64, 2, 2, 128, 16, f(1e4), 64, 64, 256, 256,
+                                    1, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_qkv_rope_fp8kv(a, a, None, a, a, a, a, a, None, 8, 64, 2, 2, 128, 16, f(1e4), 64, 64, 256, 264,
+                                    2, None) == fl.FL_ERR_ALIGNMENT
+    assert lib.fused_qkv_rope_fp8kv(a, a, None, a, a, a, None, a, None, 8, 64, 2, 2, 128, 16, f(1e4), 64, 64, 256,
+                                    256, 2, None) == fl.FL_ERR_INVALID_ARG

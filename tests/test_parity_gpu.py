@@ -438,3 +438,60 @@ def test_quant_full_workload_sampled(name):
     Yq, S = fl.fused_linear_quant(dev_bf16(ops["X"]), dev_bf16(ops["W"]), dev_bf16(ops["b"]), fmt)
     rows = sample_rows(w.M, extra=2)
     _check_quant(fmt, Yq[rows], S[rows], ops["X"][rows], ops["W"], ops["b"], name)
+
+
+# ------------------------------------------------------------------ QKV + RoPE with an FP8 K/V cache
+def _check_kv_fp8(out, ref, what):
+    Q, Kq, Vq, ks, vs = out
+    assert_bf16_close(host(Q), ref["q"], f"{what}: Q")
+    hd = 128
+    for codes, scale, r_codes, r_scale, exact, nm in ((Kq, ks, ref["kq"], ref["ks"], ref["kv"][:, :Kq.shape[1]], "K"),
+                                                      (Vq, vs, ref["vq"], ref["vs"], ref["kv"][:, Kq.shape[1]:], "V")):
+        c, s = codes.cpu().numpy(), scale.cpu().numpy().astype(np.float64)
+        assert_fp8_close(c, s, r_codes, r_scale, f"{what}: {nm}")
+        heads = np.arange(c.shape[1]) // hd
+        deq = oracle.e4m3_decode(c) * s[:, heads]
+        bound = 2.0 ** -4 * np.abs(exact) + 2.0 ** -10 * s[:, heads] + 1e-5 * np.abs(exact).max()
+        assert np.all(np.abs(deq - exact) <= bound), f"{what}: {nm} dequantised outside the E4M3 half-step"
+
+
+@pytest.mark.parametrize("pairing", [True, False])
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (2, 2)])
+def test_qkv_fp8kv_small(pairing, H, Hkv):
+    fl.set_cta_pairing(pairing)
+    M, K, D = 300, 200, 128
+    X = _draw((M, K), syn.STREAM_X)
+    Wq = _draw(((H + 2 * Hkv) * D, K), syn.STREAM_W, K ** -0.5)
+    bq = _draw(((H + 2 * Hkv) * D,), syn.STREAM_B, 0.5)
+    X[7] = 0  # without bias, row 7's K and V heads are all zero -> scale 0, codes 0
+    pos = np.random.default_rng(2).integers(0, 8192, size=M).astype(np.int32)
+    for bias in (bq, None):
+        out = fl.fused_qkv_rope_fp8kv(dev_bf16(X), dev_bf16(Wq), None if bias is None else dev_bf16(bias), n_heads=H,
+                                      n_kv_heads=Hkv, head_dim=D, positions=torch.from_numpy(pos).cuda())
+        ref = oracle.qkv_rope_kv_fp8(f64(X), f64(Wq), None if bias is None else f64(bias), H, Hkv, D, 1e4, pos)
+        _check_kv_fp8(out, ref, f"qkv fp8kv H={H} Hkv={Hkv} bias={bias is not None}")
+    assert torch.count_nonzero(out[1][7]) == 0 and torch.count_nonzero(out[4][7]) == 0
+    if H == Hkv:  # with as many kv heads as query heads, Q matches the bf16 entry point bit for bit
+        q, _, _ = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, head_dim=D,
+                                    positions=torch.from_numpy(pos).cuda())
+        assert torch.equal(q, out[0])
+
+
+def test_qkv_fp8kv_rejects_odd_heads():
+    X = dev_bf16(_draw((8, 64), syn.STREAM_X))
+    W = dev_bf16(_draw(((2 + 2) * 128, 64), syn.STREAM_W))
+    with pytest.raises(fl.FusedLinearError) as e:
+        fl.fused_qkv_rope_fp8kv(X, W, None, n_heads=2, n_kv_heads=1, head_dim=128)
+    assert e.value.status == fl.FL_ERR_UNSUPPORTED
+
+
+def test_qkv_fp8kv_full_workload_sampled():
+    w = syn.WORKLOADS["qkv_fp8kv_8192x6144x4096"]
+    ops = syn.make_operands(w)
+    out = fl.fused_qkv_rope_fp8kv(dev_bf16(ops["X"]), dev_bf16(ops["W"]), None, n_heads=w.n_heads,
+                                  n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, seq_len=w.seq_len, theta=w.theta)
+    rows = sample_rows(w.M, extra=2)
+    ri = torch.from_numpy(rows).cuda()
+    ref = oracle.qkv_rope_kv_fp8(f64(ops["X"][rows]), f64(ops["W"]), None, w.n_heads, w.n_kv_heads, w.head_dim,
+                                 w.theta, rows % w.seq_len)
+    _check_kv_fp8(tuple(t[ri] for t in out), ref, "qkv fp8kv full")
