@@ -55,12 +55,14 @@ def _lib():
         "orc_linear_cross_entropy": [P, L, P, P, L, L, P, P],
         "orc_linear_quant": [P, L, P, P, L, L, I, P, P, P],
         "orc_qkv_rope_kv_fp8": [P, L, P, P, L, L, L, L, D, P, P, P, P, P, P, P],
+        "orc_dgrad_gelu": [P, L, P, L, L, P, I, P, L, P],
+        "orc_swiglu_bwd": [P, L, P, L, L, P, P, P, L, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
         f.argtypes = args
         f.restype = None
-    for name in ("orc_gelu_erf", "orc_gelu_tanh", "orc_silu"):
+    for name in ("orc_gelu_erf", "orc_gelu_tanh", "orc_silu", "orc_gelu_erf_grad", "orc_gelu_tanh_grad"):
         getattr(lib, name).argtypes = [D]
         getattr(lib, name).restype = D
     lib.orc_rope_angle.argtypes = [D, L, L, D]
@@ -259,4 +261,30 @@ def qkv_rope_kv_fp8(X, Wqkv, bqkv, n_heads, n_kv_heads, head_dim, theta, pos):
     _lib().orc_qkv_rope_kv_fp8(_ptr(X), r, _ptr(Wqkv), _ptr(bqkv), K, int(n_heads), int(n_kv_heads), int(head_dim),
                                float(theta), _ptr(pos), _ptr(out["q"]), _ptr(out["kq"]), _ptr(out["ks"]),
                                _ptr(out["vq"]), _ptr(out["vs"]), _ptr(out["kv"]))
+    return out
+
+
+def gelu_grad(x: float, mode) -> float:
+    """GELU'(x), mode GELU_ERF or GELU_TANH."""
+    f = _lib().orc_gelu_erf_grad if mode == GELU_ERF else _lib().orc_gelu_tanh_grad
+    return f(float(x))
+
+
+def dgrad_gelu(dZ, W, H, mode, cols=None) -> np.ndarray:
+    """(dZ W)[i, n] * GELU'(H[i, n]) with W stored [Kp, N] (the contraction runs over its rows)."""
+    dZ, W, H = _f64(dZ), _f64(W), _f64(H)
+    Kp, N = W.shape
+    c = _cols(cols, N)
+    out = np.empty((dZ.shape[0], len(c)), dtype=np.float64)
+    _lib().orc_dgrad_gelu(_ptr(dZ), dZ.shape[0], _ptr(W), Kp, N, _ptr(H), int(mode), _ptr(c), len(c), _ptr(out))
+    return out
+
+
+def swiglu_bwd(dO, Wd, G, U, cols=None) -> np.ndarray:
+    """Interleaved (dg, du) pairs [r, 2 len(cols)] of SwiGLU's backward with dy = dO Wd, Wd stored [Kp, N]."""
+    dO, Wd, G, U = _f64(dO), _f64(Wd), _f64(G), _f64(U)
+    Kp, N = Wd.shape
+    c = _cols(cols, N)
+    out = np.empty((dO.shape[0], 2 * len(c)), dtype=np.float64)
+    _lib().orc_swiglu_bwd(_ptr(dO), dO.shape[0], _ptr(Wd), Kp, N, _ptr(G), _ptr(U), _ptr(c), len(c), _ptr(out))
     return out

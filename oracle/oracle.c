@@ -392,6 +392,72 @@ void orc_qkv_rope_kv_fp8(const double* X, long nrows, const double* Wqkv, const 
     free(row);
 }
 
+/* ---- Backward epilogues ---------------------------------------------------
+ * [E] §模式 D: for blocks h = x W, x' = f(h) with f acting per element, the
+ * backward pass has the same shape: the gradient w.r.t. the block input is a
+ * GEMM with the weight, and multiplying by f'(h) is an element-wise step that
+ * belongs in the epilogue of the GEMM producing that gradient.
+ * With W stored [n_out, n_in] (one row per output feature, as in orc_linear),
+ * the gradient w.r.t. the input x is dX[m, n] = sum_k dZ[m, k] W[k, n], k over
+ * the n_out outputs: the contraction runs over W's rows. */
+
+/* d/dx of the erf form: Phi(x) + x phi(x), phi(x) = exp(-x^2/2) / sqrt(2 pi). */
+double orc_gelu_erf_grad(double x) {
+    return 0.5 * (1.0 + erf(x / sqrt(2.0))) + x * exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
+}
+
+/* d/dx of the tanh form with u = c (x + a x^3), c = sqrt(2/pi), a = 0.044715:
+ * 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) c (1 + 3 a x^2). */
+double orc_gelu_tanh_grad(double x) {
+    const double c = sqrt(2.0 / M_PI), a = 0.044715;
+    const double t = tanh(c * (x + a * x * x * x));
+    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * c * (1.0 + 3.0 * a * x * x);
+}
+
+/* dgrad with W as stored: acc[i, n] = sum_k dZ[i, k] W[k, n] (k in order). */
+static double dgrad_at(const double* dz_row, const double* W, long Kp, long N, long n) {
+    double s = 0.0;
+    for (long k = 0; k < Kp; ++k) s += dz_row[k] * W[(size_t)k * (size_t)N + (size_t)n];
+    return s;
+}
+
+/* GELU backward fused into the dgrad GEMM: dH[i, n] = (dZ W)[i, n] * GELU'(H[i, n])
+ * (mode 0 = erf form, 1 = tanh form).  dZ [nrows, Kp], W [Kp, N], H [nrows, N] the
+ * saved pre-activation; out [nrows, ncols] at the columns cols. */
+void orc_dgrad_gelu(const double* dZ, long nrows, const double* W, long Kp, long N, const double* H, int mode,
+                    const long* cols, long ncols, double* out) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (long i = 0; i < nrows; ++i)
+        for (long j = 0; j < ncols; ++j) {
+            const long n = cols[j];
+            const double h = H[(size_t)i * (size_t)N + (size_t)n];
+            const double d = mode == 0 ? orc_gelu_erf_grad(h) : orc_gelu_tanh_grad(h);
+            out[i * ncols + j] = dgrad_at(dZ + (size_t)i * (size_t)Kp, W, Kp, N, n) * d;
+        }
+}
+
+/* SwiGLU backward, [E] §末尾布局调整 (SwiGLU 反向): y = SiLU(g) u, so with the upstream
+ * gradient dy = (dO W_down)[i, n] of y,
+ *   dg = dy * u * SiLU'(g),  SiLU'(g) = s (1 + g (1 - s)),  s = 1 / (1 + e^{-g}),
+ *   du = dy * SiLU(g).
+ * One input value gives two outputs: the result is twice as wide, the pair of feature n
+ * at columns 2n (dg) and 2n + 1 (du).  dO [nrows, Kp], Wd [Kp, N], G and U [nrows, N]
+ * the saved gate and up activations; out [nrows, 2 ncols] for the features cols. */
+void orc_swiglu_bwd(const double* dO, long nrows, const double* Wd, long Kp, long N, const double* G,
+                    const double* U, const long* cols, long ncols, double* out) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (long i = 0; i < nrows; ++i)
+        for (long j = 0; j < ncols; ++j) {
+            const long n = cols[j];
+            const double g = G[(size_t)i * (size_t)N + (size_t)n];
+            const double u = U[(size_t)i * (size_t)N + (size_t)n];
+            const double dy = dgrad_at(dO + (size_t)i * (size_t)Kp, Wd, Kp, N, n);
+            const double s = 1.0 / (1.0 + exp(-g));
+            out[i * 2 * ncols + 2 * j] = dy * u * s * (1.0 + g * (1.0 - s));
+            out[i * 2 * ncols + 2 * j + 1] = dy * g * s;
+        }
+}
+
 /* Number of OpenMP threads the parallel loops above use. */
 int orc_num_threads(void) {
     int n = 1;

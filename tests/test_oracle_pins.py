@@ -435,3 +435,61 @@ def test_qkv_rope_kv_fp8_against_complex_rotation_and_e4m3_bounds():
     # 4096 bytes per layer in bf16, 2048 in FP8; 64 KiB over 32 layers
     kv_bytes_fp8 = 2 * 8 * 128 * np.dtype(np.uint8).itemsize
     assert (kv_bytes_fp8, 2 * kv_bytes_fp8, 32 * kv_bytes_fp8) == (2048, 4096, 64 * 1024)
+
+
+@pytest.mark.parametrize("mode", [oracle.GELU_ERF, oracle.GELU_TANH])
+def test_gelu_grad_against_differences_and_autograd(mode):
+    """GELU' against central differences of the (pinned) forward GELU, against torch's
+    fp64 autograd of F.gelu, and at closed-form points."""
+    xs = np.concatenate([np.linspace(-8, 8, 161), [-30.0, -0.3, 1e-3, 30.0]])
+    step = 1e-5
+    fwd = oracle.gelu_erf if mode == oracle.GELU_ERF else oracle.gelu_tanh
+    for x in xs:
+        fd = (fwd(x + step) - fwd(x - step)) / (2 * step)
+        assert oracle.gelu_grad(x, mode) == pytest.approx(fd, abs=1e-8)
+    t = torch.tensor(xs, dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.gelu(t, approximate="none" if mode == oracle.GELU_ERF else "tanh").sum().backward()
+    got = np.array([oracle.gelu_grad(x, mode) for x in xs])
+    # atol: where tanh(u) rounds next to -1 (absolute step 1.1e-16) the derivative's second
+    # term multiplies that rounding by x c (1 + 3 a x^2) ~ 50 near x = -7
+    np.testing.assert_allclose(got, t.grad.numpy(), rtol=1e-13, atol=1e-14)
+    assert oracle.gelu_grad(0.0, mode) == 0.5                      # Phi(0) = 1/2, 0 * phi(0) = 0
+    assert oracle.gelu_grad(30.0, mode) == pytest.approx(1.0, abs=1e-15)
+    assert abs(oracle.gelu_grad(-30.0, mode)) < 1e-15
+
+
+def test_dgrad_gelu_against_numpy_and_autograd():
+    """(dZ W) * GELU'(H) with W stored [n_out, n_in]: against numpy's matmul times torch's
+    autograd derivative, and a transposed-operand mistake fails (W not square)."""
+    rng = np.random.default_rng(21)
+    M, Kp, N = 7, 12, 9
+    dZ, W, H = rng.standard_normal((M, Kp)), rng.standard_normal((Kp, N)), rng.standard_normal((M, N)) * 2
+    for mode, approx in ((oracle.GELU_ERF, "none"), (oracle.GELU_TANH, "tanh")):
+        h = torch.tensor(H, requires_grad=True)
+        torch.nn.functional.gelu(h, approximate=approx).backward(torch.tensor(dZ @ W))
+        np.testing.assert_allclose(oracle.dgrad_gelu(dZ, W, H, mode), h.grad.numpy(), rtol=1e-12, atol=1e-13)
+        cols = np.array([8, 0, 3])
+        np.testing.assert_allclose(oracle.dgrad_gelu(dZ, W, H, mode, cols), h.grad.numpy()[:, cols], rtol=1e-12,
+                                   atol=1e-13)
+
+
+def test_swiglu_bwd_against_autograd_and_layout():
+    """SwiGLU backward pairs against torch fp64 autograd of silu(g) * u with dy = dO Wd;
+    the pair of feature n sits at columns 2n (gate) and 2n + 1 (up); g = 0 gives
+    dg = dy u / 2 and du = 0."""
+    rng = np.random.default_rng(22)
+    M, Kp, N = 6, 10, 8
+    dO, Wd = rng.standard_normal((M, Kp)), rng.standard_normal((Kp, N))
+    G, U = rng.standard_normal((M, N)) * 3, rng.standard_normal((M, N))
+    G[2, 5] = 0.0
+    g = torch.tensor(G, requires_grad=True)
+    u = torch.tensor(U, requires_grad=True)
+    dy = dO @ Wd
+    (torch.nn.functional.silu(g) * u).backward(torch.tensor(dy))
+    out = oracle.swiglu_bwd(dO, Wd, G, U)
+    assert out.shape == (M, 2 * N)
+    np.testing.assert_allclose(out[:, 0::2], g.grad.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(out[:, 1::2], u.grad.numpy(), rtol=1e-12, atol=1e-13)
+    assert out[2, 10] == pytest.approx(dy[2, 5] * U[2, 5] / 2, rel=1e-14) and out[2, 11] == 0.0
+    sub = oracle.swiglu_bwd(dO, Wd, G, U, cols=np.array([7, 1]))
+    np.testing.assert_allclose(sub, out[:, [14, 15, 2, 3]], rtol=0, atol=0)
