@@ -198,6 +198,10 @@ class Case:
             self.out = torch.empty(w.M, dtype=torch.float32, device="cuda")
             self.ws = fl.cross_entropy_workspace(w.M, w.N)
             self.flops = 2.0 * w.M * w.N * w.K
+        elif w.kind in ("gelu_bwd", "swiglu_bwd"):
+            width = w.N if w.kind == "gelu_bwd" else 2 * w.N
+            self.out = torch.empty((w.M, width), dtype=torch.bfloat16, device="cuda")
+            self.flops = 2.0 * w.M * w.N * w.K
         elif w.kind == "quant":
             self.fmt = QUANT_FMT[w.quant]
             bs = fl.QUANT_BLOCK[self.fmt]
@@ -229,7 +233,7 @@ class Case:
             return float(b + 2 * w.M * w.N)
         if w.kind == "cross_entropy":
             return float(b + 4 * w.M + 4 * w.M)  # + labels in, loss out
-        if w.kind in ("quant", "qkv_fp8kv"):
+        if w.kind in ("quant", "qkv_fp8kv", "gelu_bwd", "swiglu_bwd"):
             return float(b + sum(t.numel() * t.element_size() for t in self.out))
         if w.kind == "rms_chain":
             # h2 is written by the first GEMM and read by the second; y is written once
@@ -252,6 +256,10 @@ class Case:
         elif w.kind == "cross_entropy":
             fl.fused_linear_cross_entropy(d["X"], d["W"], d.get("b"), self.labels, loss=self.out, workspace=self.ws,
                                           stream=stream)
+        elif w.kind == "gelu_bwd":
+            fl.fused_dgrad_gelu(d["dZ"], d["W"], d["H"], mode="tanh", dH=self.out, stream=stream)
+        elif w.kind == "swiglu_bwd":
+            fl.fused_swiglu_bwd(d["dO"], d["Wd"], d["G"], d["U"], dGU=self.out, stream=stream)
         elif w.kind == "quant":
             fl.fused_linear_quant(d["X"], d["W"], d.get("b"), self.fmt, Yq=self.out[0], scales=self.out[1],
                                   stream=stream)
@@ -343,6 +351,15 @@ def unfused_fn(case: Case):
         return lambda: F.silu(F.linear(d["X"], d["Wgate"])) * F.linear(d["X"], d["Wup"])
     if w.kind == "cross_entropy":
         return lambda: F.cross_entropy(F.linear(d["X"], d["W"]).float(), case.labels.long(), reduction="none")
+    if w.kind == "gelu_bwd":
+        return lambda: torch.ops.aten.gelu_backward(d["dZ"] @ d["W"], d["H"], approximate="tanh")
+    if w.kind == "swiglu_bwd":
+        def swiglu_bwd():
+            dy = (d["dO"] @ d["Wd"]).float()
+            g, u = d["G"].float(), d["U"].float()
+            s = torch.sigmoid(g)
+            return torch.stack((dy * u * s * (1 + g * (1 - s)), dy * g * s), dim=-1).reshape(w.M, -1).bfloat16()
+        return swiglu_bwd
     if w.kind == "quant":
         return lambda: unfused_quant(F.linear(d["X"], d["W"], d.get("b")).float(), case.fmt)
     if w.kind == "rms_chain":
@@ -494,6 +511,10 @@ def oracle_sample(w, rows: int):
         oracle.qkv_rope(f["X"], f["W"], f.get("b"), w.n_heads, w.head_dim, w.theta, np.arange(rows) % w.seq_len)
     elif w.kind == "swiglu":
         oracle.swiglu(f["X"], f["Wgate"], f["Wup"], f.get("bgate"), f.get("bup"))
+    elif w.kind == "gelu_bwd":
+        oracle.dgrad_gelu(f["dZ"], f["W"], f["H"], oracle.GELU_TANH)
+    elif w.kind == "swiglu_bwd":
+        oracle.swiglu_bwd(f["dO"], f["Wd"], f["G"], f["U"])
     elif w.kind == "qkv_fp8kv":
         oracle.qkv_rope_kv_fp8(f["X"], f["W"], f.get("b"), w.n_heads, w.n_kv_heads, w.head_dim, w.theta,
                                np.arange(rows) % w.seq_len)
@@ -591,7 +612,8 @@ def main():
     if args.rows == "all":
         for name in ("qkv_rope_8192x12288x4096", "qkv_fp8kv_8192x6144x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
                      "rmsnorm_fp8_decode_32x4096x14336", "rms_chain_8192x4096x4096_to_14336",
-                     "lm_head_ce_8192x32768x4096", "quant_fp8_1x128_8192x16384x4096",
+                     "lm_head_ce_8192x32768x4096", "gelu_bwd_8192x16384x4096", "swiglu_bwd_8192x14336x4096",
+                     "quant_fp8_1x128_8192x16384x4096",
                      "quant_int4_g32_8192x16384x4096", "quant_nvfp4_g16_8192x16384x4096"):
             c = Case(name)
             row_steps = min(args.steps, 200)

@@ -62,6 +62,10 @@ def load() -> ctypes.CDLL:
     lib.fused_linear_cross_entropy.restype = I
     lib.fused_qkv_rope_fp8kv.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I64, I64, I64, I64, I64, P]
     lib.fused_qkv_rope_fp8kv.restype = I
+    lib.fused_dgrad_gelu.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I64, I, P]
+    lib.fused_dgrad_gelu.restype = I
+    lib.fused_swiglu_bwd.argtypes = [P, P, P, P, P, I, I, I, I64, I64, I64, I64, P]
+    lib.fused_swiglu_bwd.restype = I
     lib.fused_linear_quant.argtypes = [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, P]
     lib.fused_linear_quant.restype = I
     lib.fl_cross_entropy_workspace_bytes.argtypes = [I, I]
@@ -398,6 +402,51 @@ def fused_linear_quant(X, W, b=None, fmt: int = QUANT_FP8_1X128, Yq=None, scales
                                    _stream(stream))
     _check("fused_linear_quant", st)
     return Yq, scales
+
+
+def fused_dgrad_gelu(dZ, W, H, mode: str = "tanh", dH=None, stream=None):
+    """dH = (dZ W) * GELU'(H): the next layer's weight W [K, N] as stored, H the saved pre-activation."""
+    M, K = dZ.shape
+    if W.shape[0] != K:
+        raise ValueError("W must be [K, N] with K = dZ.shape[1]")
+    N = W.shape[1]
+    _mat(dZ, "dZ", torch.bfloat16)
+    _mat(W, "W", torch.bfloat16)
+    _mat(H, "H", torch.bfloat16)
+    if tuple(H.shape) != (M, N):
+        raise ValueError("H must be [M, N]")
+    if dH is None:
+        dH = torch.empty((M, N), dtype=torch.bfloat16, device=dZ.device)
+    _mat(dH, "dH", torch.bfloat16)
+    if mode not in ("tanh", "erf"):
+        raise ValueError("mode must be 'tanh' or 'erf'")
+    st = load().fused_dgrad_gelu(_ptr(dZ), _ptr(W), _ptr(H), _ptr(dH), M, N, K, _ld(dZ, K, K), _ld(W, N, N),
+                                 _ld(H, N, N), _ld(dH, N, N), FL_GELU_TANH if mode == "tanh" else FL_GELU_ERF,
+                                 _stream(stream))
+    _check("fused_dgrad_gelu", st)
+    return dH
+
+
+def fused_swiglu_bwd(dO, Wd, G, U, dGU=None, stream=None):
+    """SwiGLU backward through the down projection Wd [K, N] (as stored): returns dGU [M, 2N]
+    with dg at column 2n and du at column 2n + 1."""
+    M, K = dO.shape
+    if Wd.shape[0] != K:
+        raise ValueError("Wd must be [K, N] with K = dO.shape[1]")
+    N = Wd.shape[1]
+    _mat(dO, "dO", torch.bfloat16)
+    _mat(Wd, "Wd", torch.bfloat16)
+    _mat(G, "G", torch.bfloat16)
+    _mat(U, "U", torch.bfloat16)
+    if tuple(G.shape) != (M, N) or tuple(U.shape) != (M, N) or _ld(G, N, N) != _ld(U, N, N):
+        raise ValueError("G and U must be [M, N] with one shared pitch")
+    if dGU is None:
+        dGU = torch.empty((M, 2 * N), dtype=torch.bfloat16, device=dO.device)
+    _mat(dGU, "dGU", torch.bfloat16)
+    st = load().fused_swiglu_bwd(_ptr(dO), _ptr(Wd), _ptr(G), _ptr(U), _ptr(dGU), M, N, K, _ld(dO, K, K),
+                                 _ld(Wd, N, N), _ld(G, N, N), _ld(dGU, 2 * N, 2 * N), _stream(stream))
+    _check("fused_swiglu_bwd", st)
+    return dGU
 
 
 def device_status(stream=None) -> int:

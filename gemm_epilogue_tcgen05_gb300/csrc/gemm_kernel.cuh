@@ -34,7 +34,10 @@ enum EpiKind : int {
   EPI_ROWSCALE = 6,     // y = r * acc + b with r = 1/sqrt(sum of the row's partials / n + eps)
   EPI_CE = 7,           // per-row online log-sum-exp state + label logit; last tile of a row block merges
   EPI_QUANT = 8,        // block-scaled quantised write-back: FP8 1x128, INT4 g32 or NVFP4 g16 + scales
-  EPI_QKV_FP8KV = 9     // QKV + RoPE, Q in bf16, K and V as E4M3 with one scale per token and kv head
+  EPI_QKV_FP8KV = 9,    // QKV + RoPE, Q in bf16, K and V as E4M3 with one scale per token and kv head
+  EPI_GELU_BWD_TANH = 10,  // dgrad (B = W as stored, MN-major) times GELU'(saved pre-activation), tanh form
+  EPI_SWIGLU_BWD = 11,     // dgrad of the down projection -> interleaved (dg, du) pairs, double width
+  EPI_GELU_BWD_ERF = 12    // as EPI_GELU_BWD_TANH with the erf form's derivative
 };
 enum QuantFmt : int { QF_FP8_1X128 = 0, QF_INT4_G32 = 1, QF_NVFP4_G16 = 2 };
 
@@ -76,6 +79,11 @@ struct alignas(128) GemmParams {
   int kv_width;
   float* kscale;
   float* vscale;
+  // backward epilogues: saved activations [M][ld_saved] (GELU: the pre-activation H;
+  // SwiGLU: the gate G and up U)
+  const __nv_bfloat16* saved0;
+  const __nv_bfloat16* saved1;
+  long long ld_saved;
   unsigned* counters;      // [2][num_m_blocks]: arrivals, finished readers
   int* status;
   unsigned long long timeout_ns;
@@ -89,6 +97,9 @@ struct EpiTraits {
   static constexpr int kMmaN = 256;                               // accumulator columns per tile
   static constexpr int kOutN = (EPI == EPI_SWIGLU) ? 128 : 256;   // output columns per tile
   static constexpr bool kFp8 = (EPI == EPI_RMSNORM_FP8);
+  // B operand MN-major (W as stored [K, N], N contiguous): TMA boxes of 64 columns x kBK rows
+  static constexpr bool kBMn = (EPI == EPI_GELU_BWD_TANH || EPI == EPI_GELU_BWD_ERF || EPI == EPI_SWIGLU_BWD);
+  static constexpr int kBChunkBytes = 64 * kBK * 2;
   static constexpr int kStages = CG == 2 ? 6 : 4;
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBRows = kMmaN / CG;                       // W rows this CTA loads per stage
@@ -179,6 +190,18 @@ __device__ __forceinline__ float gelu_tanh_f(float v) {
 }
 __device__ __forceinline__ float gelu_erf_f(float v) { return 0.5f * v * (1.f + erff(v * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+// GELU'(h) of the tanh form: 0.5 (1 + t) + 0.5 h (1 - t^2) c (1 + 3 a h^2), t = tanh(c (h + a h^3)),
+// c = sqrt(2/pi), a = 0.044715.
+__device__ __forceinline__ float gelu_tanh_grad_f(float h) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  const float h2 = h * h;
+  const float t = tanhf(c * h * fmaf(a, h2, 1.f));
+  return fmaf(0.5f * h * (1.f - t * t), c * fmaf(3.f * a, h2, 1.f), 0.5f * (1.f + t));
+}
+// GELU'(h) of the erf form: Phi(h) + h phi(h).
+__device__ __forceinline__ float gelu_erf_grad_f(float h) {
+  return fmaf(h * 0.3989422804014327f, expf(-0.5f * h * h), 0.5f * (1.f + erff(h * 0.70710678118654752f)));
+}
 
 // Writes 32 bf16 values (one row segment) into a 128B-swizzled staging row:
 // `unit` (0 or 1) selects which half of the 128-byte row they fill.
@@ -354,6 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             if (EPI == EPI_SWIGLU) {
               // the leader holds the 128 gate rows, the peer the 128 up rows of the same features
               tma_load_2d_pair(rank == 0 ? &p.map_b : &p.map_b2, full_cl, b_dst, kb * kBK, nb * 128);
+            } else if (T::kBMn) {
+              // this CTA's 128 columns of the W tile as two 64-column chunks, rows = this K block
+              for (int c = 0; c < 2; ++c)
+                tma_load_2d_pair(&p.map_b, full_cl, b_dst + c * T::kBChunkBytes,
+                                 nb * T::kMmaN + static_cast<int>(rank) * 128 + c * 64, kb * kBK);
             } else {
               tma_load_2d_pair(&p.map_b, full_cl, b_dst, kb * kBK, nb * T::kMmaN + static_cast<int>(rank) * 128);
             }
@@ -364,6 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
               // gate rows and up rows of the same 128 output features, stacked in one B stage
               tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * 128);
               tma_load_2d(&p.map_b2, &full_bar[stage], b_dst + 128 * kBK * 2, kb * kBK, nb * 128);
+            } else if (T::kBMn) {
+              for (int c = 0; c < 4; ++c)
+                tma_load_2d(&p.map_b, &full_bar[stage], b_dst + c * T::kBChunkBytes, nb * T::kMmaN + c * 64,
+                            kb * kBK);
             } else {
               tma_load_2d(&p.map_b, &full_bar[stage], b_dst, kb * kBK, nb * T::kMmaN);
             }
@@ -387,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && mma_cta) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, T::kMmaN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, T::kMmaN, T::kBMn);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -407,14 +439,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + stage * T::kStageBytes);
           const uint64_t adesc = sdesc_k_sw128(a_addr);
-          const uint64_t bdesc = sdesc_k_sw128(a_addr + T::kABytes);
+          const uint64_t bdesc = T::kBMn ? sdesc_mn_sw128(a_addr + T::kABytes, T::kBChunkBytes)
+                                         : sdesc_k_sw128(a_addr + T::kABytes);
+          // per K step of 16: A (K-major) +32 bytes inside its 128-byte swizzled rows; B +32 bytes
+          // likewise, or, MN-major, +16 rows of 128 bytes (>> 4 in the descriptor)
+          constexpr uint64_t kBStep = T::kBMn ? (16 * 128) >> 4 : 2;
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
-            // +32 bytes along K per step inside the 128-byte swizzled row (>> 4 in the descriptor)
             if constexpr (CG == 2) {
-              mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+              mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + kBStep * k, idesc, (kb | k) != 0 ? 1u : 0u);
             } else {
-              mma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+              mma_bf16(d_tmem, adesc + 2 * k, bdesc + kBStep * k, idesc, (kb | k) != 0 ? 1u : 0u);
             }
           }
           if constexpr (CG == 2) {
@@ -473,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * T::kMmaN;
 
-      if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF || EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV) {
+      if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF || EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV ||
+                    EPI == EPI_GELU_BWD_TANH || EPI == EPI_GELU_BWD_ERF) {
         if (!ok) break;
         constexpr bool kQkv = EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV;
         int n0 = nb * T::kOutN;  // first output column of the tile
@@ -630,6 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             } else if constexpr (EPI == EPI_GELU_ERF) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = gelu_erf_f(v[j]);
+            } else if constexpr (EPI == EPI_GELU_BWD_TANH || EPI == EPI_GELU_BWD_ERF) {
+              // "GEMM Epilogue 完全拆解", §模式 D: the dgrad GEMM's epilogue multiplies by f'(h)
+              float h[32];
+              load_row32(p.saved0 + static_cast<long long>(row_ok ? m : 0) * p.ld_saved, row_ok, col0, p.N, h);
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] *= EPI == EPI_GELU_BWD_TANH ? gelu_tanh_grad_f(h[j]) : gelu_erf_grad_f(h[j]);
             }  // QKV: only the unrotated V section reaches this loop
             stage_bf16_32(buf, lane, u, v);
           }
@@ -823,6 +866,38 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             p.loss[m] = l;
           }
           if (threadIdx.x == 64) p.counters[mb] = 0u;  // every tile of this row block has arrived
+        }
+        release_acc(abuf);
+      } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+        // "GEMM Epilogue 完全拆解", §末尾布局调整 (SwiGLU 反向): one upstream value dy of feature n
+        // gives (dg, du) = (dy u SiLU'(g), dy SiLU(g)); the pair is packed into one 32-bit word
+        // and the row is written at twice the width (columns 2n and 2n + 1).
+        if (!ok) break;
+        const int n0 = nb * 256;
+        const long long srow = static_cast<long long>(row_ok ? m : 0) * p.ld_saved;
+#pragma unroll 1
+        for (int u = 0; u < 8; ++u) {
+          const int col0 = n0 + u * 32;
+          float dy[32], g[32], up[32];
+          tmem_load32f(tacc + u * 32, k_empty, dy);
+          load_row32(p.saved0 + srow, row_ok, col0, p.N, g);
+          load_row32(p.saved1 + srow, row_ok, col0, p.N, up);
+          const uint32_t buf = ring.acquire(lane);
+          const uint32_t srow_s = buf + lane * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = 4 * c + i;
+              const float s = 1.f / (1.f + expf(-g[j]));
+              const float dg = dy[j] * up[j] * (s * fmaf(g[j], 1.f - s, 1.f));
+              const float du = dy[j] * (g[j] * s);
+              w[i] = pack_bf16x2(dg, du);
+            }
+            st_shared_v4(srow_s + ((c ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+          ring.commit(&p.map_out[0], buf, lane, 2 * col0, y_box);
         }
         release_acc(abuf);
       } else if constexpr (EPI == EPI_QUANT) {

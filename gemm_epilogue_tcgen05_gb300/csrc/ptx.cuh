@@ -241,11 +241,27 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+// Shared-memory descriptor of an MN-major operand in 128-byte swizzled layout, as TMA writes
+// 64-column x 64-row boxes (128-byte rows, one per K index): 64-element chunks along MN are
+// `chunk_bytes` apart (leading byte offset), groups of 8 K rows are 1024 bytes apart (stride
+// byte offset).  One K step of 16 advances the start by 16 rows = 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t smem_addr, uint32_t chunk_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);     // [0,14)  start address >> 4
+  d |= static_cast<uint64_t>((chunk_bytes >> 4) & 0x3FFFu) << 16;  // [16,30) leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                 // [32,46) stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                         // [46,48) descriptor version for tcgen05
+  d |= static_cast<uint64_t>(2) << 61;                         // [61,64) swizzle mode: 128-byte
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, A K-major; B K-major or, with
+// b_mn_major, MN-major (the transpose-B bit).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major = false) {
   return (1u << 4)                                   // D format: f32
          | (1u << 7)                                 // A format: bf16
          | (1u << 10)                                // B format: bf16
+         | (b_mn_major ? (1u << 16) : 0u)            // B major-ness: 1 = MN-major
          | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }

@@ -242,6 +242,26 @@ FL_API int fused_linear_quant(const void* X, const void* W, const void* b, void*
                               int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldq, int64_t lds,
                               int fmt, void* stream);
 
+/* Backward of Linear -> GELU, fused into the dgrad GEMM.
+ *   "GEMM Epilogue 完全拆解", §模式 D: dH = (dZ W) * GELU'(H).  dZ [M,K] bf16 is the
+ *   gradient w.r.t. the next layer's output (K = that layer's output features), W [K,N]
+ *   bf16 that layer's weight as stored (N contiguous, pitch ldw >= N), H [M,N] bf16 the
+ *   saved pre-activation, dH [M,N] bf16 (pitches in elements, multiples of 8).  mode
+ *   FL_GELU_ERF or FL_GELU_TANH picks the derivative's form.  Accumulation in fp32,
+ *   one rounding at the store. */
+FL_API int fused_dgrad_gelu(const void* dZ, const void* W, const void* H, void* dH, int M, int N, int K,
+                            int64_t ldz, int64_t ldw, int64_t ldh, int64_t ldo, int mode, void* stream);
+
+/* Backward of SwiGLU through the down projection, fused into its dgrad GEMM.
+ *   "GEMM Epilogue 完全拆解", §末尾布局调整 (SwiGLU 反向): dy = dO Wd, and per feature n
+ *   dg = dy u SiLU'(g), du = dy SiLU(g) with SiLU'(g) = s (1 + g (1 - s)), s = sigmoid(g).
+ *   The pair is packed into one 32-bit word: dGU [M, 2N] bf16 holds dg at column 2n and
+ *   du at column 2n + 1.  dO [M,K] bf16, Wd [K,N] bf16 the down projection's weight as
+ *   stored, G and U [M,N] bf16 the saved gate and up activations (shared pitch ldgu). */
+FL_API int fused_swiglu_bwd(const void* dO, const void* Wd, const void* G, const void* U, void* dGU,
+                            int M, int N, int K, int64_t ldo_in, int64_t ldw, int64_t ldgu, int64_t ldout,
+                            void* stream);
+
 /* Bytes of workspace fused_linear_residual_rmsnorm_fp8 needs for this shape
  * on the current device (0 for an empty problem). */
 FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);

@@ -208,7 +208,7 @@ def draw_numpy(seed: int, stream: int, shape, mean: float, std: float, dtype: st
 class Workload:
     """One synthetic workload: shapes, dtype and the distribution of each operand."""
     name: str
-    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain" | "cross_entropy" | "quant" | "qkv_fp8kv"
+    kind: str            # "gelu_erf" | "gelu_tanh" | "qkv_rope" | "swiglu" | "rmsnorm_fp8" | "rms_chain" | "cross_entropy" | "quant" | "qkv_fp8kv" | "gelu_bwd" | "swiglu_bwd"
     M: int
     N: int               # output features (QKV: 3*H*D; SwiGLU: d_ff)
     K: int
@@ -247,6 +247,12 @@ WORKLOADS = {
     # LM head over a 32K vocabulary with the cross-entropy in the epilogue
     "lm_head_ce_8192x32768x4096": Workload("lm_head_ce_8192x32768x4096", "cross_entropy", 8192, 32768, 4096,
                                            has_bias=False),
+    # backward of the MLP blocks: dgrad of the down projection (K = d_model) with the
+    # activation derivative in the epilogue; N = d_ff features of the saved activations
+    "gelu_bwd_8192x16384x4096": Workload("gelu_bwd_8192x16384x4096", "gelu_bwd", 8192, 16384, 4096,
+                                         has_bias=False),
+    "swiglu_bwd_8192x14336x4096": Workload("swiglu_bwd_8192x14336x4096", "swiglu_bwd", 8192, 14336, 4096,
+                                           has_bias=False),
     # up-projection whose output is written block-scaled for a low-precision consumer
     "quant_fp8_1x128_8192x16384x4096": Workload("quant_fp8_1x128_8192x16384x4096", "quant", 8192, 16384, 4096,
                                                 quant="fp8_1x128"),
@@ -261,6 +267,12 @@ def operand_specs(w: Workload):
     """(name, stream, shape, mean, std, dtype) for every operand of a workload."""
     dt = w.dtype
     w_std = 1.0 / math.sqrt(w.K)
+    if w.kind == "gelu_bwd":  # upstream gradient, next layer's weight [K, N] as stored, saved H
+        return [("dZ", STREAM_X, (w.M, w.K), 0.0, 1.0, dt), ("W", STREAM_W, (w.K, w.N), 0.0, w_std, dt),
+                ("H", STREAM_Z, (w.M, w.N), 0.0, 1.0, dt)]
+    if w.kind == "swiglu_bwd":  # upstream gradient, down projection [K, N] as stored, saved gate and up
+        return [("dO", STREAM_X, (w.M, w.K), 0.0, 1.0, dt), ("Wd", STREAM_W, (w.K, w.N), 0.0, w_std, dt),
+                ("G", STREAM_Z, (w.M, w.N), 0.0, 1.0, dt), ("U", STREAM_GAMMA, (w.M, w.N), 0.0, 1.0, dt)]
     specs = [("X", STREAM_X, (w.M, w.K), 0.0, 1.0, dt)]
     if w.kind == "swiglu":
         specs += [("Wgate", STREAM_W, (w.N, w.K), 0.0, w_std, dt),
@@ -284,15 +296,18 @@ def make_labels(w: Workload) -> np.ndarray:
     return draw_labels(w.seed, STREAM_LABEL, w.M, w.N)
 
 
+ROW_OPERANDS = ("X", "Z", "dZ", "H", "dO", "G", "U")  # operands with one row per token
+
+
 def make_operands(w: Workload, rows: tuple[int, int] | None = None) -> dict:
     """All operands of ``w`` as host arrays (bf16 as uint16 bits, f32 as float32).
 
     With ``rows=(start, count)`` only that block of the row-indexed operands
-    (X, Z) is produced; weights and vectors are always produced whole.
+    (those in ROW_OPERANDS) is produced; weights and vectors are always produced whole.
     """
     out = {}
     for name, stream, shape, mean, std, dt in operand_specs(w):
-        if rows is not None and name in ("X", "Z"):
+        if rows is not None and name in ROW_OPERANDS:
             out[name] = draw(w.seed, stream, shape, mean, std, dt, rows[0], rows[1])
         else:
             out[name] = draw(w.seed, stream, shape, mean, std, dt)

@@ -97,3 +97,14 @@ def test_qkv_fp8kv_rejects_bad_arguments_on_host(lib):
                                     2, None) == fl.FL_ERR_ALIGNMENT
     assert lib.fused_qkv_rope_fp8kv(a, a, None, a, a, a, None, a, None, 8, 64, 2, 2, 128, 16, f(1e4), 64, 64, 256,
                                     256, 2, None) == fl.FL_ERR_INVALID_ARG
+
+
+def test_backward_entry_points_reject_bad_arguments_on_host(lib):
+    a = P(0x10000)
+    # bad GELU form, W pitch below N, H pitch not a multiple of 8 elements, missing U
+    assert lib.fused_dgrad_gelu(a, a, a, a, 8, 16, 8, 8, 16, 16, 16, 7, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_dgrad_gelu(a, a, a, a, 8, 16, 8, 8, 8, 16, 16, 1, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_dgrad_gelu(a, a, a, a, 8, 16, 8, 8, 16, 20, 16, 1, None) == fl.FL_ERR_ALIGNMENT
+    assert lib.fused_swiglu_bwd(a, a, a, None, a, 8, 16, 8, 8, 16, 16, 32, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_swiglu_bwd(a, a, a, a, a, 8, 16, 8, 8, 16, 16, 24, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_swiglu_bwd(None, None, None, None, None, 0, 16, 8, 8, 16, 16, 32, None) == fl.FL_OK

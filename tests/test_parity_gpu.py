@@ -495,3 +495,60 @@ def test_qkv_fp8kv_full_workload_sampled():
     ref = oracle.qkv_rope_kv_fp8(f64(ops["X"][rows]), f64(ops["W"]), None, w.n_heads, w.n_kv_heads, w.head_dim,
                                  w.theta, rows % w.seq_len)
     _check_kv_fp8(tuple(t[ri] for t in out), ref, "qkv fp8kv full")
+
+
+# ------------------------------------------------------------------ backward epilogues (dgrad, W as stored)
+@pytest.mark.parametrize("pairing", [True, False])
+@pytest.mark.parametrize("mode", ["tanh", "erf"])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (1, 72, 40), (257, 1024, 136)])
+def test_dgrad_gelu_small(mode, pairing, M, N, K):
+    fl.set_cta_pairing(pairing)
+    dZ = _draw((M, K), syn.STREAM_X)
+    W = _draw((K, N), syn.STREAM_W, K ** -0.5)
+    H = _draw((M, N), syn.STREAM_Z, 2.0)
+    dH = fl.fused_dgrad_gelu(dev_bf16(dZ), dev_bf16(W), dev_bf16(H), mode=mode)
+    m = oracle.GELU_TANH if mode == "tanh" else oracle.GELU_ERF
+    assert_bf16_close(host(dH), oracle.dgrad_gelu(f64(dZ), f64(W), f64(H), m), f"dgrad gelu {mode} {M}x{N}x{K}")
+
+
+def test_dgrad_gelu_strided_and_k_zero():
+    M, N, K = 130, 264, 72
+    dZ = _draw((M, K + 8), syn.STREAM_X)
+    W = _draw((K, N + 16), syn.STREAM_W, K ** -0.5)
+    H = _draw((M, N + 24), syn.STREAM_Z, 2.0)
+    out = torch.zeros((M, N + 40), dtype=torch.bfloat16, device="cuda")
+    fl.fused_dgrad_gelu(dev_bf16(dZ)[:, :K], dev_bf16(W)[:, :N], dev_bf16(H)[:, :N], mode="erf", dH=out[:, :N])
+    ref = oracle.dgrad_gelu(f64(dZ[:, :K]), f64(W[:, :N]), f64(H[:, :N]), oracle.GELU_ERF)
+    assert_bf16_close(host(out[:, :N]), ref, "strided")
+    assert torch.count_nonzero(out[:, N:]) == 0
+    z = fl.fused_dgrad_gelu(torch.empty((M, 0), dtype=torch.bfloat16, device="cuda"),
+                            torch.empty((0, N), dtype=torch.bfloat16, device="cuda"), dev_bf16(H)[:, :N])
+    assert torch.count_nonzero(z) == 0  # K = 0: the gradient is zero
+
+
+@pytest.mark.parametrize("pairing", [True, False])
+@pytest.mark.parametrize("M,N,K", [(300, 264, 200), (1, 64, 40), (257, 768, 136)])
+def test_swiglu_bwd_small(pairing, M, N, K):
+    fl.set_cta_pairing(pairing)
+    dO = _draw((M, K), syn.STREAM_X)
+    Wd = _draw((K, N), syn.STREAM_W, K ** -0.5)
+    G = _draw((M, N), syn.STREAM_Z, 3.0)
+    U = _draw((M, N), syn.STREAM_GAMMA)
+    out = fl.fused_swiglu_bwd(dev_bf16(dO), dev_bf16(Wd), dev_bf16(G), dev_bf16(U))
+    assert tuple(out.shape) == (M, 2 * N)
+    ref = oracle.swiglu_bwd(f64(dO), f64(Wd), f64(G), f64(U))
+    assert_bf16_close(host(out), ref, f"swiglu bwd {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("name", ["gelu_bwd_8192x16384x4096", "swiglu_bwd_8192x14336x4096"])
+def test_backward_full_workload_sampled(name):
+    w = syn.WORKLOADS[name]
+    ops = syn.make_operands(w)
+    rows = sample_rows(w.M, extra=2)
+    if w.kind == "gelu_bwd":
+        out = fl.fused_dgrad_gelu(dev_bf16(ops["dZ"]), dev_bf16(ops["W"]), dev_bf16(ops["H"]), mode="tanh")
+        ref = oracle.dgrad_gelu(f64(ops["dZ"][rows]), f64(ops["W"]), f64(ops["H"][rows]), oracle.GELU_TANH)
+    else:
+        out = fl.fused_swiglu_bwd(dev_bf16(ops["dO"]), dev_bf16(ops["Wd"]), dev_bf16(ops["G"]), dev_bf16(ops["U"]))
+        ref = oracle.swiglu_bwd(f64(ops["dO"][rows]), f64(ops["Wd"]), f64(ops["G"][rows]), f64(ops["U"][rows]))
+    assert_bf16_close(host(out[torch.from_numpy(rows).cuda()]), ref, name)
