@@ -154,6 +154,38 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* row, bool row_ok
   load_vec32(row, col0, n_limit, v);
 }
 
+// 32 bf16 values of a row as raw 16-byte words (zero outside the row or past n_limit), so a
+// load can be issued one unit ahead of its use and unpacked later.
+__device__ __forceinline__ void load_raw32(const __nv_bfloat16* row, bool row_ok, int col0, int n_limit,
+                                           uint4 (&w)[4]) {
+  if (row_ok && col0 + 32 <= n_limit) {
+    const uint4* q = reinterpret_cast<const uint4*>(row + col0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = __ldg(q + i);
+    return;
+  }
+  const unsigned short* r = reinterpret_cast<const unsigned short*>(row);
+  uint32_t e[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int c = col0 + 2 * k;
+    const uint32_t lo = (row_ok && c < n_limit) ? __ldg(r + c) : 0u;
+    const uint32_t hi = (row_ok && c + 1 < n_limit) ? __ldg(r + c + 1) : 0u;
+    e[k] = lo | (hi << 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = make_uint4(e[4 * i], e[4 * i + 1], e[4 * i + 2], e[4 * i + 3]);
+}
+__device__ __forceinline__ void unpack32(const uint4 (&w)[4], float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[8 * i + 0] = bf16_lo(w[i].x); v[8 * i + 1] = bf16_hi(w[i].x);
+    v[8 * i + 2] = bf16_lo(w[i].y); v[8 * i + 3] = bf16_hi(w[i].y);
+    v[8 * i + 4] = bf16_lo(w[i].z); v[8 * i + 5] = bf16_hi(w[i].z);
+    v[8 * i + 6] = bf16_lo(w[i].w); v[8 * i + 7] = bf16_hi(w[i].w);
+  }
+}
+
 __device__ __forceinline__ void tmem_load32f(uint32_t taddr, bool zero, float (&v)[32]) {
   if (zero) {
 #pragma unroll
@@ -195,12 +227,12 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __
 __device__ __forceinline__ float gelu_tanh_grad_f(float h) {
   const float c = 0.7978845608028654f, a = 0.044715f;
   const float h2 = h * h;
-  const float t = tanhf(c * h * fmaf(a, h2, 1.f));
+  const float t = tanh_approx(c * h * fmaf(a, h2, 1.f));
   return fmaf(0.5f * h * (1.f - t * t), c * fmaf(3.f * a, h2, 1.f), 0.5f * (1.f + t));
 }
 // GELU'(h) of the erf form: Phi(h) + h phi(h).
 __device__ __forceinline__ float gelu_erf_grad_f(float h) {
-  return fmaf(h * 0.3989422804014327f, expf(-0.5f * h * h), 0.5f * (1.f + erff(h * 0.70710678118654752f)));
+  return fmaf(h * 0.3989422804014327f, __expf(-0.5f * h * h), 0.5f * (1.f + erff(h * 0.70710678118654752f)));
 }
 
 // Writes 32 bf16 values (one row segment) into a 128B-swizzled staging row:
@@ -508,8 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + abuf * T::kMmaN;
 
-      if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF || EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV ||
-                    EPI == EPI_GELU_BWD_TANH || EPI == EPI_GELU_BWD_ERF) {
+      if constexpr (EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF || EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV) {
         if (!ok) break;
         constexpr bool kQkv = EPI == EPI_QKV_ROPE || EPI == EPI_QKV_FP8KV;
         int n0 = nb * T::kOutN;  // first output column of the tile
@@ -666,13 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             } else if constexpr (EPI == EPI_GELU_ERF) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = gelu_erf_f(v[j]);
-            } else if constexpr (EPI == EPI_GELU_BWD_TANH || EPI == EPI_GELU_BWD_ERF) {
-              // "GEMM Epilogue 完全拆解", §模式 D: the dgrad GEMM's epilogue multiplies by f'(h)
-              float h[32];
-              load_row32(p.saved0 + static_cast<long long>(row_ok ? m : 0) * p.ld_saved, row_ok, col0, p.N, h);
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                v[j] *= EPI == EPI_GELU_BWD_TANH ? gelu_tanh_grad_f(h[j]) : gelu_erf_grad_f(h[j]);
+
             }  // QKV: only the unrotated V section reaches this loop
             stage_bf16_32(buf, lane, u, v);
           }
@@ -868,20 +893,54 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
           if (threadIdx.x == 64) p.counters[mb] = 0u;  // every tile of this row block has arrived
         }
         release_acc(abuf);
+      } else if constexpr (EPI == EPI_GELU_BWD_TANH || EPI == EPI_GELU_BWD_ERF) {
+        // "GEMM Epilogue 完全拆解", §模式 D: the dgrad GEMM's epilogue multiplies by f'(h).  The
+        // saved pre-activation of the next 32-column unit is loaded while this one is computed.
+        if (!ok) break;
+        const int n0 = nb * 256;
+        const __nv_bfloat16* hrow = p.saved0 + static_cast<long long>(row_ok ? m : 0) * p.ld_saved;
+        uint4 hq[4];
+        load_raw32(hrow, row_ok, n0, p.N, hq);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t buf = ring.acquire(lane);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col0 = n0 + c * 64 + u * 32;
+            float h[32], v[32];
+            unpack32(hq, h);
+            if (c * 2 + u < 7) load_raw32(hrow, row_ok, col0 + 32, p.N, hq);
+            tmem_load32f(tacc + c * 64 + u * 32, k_empty, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              v[j] *= EPI == EPI_GELU_BWD_TANH ? gelu_tanh_grad_f(h[j]) : gelu_erf_grad_f(h[j]);
+            stage_bf16_32(buf, lane, u, v);
+          }
+          ring.commit(&p.map_out[0], buf, lane, n0 + c * 64, y_box);
+        }
+        release_acc(abuf);
       } else if constexpr (EPI == EPI_SWIGLU_BWD) {
         // "GEMM Epilogue 完全拆解", §末尾布局调整 (SwiGLU 反向): one upstream value dy of feature n
         // gives (dg, du) = (dy u SiLU'(g), dy SiLU(g)); the pair is packed into one 32-bit word
-        // and the row is written at twice the width (columns 2n and 2n + 1).
+        // and the row is written at twice the width (columns 2n and 2n + 1).  The saved gate and
+        // up values of the next 32-column unit are loaded while this one is computed.
         if (!ok) break;
         const int n0 = nb * 256;
         const long long srow = static_cast<long long>(row_ok ? m : 0) * p.ld_saved;
+        uint4 gq[4], uq[4];
+        load_raw32(p.saved0 + srow, row_ok, n0, p.N, gq);
+        load_raw32(p.saved1 + srow, row_ok, n0, p.N, uq);
 #pragma unroll 1
         for (int u = 0; u < 8; ++u) {
           const int col0 = n0 + u * 32;
-          float dy[32], g[32], up[32];
+          float g[32], up[32], dy[32];
+          unpack32(gq, g);
+          unpack32(uq, up);
+          if (u < 7) {
+            load_raw32(p.saved0 + srow, row_ok, col0 + 32, p.N, gq);
+            load_raw32(p.saved1 + srow, row_ok, col0 + 32, p.N, uq);
+          }
           tmem_load32f(tacc + u * 32, k_empty, dy);
-          load_row32(p.saved0 + srow, row_ok, col0, p.N, g);
-          load_row32(p.saved1 + srow, row_ok, col0, p.N, up);
           const uint32_t buf = ring.acquire(lane);
           const uint32_t srow_s = buf + lane * 128;
 #pragma unroll
@@ -890,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int j = 4 * c + i;
-              const float s = 1.f / (1.f + expf(-g[j]));
+              const float s = __fdividef(1.f, 1.f + __expf(-g[j]));  // sigmoid; 0 when e^{-g} overflows
               const float dg = dy[j] * up[j] * (s * fmaf(g[j], 1.f - s, 1.f));
               const float du = dy[j] * (g[j] * s);
               w[i] = pack_bf16x2(dg, du);
