@@ -466,21 +466,24 @@ def time_graph_rotating(case: Case, calls: int = 20, copies: int = 3, replays: i
 
 
 def time_e2e(case: Case, steps: int, warmup: int, barrier):
-    """Per-step time (ms) with host->device input copies and device->host output copies inside."""
+    """Per-step time (ms) of the public host-buffer call: pinned host inputs in, GEMM + epilogue,
+    host output out, every step (fused_linear_gelu_host overlaps the copies with the GEMM)."""
+    fl, w = case.fl, case.w
     stream = torch.cuda.current_stream()
-    pinned_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).pin_memory()
-                 for k, v in case.host.items()}
-    outs = case.outputs()
-    pinned_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    Xh, Wh = pinned(case.host["X"]), pinned(case.host["W"])
+    bh = pinned(case.host["b"]) if "b" in case.host else None
+    Yh = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    buf = fl.linear_gelu_host_buffer(w.M, w.N, w.K)
+    h2d = sum(t.numel() * t.element_size() for t in (Xh, Wh, bh) if t is not None)
+    d2h = Yh.numel() * Yh.element_size()
+    mode = "tanh" if w.kind == "gelu_tanh" else "erf"
 
     def step():
-        for k, t in pinned_in.items():
-            case.dev[k].view(torch.int16).copy_(t, non_blocking=True)
-        case.run(stream)
-        for o, p in zip(outs, pinned_out):
-            p.copy_(o, non_blocking=True)
+        fl.fused_linear_gelu_host(Xh, Wh, bh, Y=Yh, mode=mode, dev_buf=buf, stream=stream)
 
     for _ in range(warmup):
         step()
@@ -494,6 +497,7 @@ def time_e2e(case: Case, steps: int, warmup: int, barrier):
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier()
+    del buf
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], h2d, d2h
 
 

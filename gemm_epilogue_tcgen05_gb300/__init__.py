@@ -66,6 +66,10 @@ def load() -> ctypes.CDLL:
     lib.fused_dgrad_gelu.restype = I
     lib.fused_swiglu_bwd.argtypes = [P, P, P, P, P, I, I, I, I64, I64, I64, I64, P]
     lib.fused_swiglu_bwd.restype = I
+    lib.fused_linear_gelu_host.argtypes = [P, P, P, P, I, I, I, I, P, SZ, P]
+    lib.fused_linear_gelu_host.restype = I
+    lib.fl_linear_gelu_host_buffer_bytes.argtypes = [I, I, I]
+    lib.fl_linear_gelu_host_buffer_bytes.restype = SZ
     lib.fused_linear_quant.argtypes = [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, P]
     lib.fused_linear_quant.restype = I
     lib.fl_cross_entropy_workspace_bytes.argtypes = [I, I]
@@ -161,6 +165,39 @@ def fused_linear_gelu(X, W, b=None, Y=None, mode: str = "tanh", stream=None):
                                   _ld(Y, N, N), FL_BF16 if dtype == torch.bfloat16 else FL_F32, m,
                                   _stream(stream))
     _check("fused_linear_gelu", st)
+    return Y
+
+
+def linear_gelu_host_buffer(M: int, N: int, K: int, device=None) -> torch.Tensor:
+    """Device buffer for fused_linear_gelu_host (256-byte aligned, as torch allocates)."""
+    n = int(load().fl_linear_gelu_host_buffer_bytes(M, N, K))
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def fused_linear_gelu_host(X, W, b=None, Y=None, mode: str = "tanh", dev_buf=None, stream=None):
+    """fused_linear_gelu on host (CPU, ideally pinned) bf16 tensors, copies overlapped with the GEMM.
+
+    Returns Y (host); it is complete once `stream` (default: the current stream) has finished.
+    """
+    M, K = X.shape
+    N = W.shape[0]
+    for t, nm in ((X, "X"), (W, "W"), (b, "b"), (Y, "Y")):
+        if t is not None and (t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous()):
+            raise ValueError(f"{nm}: expected a contiguous bf16 host tensor")
+    if b is not None and b.numel() != N:
+        raise ValueError("b must have N elements")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+    if tuple(Y.shape) != (M, N):
+        raise ValueError("Y must be [M, N]")
+    if dev_buf is None:
+        dev_buf = linear_gelu_host_buffer(M, N, K)
+    if mode not in ("tanh", "erf"):
+        raise ValueError("mode must be 'tanh' or 'erf'")
+    st = load().fused_linear_gelu_host(_ptr(X), _ptr(W), _ptr(b), _ptr(Y), M, N, K,
+                                       FL_GELU_TANH if mode == "tanh" else FL_GELU_ERF, _ptr(dev_buf),
+                                       dev_buf.numel(), _stream(stream))
+    _check("fused_linear_gelu_host", st)
     return Y
 
 

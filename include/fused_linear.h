@@ -262,6 +262,24 @@ FL_API int fused_swiglu_bwd(const void* dO, const void* Wd, const void* G, const
                             int M, int N, int K, int64_t ldo_in, int64_t ldw, int64_t ldgu, int64_t ldout,
                             void* stream);
 
+/* fused_linear_gelu (bf16) on HOST buffers: copies in, GEMM + epilogue, copies out.
+ *   X [M,K], W [N,K], b [N] (nullable) and Y [M,N] are contiguous bf16 arrays in host
+ *   memory (page-locked for the copies to overlap; pageable memory works, serialised).
+ *   The pipeline is this library's: X and b are uploaded first, then W in blocks of
+ *   whole 256-column output tiles (about N/8 columns each); each block's GEMM starts as
+ *   soon as its rows of W have landed, and its columns of Y return to the host (one 2-D
+ *   copy) on a second copy stream while later blocks upload and compute.
+ * dev_buf: caller-owned device memory of fl_linear_gelu_host_buffer_bytes(M, N, K)
+ *   bytes, 256-byte aligned (holds X, W, b and Y on the device; no allocation per call).
+ * Asynchronous with respect to the host: the call enqueues everything and returns; the
+ *   kernels run on `stream`, the copies on two library-owned streams ordered after the
+ *   work already on `stream`, and `stream` waits for the last copy out.  The host arrays
+ *   must stay valid until `stream` has completed.  N and K must be multiples of 8
+ *   (FL_ERR_ALIGNMENT); FL_ERR_WORKSPACE if dev_buf is too small. */
+FL_API int fused_linear_gelu_host(const void* X, const void* W, const void* b, void* Y, int M, int N, int K,
+                                  int mode, void* dev_buf, size_t dev_buf_bytes, void* stream);
+FL_API size_t fl_linear_gelu_host_buffer_bytes(int M, int N, int K);
+
 /* Bytes of workspace fused_linear_residual_rmsnorm_fp8 needs for this shape
  * on the current device (0 for an empty problem). */
 FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);

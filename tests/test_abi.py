@@ -108,3 +108,16 @@ def test_backward_entry_points_reject_bad_arguments_on_host(lib):
     assert lib.fused_swiglu_bwd(a, a, a, None, a, 8, 16, 8, 8, 16, 16, 32, None) == fl.FL_ERR_INVALID_ARG
     assert lib.fused_swiglu_bwd(a, a, a, a, a, 8, 16, 8, 8, 16, 16, 24, None) == fl.FL_ERR_INVALID_ARG
     assert lib.fused_swiglu_bwd(None, None, None, None, None, 0, 16, 8, 8, 16, 16, 32, None) == fl.FL_OK
+
+
+def test_host_pipeline_rejects_bad_arguments_on_host(lib):
+    a = P(0x10000)
+    need = lib.fl_linear_gelu_host_buffer_bytes(64, 256, 64)
+    assert need >= 2 * (64 * 64 + 256 * 64 + 256 + 64 * 256)
+    # bad mode, missing device buffer, N not a multiple of 8, buffer too small, misaligned buffer
+    assert lib.fused_linear_gelu_host(a, a, None, a, 64, 256, 64, 3, a, need, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_gelu_host(a, a, None, a, 64, 256, 64, 1, None, need, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_gelu_host(a, a, None, a, 64, 252, 64, 1, a, need, None) == fl.FL_ERR_ALIGNMENT
+    assert lib.fused_linear_gelu_host(a, a, None, a, 64, 256, 64, 1, a, need - 1, None) == fl.FL_ERR_WORKSPACE
+    assert lib.fused_linear_gelu_host(a, a, None, a, 64, 256, 64, 1, P(0x10010), need, None) == fl.FL_ERR_ALIGNMENT
+    assert lib.fused_linear_gelu_host(None, None, None, None, 0, 256, 64, 1, None, 0, None) == fl.FL_OK

@@ -552,3 +552,27 @@ def test_backward_full_workload_sampled(name):
         out = fl.fused_swiglu_bwd(dev_bf16(ops["dO"]), dev_bf16(ops["Wd"]), dev_bf16(ops["G"]), dev_bf16(ops["U"]))
         ref = oracle.swiglu_bwd(f64(ops["dO"][rows]), f64(ops["Wd"]), f64(ops["G"][rows]), f64(ops["U"][rows]))
     assert_bf16_close(host(out[torch.from_numpy(rows).cuda()]), ref, name)
+
+
+# ------------------------------------------------------------------ host-buffer pipeline
+@pytest.mark.parametrize("M,N,K,bias", [(300, 520, 200, True), (1024, 4096, 512, False), (5, 8, 8, True)])
+def test_linear_gelu_host_pipeline(M, N, K, bias):
+    """Host buffers in and out, column blocks overlapped: the same values as the device
+    entry point bit for bit (same kernel, same accumulation order), and the oracle."""
+    X = _draw((M, K), syn.STREAM_X)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5)
+    b = _draw((N,), syn.STREAM_B, 0.5) if bias else None
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    Xh, Wh = pinned(X), pinned(W)
+    bh = pinned(b) if bias else None
+    buf = fl.linear_gelu_host_buffer(M, N, K)
+    for _ in range(2):  # the buffer and the library's streams are reused
+        Yh = fl.fused_linear_gelu_host(Xh, Wh, bh, mode="tanh", dev_buf=buf)
+        torch.cuda.current_stream().synchronize()
+        Yd = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), dev_bf16(b) if bias else None, mode="tanh")
+        assert torch.equal(Yh, Yd.cpu())
+    assert_bf16_close(host(Yh), oracle.linear_gelu(f64(X), f64(W), f64(b) if bias else None, oracle.GELU_TANH),
+                      f"host pipeline {M}x{N}x{K}")
