@@ -34,6 +34,9 @@ constexpr int kDecMaxSeg = 32;
 // first kDecHoldTiles finished feature tiles wait there for the grid-wide statistics.
 constexpr int kDecGatherSlots = 10;
 constexpr int kDecHoldTiles = 2;
+// W units (16 KB each) of its range that a CTA pulls into L2 before waiting for the
+// preceding kernel on the stream (programmatic dependent launch).
+constexpr int kDecL2PrefetchUnits = 24;
 constexpr int kDecSmemBytes = kDecStages * kDecStageBytes + 32 * 129 * 4 + 128 * 4 + 1024 + 1024;
 
 struct alignas(128) DecodeParams {
@@ -124,6 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
   const int u_end = dec_unit_begin(blockIdx.x + 1, p.units, G);
   const int f_first = u_begin / p.num_kb;  // the loops below walk units without dividing
 
+  // The next kernel on the stream may be scheduled now: it only runs on SMs this grid has
+  // left, and waits for this grid's completion before touching anything it writes.
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kDecStages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -142,6 +148,17 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.map_w);
     tma_prefetch_desc(&p.map_x);
+    // The weight stream does not depend on earlier work on the stream: start pulling the
+    // first units of this CTA's range into L2 while that work may still be finishing (an L2
+    // prefetch is coherent with any write, so this is safe whatever precedes).
+    int f = f_first, kb = u_begin - f_first * p.num_kb;
+    for (int u = u_begin; u < u_end && u < u_begin + kDecL2PrefetchUnits; ++u, ++kb) {
+      if (kb == p.num_kb) {
+        kb = 0;
+        ++f;
+      }
+      tma_prefetch_l2_2d(&p.map_w, kb * kBK, f * 128);
+    }
   }
   if (warp == 2 && u_end > u_begin) {
     // (An epilogue warp, idle until the first partial, so the weight stream starts at once.)
@@ -168,6 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // X, Z, gamma, b and the workspace may be written by the preceding kernel.
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer: W and X tiles per unit

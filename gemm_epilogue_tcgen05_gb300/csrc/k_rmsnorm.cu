@@ -130,9 +130,13 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kDecSmemBytes;
     cfg.stream = s;
+    // Programmatic dependent launch: the kernel may start on SMs the preceding kernel has left
+    // and prefetch weights into L2, then waits for that kernel (griddepcontrol.wait).  The grid
+    // never exceeds one CTA per SM, so every CTA is resident once the preceding kernel's CTAs,
+    // which never wait on this one, have left.
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, rmsnorm_fp8_decode_kernel, p) == cudaSuccess ? FL_OK : FL_ERR_CUDA;

@@ -141,6 +141,17 @@ __device__ __forceinline__ void tma_store_2d_u32(const void* map, uint32_t src_s
                : "memory");
 }
 // Hint: bring [src, src + bytes) into L2 (16-byte aligned, size a multiple of 16).
+// L2 prefetch of one tensor-map tile (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+// Programmatic dependent launch: allow the next kernel on the stream to be scheduled, and
+// wait until the preceding kernel has completed and its memory operations are visible
+// (returns at once when the kernel was not launched as a dependent).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                : "memory");

@@ -248,6 +248,46 @@ def test_rmsnorm_fp8_workspace_reuse_and_few_ctas():
         assert_fp8_close(q1, s1, q_ref, s_ref, f"reuse M={M}")
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_rmsnorm_fp8_decode_back_to_back_shared_workspace(graph):
+    """Decode calls launched back to back (programmatic dependent launches: each may start
+    while the previous one finishes) over three operand sets sharing one workspace, eagerly
+    and inside a CUDA graph: every call's output matches its own oracle result."""
+    M, N, K = 32, 2048, 1024
+    sets = [_rms_case(M, N, K, bias, seed=sd) for sd, bias in ((11, True), (12, False), (13, True))]
+    dev = [tuple(None if a is None else dev_bf16(a) for a in c) for c in sets]
+    ws = fl.rmsnorm_fp8_workspace(M, N, K)
+    order = [0, 1, 2, 0, 2, 1, 1, 0]
+    outs = [(torch.empty((M, N), dtype=torch.uint8, device="cuda"), torch.empty(M, dtype=torch.float32, device="cuda"))
+            for _ in order]
+
+    def run():
+        for (Yq, rs), j in zip(outs, order):
+            X, W, b, Z, g = dev[j]
+            fl.fused_linear_residual_rmsnorm_fp8(X, W, b, Z, g, 1e-6, Yq=Yq, row_scale=rs, workspace=ws)
+
+    if graph:
+        run()  # warm-up outside capture (module load, attributes)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            run()
+        for Yq, rs in outs:
+            Yq.zero_()
+            rs.zero_()
+        gr.replay()
+        gr.replay()
+    else:
+        run()
+    torch.cuda.synchronize()
+    refs = [oracle.rmsnorm_fp8(f64(X), f64(W), None if b is None else f64(b), f64(Z), f64(g), 1e-6)
+            for X, W, b, Z, g in sets]
+    for i, ((Yq, rs), j) in enumerate(zip(outs, order)):
+        q_ref, s_ref, _ = refs[j]
+        assert_fp8_close(Yq.cpu().numpy(), rs.cpu().numpy().astype(np.float64), q_ref, s_ref, f"call {i} (set {j})")
+    assert torch.count_nonzero(ws[:256]) == 0, "counters not reset"
+
+
 def test_rmsnorm_fp8_prefill_full_workload_sampled():
     w = syn.WORKLOADS["rmsnorm_fp8_prefill_8192x4096x14336"]
     ops = syn.make_operands(w)
