@@ -1,0 +1,326 @@
+// Decode-shaped (M <= 32 tokens) down projection + residual + RMSNorm + FP8, one thread-block
+// cluster per 128-feature tile.
+//
+// The same computation as rmsnorm_fp8_decode_kernel, organised so that no partial result
+// leaves the chip before the row statistics:
+//   * cluster f (C CTAs) owns features [128 f, 128 f + 128); CTA r of the cluster streams the
+//     k blocks [r K/C, (r+1) K/C) of that W tile (swap-AB on tcgen05: D^T[128 x 32 tokens]
+//     in TMEM), so every CTA reads the same number of W bytes;
+//   * the C partial tiles are summed through distributed shared memory, in rank order (so the
+//     result is deterministic), each CTA reducing 128/C of the features and adding bias and
+//     residual; the resulting h and the per-token partial sums of h^2 and max |h * gamma| go
+//     to the cluster leader's shared memory, and every other CTA of the cluster leaves, so
+//     the SMs free up for the next kernel on the stream;
+//   * the leaders publish their cluster's per-token partials ("GEMM Epilogue 完全拆解",
+//     §模式 A: the tile-local half of the two-level row reduction), wait for a grid-wide
+//     count (bounded spin; every cluster is resident, the host checks), merge the num_f
+//     partials per token and write the E4M3 codes and the per-token scale
+//     (§仿射量化与尾声的五步).
+// Every CTA passes the cluster barriers it shares with its peers whatever happens (errors only
+// skip work), so a timed-out wait can never leave a peer blocked at a barrier.
+#pragma once
+#include "decode_kernel.cuh"
+
+namespace fl {
+
+constexpr int kDcStages = 10;
+// W tiles (16 KB) of its k range that a CTA pulls into L2 before waiting for the preceding
+// kernel (measured back to back: 0 -> 28.6 us per call, 8 -> 27.5, 16 -> 26.9, 32 -> 29.4).
+constexpr int kDcL2PrefetchUnits = 16;
+constexpr int kDcSmallBytes = 8192;  // per-token partials (T, Sall), scales, flags
+constexpr int kDcSmemBytes = kDcStages * kDecStageBytes + kDcSmallBytes + 1024 /*bars*/ + 1024 /*align*/;
+
+template <int C>
+__global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel(const __grid_constant__ DecodeParams p) {
+  static_assert(C == 1 || C == 2 || C == 4 || C == 8, "cluster size");
+  constexpr int kRows = 128 / C;          // feature rows this CTA reduces
+  constexpr int kGroups = kRows / 8;      // groups of 8 features per token
+  constexpr int kItems = 32 * kGroups;    // (token, group) items
+  constexpr int kIpt = (kItems + 127) / 128;  // items per epilogue thread
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_mem = smem;
+  float* P = reinterpret_cast<float*>(stage_mem);  // [32 tokens][128 features] after the stream
+  uint8_t* small = smem + kDcStages * kDecStageBytes;
+  float2* T = reinterpret_cast<float2*>(small);            // [32][16] item partials (kGroups <= 16 used)
+  float2* Sall = T + 32 * 16;                              // [8][32] the ranks' per-token partials (leader)
+  float* qs_s = reinterpret_cast<float*>(Sall + 8 * 32);   // [32] 448 / max |h gamma| per token
+  volatile int* flags = reinterpret_cast<volatile int*>(qs_s + 32);  // [0] ok, [1] grid count reached
+  uint64_t* bars = reinterpret_cast<uint64_t*>(small + kDcSmallBytes);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + kDcStages;
+  uint64_t* tfull_bar = bars + 2 * kDcStages;
+  uint64_t* drain_bar = tfull_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtx wctx{abort_flag, p.status, p.timeout_ns};
+  const uint32_t rank = C > 1 ? cluster_ctarank() : 0u;
+  const int f = static_cast<int>(blockIdx.x) / C;  // feature tile of this cluster
+  const int kb0 = static_cast<int>(rank) * p.num_kb / C;
+  const int kb1 = (static_cast<int>(rank) + 1) * p.num_kb / C;
+
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDcStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    flags[0] = 1;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.map_w);
+    tma_prefetch_desc(&p.map_x);
+    // weights do not depend on earlier work on the stream: pull the first tiles into L2 now
+    for (int kb = kb0; kb < kb1 && kb < kb0 + kDcL2PrefetchUnits; ++kb) tma_prefetch_l2_2d(&p.map_w, kb * kBK, f * 128);
+  }
+  if (warp == 2) {
+    // residual rows, gamma and bias of this cluster's features into L2 (one 256-byte run each)
+    const int n0 = f * 128;
+    const uint32_t bytes = static_cast<uint32_t>(min(128, p.N - n0) * 2) & ~15u;
+    if (bytes != 0)
+      for (int t = lane; t < p.M + 2; t += 32) {
+        if (t == p.M + 1 && p.bias == nullptr) continue;
+        const __nv_bfloat16* src = t < p.M ? p.resid + static_cast<size_t>(t) * p.ldz + n0
+                                           : (t == p.M ? p.gamma + n0 : p.bias + n0);
+        bulk_prefetch_l2(src, bytes);
+      }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // X, Z, gamma, b and the workspace may be written by the preceding kernel
+
+  // ---------------------------------------------------------------- phase 1: stream W, partial tile
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      const uint64_t w_policy = l2_policy_evict_first();
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wctx, W_PRODUCER_EMPTY)) { ok = false; break; }
+        uint8_t* a_dst = stage_mem + stage * kDecStageBytes;
+        mbar_arrive_expect_tx(&full_bar[stage], kDecStageBytes);
+        tma_load_2d_hint(&p.map_w, &full_bar[stage], a_dst, kb * kBK, f * 128, w_policy);
+        tma_load_2d(&p.map_x, &full_bar[stage], a_dst + kDecABytes, kb * kBK, 0);
+        issued_mask |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == kDcStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) {
+        flags[0] = 0;
+        for (int s = 0; s < kDcStages; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_quiet(&full_bar[s], (issued_phase >> s) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kDecTokens);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, wctx, W_MMA_FULL)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(stage_mem + stage * kDecStageBytes);
+        const uint64_t adesc = sdesc_k_sw128(a_addr);
+        const uint64_t bdesc = sdesc_k_sw128(a_addr + kDecABytes);
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k)
+          mma_bf16(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        mma_commit(&empty_bar[stage]);
+        if (++stage == kDcStages) { stage = 0; phase ^= 1u; }
+      }
+      if (ok) mma_commit(tfull_bar);
+      else flags[0] = 0;
+      mma_commit(drain_bar);
+      mbar_wait_quiet(drain_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // TMEM lane quarter q = feature rows 32 q .. 32 q + 31; each thread one row, 32 tokens.
+    const int q = warp & 3;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar, 0, wctx, W_EPI_TMEM_FULL));
+    if (ok) {
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16), acc);
+      tmem_ld_wait();
+      // P[t][n]: for a fixed token the warp writes 32 consecutive floats (no bank conflict)
+      const int n = q * 32 + lane;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) P[t * 128 + n] = __uint_as_float(acc[t]);
+    } else if (lane == 0) {
+      flags[0] = 0;
+    }
+  }
+  __syncthreads();
+  if (C > 1) cluster_sync_all();  // every CTA of the cluster has its partial tile in P
+
+  // ---------------------------------------------------------------- phase 2: cluster reduce, h, statistics
+  // In the leader's shared memory: H [32 tokens][128 features] fp32 right after P, and the
+  // ranks' per-token partials Sall [C][32].
+  float* H = P + 32 * 128;
+  const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
+  bool cl_ok = flags[0] != 0;
+  if (C > 1) {
+    for (int j = 0; j < C; ++j)
+      cl_ok = cl_ok && ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(flags)), static_cast<uint32_t>(j))) != 0;
+  }
+  if (ti >= 0 && cl_ok) {
+#pragma unroll
+    for (int it = 0; it < kIpt; ++it) {
+      const int item = ti + 128 * it;
+      if (item >= kItems) continue;
+      const int t = item / kGroups, g = item % kGroups;
+      const int row = static_cast<int>(rank) * kRows + g * 8;  // first feature row within the tile
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      const uint32_t local = smem_u32(P + t * 128 + row);
+      for (int j = 0; j < C; ++j) {  // rank order: deterministic
+        const uint32_t ra = C > 1 ? mapa_shared(local, static_cast<uint32_t>(j)) : local;
+        const float4 x = C > 1 ? ld_dsmem_f4(ra) : *reinterpret_cast<const float4*>(P + t * 128 + row);
+        const float4 y = C > 1 ? ld_dsmem_f4(ra + 16) : *reinterpret_cast<const float4*>(P + t * 128 + row + 4);
+        a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+        b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+      }
+      const int n = f * 128 + row;
+      float z[8], bb[8], gg[8];
+      load_bf16x4(p.resid + static_cast<size_t>(t) * p.ldz, n, t < p.M ? p.N : 0, *reinterpret_cast<float(*)[4]>(z));
+      load_bf16x4(p.resid + static_cast<size_t>(t) * p.ldz, n + 4, t < p.M ? p.N : 0,
+                  *reinterpret_cast<float(*)[4]>(z + 4));
+      load_bf16x4(p.bias, n, p.bias ? p.N : 0, *reinterpret_cast<float(*)[4]>(bb));
+      load_bf16x4(p.bias, n + 4, p.bias ? p.N : 0, *reinterpret_cast<float(*)[4]>(bb + 4));
+      load_bf16x4(p.gamma, n, p.N, *reinterpret_cast<float(*)[4]>(gg));
+      load_bf16x4(p.gamma, n + 4, p.N, *reinterpret_cast<float(*)[4]>(gg + 4));
+      const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      float hv[8], ss = 0.f, am = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        hv[e] = s8[e] + bb[e] + z[e];  // features past N: W rows, b and z are zero there
+        ss += hv[e] * hv[e];
+        am = fmaxf(am, fabsf(hv[e] * gg[e]));
+      }
+      T[t * 16 + g] = make_float2(ss, am);
+      // h to the leader's H[t][row ..]
+      const uint32_t hl = smem_u32(H + t * 128 + row);
+      const uint32_t hr = C > 1 ? mapa_shared(hl, 0u) : hl;
+      if (C > 1) {
+        st_dsmem_f4(hr, make_float4(hv[0], hv[1], hv[2], hv[3]));
+        st_dsmem_f4(hr + 16, make_float4(hv[4], hv[5], hv[6], hv[7]));
+      } else {
+        *reinterpret_cast<float4*>(H + t * 128 + row) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<float4*>(H + t * 128 + row + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
+      }
+    }
+  }
+  __syncthreads();
+  if (ti >= 0 && ti < 32 && cl_ok) {
+    float ss = 0.f, am = 0.f;
+    for (int g = 0; g < kGroups; ++g) {
+      const float2 v = T[ti * 16 + g];
+      ss += v.x;
+      am = fmaxf(am, v.y);
+    }
+    // this rank's per-token partial to the leader's Sall[rank][t]
+    const uint32_t sl = smem_u32(Sall + rank * 32 + ti);
+    if (C > 1) st_dsmem_f2(mapa_shared(sl, 0u), make_float2(ss, am));
+    else Sall[ti] = make_float2(ss, am);
+  }
+  __syncthreads();
+  // Every read of a peer's P and every write into the leader's H and Sall is done after this
+  // barrier; the other CTAs of the cluster then leave.
+  if (C > 1) cluster_sync_all();
+  const bool leader = rank == 0;
+
+  // ---------------------------------------------------------------- phase 3: publish, grid-wide count (leaders)
+  if (leader && ti >= 0 && ti < 32 && cl_ok) {
+    float ss = 0.f, am = 0.f;
+    for (int j = 0; j < C; ++j) {  // rank order: deterministic
+      const float2 v = Sall[j * 32 + ti];
+      ss += v.x;
+      am = fmaxf(am, v.y);
+    }
+    __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + ti, make_float2(ss, am));
+    __threadfence();
+  }
+  __syncthreads();
+  if (leader && threadIdx.x == 64) {
+    bool reached = false;
+    if (cl_ok) {
+      __threadfence();
+      atomicAdd(p.counters + p.num_f, 1u);
+      reached = spin_until(p.counters + p.num_f, static_cast<unsigned>(p.num_f), p.status, p.timeout_ns, p.status,
+                           W_DECODE_ROWS, p.num_f);
+    }
+    flags[1] = reached ? 1 : 0;
+  }
+  __syncthreads();
+  const bool finish = leader && flags[1] != 0;
+
+  // ---------------------------------------------------------------- phase 4: merge statistics, quantise (leaders)
+  if (finish && ti >= 0 && ti < 32) {
+    const int t = ti;
+    float SS = 0.f, A = 0.f;
+    for (int c = 0; c < p.num_f; ++c) {  // cluster order: deterministic
+      const float2 v = __ldcg(p.stats + static_cast<size_t>(c) * kDecTokens + t);
+      SS += v.x;
+      A = fmaxf(A, v.y);
+    }
+    qs_s[t] = A > 0.f ? 448.f / A : 0.f;
+    if (f == 0 && t < p.M) p.row_scale[t] = rsqrtf(SS / static_cast<float>(p.N) + p.eps) * A * (1.f / 448.f);
+  }
+  __syncthreads();
+  if (finish && ti >= 0) {
+    // thread: token t = ti / 4, features 32 (ti % 4) .. + 31 of the tile; 32 codes, two 16-byte stores
+    const int t = ti >> 2, c0 = (ti & 3) * 32;
+    const int n = f * 128 + c0;
+    if (t < p.M && n < p.N) {
+      const float qs = qs_s[t];
+      uint32_t w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 hv = *reinterpret_cast<const float4*>(H + t * 128 + c0 + 4 * k);
+        float gg[4];
+        load_bf16x4(p.gamma, n + 4 * k, p.N, gg);
+        w[k] = f32x2_to_e4m3x2(hv.x * gg[0] * qs, hv.y * gg[1] * qs) |
+               (f32x2_to_e4m3x2(hv.z * gg[2] * qs, hv.w * gg[3] * qs) << 16);
+      }
+      uint8_t* dst = p.yq + static_cast<size_t>(t) * p.ldq + n;
+      if (n + 32 <= p.N) {  // 16-byte aligned: ldq % 16 == 0, n % 32 == 0
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < p.N) dst[j] = static_cast<uint8_t>(w[j >> 2] >> (8 * (j & 3)));
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 64 && finish) {
+    // the last leader to leave resets the counters for the next call
+    const unsigned old = atomicAdd(p.counters + p.num_f + 1, 1u);
+    if (old + 1u == static_cast<unsigned>(p.num_f)) {
+      p.counters[p.num_f] = 0u;
+      p.counters[p.num_f + 1] = 0u;
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 32);
+  }
+}
+
+}  // namespace fl

@@ -3,7 +3,12 @@
 //   "GEMM Epilogue 完全拆解" (pinghaoyang.com.cn), §模式 A and §仿射量化与尾声的五步.
 // M > 32: persistent tcgen05 kernel; the 256-column tiles of one 128-row block
 //         exchange per-row partials through the workspace inside the kernel.
-// M <= 32: split-K swap-AB decode kernel (decode_kernel.cuh).
+// M <= 32: swap-AB decode kernels: one cluster per 128-feature tile with the split-K partials
+//          reduced in distributed shared memory (decode_cluster_kernel.cuh) when every tile's
+//          cluster fits on the device at once, else split-K over all SMs (decode_kernel.cuh).
+#include <mutex>
+
+#include "decode_cluster_kernel.cuh"
 #include "decode_kernel.cuh"
 #include "host_common.h"
 
@@ -21,6 +26,85 @@ struct WsLayout {
 };
 
 bool use_decode(int M, int K) { return M <= kDecTokens && K > 0; }
+
+// Cluster decode kernel: launch configuration and the number of its clusters the device
+// can hold at once (cached per device and cluster size).
+template <int C>
+void cluster_cfg(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int grid, cudaStream_t s) {
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDcSmemBytes;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch, as for the flat decode kernel
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+}
+
+template <int C>
+int max_active_clusters(const DeviceInfo& di) {
+  static std::mutex mu;
+  static int cache[64];
+  static bool known[64];
+  if (di.device < 0 || di.device >= 64) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!known[di.device]) {
+    int n = 0;
+    const void* kfn = reinterpret_cast<const void*>(&rmsnorm_fp8_decode_cluster_kernel<C>);
+    if (ensure_smem_attr(kfn, di.device, kDcSmemBytes)) {
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr[2];
+      cluster_cfg<C>(cfg, attr, C * di.num_sms / C, nullptr);
+      cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
+      if (cudaOccupancyMaxActiveClusters(&n, kfn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+    }
+    cache[di.device] = n;
+    known[di.device] = true;
+  }
+  return cache[di.device];
+}
+
+// Cluster size for the cluster decode kernel, or 0 to run the flat split-K kernel: every
+// feature tile gets a resident cluster of C CTAs, each CTA streams at least one k block, and
+// at least three quarters of the SMs take part in the weight stream.
+int pick_decode_cluster(const DeviceInfo& di, int num_f, int num_kb, int sms) {
+  const int cs[4] = {8, 4, 2, 1};
+  for (int C : cs) {
+    if (C > num_kb || static_cast<long long>(num_f) * C > sms) continue;
+    if (4LL * num_f * C < 3LL * sms) return 0;  // too few SMs would stream: the flat kernel uses them all
+    const int fit = C == 8   ? max_active_clusters<8>(di)
+                    : C == 4 ? max_active_clusters<4>(di)
+                    : C == 2 ? max_active_clusters<2>(di)
+                             : max_active_clusters<1>(di);
+    if (fit >= num_f) return C;
+  }
+  return 0;
+}
+
+template <int C>
+int launch_decode_cluster(const DecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
+  const void* kfn = reinterpret_cast<const void*>(&rmsnorm_fp8_decode_cluster_kernel<C>);
+  if (!ensure_smem_attr(kfn, di.device, kDcSmemBytes)) return FL_ERR_CUDA;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  cluster_cfg<C>(cfg, attr, p.num_f * C, s);
+  return cudaLaunchKernelEx(&cfg, rmsnorm_fp8_decode_cluster_kernel<C>, p) == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+// SMs the decode grid may use: all of them, or fewer under fl_set_max_ctas.
+int decode_sms(const DeviceInfo& di) {
+  const int cap = max_ctas_override();
+  return cap > 0 && cap < di.num_sms ? cap : di.num_sms;
+}
 
 WsLayout layout(int M, int N, int K, int num_sms) {
   WsLayout w{};
@@ -62,7 +146,7 @@ extern "C" size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K) {
   using namespace fl;
   DeviceInfo di;
   if (current_device(&di) == FL_ERR_CUDA) return 0;
-  return layout(M, N, K, di.num_sms).total;
+  return layout(M, N, K, decode_sms(di)).total;
 }
 
 extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const void* b, const void* Z,
@@ -85,7 +169,7 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
   DeviceInfo di;
   int st = current_device(&di);
   if (st != FL_OK) return st;
-  const WsLayout wl = layout(M, N, K, di.num_sms);
+  const WsLayout wl = layout(M, N, K, decode_sms(di));
   if (workspace == nullptr || workspace_bytes < wl.total) return FL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FL_ERR_ALIGNMENT;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -122,6 +206,13 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
     p.status = device_status_ptr(di.device);
     p.timeout_ns = wait_timeout_ns();
     if (p.status == nullptr) return FL_ERR_CUDA;
+    switch (pick_decode_cluster(di, p.num_f, p.num_kb, decode_sms(di))) {
+      case 8: return launch_decode_cluster<8>(p, di, s);
+      case 4: return launch_decode_cluster<4>(p, di, s);
+      case 2: return launch_decode_cluster<2>(p, di, s);
+      case 1: return launch_decode_cluster<1>(p, di, s);
+      default: break;
+    }
     const void* kfn = reinterpret_cast<const void*>(&rmsnorm_fp8_decode_kernel);
     if (!ensure_smem_attr(kfn, di.device, kDecSmemBytes)) return FL_ERR_CUDA;
     cudaLaunchConfig_t cfg;

@@ -223,13 +223,30 @@ def test_rmsnorm_fp8_prefill_small(M, N, K, bias, ldq):
 
 
 @pytest.mark.parametrize("M,N,K,bias", [(32, 4096, 1024, False), (1, 512, 200, True), (17, 1000, 320, True),
-                                        (32, 256, 64, False)])
+                                        (32, 256, 64, False),
+                                        # cluster decode kernel with clusters of 8, 2 and 1 CTAs (4: the first case)
+                                        (32, 2048, 512, True), (8, 7680, 256, True), (5, 15360, 128, False)])
 def test_rmsnorm_fp8_decode_small(M, N, K, bias):
     X, W, b, Z, g = _rms_case(M, N, K, bias)
     ldq = -(-N // 16) * 16
     q, s = _rms_run(X, W, b, Z, g, ldq=ldq if ldq != N else None)
     q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None if b is None else f64(b), f64(Z), f64(g), 1e-6)
     assert_fp8_close(q, s, q_ref, s_ref, f"decode {M}x{N}x{K}")
+
+
+def test_rmsnorm_fp8_decode_flat_kernel_under_cta_cap():
+    """Under a CTA cap too small for one cluster per feature tile the flat split-K kernel runs;
+    both decode kernels give the oracle's codes on the same inputs."""
+    M, N, K = 24, 4096, 768
+    X, W, b, Z, g = _rms_case(M, N, K, True, seed=5)
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), f64(b), f64(Z), f64(g), 1e-6)
+    for cap in (0, 100, 40):
+        fl.set_max_ctas(cap)
+        ws = fl.rmsnorm_fp8_workspace(M, N, K)
+        q, s = _rms_run(X, W, b, Z, g, workspace=ws)
+        assert_fp8_close(q, s, q_ref, s_ref, f"cap {cap}")
+        assert torch.count_nonzero(ws[:256]) == 0, "counters not reset"
+    fl.set_max_ctas(0)
 
 
 def test_rmsnorm_fp8_workspace_reuse_and_few_ctas():
@@ -307,11 +324,13 @@ def test_rmsnorm_fp8_decode_full_workload():
     assert_fp8_close(q, s, q_ref, s_ref, "decode full")
 
 
-@pytest.mark.parametrize("M", [256, 16])
-def test_rmsnorm_fp8_wait_timeout_reports_status(M):
+@pytest.mark.parametrize("M,N", [(256, 1024), (16, 1024), (16, 4096)])
+def test_rmsnorm_fp8_wait_timeout_reports_status(M, N):
     # A counter that never reaches its target makes the exchange wait run out:
     # the kernel records FL_ERR_TIMEOUT, drains and returns; the context stays usable.
-    N, K = 1024, 128
+    # (M = 16: N = 1024 runs the flat decode kernel, N = 4096 the cluster one; both keep
+    # their grid-wide count at counters[N / 128].)
+    K = 512
     X, W, b, Z, g = _rms_case(M, N, K, False)
     ws = fl.rmsnorm_fp8_workspace(M, N, K)
     ws[:4] = torch.tensor([100, 0, 0, 0], dtype=torch.uint8)  # counters[0] = 100: never equals its target
