@@ -65,7 +65,9 @@ enum { FL_GELU_ERF = 0, FL_GELU_TANH = 1 };
  *   0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))).
  * X [M,K], W [N,K], b [N] (nullable: no bias), Y [M,N].  X, W, b and Y all have
  * dtype `dtype`: FL_BF16 (tcgen05 bf16 MMA, fp32 accumulate, one bf16 rounding
- * at the store) or FL_F32 (fp32 operands and output; computed with fp32 FMA).
+ * at the store) or FL_F32 (fp32 operands and output; on the tensor cores as three
+ * TF32 products per term, hi*hi + hi*lo + lo*hi with x = hi + lo split exactly, fp32
+ * accumulate: within ~2^-21 of each product, where one TF32 product would miss fp32 accuracy).
  * mode: FL_GELU_ERF or FL_GELU_TANH.  Y must not alias X, W or b.
  */
 FL_API int fused_linear_gelu(const void* X, const void* W, const void* b, void* Y,

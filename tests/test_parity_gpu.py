@@ -89,6 +89,35 @@ def test_gelu_tiny_fp32_workload():
     assert_f32_close(host(Y), ref, "tiny fp32 erf")
 
 
+@pytest.mark.parametrize("mode", ["erf", "tanh"])
+@pytest.mark.parametrize("M,N,K,bias", [(1, 8, 8, True), (130, 264, 72, True), (300, 520, 200, False),
+                                        (64, 256, 1000, True)])
+def test_gelu_fp32_tf32x3(mode, M, N, K, bias):
+    """fp32 operands on the tensor cores as three TF32 products: within 1e-4 of the oracle."""
+    X = _draw((M, K), syn.STREAM_X, dtype="f32")
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, dtype="f32")
+    b = _draw((N,), syn.STREAM_B, 0.5, dtype="f32") if bias else None
+    Y = fl.fused_linear_gelu(dev_f32(X), dev_f32(W), dev_f32(b) if bias else None, mode=mode)
+    m = oracle.GELU_ERF if mode == "erf" else oracle.GELU_TANH
+    ref = oracle.linear_gelu(f64(X, "f32"), f64(W, "f32"), f64(b, "f32") if bias else None, m)
+    assert_f32_close(host(Y), ref, f"fp32 {mode} {M}x{N}x{K}")
+
+
+def test_gelu_fp32_strided_and_k_zero():
+    M, N, K = 70, 296, 96
+    X = _draw((M, K + 4), syn.STREAM_X, dtype="f32")
+    W = _draw((N, K + 8), syn.STREAM_W, K ** -0.5, dtype="f32")
+    Yfull = torch.zeros((M, N + 12), dtype=torch.float32, device="cuda")
+    fl.fused_linear_gelu(dev_f32(X)[:, :K], dev_f32(W)[:, :K], None, Y=Yfull[:, :N], mode="erf")
+    ref = oracle.linear_gelu(f64(X[:, :K], "f32"), f64(W[:, :K], "f32"), None, oracle.GELU_ERF)
+    assert_f32_close(host(Yfull[:, :N]), ref, "fp32 strided")
+    assert torch.count_nonzero(Yfull[:, N:]) == 0
+    b = _draw((N,), syn.STREAM_B, 0.5, dtype="f32")
+    Y0 = fl.fused_linear_gelu(torch.empty((M, 0), dtype=torch.float32, device="cuda"),
+                              torch.empty((N, 0), dtype=torch.float32, device="cuda"), dev_f32(b), mode="tanh")
+    assert_f32_close(host(Y0), oracle.gelu(np.broadcast_to(f64(b, "f32"), (M, N)).copy(), oracle.GELU_TANH), "fp32 K=0")
+
+
 def test_gelu_full_workload_sampled():
     w = syn.WORKLOADS["gelu_tanh_8192x16384x4096"]
     ops = syn.make_operands(w)
