@@ -298,8 +298,11 @@ FL_API int fl_device_status(void* stream);
  * the default.  Process-wide; intended for tests and diagnostics. */
 FL_API void fl_set_wait_timeout_ns(uint64_t ns);
 
-/* Caps the number of CTAs of the persistent kernels (0 = one per SM).  Used by
- * tests to make each CTA walk many tiles.  Process-wide. */
+/* Caps the number of CTAs of the persistent kernels and of the decode kernels
+ * (0 = one per SM).  Used by tests to make each CTA walk many tiles, or to run the
+ * flat split-K decode kernel where the cluster one would not fit under the cap; the
+ * RMSNorm workspace size depends on it, so size the workspace under the same cap.
+ * Process-wide. */
 FL_API void fl_set_max_ctas(int n);
 
 /* Two-CTA tensor-core mode of the prefill kernels: with 1 (the default) a pair
