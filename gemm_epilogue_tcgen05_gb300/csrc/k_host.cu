@@ -1,12 +1,14 @@
 // fused_linear_gelu_host: Linear + bias + GELU on host buffers, with the copies in, the
 // GEMM and the copies out overlapped.
 //   The operation is fused_linear_gelu's ("Triton 算子融合: Linear 与 Attention", §Linear算子剖析
-//   and §GELU激活融合).  The pipeline is this library's own: X and b go up first, then W in
-//   blocks of output columns; the GEMM of a column block starts as soon as its rows of W
-//   have landed, and its columns of Y go back on a second copy stream while later blocks
-//   are still uploading or computing, so both copy engines and the tensor cores run at
-//   once.  A column block of Y is a strided region of the row-major host array and is
-//   copied with one 2-D copy.
+//   and §GELU激活融合).  The pipeline is this library's own: X is cut into row blocks and W into
+//   blocks of output columns, uploaded in an interleaved order (X0, W0, X1, ..., X(R-1), W1, ...,
+//   W(C-1)); the GEMM of output block (r, c) starts as soon as X_r and W_c have landed, and the
+//   block goes back to the host (one 2-D copy of a strided region of the row-major array) on a
+//   second copy stream while later blocks are still uploading or computing.  The first output
+//   leaves after one row block of X and one column block of W, and from then on every column
+//   block of W unlocks R output blocks, so the copy engines in both directions and the tensor
+//   cores run at once.
 #include <mutex>
 
 #include "host_common.h"
@@ -14,16 +16,19 @@
 namespace fl {
 namespace {
 
-constexpr int kHostChunks = 8;         // target number of column blocks
-constexpr int kHostMaxChunks = 16;
+constexpr int kHostColBlocks = 8;      // target number of column blocks (of whole 256-column tiles)
+constexpr int kHostRowBlocks = 4;      // target number of row blocks (of whole 128-row tiles)
+constexpr int kHostMaxCol = 16;
+constexpr int kHostMaxRow = 8;
 constexpr int kMaxHostDevices = 64;
 
 struct HostPipe {
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
-  cudaEvent_t w_ready[kHostMaxChunks] = {};
-  cudaEvent_t y_ready[kHostMaxChunks] = {};
+  cudaEvent_t x_ready[kHostMaxRow] = {};
+  cudaEvent_t w_ready[kHostMaxCol] = {};
+  cudaEvent_t y_ready[kHostMaxRow * kHostMaxCol] = {};
 };
 std::mutex g_host_mu;
 HostPipe g_pipe[kMaxHostDevices];
@@ -35,10 +40,12 @@ bool init_pipe(HostPipe& hp) {
       cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&hp.start, ev) != cudaSuccess || cudaEventCreateWithFlags(&hp.done, ev) != cudaSuccess)
     return false;
-  for (int i = 0; i < kHostMaxChunks; ++i)
-    if (cudaEventCreateWithFlags(&hp.w_ready[i], ev) != cudaSuccess ||
-        cudaEventCreateWithFlags(&hp.y_ready[i], ev) != cudaSuccess)
-      return false;
+  for (int i = 0; i < kHostMaxRow; ++i)
+    if (cudaEventCreateWithFlags(&hp.x_ready[i], ev) != cudaSuccess) return false;
+  for (int i = 0; i < kHostMaxCol; ++i)
+    if (cudaEventCreateWithFlags(&hp.w_ready[i], ev) != cudaSuccess) return false;
+  for (int i = 0; i < kHostMaxRow * kHostMaxCol; ++i)
+    if (cudaEventCreateWithFlags(&hp.y_ready[i], ev) != cudaSuccess) return false;
   hp.ready = true;
   return true;
 }
@@ -90,38 +97,57 @@ extern "C" int fused_linear_gelu_host(const void* X, const void* W, const void* 
   auto* dW = reinterpret_cast<__nv_bfloat16*>(base + L.w);
   auto* db = reinterpret_cast<__nv_bfloat16*>(base + L.b);
   auto* dY = reinterpret_cast<__nv_bfloat16*>(base + L.y);
-  const int nc = ((cdiv(N, kHostChunks) + 255) / 256) * 256;  // columns per block, whole 256-column tiles
-  const int chunks = cdiv(N, nc);
-  if (chunks > kHostMaxChunks) return FL_ERR_UNSUPPORTED;
+  const int nc = ((cdiv(N, kHostColBlocks) + 255) / 256) * 256;  // columns per block
+  const int mr = ((cdiv(M, kHostRowBlocks) + 127) / 128) * 128;    // rows per block
+  const int cols = cdiv(N, nc), rows = cdiv(M, mr);
+  if (cols > kHostMaxCol || rows > kHostMaxRow) return FL_ERR_UNSUPPORTED;
 
-  bool ok = true;
   // uploads wait for earlier work on the caller's stream (which may still read dev_buf)
-  ok = ok && cudaEventRecord(hp.start, s) == cudaSuccess && cudaStreamWaitEvent(hp.in, hp.start, 0) == cudaSuccess &&
-       cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess;
-  if (K > 0)
-    ok = ok && cudaMemcpyAsync(dX, X, static_cast<size_t>(M) * K * 2, cudaMemcpyHostToDevice, hp.in) == cudaSuccess;
-  if (b != nullptr)
-    ok = ok && cudaMemcpyAsync(db, b, static_cast<size_t>(N) * 2, cudaMemcpyHostToDevice, hp.in) == cudaSuccess;
-  for (int j = 0; j < chunks && ok; ++j) {
-    const int n0 = j * nc, ncj = N - n0 < nc ? N - n0 : nc;
-    if (K > 0)
-      ok = cudaMemcpyAsync(dW + static_cast<size_t>(n0) * K, static_cast<const __nv_bfloat16*>(W) +
-                                                                 static_cast<size_t>(n0) * K,
-                           static_cast<size_t>(ncj) * K * 2, cudaMemcpyHostToDevice, hp.in) == cudaSuccess;
-    ok = ok && cudaEventRecord(hp.w_ready[j], hp.in) == cudaSuccess;
-  }
+  if (cudaEventRecord(hp.start, s) != cudaSuccess || cudaStreamWaitEvent(hp.in, hp.start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp.out, hp.start, 0) != cudaSuccess)
+    return FL_ERR_CUDA;
+  auto up_x = [&](int r) -> bool {
+    const int m0 = r * mr, mrr = M - m0 < mr ? M - m0 : mr;
+    if (K > 0 && cudaMemcpyAsync(dX + static_cast<size_t>(m0) * K,
+                                 static_cast<const __nv_bfloat16*>(X) + static_cast<size_t>(m0) * K,
+                                 static_cast<size_t>(mrr) * K * 2, cudaMemcpyHostToDevice, hp.in) != cudaSuccess)
+      return false;
+    return cudaEventRecord(hp.x_ready[r], hp.in) == cudaSuccess;
+  };
+  auto up_w = [&](int c) -> bool {
+    const int n0 = c * nc, ncc = N - n0 < nc ? N - n0 : nc;
+    if (K > 0 && cudaMemcpyAsync(dW + static_cast<size_t>(n0) * K,
+                                 static_cast<const __nv_bfloat16*>(W) + static_cast<size_t>(n0) * K,
+                                 static_cast<size_t>(ncc) * K * 2, cudaMemcpyHostToDevice, hp.in) != cudaSuccess)
+      return false;
+    return cudaEventRecord(hp.w_ready[c], hp.in) == cudaSuccess;
+  };
+  // upload order: b, X0, W0, X1 .. X(R-1), W1 .. W(C-1)
+  bool ok = b == nullptr ||
+            cudaMemcpyAsync(db, b, static_cast<size_t>(N) * 2, cudaMemcpyHostToDevice, hp.in) == cudaSuccess;
+  ok = ok && up_x(0) && up_w(0);
+  for (int r = 1; r < rows && ok; ++r) ok = up_x(r);
+  for (int c = 1; c < cols && ok; ++c) ok = up_w(c);
   if (!ok) return FL_ERR_CUDA;
-  for (int j = 0; j < chunks; ++j) {
-    const int n0 = j * nc, ncj = N - n0 < nc ? N - n0 : nc;
-    if (cudaStreamWaitEvent(s, hp.w_ready[j], 0) != cudaSuccess) return FL_ERR_CUDA;
-    st = fused_linear_gelu(dX, dW + static_cast<size_t>(n0) * K, b != nullptr ? db + n0 : nullptr, dY + n0, M, ncj,
-                           K, K, K, N, FL_BF16, mode, s);
-    if (st != FL_OK) return st;
-    if (cudaEventRecord(hp.y_ready[j], s) != cudaSuccess || cudaStreamWaitEvent(hp.out, hp.y_ready[j], 0) != cudaSuccess ||
-        cudaMemcpy2DAsync(static_cast<__nv_bfloat16*>(Y) + n0, static_cast<size_t>(N) * 2, dY + n0,
-                          static_cast<size_t>(N) * 2, static_cast<size_t>(ncj) * 2, M, cudaMemcpyDeviceToHost,
-                          hp.out) != cudaSuccess)
-      return FL_ERR_CUDA;
+  // output blocks in the order their inputs arrive: column 0 for every row block, then column by column
+  for (int c = 0; c < cols; ++c) {
+    const int n0 = c * nc, ncc = N - n0 < nc ? N - n0 : nc;
+    if (cudaStreamWaitEvent(s, hp.w_ready[c], 0) != cudaSuccess) return FL_ERR_CUDA;
+    for (int r = 0; r < rows; ++r) {
+      const int m0 = r * mr, mrr = M - m0 < mr ? M - m0 : mr;
+      if (c == 0 && cudaStreamWaitEvent(s, hp.x_ready[r], 0) != cudaSuccess) return FL_ERR_CUDA;
+      st = fused_linear_gelu(dX + static_cast<size_t>(m0) * K, dW + static_cast<size_t>(n0) * K,
+                             b != nullptr ? db + n0 : nullptr, dY + static_cast<size_t>(m0) * N + n0, mrr, ncc, K, K,
+                             K, N, FL_BF16, mode, s);
+      if (st != FL_OK) return st;
+      cudaEvent_t e = hp.y_ready[r * kHostMaxCol + c];
+      if (cudaEventRecord(e, s) != cudaSuccess || cudaStreamWaitEvent(hp.out, e, 0) != cudaSuccess ||
+          cudaMemcpy2DAsync(static_cast<__nv_bfloat16*>(Y) + static_cast<size_t>(m0) * N + n0,
+                            static_cast<size_t>(N) * 2, dY + static_cast<size_t>(m0) * N + n0,
+                            static_cast<size_t>(N) * 2, static_cast<size_t>(ncc) * 2, mrr, cudaMemcpyDeviceToHost,
+                            hp.out) != cudaSuccess)
+        return FL_ERR_CUDA;
+    }
   }
   // the caller's stream resumes once every column block is back on the host
   if (cudaEventRecord(hp.done, hp.out) != cudaSuccess || cudaStreamWaitEvent(s, hp.done, 0) != cudaSuccess)
