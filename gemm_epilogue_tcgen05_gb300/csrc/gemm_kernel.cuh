@@ -680,6 +680,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             continue;
           }
         }
+        // GELU: the bias of the next 32-column unit is loaded while this one is computed
+        // (measured +1 % on the GELU kernels; the QKV kernels keep plain loads, -1 % otherwise)
+        constexpr bool kBiasAhead = EPI == EPI_GELU_TANH || EPI == EPI_GELU_ERF;
+        const bool has_bias = bias != nullptr;
+        uint4 bq[4];
+        if constexpr (kBiasAhead) load_raw32(bias, has_bias, n0, n_limit, bq);
 #pragma unroll 1
         for (int c = 0; c < T::kOutN / 64; ++c) {
           const uint32_t buf = ring.acquire(lane);
@@ -687,8 +693,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
           for (int u = 0; u < 2; ++u) {
             const int col0 = n0 + c * 64 + u * 32;
             float v[32], b[32];
+            if constexpr (kBiasAhead) {
+              unpack32(bq, b);
+              if (c * 2 + u + 1 < T::kOutN / 32) load_raw32(bias, has_bias, col0 + 32, n_limit, bq);
+            } else {
+              load_vec32(bias, col0, n_limit, b);
+            }
             tmem_load32f(tacc + c * 64 + u * 32, k_empty, v);
-            load_vec32(bias, col0, n_limit, b);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] += b[j];
             if constexpr (EPI == EPI_GELU_TANH) {
