@@ -78,7 +78,10 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.map_w);
     tma_prefetch_desc(&p.map_x);
-    // weights do not depend on earlier work on the stream: pull the first tiles into L2 now
+    // The weights do not depend on earlier work on the stream: pull the first tiles into L2 now,
+    // before the wait below (an L2 prefetch is coherent with any write).  Measured: issuing them
+    // here, ahead of the producer's own loads of the same tiles, beats issuing them from another
+    // warp while the producer starts (25.4 vs 27.7 us per call back to back).
     for (int kb = kb0; kb < kb1 && kb < kb0 + kDcL2PrefetchUnits; ++kb) tma_prefetch_l2_2d(&p.map_w, kb * kBK, f * 128);
   }
   if (warp == 2) {
@@ -166,6 +169,27 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
       flags[0] = 0;
     }
   }
+  // Residual, bias and gamma of this thread's items, loaded before the barrier so their
+  // latency overlaps with the wait for the peers' partial tiles.
+  const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
+  float zs[kIpt][8], bs[kIpt][8], gs[kIpt][8];
+  if (ti >= 0) {
+#pragma unroll
+    for (int it = 0; it < kIpt; ++it) {
+      const int item = ti + 128 * it;
+      const int t = item / kGroups, g = item % kGroups;
+      const int n = f * 128 + static_cast<int>(rank) * kRows + g * 8;
+      const bool in = item < kItems;
+      const __nv_bfloat16* zr = p.resid + static_cast<size_t>(in && t < p.M ? t : 0) * p.ldz;
+      const int zl = in && t < p.M ? p.N : 0, bl = in && p.bias ? p.N : 0, gl = in ? p.N : 0;
+      load_bf16x4(zr, n, zl, *reinterpret_cast<float(*)[4]>(zs[it]));
+      load_bf16x4(zr, n + 4, zl, *reinterpret_cast<float(*)[4]>(zs[it] + 4));
+      load_bf16x4(p.bias, n, bl, *reinterpret_cast<float(*)[4]>(bs[it]));
+      load_bf16x4(p.bias, n + 4, bl, *reinterpret_cast<float(*)[4]>(bs[it] + 4));
+      load_bf16x4(p.gamma, n, gl, *reinterpret_cast<float(*)[4]>(gs[it]));
+      load_bf16x4(p.gamma, n + 4, gl, *reinterpret_cast<float(*)[4]>(gs[it] + 4));
+    }
+  }
   __syncthreads();
   if (C > 1) cluster_sync_all();  // every CTA of the cluster has its partial tile in P
 
@@ -173,7 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   // In the leader's shared memory: H [32 tokens][128 features] fp32 right after P, and the
   // ranks' per-token partials Sall [C][32].
   float* H = P + 32 * 128;
-  const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
   bool cl_ok = flags[0] != 0;
   if (C > 1) {
     for (int j = 0; j < C; ++j)
@@ -195,22 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
         a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
         b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
       }
-      const int n = f * 128 + row;
-      float z[8], bb[8], gg[8];
-      load_bf16x4(p.resid + static_cast<size_t>(t) * p.ldz, n, t < p.M ? p.N : 0, *reinterpret_cast<float(*)[4]>(z));
-      load_bf16x4(p.resid + static_cast<size_t>(t) * p.ldz, n + 4, t < p.M ? p.N : 0,
-                  *reinterpret_cast<float(*)[4]>(z + 4));
-      load_bf16x4(p.bias, n, p.bias ? p.N : 0, *reinterpret_cast<float(*)[4]>(bb));
-      load_bf16x4(p.bias, n + 4, p.bias ? p.N : 0, *reinterpret_cast<float(*)[4]>(bb + 4));
-      load_bf16x4(p.gamma, n, p.N, *reinterpret_cast<float(*)[4]>(gg));
-      load_bf16x4(p.gamma, n + 4, p.N, *reinterpret_cast<float(*)[4]>(gg + 4));
       const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
       float hv[8], ss = 0.f, am = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        hv[e] = s8[e] + bb[e] + z[e];  // features past N: W rows, b and z are zero there
+        hv[e] = s8[e] + bs[it][e] + zs[it][e];  // features past N: W rows, b and z are zero there
         ss += hv[e] * hv[e];
-        am = fmaxf(am, fabsf(hv[e] * gg[e]));
+        am = fmaxf(am, fabsf(hv[e] * gs[it][e]));
       }
       T[t * 16 + g] = make_float2(ss, am);
       // h to the leader's H[t][row ..]
@@ -255,6 +269,14 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
     __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + ti, make_float2(ss, am));
     __threadfence();
   }
+  // gamma of this thread's quantisation slice (token ti / 4, features 32 (ti % 4) ..), loaded
+  // before the grid-wide wait
+  float gq[32];
+  if (leader && ti >= 0) {
+    const int n = f * 128 + (ti & 3) * 32;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) load_bf16x4(p.gamma, n + 4 * k, p.N, *reinterpret_cast<float(*)[4]>(gq + 4 * k));
+  }
   __syncthreads();
   if (leader && threadIdx.x == 64) {
     bool reached = false;
@@ -273,10 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   if (finish && ti >= 0 && ti < 32) {
     const int t = ti;
     float SS = 0.f, A = 0.f;
-    for (int c = 0; c < p.num_f; ++c) {  // cluster order: deterministic
-      const float2 v = __ldcg(p.stats + static_cast<size_t>(c) * kDecTokens + t);
-      SS += v.x;
-      A = fmaxf(A, v.y);
+    for (int c0 = 0; c0 < p.num_f; c0 += 32) {  // cluster order: deterministic; 32 loads in flight
+      float2 w[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        w[j] = c0 + j < p.num_f ? __ldcg(p.stats + static_cast<size_t>(c0 + j) * kDecTokens + t) : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        SS += w[j].x;
+        A = fmaxf(A, w[j].y);
+      }
     }
     qs_s[t] = A > 0.f ? 448.f / A : 0.f;
     if (f == 0 && t < p.M) p.row_scale[t] = rsqrtf(SS / static_cast<float>(p.N) + p.eps) * A * (1.f / 448.f);
@@ -292,8 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const float4 hv = *reinterpret_cast<const float4*>(H + t * 128 + c0 + 4 * k);
-        float gg[4];
-        load_bf16x4(p.gamma, n + 4 * k, p.N, gg);
+        const float* gg = gq + 4 * k;
         w[k] = f32x2_to_e4m3x2(hv.x * gg[0] * qs, hv.y * gg[1] * qs) |
                (f32x2_to_e4m3x2(hv.z * gg[2] * qs, hv.w * gg[3] * qs) << 16);
       }
