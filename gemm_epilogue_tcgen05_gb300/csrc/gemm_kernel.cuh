@@ -13,9 +13,14 @@
 //   warps 2..5  epilogue: tcgen05.ld -> registers -> tile function -> smem ->
 //               TMA store; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31,
 //               i.e. tile rows 32*(w%4)+lane, one row per thread.
-// Tiles are walked in a static persistent order (tile = blockIdx.x + i*gridDim.x)
+// CG = 2 (the default): two CTAs on neighbouring SMs form a cluster and compute a
+// 256-row tile with tcgen05.mma.cta_group::2; each loads its 128 rows of X and half
+// of the W tile, the leader issues the MMAs and multicasts its commits.  CG = 1:
+// one CTA per 128-row tile.  B is K-major (W stored [N, K]) or, for the dgrad
+// epilogues, MN-major (W stored [K, N]).
+// Tiles are walked in a static persistent order (tile = blockIdx.x / CG + i * clusters)
 // with grouped rasterisation so that concurrently running CTAs share X and W
-// panels in L2.
+// panels in L2; the RMSNorm epilogue walks them row-major (raster groups of one row block).
 #pragma once
 #include "ptx.cuh"
 
