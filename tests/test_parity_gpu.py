@@ -664,3 +664,57 @@ def test_linear_gelu_host_pipeline(M, N, K, bias):
         assert torch.equal(Yh, Yd.cpu())
     assert_bf16_close(host(Yh), oracle.linear_gelu(f64(X), f64(W), f64(b) if bias else None, oracle.GELU_TANH),
                       f"host pipeline {M}x{N}x{K}")
+
+
+# ------------------------------------------------------------------ CUDA graphs
+def test_graph_capture_of_every_entry_point_matches_eager():
+    """One call of each kind captured in a CUDA graph (cooperative and cluster launches,
+    workspace counters reset by the kernels) replays bit-identically to eager execution:
+    every reduction merges in a fixed order."""
+    M, N, K = 300, 512, 192
+    X = dev_bf16(_draw((M, K), syn.STREAM_X))
+    W = dev_bf16(_draw((N, K), syn.STREAM_W, K ** -0.5))
+    b = dev_bf16(_draw((N,), syn.STREAM_B, 0.5))
+    Z = dev_bf16(_draw((M, N), syn.STREAM_Z))
+    g = dev_bf16(_draw((N,), syn.STREAM_GAMMA, 0.1, 1.0))
+    Wt = dev_bf16(_draw((K, N), syn.STREAM_W2, K ** -0.5))           # [K, N] as stored, for the dgrad
+    W1 = dev_bf16(_draw((256, N), syn.STREAM_W2, N ** -0.5, seed=1))  # second GEMM of the chain
+    Wq = dev_bf16(_draw((3 * 256, K), syn.STREAM_WUP, K ** -0.5))   # 2 heads of 128
+    Xd = X[:16].contiguous()
+    Zd = dev_bf16(_draw((16, 4096), syn.STREAM_Z, seed=2))
+    Wd = dev_bf16(_draw((4096, K), syn.STREAM_W, K ** -0.5, seed=2))
+    gd = dev_bf16(_draw((4096,), syn.STREAM_GAMMA, 0.1, 1.0, seed=2))
+    lab = torch.from_numpy(syn.draw_labels(0, syn.STREAM_LABEL, M, N)).cuda()
+    Xf, Wf = X.float(), W.float()
+    ws_p = fl.rmsnorm_fp8_workspace(M, N, K)
+    ws_d = fl.rmsnorm_fp8_workspace(16, 4096, K)
+    ws_c = fl.cross_entropy_workspace(M, N)
+    parts = torch.empty((fl.rms_partials_per_row(N), M), dtype=torch.float32, device="cuda")
+
+    def run():
+        outs = [fl.fused_linear_gelu(X, W, b, mode="tanh"),
+                *fl.fused_qkv_rope(X, Wq, None, n_heads=2, head_dim=128, seq_len=64),
+                fl.fused_swiglu(X, W, W),
+                *fl.fused_linear_residual_rmsnorm_fp8(X, W, b, Z, g, 1e-6, workspace=ws_p),
+                *fl.fused_linear_residual_rmsnorm_fp8(Xd, Wd, None, Zd, gd, 1e-6, workspace=ws_d)]
+        h2, _, _ = fl.fused_linear_residual_gamma(X, W, b, Z, g, store_h1=False, rms_partials=parts)
+        outs.append(fl.fused_linear_rms_rowscale(h2, W1, None, parts, N, 1e-6))
+        outs.append(fl.fused_linear_cross_entropy(X, W, None, lab, workspace=ws_c)[0])
+        outs += list(fl.fused_linear_quant(X, W, b, fl.QUANT_NVFP4_G16))
+        outs.append(fl.fused_dgrad_gelu(X, Wt, Z, mode="erf"))
+        outs.append(fl.fused_linear_gelu(Xf, Wf, None, mode="erf"))
+        return outs
+
+    eager = [t.clone() for t in run()]
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        captured = run()
+    for _ in range(2):
+        for t in captured:
+            t.zero_()
+        gr.replay()
+        torch.cuda.synchronize()
+        for i, (a, c) in enumerate(zip(eager, captured)):
+            assert torch.equal(a, c), f"output {i} differs after replay"
+    assert torch.count_nonzero(ws_p[:256]) == 0 and torch.count_nonzero(ws_c[:256]) == 0
