@@ -68,6 +68,11 @@ def peaks():
                 "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS, "source": "fallback"}
 
 
+# Vendor figures for context beside the measured peaks: dense bf16 tensor rate and HBM3e bandwidth.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_epilogue_tcgen05_gb300", "csrc")
@@ -604,6 +609,7 @@ def main():
                 "frac": kernel_tflops / peak, "traffic": traffic,
                 "peak_source": f"bf16 {which}, {'of measured' if pk['source'] == 'measured' else 'of fallback'}",
                 "frac_of_burst_peak": kernel_tflops / pk["bf16_tflops"],
+                "frac_of_nominal": kernel_tflops / NOMINAL_BF16_TFLOPS, "nominal": NOMINAL_BF16_TFLOPS,
                 "algorithmic_bytes": head.bytes, "traffic_unit": "bytes per launch (ncu dram read + write)"}
     head_unfused = time_fn(unfused_fn(head), 20, 3, flush)
     e_times, h2d, d2h = time_e2e(head, max(3, min(args.steps, 100) // 2), 2, barrier)
@@ -634,6 +640,7 @@ def main():
                                                "timing": "one launch, L2 flushed before it"},
                              "roofline": {"bound": "hbm", "achieved": g_ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                           "frac": g_ach / pk["hbm_gbs"], "traffic": recorded_traffic(name),
+                                          "frac_of_nominal": g_ach / NOMINAL_HBM_GBS,
                                           "algorithmic_bytes": c.bytes},
                              "unfused_torch_us": unf * 1e3, "speedup_vs_unfused": unf / m})
             else:
@@ -641,6 +648,7 @@ def main():
                 rows.append({"workload": name, "value": ach, "unit": "TFLOP/s", "ms_per_launch": m,
                              "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
                                           "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
+                                          "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS,
                                           "traffic": recorded_traffic(name), "algorithmic_bytes": c.bytes},
                              "unfused_torch_ms": unf, "speedup_vs_unfused": unf / m})
             del c
