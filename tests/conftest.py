@@ -20,3 +20,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Table of the parity comparisons made in this session (GPU against the oracle)."""
+    try:
+        from parity_utils import REPORT
+    except ImportError:
+        return
+    if not REPORT:
+        return
+    tr = terminalreporter
+    tr.section("parity against the fp64 oracle")
+    for r in REPORT:
+        stats = "  ".join(f"{k}={v:.3g}" for k, v in r.items() if k not in ("kind", "what", "n"))
+        tr.write_line(f"{r['kind']:10s} | {r['what'][:60]:60s} | n {r['n']:<9d} | {stats}")

@@ -12,6 +12,14 @@ BF16_ATOL, BF16_RTOL = 2e-2, 1e-2
 F32_ATOL = 1e-4
 SCALE_RTOL = 1e-3
 
+# Error statistics of every comparison, printed as a table at the end of a test session
+# (tol_used: the largest error as a fraction of the allowed one).
+REPORT = []
+
+
+def _record(kind: str, what: str, n: int, **stats):
+    REPORT.append({"kind": kind, "what": what, "n": int(n), **{k: float(v) for k, v in stats.items()}})
+
 
 def dev_bf16(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
@@ -31,6 +39,8 @@ def host(t: torch.Tensor) -> np.ndarray:
 
 def assert_bf16_close(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
     err = np.abs(gpu - ref)
+    _record("bf16", what, err.size, max_abs=err.max(initial=0),
+            tol_used=(err / (BF16_ATOL + BF16_RTOL * np.abs(ref))).max(initial=0))
     bad = err > BF16_ATOL + BF16_RTOL * np.abs(ref)
     assert not bad.any(), (f"{what}: {int(bad.sum())}/{bad.size} outside 2e-2+1e-2|ref|; "
                            f"max abs err {err.max():.4g} at {np.unravel_index(np.argmax(err), err.shape)}")
@@ -39,6 +49,7 @@ def assert_bf16_close(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
 
 def assert_f32_close(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
     err = np.abs(gpu - ref)
+    _record("fp32", what, err.size, max_abs=err.max(initial=0), tol_used=err.max(initial=0) / F32_ATOL)
     assert err.max() <= F32_ATOL, f"{what}: max abs err {err.max():.3g} > 1e-4"
 
 
@@ -49,6 +60,8 @@ def ordered_e4m3(codes: np.ndarray) -> np.ndarray:
 
 def assert_fp8_close(codes: np.ndarray, scale: np.ndarray, q_ref: np.ndarray, s_ref: np.ndarray, what=""):
     d = np.abs(ordered_e4m3(codes) - ordered_e4m3(q_ref))
+    _record("e4m3", what, d.size, max_code_dist=d.max(initial=0), frac_codes_differ=np.mean(d != 0),
+            scale_max_rel=(np.abs(scale - s_ref) / np.maximum(np.abs(s_ref), 1e-30)).max(initial=0))
     assert d.max() <= 1, f"{what}: code distance {d.max()} at {np.unravel_index(np.argmax(d), d.shape)}"
     rel = np.abs(scale - s_ref) / np.maximum(np.abs(s_ref), 1e-30)
     assert rel.max() <= SCALE_RTOL, f"{what}: scale rel err {rel.max():.3g}"
@@ -113,6 +126,8 @@ def assert_quant_close(fmt: int, codes, scales, q_ref, s_ref, y_ref, decode, wha
         rel = np.abs(s_val - s_ref) / np.maximum(np.abs(s_ref), 1e-30)
         assert rel.max() <= SCALE_RTOL, f"{what}: scale rel err {rel.max():.3g}"
     d = np.abs(oc - orf)
+    _record({0: "fp8 1x128", 1: "int4 g32", 2: "nvfp4 g16"}[fmt], what, d.size, max_code_dist=d.max(initial=0),
+            frac_codes_differ=np.mean(d != 0))
     mask = same_scale[:, blk]
     assert d[mask].max(initial=0) <= 1, f"{what}: code distance {d[mask].max()}"
     assert np.mean(d != 0) < 0.02, f"{what}: {np.mean(d != 0):.3%} of codes differ"

@@ -35,15 +35,16 @@ def _draw(shape, stream, std=1.0, mean=0.0, seed=0, dtype="bf16"):
 
 
 # ------------------------------------------------------------------ GELU
+@pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("mode", ["tanh", "erf"])
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (130, 264, 72), (300, 520, 200), (256, 256, 1024)])
-def test_gelu_small(mode, M, N, K):
-    X = _draw((M, K), syn.STREAM_X)
-    W = _draw((N, K), syn.STREAM_W, K ** -0.5)
-    b = _draw((N,), syn.STREAM_B, 0.02)
+def test_gelu_small(mode, M, N, K, seed):
+    X = _draw((M, K), syn.STREAM_X, seed=seed)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=seed)
+    b = _draw((N,), syn.STREAM_B, 0.02, seed=seed)
     Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), dev_bf16(b), mode=mode)
     m = oracle.GELU_TANH if mode == "tanh" else oracle.GELU_ERF
-    assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), f64(b), m), f"gelu {mode} {M}x{N}x{K}")
+    assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), f64(b), m), f"gelu {mode} {M}x{N}x{K} seed {seed}")
 
 
 def test_gelu_no_bias_and_k_zero():
