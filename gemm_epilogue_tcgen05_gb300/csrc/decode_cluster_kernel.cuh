@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
     for (int j = 0; j < C; ++j)
       cl_ok = cl_ok && ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(flags)), static_cast<uint32_t>(j))) != 0;
   }
+  float hk[kIpt][8];  // this thread's h values, pushed to the leader after the statistics
   if (ti >= 0 && cl_ok) {
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
@@ -227,16 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
         am = fmaxf(am, fabsf(hv[e] * gs[it][e]));
       }
       T[t * 16 + g] = make_float2(ss, am);
-      // h to the leader's H[t][row ..]
-      const uint32_t hl = smem_u32(H + t * 128 + row);
-      const uint32_t hr = C > 1 ? mapa_shared(hl, 0u) : hl;
-      if (C > 1) {
-        st_dsmem_f4(hr, make_float4(hv[0], hv[1], hv[2], hv[3]));
-        st_dsmem_f4(hr + 16, make_float4(hv[4], hv[5], hv[6], hv[7]));
-      } else {
-        *reinterpret_cast<float4*>(H + t * 128 + row) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<float4*>(H + t * 128 + row + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
-      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) hk[it][e] = hv[e];
     }
   }
   __syncthreads();
@@ -253,9 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
     else Sall[ti] = make_float2(ss, am);
   }
   __syncthreads();
-  // Every read of a peer's P and every write into the leader's H and Sall is done after this
-  // barrier; the other CTAs of the cluster then leave.
-  if (C > 1) cluster_sync_all();
+  if (C > 1) cluster_sync_all();  // the leader has every rank's per-token partials (Sall)
   const bool leader = rank == 0;
 
   // ---------------------------------------------------------------- phase 3: publish, grid-wide count (leaders)
@@ -278,14 +269,37 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
     for (int k = 0; k < 8; ++k) load_bf16x4(p.gamma, n + 4 * k, p.N, *reinterpret_cast<float(*)[4]>(gq + 4 * k));
   }
   __syncthreads();
-  if (leader && threadIdx.x == 64) {
-    bool reached = false;
-    if (cl_ok) {
-      __threadfence();
-      atomicAdd(p.counters + p.num_f, 1u);
-      reached = spin_until(p.counters + p.num_f, static_cast<unsigned>(p.num_f), p.status, p.timeout_ns, p.status,
-                           W_DECODE_ROWS, p.num_f);
+  if (leader && threadIdx.x == 64 && cl_ok) {
+    // publish before the h values move: the grid-wide count starts as early as possible
+    __threadfence();
+    atomicAdd(p.counters + p.num_f, 1u);
+  }
+  // h to the leader's H[t][row ..], then the peers are done
+  if (ti >= 0 && cl_ok) {
+#pragma unroll
+    for (int it = 0; it < kIpt; ++it) {
+      const int item = ti + 128 * it;
+      if (item >= kItems) continue;
+      const int t = item / kGroups, g = item % kGroups;
+      const int row = static_cast<int>(rank) * kRows + g * 8;
+      const uint32_t hl = smem_u32(H + t * 128 + row);
+      if (C > 1) {
+        const uint32_t hr = mapa_shared(hl, 0u);
+        st_dsmem_f4(hr, make_float4(hk[it][0], hk[it][1], hk[it][2], hk[it][3]));
+        st_dsmem_f4(hr + 16, make_float4(hk[it][4], hk[it][5], hk[it][6], hk[it][7]));
+      } else {
+        *reinterpret_cast<float4*>(H + t * 128 + row) = make_float4(hk[it][0], hk[it][1], hk[it][2], hk[it][3]);
+        *reinterpret_cast<float4*>(H + t * 128 + row + 4) = make_float4(hk[it][4], hk[it][5], hk[it][6], hk[it][7]);
+      }
     }
+  }
+  __syncthreads();
+  // Every read of a peer's P and every write into the leader's H is done after this barrier;
+  // the other CTAs of the cluster then leave.
+  if (C > 1) cluster_sync_all();
+  if (leader && threadIdx.x == 64) {
+    const bool reached = cl_ok && spin_until(p.counters + p.num_f, static_cast<unsigned>(p.num_f), p.status,
+                                             p.timeout_ns, p.status, W_DECODE_ROWS, p.num_f);
     flags[1] = reached ? 1 : 0;
   }
   __syncthreads();
