@@ -138,6 +138,12 @@ def _vec(t, name, dtype, n):
     return t
 
 
+def _out(rows: int, cols: int, dtype, device):
+    """An output [rows, cols] whose row pitch is rounded up to 16 bytes (the TMA store rule)."""
+    per = 16 // torch.empty((), dtype=dtype).element_size()
+    return torch.empty((rows, -(-cols // per) * per), dtype=dtype, device=device)[:, :cols]
+
+
 def _ld(t, width, fallback):
     # Leading dimension of a [rows, width] row-major matrix.  A one-row matrix
     # never reads past its first row, so any pitch >= width works; take one
@@ -158,7 +164,7 @@ def fused_linear_gelu(X, W, b=None, Y=None, mode: str = "tanh", stream=None):
     _mat(W, "W", dtype)
     _vec(b, "b", dtype, N)
     if Y is None:
-        Y = torch.empty((M, N), dtype=dtype, device=X.device)
+        Y = _out(M, N, dtype, X.device)
     _mat(Y, "Y", dtype)
     m = {"erf": FL_GELU_ERF, "tanh": FL_GELU_TANH}[mode]
     st = load().fused_linear_gelu(_ptr(X), _ptr(W), _ptr(b), _ptr(Y), M, N, K, _ld(X, K, K), _ld(W, K, K),
@@ -278,7 +284,7 @@ def fused_swiglu(X, Wgate, Wup, bgate=None, bup=None, Y=None, stream=None):
     _vec(bgate, "bgate", torch.bfloat16, N)
     _vec(bup, "bup", torch.bfloat16, N)
     if Y is None:
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+        Y = _out(M, N, torch.bfloat16, X.device)
     _mat(Y, "Y", torch.bfloat16)
     st = load().fused_swiglu(_ptr(X), _ptr(Wgate), _ptr(Wup), _ptr(bgate), _ptr(bup), _ptr(Y), M, N, K,
                              _ld(X, K, K), _ld(Wgate, K, K), _ld(Y, N, N), _stream(stream))
@@ -306,8 +312,8 @@ def fused_linear_residual_rmsnorm_fp8(X, W, b, Z, gamma, eps: float = 1e-6, Yq=N
     _mat(Z, "Z", torch.bfloat16)
     _vec(b, "b", torch.bfloat16, N)
     _vec(gamma, "gamma", torch.bfloat16, N)
-    if Yq is None:
-        Yq = torch.empty((M, N), dtype=torch.uint8, device=X.device)
+    if Yq is None:  # row pitch rounded up to 16 bytes, as the TMA store needs
+        Yq = _out(M, N, torch.uint8, X.device)
     if Yq.dtype != torch.uint8:
         Yq = Yq.view(torch.uint8)
     _mat(Yq, "Yq", torch.uint8)
@@ -339,9 +345,9 @@ def fused_linear_residual_gamma(X, W, b, Z, gamma, store_h1: bool = True, H2=Non
     _vec(b, "b", torch.bfloat16, N)
     _vec(gamma, "gamma", torch.bfloat16, N)
     if H2 is None:
-        H2 = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+        H2 = _out(M, N, torch.bfloat16, X.device)
     if H1 is None and store_h1:
-        H1 = torch.empty_like(H2)
+        H1 = _out(M, N, torch.bfloat16, X.device)
     _mat(H2, "H2", torch.bfloat16)
     if H1 is not None and (_mat(H1, "H1", torch.bfloat16) != _mat(H2, "H2", torch.bfloat16) and M > 1):
         raise ValueError("H1 and H2 must share one leading dimension")
@@ -365,7 +371,7 @@ def fused_linear_rms_rowscale(H2, W1, b1, rms_partials, n_norm: int, eps: float 
     _mat(W1, "W1", torch.bfloat16)
     _vec(b1, "b1", torch.bfloat16, N)
     if Y is None:
-        Y = torch.empty((M, N), dtype=torch.bfloat16, device=H2.device)
+        Y = _out(M, N, torch.bfloat16, H2.device)
     _mat(Y, "Y", torch.bfloat16)
     st = load().fused_linear_rms_rowscale(_ptr(H2), _ptr(W1), _ptr(b1), _ptr(rms_partials), int(n_norm), float(eps),
                                           _ptr(Y), M, N, K, _ld(H2, K, K), _ld(W1, K, K), _ld(Y, N, N),
@@ -393,7 +399,7 @@ def fused_linear_cross_entropy(X, W, b, labels, loss=None, logits=None, store_lo
         loss = torch.empty(M, dtype=torch.float32, device=X.device)
     _vec(loss, "loss", torch.float32, M)
     if logits is None and store_logits:
-        logits = torch.empty((M, V), dtype=torch.bfloat16, device=X.device)
+        logits = _out(M, V, torch.bfloat16, X.device)
     ldl = 0
     if logits is not None:
         _mat(logits, "logits", torch.bfloat16)
@@ -429,7 +435,7 @@ def fused_linear_quant(X, W, b=None, fmt: int = QUANT_FP8_1X128, Yq=None, scales
     nblocks = -(-N // QUANT_BLOCK[fmt])
     sdt = torch.uint8 if fmt == QUANT_NVFP4_G16 else torch.float32
     if Yq is None:  # row pitch rounded up to 16 bytes, as the TMA store needs
-        Yq = torch.empty((M, -(-qbytes // 16) * 16), dtype=torch.uint8, device=X.device)[:, :qbytes]
+        Yq = _out(M, qbytes, torch.uint8, X.device)
     if scales is None:
         scales = torch.empty((M, nblocks), dtype=sdt, device=X.device)
     _mat(Yq, "Yq", torch.uint8)
@@ -453,7 +459,7 @@ def fused_dgrad_gelu(dZ, W, H, mode: str = "tanh", dH=None, stream=None):
     if tuple(H.shape) != (M, N):
         raise ValueError("H must be [M, N]")
     if dH is None:
-        dH = torch.empty((M, N), dtype=torch.bfloat16, device=dZ.device)
+        dH = _out(M, N, torch.bfloat16, dZ.device)
     _mat(dH, "dH", torch.bfloat16)
     if mode not in ("tanh", "erf"):
         raise ValueError("mode must be 'tanh' or 'erf'")
@@ -478,7 +484,7 @@ def fused_swiglu_bwd(dO, Wd, G, U, dGU=None, stream=None):
     if tuple(G.shape) != (M, N) or tuple(U.shape) != (M, N) or _ld(G, N, N) != _ld(U, N, N):
         raise ValueError("G and U must be [M, N] with one shared pitch")
     if dGU is None:
-        dGU = torch.empty((M, 2 * N), dtype=torch.bfloat16, device=dO.device)
+        dGU = _out(M, 2 * N, torch.bfloat16, dO.device)
     _mat(dGU, "dGU", torch.bfloat16)
     st = load().fused_swiglu_bwd(_ptr(dO), _ptr(Wd), _ptr(G), _ptr(U), _ptr(dGU), M, N, K, _ld(dO, K, K),
                                  _ld(Wd, N, N), _ld(G, N, N), _ld(dGU, 2 * N, 2 * N), _stream(stream))

@@ -719,3 +719,149 @@ def test_graph_capture_of_every_entry_point_matches_eager():
         for i, (a, c) in enumerate(zip(eager, captured)):
             assert torch.equal(a, c), f"output {i} differs after replay"
     assert torch.count_nonzero(ws_p[:256]) == 0 and torch.count_nonzero(ws_c[:256]) == 0
+
+
+# ------------------------------------------------------------------ random shapes, streams, threads
+def _rand_shapes(seed, count, m_max=600, n_max=1200, k_max=700):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        M = int(rng.integers(1, m_max))
+        N = int(rng.integers(1, n_max // 8)) * 8      # 16-byte row pitches in bf16
+        K = int(rng.integers(1, k_max // 8)) * 8
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("pairing", [True, False])
+def test_random_shapes_gelu_swiglu_quant_dgrad(pairing):
+    """Seeded random shapes (ragged in M, N and K) for four epilogues, against the oracle."""
+    fl.set_cta_pairing(pairing)
+    for i, (M, N, K) in enumerate(_rand_shapes(7 + pairing, 6)):
+        X = _draw((M, K), syn.STREAM_X, seed=i)
+        W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=i)
+        b = _draw((N,), syn.STREAM_B, 0.3, seed=i)
+        mode = "tanh" if i % 2 else "erf"
+        Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), dev_bf16(b), mode=mode)
+        m = oracle.GELU_TANH if mode == "tanh" else oracle.GELU_ERF
+        assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), f64(b), m), f"random gelu {M}x{N}x{K}")
+        Wu = _draw((N, K), syn.STREAM_WUP, K ** -0.5, seed=i)
+        Ys = fl.fused_swiglu(dev_bf16(X), dev_bf16(W), dev_bf16(Wu))
+        assert_bf16_close(host(Ys), oracle.swiglu(f64(X), f64(W), f64(Wu)), f"random swiglu {M}x{N}x{K}")
+        if N % 16 == 0:
+            fmt = i % 3
+            Yq, S = fl.fused_linear_quant(dev_bf16(X), dev_bf16(W), dev_bf16(b), fmt)
+            q_ref, s_ref, y_ref = oracle.linear_quant(f64(X), f64(W), f64(b), fmt)
+            e2m1 = np.array([oracle.e2m1_decode(c) for c in range(16)])
+            dec = {"scale": oracle.e4m3_decode,
+                   "value": (oracle.e4m3_decode if fmt == 0 else
+                             (lambda c: np.where(c & 8, c.astype(np.int32) - 16, c).astype(np.float64)) if fmt == 1 else
+                             (lambda c: e2m1[c]))}
+            assert_quant_close(fmt, Yq.cpu().numpy(), S.cpu().numpy(), q_ref, s_ref, y_ref, dec,
+                               f"random quant {fmt} {M}x{N}x{K}")
+        Wt = _draw((K, N), syn.STREAM_W2, K ** -0.5, seed=i)
+        H = _draw((M, N), syn.STREAM_Z, 2.0, seed=i)
+        dH = fl.fused_dgrad_gelu(dev_bf16(X), dev_bf16(Wt), dev_bf16(H), mode=mode)
+        assert_bf16_close(host(dH), oracle.dgrad_gelu(f64(X), f64(Wt), f64(H), m), f"random dgrad {M}x{N}x{K}")
+
+
+def test_random_shapes_rmsnorm_and_cross_entropy():
+    for i, (M, N, K) in enumerate(_rand_shapes(11, 6, n_max=2000)):
+        X, W, b, Z, g = _rms_case(M, N, K, i % 2 == 0, seed=i)
+        q, s = _rms_run(X, W, b, Z, g)
+        q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None if b is None else f64(b), f64(Z), f64(g), 1e-6)
+        assert_fp8_close(q, s, q_ref, s_ref, f"random rmsnorm {M}x{N}x{K}")
+        Md = int(np.random.default_rng(i).integers(1, 33))  # decode shape
+        q, s = _rms_run(X[:Md], W, b, Z[:Md], g)
+        q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X[:Md]), f64(W), None if b is None else f64(b), f64(Z[:Md]),
+                                             f64(g), 1e-6)
+        assert_fp8_close(q, s, q_ref, s_ref, f"random rmsnorm decode {Md}x{N}x{K}")
+        lab = syn.draw_labels(i, syn.STREAM_LABEL, M, N)
+        loss, _ = fl.fused_linear_cross_entropy(dev_bf16(X), dev_bf16(W), None, torch.from_numpy(lab).cuda())
+        _assert_loss_close(loss.cpu().numpy().astype(np.float64),
+                           oracle.linear_cross_entropy(f64(X), f64(W), None, lab), f"random ce {M}x{N}x{K}")
+
+
+def test_two_streams_interleaved():
+    """Launches alternating between two streams (each with its own workspaces) give the same
+    results as on the default stream."""
+    M, N, K = 300, 1024, 256
+    X = dev_bf16(_draw((M, K), syn.STREAM_X))
+    W = dev_bf16(_draw((N, K), syn.STREAM_W, K ** -0.5))
+    Z = dev_bf16(_draw((M, N), syn.STREAM_Z))
+    g = dev_bf16(_draw((N,), syn.STREAM_GAMMA, 0.1, 1.0))
+    ref_gelu = fl.fused_linear_gelu(X, W, None).clone()
+    ref_q, ref_s = [t.clone() for t in fl.fused_linear_residual_rmsnorm_fp8(X, W, None, Z, g, 1e-6)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ws = [fl.rmsnorm_fp8_workspace(M, N, K) for _ in streams]
+    outs = []
+    for it in range(6):
+        k = it % 2
+        with torch.cuda.stream(streams[k]):
+            outs.append((fl.fused_linear_gelu(X, W, None, stream=streams[k]),
+                         fl.fused_linear_residual_rmsnorm_fp8(X, W, None, Z, g, 1e-6, workspace=ws[k],
+                                                              stream=streams[k])))
+    torch.cuda.synchronize()
+    for y, (q, s) in outs:
+        assert torch.equal(y, ref_gelu) and torch.equal(q, ref_q) and torch.equal(s, ref_s)
+
+
+def test_host_threads_on_separate_streams():
+    """Four host threads, each with its own stream and workspace, call the library concurrently
+    (the ctypes calls release the interpreter lock): every result matches the single-thread one."""
+    import threading
+    M, N, K = 200, 768, 192
+    X = dev_bf16(_draw((M, K), syn.STREAM_X))
+    W = dev_bf16(_draw((N, K), syn.STREAM_W, K ** -0.5))
+    Z = dev_bf16(_draw((M, N), syn.STREAM_Z))
+    g = dev_bf16(_draw((N,), syn.STREAM_GAMMA, 0.1, 1.0))
+    lab = torch.from_numpy(syn.draw_labels(0, syn.STREAM_LABEL, M, N)).cuda()
+    ref = (fl.fused_linear_gelu(X, W, None, mode="erf").clone(),
+           *[t.clone() for t in fl.fused_linear_residual_rmsnorm_fp8(X, W, None, Z, g, 1e-6)],
+           fl.fused_linear_cross_entropy(X, W, None, lab)[0].clone())
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(tid):
+        try:
+            st = torch.cuda.Stream()
+            ws = fl.rmsnorm_fp8_workspace(M, N, K)
+            wc = fl.cross_entropy_workspace(M, N)
+            with torch.cuda.stream(st):
+                for _ in range(5):
+                    y = fl.fused_linear_gelu(X, W, None, mode="erf", stream=st)
+                    q, s = fl.fused_linear_residual_rmsnorm_fp8(X, W, None, Z, g, 1e-6, workspace=ws, stream=st)
+                    loss, _ = fl.fused_linear_cross_entropy(X, W, None, lab, workspace=wc, stream=st)
+                    st.synchronize()
+                    for a, b2 in zip(ref, (y, q, s, loss)):
+                        if not torch.equal(a, b2):
+                            errors.append(f"thread {tid}: result differs")
+        except Exception as e:  # reported below
+            errors.append(f"thread {tid}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:3]
+
+
+def test_default_outputs_accept_ragged_widths():
+    """Outputs the binding allocates get 16-byte row pitches, so widths that are not a multiple of
+    the 16-byte element count work: N = 300 (bf16) and N = 1000 (E4M3).  Inputs keep the rule
+    (the residual here is given a padded pitch)."""
+    M, K = 130, 64
+    X = _draw((M, K), syn.STREAM_X)
+    for N in (300, 1000):
+        W = _draw((N, K), syn.STREAM_W, K ** -0.5)
+        Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), None, mode="tanh")
+        assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), None, oracle.GELU_TANH), f"ragged gelu N={N}")
+        Z = _draw((M, N), syn.STREAM_Z)
+        g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0)
+        Zd = torch.zeros((M, -(-N // 8) * 8), dtype=torch.bfloat16, device="cuda")[:, :N]  # inputs: 16-byte pitch
+        Zd.copy_(dev_bf16(Z))
+        q, s = fl.fused_linear_residual_rmsnorm_fp8(dev_bf16(X), dev_bf16(W), None, Zd, dev_bf16(g), 1e-6)
+        q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None, f64(Z), f64(g), 1e-6)
+        assert_fp8_close(q.cpu().numpy(), s.cpu().numpy().astype(np.float64), q_ref, s_ref, f"ragged rmsnorm N={N}")
