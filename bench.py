@@ -665,6 +665,12 @@ def main():
         "unfused_baseline": {"ms_per_step": head_unfused, "speedup": head_unfused / ms,
                              "what": "torch F.gelu(F.linear(X, W, b), approximate='tanh'): cuBLAS GEMM + separate GELU"},
         "rows": rows, "wall_s_timed_region": wall,
+        # numbers the source pages print, for context only (other hardware, other kernels)
+        "pages_context": {
+            "unfused_layernorm_gelu_8x4096x4096_fp16_a100_ms": 0.5,
+            "fused_layernorm_gelu_speedup": "about 2x (LayerNorm + GeLU fusion page)",
+            "linear_gelu_fusion_speedup": "1.2-2x in general (Triton Linear + Attention fusion page)",
+            "non_gemm_share_h100": "non-negligible, no figure (GEMM epilogue page, on CODA)"},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(HEADLINE)
