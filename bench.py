@@ -561,6 +561,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(syn.WORKLOADS),
                     help="workload timed as the step (default: the headline); used for profiling runs")
+    ap.add_argument("--unfused", action="store_true",
+                    help="with --workload: time the unfused torch/cuBLAS sequence of that workload instead "
+                         "(comparison baseline); one extra call runs inside the NVTX range 'unfused_step'")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -588,6 +591,8 @@ def main():
 
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    if args.unfused:
+        return unfused_workload(args, world, rank, local, dist)
     if args.workload != HEADLINE:
         return single_workload(args, world, rank, local, barrier, dist)
     head = Case(HEADLINE)
@@ -699,6 +704,34 @@ def single_workload(args, world, rank, local, barrier, dist):
             "roofline": {"bound": "hbm" if c.hbm_bound else "tensor", "achieved": val, "peak": pkv,
                          "unit": unit, "frac": val / pkv, "traffic": recorded_traffic(args.workload)},
             "gpu_launches": args.steps, "clocks": clk.summary()}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def unfused_workload(args, world, rank, local, dist):
+    """The unfused torch/cuBLAS sequence of one workload, timed like the fused kernel; one more call
+    runs inside the NVTX range 'unfused_step' so a profiler can capture exactly its kernels."""
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    c = Case(args.workload)
+    fn = unfused_fn(c)
+    with ClockSampler(local) as clk:
+        m = time_fn(fn, args.steps, args.warmup, flush)
+    flush.zero_()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("unfused_step")
+    fn()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    if c.hbm_bound:
+        val, unit = c.bytes / (m * 1e-3) / 1e9, "GB/s"
+    else:
+        val, unit = c.flops / (m * 1e-3) / 1e12, "TFLOP/s"
+    line = {"impl": "unfused_torch", "metric": METRIC, "value": world * val, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": m, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload}, "clocks": clk.summary()}
     if dist is not None:
         dist.destroy_process_group()
     if rank == 0:
