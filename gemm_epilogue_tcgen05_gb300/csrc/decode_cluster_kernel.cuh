@@ -27,7 +27,7 @@ constexpr int kDcStages = 10;
 // W tiles (16 KB) of its k range that a CTA pulls into L2 before waiting for the preceding
 // kernel (measured back to back: 0 -> 28.6 us per call, 8 -> 27.5, 16 -> 26.9, 32 -> 29.4).
 constexpr int kDcL2PrefetchUnits = 16;
-constexpr int kDcSmallBytes = 8192;  // per-token partials (T, Sall), scales, flags
+constexpr int kDcSmallBytes = 8192;  // per-token partials of the ranks (Sall), flags
 constexpr int kDcSmemBytes = kDcStages * kDecStageBytes + kDcSmallBytes + 1024 /*bars*/ + 1024 /*align*/;
 
 template <int C>
@@ -42,10 +42,8 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   uint8_t* stage_mem = smem;
   float* P = reinterpret_cast<float*>(stage_mem);  // [32 tokens][128 features] after the stream
   uint8_t* small = smem + kDcStages * kDecStageBytes;
-  float2* T = reinterpret_cast<float2*>(small);            // [32][16] item partials (kGroups <= 16 used)
-  float2* Sall = T + 32 * 16;                              // [8][32] the ranks' per-token partials (leader)
-  float* qs_s = reinterpret_cast<float*>(Sall + 8 * 32);   // [32] 448 / max |h gamma| per token
-  volatile int* flags = reinterpret_cast<volatile int*>(qs_s + 32);  // [0] ok, [1] grid count reached
+  float2* Sall = reinterpret_cast<float2*>(small);         // [8][32] the ranks' per-token partials (leader)
+  volatile int* flags = reinterpret_cast<volatile int*>(Sall + 8 * 32);  // [0] ok, [1] grid count reached
   uint64_t* bars = reinterpret_cast<uint64_t*>(small + kDcSmallBytes);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + kDcStages;
@@ -190,172 +188,184 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
       load_bf16x4(p.gamma, n + 4, gl, *reinterpret_cast<float(*)[4]>(gs[it] + 4));
     }
   }
-  __syncthreads();
-  if (C > 1) cluster_sync_all();  // every CTA of the cluster has its partial tile in P
+  // Cluster barrier A: every CTA of the cluster has its partial tile in P (each thread's arrive
+  // releases its own writes, so the CTA needs no barrier of its own in front of it).
+  __syncwarp();
+  if (C > 1) cluster_sync_all();
+  else __syncthreads();
 
   // ---------------------------------------------------------------- phase 2: cluster reduce, h, statistics
   // In the leader's shared memory: H [32 tokens][128 features] fp32 right after P, and the
   // ranks' per-token partials Sall [C][32].
   float* H = P + 32 * 128;
   bool cl_ok = flags[0] != 0;
-  if (C > 1) {
-    for (int j = 0; j < C; ++j)
-      cl_ok = cl_ok && ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(flags)), static_cast<uint32_t>(j))) != 0;
+  if constexpr (C > 1) {
+    int fv[C];
+#pragma unroll
+    for (int j = 0; j < C; ++j)  // all C loads in flight at once
+      fv[j] = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(flags)), static_cast<uint32_t>(j)));
+    int all = 1;
+#pragma unroll
+    for (int j = 0; j < C; ++j) all &= fv[j] != 0 ? 1 : 0;
+    cl_ok = all != 0;
   }
-  float hk[kIpt][8];  // this thread's h values, pushed to the leader after the statistics
   if (ti >= 0 && cl_ok) {
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
+      // The groups of one token sit in kGroups consecutive lanes; kItems is a multiple of 32, so
+      // whether a thread has an item is the same across its warp.
       const int item = ti + 128 * it;
-      if (item >= kItems) continue;
+      const bool has = item < kItems;
       const int t = item / kGroups, g = item % kGroups;
       const int row = static_cast<int>(rank) * kRows + g * 8;  // first feature row within the tile
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      const uint32_t local = smem_u32(P + t * 128 + row);
-      for (int j = 0; j < C; ++j) {  // rank order: deterministic
-        const uint32_t ra = C > 1 ? mapa_shared(local, static_cast<uint32_t>(j)) : local;
-        const float4 x = C > 1 ? ld_dsmem_f4(ra) : *reinterpret_cast<const float4*>(P + t * 128 + row);
-        const float4 y = C > 1 ? ld_dsmem_f4(ra + 16) : *reinterpret_cast<const float4*>(P + t * 128 + row + 4);
-        a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-        b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+      float ss = 0.f, am = 0.f;
+      if (has) {
+        const uint32_t local = smem_u32(P + t * 128 + row);
+        float4 xa[C], xb[C];
+#pragma unroll
+        for (int j = 0; j < C; ++j) {  // every rank's partial in flight at once
+          if constexpr (C > 1) {
+            const uint32_t ra = mapa_shared(local, static_cast<uint32_t>(j));
+            xa[j] = ld_dsmem_f4(ra);
+            xb[j] = ld_dsmem_f4(ra + 16);
+          } else {
+            xa[j] = *reinterpret_cast<const float4*>(P + t * 128 + row);
+            xb[j] = *reinterpret_cast<const float4*>(P + t * 128 + row + 4);
+          }
+        }
+        float4 a = xa[0], b = xb[0];
+#pragma unroll
+        for (int j = 1; j < C; ++j) {  // rank order: deterministic
+          a.x += xa[j].x; a.y += xa[j].y; a.z += xa[j].z; a.w += xa[j].w;
+          b.x += xb[j].x; b.y += xb[j].y; b.z += xb[j].z; b.w += xb[j].w;
+        }
+        const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float hv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          hv[e] = s8[e] + bs[it][e] + zs[it][e];  // features past N: W rows, b and z are zero there
+          ss += hv[e] * hv[e];
+          am = fmaxf(am, fabsf(hv[e] * gs[it][e]));
+        }
+        // h to the leader's H[t][row ..]
+        const uint32_t hl = smem_u32(H + t * 128 + row);
+        if constexpr (C > 1) {
+          const uint32_t hr = mapa_shared(hl, 0u);
+          st_dsmem_f4(hr, make_float4(hv[0], hv[1], hv[2], hv[3]));
+          st_dsmem_f4(hr + 16, make_float4(hv[4], hv[5], hv[6], hv[7]));
+        } else {
+          *reinterpret_cast<float4*>(H + t * 128 + row) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<float4*>(H + t * 128 + row + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
+        }
       }
-      const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      float hv[8], ss = 0.f, am = 0.f;
+      // this rank's per-token partial over its kRows features: a butterfly over the token's lanes
+      // (every lane ends with the same bits, whatever the run)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        hv[e] = s8[e] + bs[it][e] + zs[it][e];  // features past N: W rows, b and z are zero there
-        ss += hv[e] * hv[e];
-        am = fmaxf(am, fabsf(hv[e] * gs[it][e]));
+      for (int o = kGroups / 2; o > 0; o >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
       }
-      T[t * 16 + g] = make_float2(ss, am);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) hk[it][e] = hv[e];
-    }
-  }
-  __syncthreads();
-  if (ti >= 0 && ti < 32 && cl_ok) {
-    float ss = 0.f, am = 0.f;
-    for (int g = 0; g < kGroups; ++g) {
-      const float2 v = T[ti * 16 + g];
-      ss += v.x;
-      am = fmaxf(am, v.y);
-    }
-    // this rank's per-token partial to the leader's Sall[rank][t]
-    const uint32_t sl = smem_u32(Sall + rank * 32 + ti);
-    if (C > 1) st_dsmem_f2(mapa_shared(sl, 0u), make_float2(ss, am));
-    else Sall[ti] = make_float2(ss, am);
-  }
-  __syncthreads();
-  if (C > 1) cluster_sync_all();  // the leader has every rank's per-token partials (Sall)
-  const bool leader = rank == 0;
-
-  // ---------------------------------------------------------------- phase 3: publish, grid-wide count (leaders)
-  if (leader && ti >= 0 && ti < 32 && cl_ok) {
-    float ss = 0.f, am = 0.f;
-    for (int j = 0; j < C; ++j) {  // rank order: deterministic
-      const float2 v = Sall[j * 32 + ti];
-      ss += v.x;
-      am = fmaxf(am, v.y);
-    }
-    __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + ti, make_float2(ss, am));
-    __threadfence();
-  }
-  // gamma of this thread's quantisation slice (token ti / 4, features 32 (ti % 4) ..), loaded
-  // before the grid-wide wait
-  float gq[32];
-  if (leader && ti >= 0) {
-    const int n = f * 128 + (ti & 3) * 32;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) load_bf16x4(p.gamma, n + 4 * k, p.N, *reinterpret_cast<float(*)[4]>(gq + 4 * k));
-  }
-  __syncthreads();
-  if (leader && threadIdx.x == 64 && cl_ok) {
-    // publish before the h values move: the grid-wide count starts as early as possible
-    __threadfence();
-    atomicAdd(p.counters + p.num_f, 1u);
-  }
-  // h to the leader's H[t][row ..], then the peers are done
-  if (ti >= 0 && cl_ok) {
-#pragma unroll
-    for (int it = 0; it < kIpt; ++it) {
-      const int item = ti + 128 * it;
-      if (item >= kItems) continue;
-      const int t = item / kGroups, g = item % kGroups;
-      const int row = static_cast<int>(rank) * kRows + g * 8;
-      const uint32_t hl = smem_u32(H + t * 128 + row);
-      if (C > 1) {
-        const uint32_t hr = mapa_shared(hl, 0u);
-        st_dsmem_f4(hr, make_float4(hk[it][0], hk[it][1], hk[it][2], hk[it][3]));
-        st_dsmem_f4(hr + 16, make_float4(hk[it][4], hk[it][5], hk[it][6], hk[it][7]));
-      } else {
-        *reinterpret_cast<float4*>(H + t * 128 + row) = make_float4(hk[it][0], hk[it][1], hk[it][2], hk[it][3]);
-        *reinterpret_cast<float4*>(H + t * 128 + row + 4) = make_float4(hk[it][4], hk[it][5], hk[it][6], hk[it][7]);
+      if (has && g == 0) {
+        const uint32_t sl = smem_u32(Sall + rank * 32 + t);
+        if constexpr (C > 1) st_dsmem_f2(mapa_shared(sl, 0u), make_float2(ss, am));
+        else Sall[t] = make_float2(ss, am);
       }
     }
   }
-  __syncthreads();
-  // Every read of a peer's P and every write into the leader's H is done after this barrier;
-  // the other CTAs of the cluster then leave.
+  // Cluster barrier B: every read of a peer's P and every write into the leader's H and Sall is
+  // done; the other CTAs of the cluster then leave, freeing their SMs for the next kernel.
+  __syncwarp();
   if (C > 1) cluster_sync_all();
-  if (leader && threadIdx.x == 64) {
-    const bool reached = cl_ok && spin_until(p.counters + p.num_f, static_cast<unsigned>(p.num_f), p.status,
-                                             p.timeout_ns, p.status, W_DECODE_ROWS, p.num_f);
-    flags[1] = reached ? 1 : 0;
-  }
-  __syncthreads();
-  const bool finish = leader && flags[1] != 0;
+  else __syncthreads();
 
-  // ---------------------------------------------------------------- phase 4: merge statistics, quantise (leaders)
-  if (finish && ti >= 0 && ti < 32) {
-    const int t = ti;
-    float SS = 0.f, A = 0.f;
-    for (int c0 = 0; c0 < p.num_f; c0 += 32) {  // cluster order: deterministic; 32 loads in flight
-      float2 w[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        w[j] = c0 + j < p.num_f ? __ldcg(p.stats + static_cast<size_t>(c0 + j) * kDecTokens + t) : make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        SS += w[j].x;
-        A = fmaxf(A, w[j].y);
-      }
-    }
-    qs_s[t] = A > 0.f ? 448.f / A : 0.f;
-    if (f == 0 && t < p.M) p.row_scale[t] = rsqrtf(SS / static_cast<float>(p.N) + p.eps) * A * (1.f / 448.f);
-  }
-  __syncthreads();
-  if (finish && ti >= 0) {
-    // thread: token t = ti / 4, features 32 (ti % 4) .. + 31 of the tile; 32 codes, two 16-byte stores
-    const int t = ti >> 2, c0 = (ti & 3) * 32;
+  if (rank == 0) {
+    // ---------------------------------------------------------------- phase 3: publish, grid-wide count (leader)
+    // this thread's quantisation slice: token tq, features 32 (ti % 4) .. + 31 of the tile; its
+    // gamma is loaded before the grid-wide wait
+    const int tq = ti >> 2, c0 = (ti & 3) * 32;
     const int n = f * 128 + c0;
-    if (t < p.M && n < p.N) {
-      const float qs = qs_s[t];
-      uint32_t w[8];
+    float gq[32];
+    if (ti >= 0) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 hv = *reinterpret_cast<const float4*>(H + t * 128 + c0 + 4 * k);
-        const float* gg = gq + 4 * k;
-        w[k] = f32x2_to_e4m3x2(hv.x * gg[0] * qs, hv.y * gg[1] * qs) |
-               (f32x2_to_e4m3x2(hv.z * gg[2] * qs, hv.w * gg[3] * qs) << 16);
+      for (int k = 0; k < 8; ++k) load_bf16x4(p.gamma, n + 4 * k, p.N, *reinterpret_cast<float(*)[4]>(gq + 4 * k));
+    }
+    if (warp == 2 && cl_ok) {
+      float ss = 0.f, am = 0.f;
+      for (int j = 0; j < C; ++j) {  // rank order: deterministic
+        const float2 v = Sall[j * 32 + lane];
+        ss += v.x;
+        am = fmaxf(am, v.y);
       }
-      uint8_t* dst = p.yq + static_cast<size_t>(t) * p.ldq + n;
-      if (n + 32 <= p.N) {  // 16-byte aligned: ldq % 16 == 0, n % 32 == 0
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n + j < p.N) dst[j] = static_cast<uint8_t>(w[j >> 2] >> (8 * (j & 3)));
+      __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + lane, make_float2(ss, am));
+      __syncwarp();
+      if (lane == 0) {
+        // the warp's stores are ordered before the fence by the warp barrier; the fence is
+        // cumulative, so the count publishes them
+        __threadfence();
+        atomicAdd(p.counters + p.num_f, 1u);
+        flags[1] = spin_until(p.counters + p.num_f, static_cast<unsigned>(p.num_f), p.status, p.timeout_ns,
+                              p.status, W_DECODE_ROWS, p.num_f)
+                       ? 1
+                       : 0;
       }
     }
-  }
-  __syncthreads();
-  if (threadIdx.x == 64 && finish) {
-    // the last leader to leave resets the counters for the next call
-    const unsigned old = atomicAdd(p.counters + p.num_f + 1, 1u);
-    if (old + 1u == static_cast<unsigned>(p.num_f)) {
-      p.counters[p.num_f] = 0u;
-      p.counters[p.num_f + 1] = 0u;
+    __syncthreads();
+    const bool finish = flags[1] != 0;
+
+    // ---------------------------------------------------------------- phase 4: merge statistics, quantise (leader)
+    if (finish && ti >= 0) {
+      // The four threads of token tq each merge every fourth cluster's partial (fixed order),
+      // then combine by a butterfly, so all four hold the same bits.
+      float SS = 0.f, A = 0.f;
+      for (int cb = ti & 3; cb < p.num_f; cb += 32) {  // 8 loads in flight
+        float2 w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = cb + 4 * j;
+          w[j] = c < p.num_f ? __ldcg(p.stats + static_cast<size_t>(c) * kDecTokens + tq) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          SS += w[j].x;
+          A = fmaxf(A, w[j].y);
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        SS += __shfl_xor_sync(0xffffffffu, SS, o);
+        A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, o));
+      }
+      const float qs = A > 0.f ? 448.f / A : 0.f;
+      if (f == 0 && (ti & 3) == 0 && tq < p.M)
+        p.row_scale[tq] = rsqrtf(SS / static_cast<float>(p.N) + p.eps) * A * (1.f / 448.f);
+      if (tq < p.M && n < p.N) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 hv = *reinterpret_cast<const float4*>(H + tq * 128 + c0 + 4 * k);
+          const float* gg = gq + 4 * k;
+          w[k] = f32x2_to_e4m3x2(hv.x * gg[0] * qs, hv.y * gg[1] * qs) |
+                 (f32x2_to_e4m3x2(hv.z * gg[2] * qs, hv.w * gg[3] * qs) << 16);
+        }
+        uint8_t* dst = p.yq + static_cast<size_t>(tq) * p.ldq + n;
+        if (n + 32 <= p.N) {  // 16-byte aligned: ldq % 16 == 0, n % 32 == 0
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n + j < p.N) dst[j] = static_cast<uint8_t>(w[j >> 2] >> (8 * (j & 3)));
+        }
+      }
+    }
+    if (threadIdx.x == 64 && finish) {
+      // the last leader to leave resets the counters for the next call (this thread passed the
+      // count itself, so every leader has read it once the leavers are complete)
+      const unsigned old = atomicAdd(p.counters + p.num_f + 1, 1u);
+      if (old + 1u == static_cast<unsigned>(p.num_f)) {
+        p.counters[p.num_f] = 0u;
+        p.counters[p.num_f + 1] = 0u;
+      }
     }
   }
   if (warp == 1) {
