@@ -198,17 +198,42 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   // In the leader's shared memory: H [32 tokens][128 features] fp32 right after P, and the
   // ranks' per-token partials Sall [C][32].
   float* H = P + 32 * 128;
-  bool cl_ok = flags[0] != 0;
+  // The ranks' ok flags and partial tiles are all loaded at once (reading a peer's P is safe
+  // whatever its flag says: the partials are used only when every flag is set).
+  int fv[C];
+  float4 xa[kIpt][C], xb[kIpt][C];
   if constexpr (C > 1) {
-    int fv[C];
 #pragma unroll
-    for (int j = 0; j < C; ++j)  // all C loads in flight at once
+    for (int j = 0; j < C; ++j)
       fv[j] = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(flags)), static_cast<uint32_t>(j)));
-    int all = 1;
-#pragma unroll
-    for (int j = 0; j < C; ++j) all &= fv[j] != 0 ? 1 : 0;
-    cl_ok = all != 0;
+  } else {
+    fv[0] = flags[0];
   }
+  if (ti >= 0) {
+#pragma unroll
+    for (int it = 0; it < kIpt; ++it) {
+      const int item = ti + 128 * it;
+      if (item >= kItems) continue;
+      const int t = item / kGroups, g = item % kGroups;
+      const int row = static_cast<int>(rank) * kRows + g * 8;
+      const uint32_t local = smem_u32(P + t * 128 + row);
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if constexpr (C > 1) {
+          const uint32_t ra = mapa_shared(local, static_cast<uint32_t>(j));
+          xa[it][j] = ld_dsmem_f4(ra);
+          xb[it][j] = ld_dsmem_f4(ra + 16);
+        } else {
+          xa[it][j] = *reinterpret_cast<const float4*>(P + t * 128 + row);
+          xb[it][j] = *reinterpret_cast<const float4*>(P + t * 128 + row + 4);
+        }
+      }
+    }
+  }
+  int all = 1;
+#pragma unroll
+  for (int j = 0; j < C; ++j) all &= fv[j] != 0 ? 1 : 0;
+  const bool cl_ok = all != 0;
   if (ti >= 0 && cl_ok) {
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
@@ -220,24 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
       const int row = static_cast<int>(rank) * kRows + g * 8;  // first feature row within the tile
       float ss = 0.f, am = 0.f;
       if (has) {
-        const uint32_t local = smem_u32(P + t * 128 + row);
-        float4 xa[C], xb[C];
-#pragma unroll
-        for (int j = 0; j < C; ++j) {  // every rank's partial in flight at once
-          if constexpr (C > 1) {
-            const uint32_t ra = mapa_shared(local, static_cast<uint32_t>(j));
-            xa[j] = ld_dsmem_f4(ra);
-            xb[j] = ld_dsmem_f4(ra + 16);
-          } else {
-            xa[j] = *reinterpret_cast<const float4*>(P + t * 128 + row);
-            xb[j] = *reinterpret_cast<const float4*>(P + t * 128 + row + 4);
-          }
-        }
-        float4 a = xa[0], b = xb[0];
+        float4 a = xa[it][0], b = xb[it][0];
 #pragma unroll
         for (int j = 1; j < C; ++j) {  // rank order: deterministic
-          a.x += xa[j].x; a.y += xa[j].y; a.z += xa[j].z; a.w += xa[j].w;
-          b.x += xb[j].x; b.y += xb[j].y; b.z += xb[j].z; b.w += xb[j].w;
+          a.x += xa[it][j].x; a.y += xa[it][j].y; a.z += xa[it][j].z; a.w += xa[it][j].w;
+          b.x += xb[it][j].x; b.y += xb[it][j].y; b.z += xb[it][j].z; b.w += xb[it][j].w;
         }
         const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         float hv[8];
@@ -289,7 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
 #pragma unroll
       for (int k = 0; k < 8; ++k) load_bf16x4(p.gamma, n + 4 * k, p.N, *reinterpret_cast<float(*)[4]>(gq + 4 * k));
     }
-    if (warp == 2 && cl_ok) {
+    if (warp == 1 && cl_ok) {
+      // the MMA warp is idle now: it merges the ranks' partials (lane = token), publishes them
+      // and waits for the grid-wide count while the epilogue warps load gamma
       float ss = 0.f, am = 0.f;
       for (int j = 0; j < C; ++j) {  // rank order: deterministic
         const float2 v = Sall[j * 32 + lane];
@@ -299,10 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
       __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + lane, make_float2(ss, am));
       __syncwarp();
       if (lane == 0) {
-        // the warp's stores are ordered before the fence by the warp barrier; the fence is
-        // cumulative, so the count publishes them
-        __threadfence();
-        atomicAdd(p.counters + p.num_f, 1u);
+        // the warp's stores are ordered before this release by the warp barrier, so the count
+        // publishes them
+        red_release_add_u32(p.counters + p.num_f, 1u);
         flags[1] = spin_until(p.counters + p.num_f, static_cast<unsigned>(p.num_f), p.status, p.timeout_ns,
                               p.status, W_DECODE_ROWS, p.num_f)
                        ? 1
