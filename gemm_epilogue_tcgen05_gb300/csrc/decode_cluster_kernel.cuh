@@ -104,6 +104,11 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();  // X, Z, gamma, b and the workspace may be written by the preceding kernel
 
+  // Residual, bias and gamma of the epilogue threads' reduce items (phase 2): loaded by the
+  // epilogue warps while the weights stream, so none of their latency is left for the tail.
+  const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
+  float zs[kIpt][8], bs[kIpt][8], gs[kIpt][8];
+
   // ---------------------------------------------------------------- phase 1: stream W, partial tile
   if (warp == 0) {
     if (lane == 0) {
@@ -153,25 +158,6 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   } else {
     // TMEM lane quarter q = feature rows 32 q .. 32 q + 31; each thread one row, 32 tokens.
     const int q = warp & 3;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar, 0, wctx, W_EPI_TMEM_FULL));
-    if (ok) {
-      tc_fence_after();
-      uint32_t acc[32];
-      tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16), acc);
-      tmem_ld_wait();
-      // P[t][n]: for a fixed token the warp writes 32 consecutive floats (no bank conflict)
-      const int n = q * 32 + lane;
-#pragma unroll
-      for (int t = 0; t < 32; ++t) P[t * 128 + n] = __uint_as_float(acc[t]);
-    } else if (lane == 0) {
-      flags[0] = 0;
-    }
-  }
-  // Residual, bias and gamma of this thread's items, loaded before the barrier so their
-  // latency overlaps with the wait for the peers' partial tiles.
-  const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
-  float zs[kIpt][8], bs[kIpt][8], gs[kIpt][8];
-  if (ti >= 0) {
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
       const int item = ti + 128 * it;
@@ -186,6 +172,19 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
       load_bf16x4(p.bias, n + 4, bl, *reinterpret_cast<float(*)[4]>(bs[it] + 4));
       load_bf16x4(p.gamma, n, gl, *reinterpret_cast<float(*)[4]>(gs[it]));
       load_bf16x4(p.gamma, n + 4, gl, *reinterpret_cast<float(*)[4]>(gs[it] + 4));
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar, 0, wctx, W_EPI_TMEM_FULL));
+    if (ok) {
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16), acc);
+      tmem_ld_wait();
+      // P[t][n]: for a fixed token the warp writes 32 consecutive floats (no bank conflict)
+      const int n = q * 32 + lane;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) P[t * 128 + n] = __uint_as_float(acc[t]);
+    } else if (lane == 0) {
+      flags[0] = 0;
     }
   }
   // Cluster barrier A: every CTA of the cluster has its partial tile in P (each thread's arrive
