@@ -45,6 +45,12 @@ int launch_dgrad(const void* dZ, const void* W, const void* s0, const void* s1, 
     p.saved0 = static_cast<const __nv_bfloat16*>(s0);
     p.saved1 = static_cast<const __nv_bfloat16*>(s1);
     p.ld_saved = lds;
+    // saved activations [M, N]: boxes of 32 columns x 32 rows (one epilogue warp's unit)
+    if (!encode_2d(&p.map_saved[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s0, N, M, lds, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B) ||
+        (s1 != nullptr && !encode_2d(&p.map_saved[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s1, N, M, lds, 32, 32,
+                                     CU_TENSOR_MAP_SWIZZLE_64B)))
+      return false;
     return true;
   };
   return run_gemm<EPI>(M, setup, di, stream, false, 1);

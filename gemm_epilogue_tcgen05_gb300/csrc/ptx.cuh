@@ -17,7 +17,7 @@ enum : int { STATUS_TIMEOUT = 6 };
 // Where a wait gave up (recorded in ST_WHERE).
 enum : int {
   W_PRODUCER_EMPTY = 1, W_MMA_FULL = 2, W_MMA_TMEM_EMPTY = 3, W_EPI_TMEM_FULL = 4,
-  W_ROW_EXCHANGE = 5, W_DRAIN = 6, W_SPLITK = 7, W_DECODE_ROWS = 8
+  W_ROW_EXCHANGE = 5, W_DRAIN = 6, W_SPLITK = 7, W_DECODE_ROWS = 8, W_EPI_SAVED = 9
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -107,6 +107,15 @@ __device__ __forceinline__ bool mbar_wait_quiet(uint64_t* bar, uint32_t parity, 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Same with an L2 cache policy, the destination given as a shared-memory address.
+__device__ __forceinline__ void tma_load_2d_to_hint(const void* map, uint64_t* bar, uint32_t dst, int x, int y,
+                                                    uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(const void* map, uint64_t* bar, void* dst, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -134,11 +143,13 @@ __device__ __forceinline__ void tma_store_2d(const void* map, const void* src, i
                "r"(smem_u32(src)), "r"(x), "r"(y)
                : "memory");
 }
-__device__ __forceinline__ void tma_store_2d_u32(const void* map, uint32_t src_smem, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src_smem), "r"(x), "r"(y)
-               : "memory");
+__device__ __forceinline__ void tma_store_2d_u32_hint(const void* map, uint32_t src_smem, int x, int y,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src_smem), "r"(x), "r"(y), "l"(policy)
+      : "memory");
 }
 // Hint: bring [src, src + bytes) into L2 (16-byte aligned, size a multiple of 16).
 // L2 prefetch of one tensor-map tile (no shared memory, no completion to wait for).
@@ -460,6 +471,12 @@ __device__ __forceinline__ float round_to_e4m3(float v, uint32_t& code) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
