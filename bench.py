@@ -507,11 +507,22 @@ def time_e2e(case: Case, steps: int, warmup: int, barrier):
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
-def oracle_sample(w, rows: int):
-    """Oracle on the first `rows` rows of the workload (all output columns); returns seconds."""
-    import oracle
+def oracle_inputs(w, rows: int) -> dict:
+    """The first `rows` rows of the workload's operands (weights whole), as exact fp64 arrays."""
     ops = syn.make_operands(w, rows=(0, rows))
-    f = {k: syn.to_f64(v, w.dtype) for k, v in ops.items()}
+    return {k: syn.to_f64(v, w.dtype) for k, v in ops.items()}
+
+
+def first_rows(f: dict, rows: int) -> dict:
+    """The same operands cut to their first `rows` rows."""
+    return {k: (v[:rows] if k in syn.ROW_OPERANDS else v) for k, v in f.items()}
+
+
+def oracle_sample(w, rows: int, f: dict | None = None):
+    """Oracle on the first `rows` rows of the workload (all output columns); returns seconds.
+    `f` (from oracle_inputs, at least `rows` rows) saves regenerating the operands."""
+    import oracle
+    f = oracle_inputs(w, rows) if f is None else first_rows(f, rows)
     t0 = time.perf_counter()
     if w.kind in ("gelu_tanh", "gelu_erf"):
         oracle.linear_gelu(f["X"], f["W"], f.get("b"), oracle.GELU_TANH if w.kind == "gelu_tanh"
@@ -746,12 +757,15 @@ def reference_arm(args, world, rank):
     oracle.build()
     syn.build()
     w = syn.WORKLOADS[HEADLINE]
-    t1 = oracle_sample(w, 1)
+    f1 = oracle_inputs(w, 1)
+    t1 = min(oracle_sample(w, 1, f1) for _ in range(3))
     per_step_target = 8.0 if args.steps <= 10 else 80.0 / args.steps
     rows = int(max(1, min(w.M, math.floor(per_step_target / max(t1, 1e-6)))))
+    # operands generated once (the timed region is the oracle call alone); warm-up on one row
+    f = oracle_inputs(w, rows)
     for _ in range(args.warmup):
-        oracle_sample(w, 1)
-    secs = [oracle_sample(w, rows) for _ in range(args.steps)]
+        oracle_sample(w, 1, f)
+    secs = [oracle_sample(w, rows, f) for _ in range(args.steps)]
     s = statistics.mean(secs)
     value = 2.0 * rows * w.N * w.K / s / 1e12
     sample = f"{rows} of {w.M} rows of {HEADLINE} per step, all {w.N} output columns, fp64"
