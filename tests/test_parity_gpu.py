@@ -721,6 +721,54 @@ def test_graph_capture_of_every_entry_point_matches_eager():
     assert torch.count_nonzero(ws_p[:256]) == 0 and torch.count_nonzero(ws_c[:256]) == 0
 
 
+def test_every_entry_point_is_deterministic_across_calls():
+    """Each entry point called twice on the same inputs, with other work in between, gives
+    bit-identical outputs at shapes that span several waves of the persistent grid (and, for decode,
+    both decode kernels): no reduction depends on scheduling or arrival order."""
+    M, N, K = 2048, 4096, 1024
+    X = dev_bf16(_draw((M, K), syn.STREAM_X, seed=11))
+    W = dev_bf16(_draw((N, K), syn.STREAM_W, K ** -0.5, seed=11))
+    b = dev_bf16(_draw((N,), syn.STREAM_B, 0.5, seed=11))
+    Z = dev_bf16(_draw((M, N), syn.STREAM_Z, seed=11))
+    g = dev_bf16(_draw((N,), syn.STREAM_GAMMA, 0.1, 1.0, seed=11))
+    Wt = dev_bf16(_draw((K, N), syn.STREAM_W2, K ** -0.5, seed=11))    # [K, N] as stored (dgrad)
+    G = dev_bf16(_draw((M, N), syn.STREAM_WUP, seed=12))
+    Wq = dev_bf16(_draw((2 * 2048, K), syn.STREAM_WUP, K ** -0.5, seed=11))  # GQA 16 / 8 heads of 128
+    Xd = X[:32].contiguous()
+    ws_p = fl.rmsnorm_fp8_workspace(M, N, K)
+    ws_c = fl.cross_entropy_workspace(M, N)
+    lab = torch.from_numpy(syn.draw_labels(11, syn.STREAM_LABEL, M, N)).cuda()
+    calls = {
+        "gelu": lambda: [fl.fused_linear_gelu(X, W, b, mode="tanh")],
+        "qkv": lambda: list(fl.fused_qkv_rope(X, Wq[:3 * 1024], None, n_heads=8, head_dim=128, seq_len=512)),
+        "qkv_fp8kv": lambda: list(fl.fused_qkv_rope_fp8kv(X, Wq, None, n_heads=16, n_kv_heads=8, head_dim=128,
+                                                          seq_len=512)),
+        "swiglu": lambda: [fl.fused_swiglu(X, W, W)],
+        "rmsnorm_prefill": lambda: list(fl.fused_linear_residual_rmsnorm_fp8(X, W, b, Z, g, 1e-6, workspace=ws_p)),
+        "rmsnorm_decode": lambda: list(fl.fused_linear_residual_rmsnorm_fp8(Xd, W, b, Z[:32].contiguous(), g, 1e-6)),
+        "cross_entropy": lambda: list(fl.fused_linear_cross_entropy(X, W, b, lab, workspace=ws_c))[:1],
+        "quant_fp8": lambda: list(fl.fused_linear_quant(X, W, b, fl.QUANT_FP8_1X128)),
+        "quant_int4": lambda: list(fl.fused_linear_quant(X, W, b, fl.QUANT_INT4_G32)),
+        "dgrad_gelu": lambda: [fl.fused_dgrad_gelu(X, Wt, Z, mode="tanh")],
+        "swiglu_bwd": lambda: [fl.fused_swiglu_bwd(X, Wt, G, Z)],
+    }
+    first = {k: [t.clone() for t in f()] for k, f in calls.items()}
+    fl.set_max_ctas(40)  # decode on the flat split-K kernel, the GEMMs on fewer CTAs
+    capped = {k: [t.clone() for t in calls[k]()] for k in ("rmsnorm_decode", "gelu", "swiglu_bwd")}
+    for i, (a, c) in enumerate(zip(capped["rmsnorm_decode"], calls["rmsnorm_decode"]())):
+        assert torch.equal(a, c), f"flat decode kernel: output {i} differs between two calls"
+    fl.set_max_ctas(0)
+    for k, f in reversed(list(calls.items())):  # the second pass in another order
+        again = f()
+        for i, (a, c) in enumerate(zip(first[k], again)):
+            assert torch.equal(a, c), f"{k}: output {i} differs between two calls"
+    for k in ("gelu", "swiglu_bwd"):  # the tile walk changes with the grid, the arithmetic does not
+        for i, (a, c) in enumerate(zip(first[k], capped[k])):
+            assert torch.equal(a, c), f"{k}: output {i} differs under a smaller grid"
+    torch.cuda.synchronize()
+    assert fl.device_status() == fl.FL_OK
+
+
 # ------------------------------------------------------------------ random shapes, streams, threads
 def _rand_shapes(seed, count, m_max=600, n_max=1200, k_max=700):
     rng = np.random.default_rng(seed)
