@@ -226,7 +226,8 @@ class Case:
             self.ws = fl.rmsnorm_fp8_workspace(w.M, w.N, w.K)
             self.flops = 2.0 * w.M * w.N * w.K
         self.bytes = self.algorithmic_bytes()
-        self.hbm_bound = w.kind == "rmsnorm_fp8" and w.M <= 32
+        # decode shapes (32 tokens): the weight stream bounds them
+        self.hbm_bound = w.M <= 32 and w.kind in ("rmsnorm_fp8", "gelu_tanh", "qkv_rope")
 
     def algorithmic_bytes(self) -> float:
         """Each operand read once and each output written once (bytes)."""
@@ -245,14 +246,18 @@ class Case:
             return float(b + 2 * (2 * w.M * w.N) + 2 * w.M * w.N2)
         return float(b + 2 * w.M * w.N)
 
-    def run(self, stream=None):
-        fl, w, d = self.fl, self.w, self.dev
+    def run(self, stream=None, d=None, out=None, ws=None):
+        """One call; `d`, `out` and `ws` replace the case's own operands, outputs and workspace."""
+        fl, w = self.fl, self.w
+        d = self.dev if d is None else d
+        out = self.out if out is None else out
+        ws = getattr(self, "ws", None) if ws is None else ws
         if w.kind in ("gelu_tanh", "gelu_erf"):
-            fl.fused_linear_gelu(d["X"], d["W"], d.get("b"), Y=self.out,
+            fl.fused_linear_gelu(d["X"], d["W"], d.get("b"), Y=out,
                                  mode="tanh" if w.kind == "gelu_tanh" else "erf", stream=stream)
         elif w.kind == "qkv_rope":
             fl.fused_qkv_rope(d["X"], d["W"], d.get("b"), n_heads=w.n_heads, head_dim=w.head_dim,
-                              seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
+                              seq_len=w.seq_len, theta=w.theta, out=out, stream=stream)
         elif w.kind == "qkv_fp8kv":
             fl.fused_qkv_rope_fp8kv(d["X"], d["W"], d.get("b"), n_heads=w.n_heads, n_kv_heads=w.n_kv_heads,
                                     head_dim=w.head_dim, seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
@@ -274,8 +279,7 @@ class Case:
             fl.fused_linear_rms_rowscale(self.h2, d["W2"], None, self.part, w.N, w.eps, Y=self.out, stream=stream)
         else:
             fl.fused_linear_residual_rmsnorm_fp8(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], w.eps,
-                                                 Yq=self.out[0], row_scale=self.out[1], workspace=self.ws,
-                                                 stream=stream)
+                                                 Yq=out[0], row_scale=out[1], workspace=ws, stream=stream)
 
     def outputs(self):
         return self.out if isinstance(self.out, tuple) else (self.out,)
@@ -429,14 +433,15 @@ def time_graph_rotating(case: Case, calls: int = 20, copies: int = 3, replays: i
     import gemm_epilogue_tcgen05_gb300 as fl
     w = case.w
     sets = [case.dev] + [{k: v.clone() for k, v in case.dev.items()} for _ in range(copies - 1)]
-    outs = [(torch.empty_like(case.out[0]), torch.empty_like(case.out[1])) for _ in range(copies)]
-    wss = [fl.rmsnorm_fp8_workspace(w.M, w.N, w.K) for _ in range(copies)]
+    outs = [case.outputs()] + [tuple(torch.empty_like(t) for t in case.outputs()) for _ in range(copies - 1)]
+    single = not isinstance(case.out, tuple)
+    wss = [getattr(case, "ws", None)] + [fl.rmsnorm_fp8_workspace(w.M, w.N, w.K) if w.kind == "rmsnorm_fp8" else None
+                                         for _ in range(copies - 1)]
 
     def seq(stream):
         for i in range(calls):
-            d, o, ws = sets[i % copies], outs[i % copies], wss[i % copies]
-            fl.fused_linear_residual_rmsnorm_fp8(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], w.eps,
-                                                 Yq=o[0], row_scale=o[1], workspace=ws, stream=stream)
+            o = outs[i % copies]
+            case.run(stream, d=sets[i % copies], out=o[0] if single else o, ws=wss[i % copies])
 
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
@@ -637,7 +642,8 @@ def main():
     rows = []
     if args.rows == "all":
         for name in ("qkv_rope_8192x12288x4096", "qkv_fp8kv_8192x6144x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
-                     "rmsnorm_fp8_decode_32x4096x14336", "rms_chain_8192x4096x4096_to_14336",
+                     "rmsnorm_fp8_decode_32x4096x14336", "gelu_decode_32x16384x4096", "qkv_decode_32x12288x4096",
+                     "rms_chain_8192x4096x4096_to_14336",
                      "lm_head_ce_8192x32768x4096", "gelu_bwd_8192x16384x4096", "swiglu_bwd_8192x14336x4096",
                      "quant_fp8_1x128_8192x16384x4096",
                      "quant_int4_g32_8192x16384x4096", "quant_nvfp4_g16_8192x16384x4096"):

@@ -86,6 +86,8 @@ def load() -> ctypes.CDLL:
     lib.fl_set_max_ctas.restype = None
     lib.fl_set_cta_pairing.argtypes = [I]
     lib.fl_set_cta_pairing.restype = None
+    lib.fl_set_linear_decode.argtypes = [I]
+    lib.fl_set_linear_decode.restype = None
     lib.fl_status_string.argtypes = [I]
     lib.fl_status_string.restype = ctypes.c_char_p
     lib.fl_version.argtypes = []
@@ -508,3 +510,9 @@ def set_max_ctas(n: int) -> None:
 def set_cta_pairing(enable: bool) -> None:
     """Two-CTA (cta_group::2) prefill tiles on (default) or off; results are the same."""
     load().fl_set_cta_pairing(1 if enable else 0)
+
+
+def set_linear_decode(enable: bool) -> None:
+    """Decode kernels for M <= 32 calls of fused_linear_gelu (bf16), fused_swiglu and fused_qkv_rope
+    on (default) or off (the prefill GEMM kernel then takes them)."""
+    load().fl_set_linear_decode(1 if enable else 0)

@@ -24,6 +24,7 @@ int* g_status_ptr[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_max_ctas{0};
 std::atomic<int> g_pairing{1};
+std::atomic<int> g_linear_decode{1};
 
 struct SmemAttr {
   const void* fn;
@@ -86,6 +87,7 @@ int* device_status_ptr(int device) {
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 int max_ctas_override() { return g_max_ctas.load(); }
 int cta_pairing_mode() { return g_pairing.load(); }
+int linear_decode_mode() { return g_linear_decode.load(); }
 
 bool launch_tool_attached() {
   // Nsight tools announce their injection through these variables in the target process.
@@ -144,6 +146,8 @@ void fl_set_wait_timeout_ns(uint64_t ns) { fl::g_timeout_ns.store(ns == 0 ? fl::
 void fl_set_max_ctas(int n) { fl::g_max_ctas.store(n < 0 ? 0 : n); }
 
 void fl_set_cta_pairing(int enable) { fl::g_pairing.store(enable != 0 ? 1 : 0); }
+
+void fl_set_linear_decode(int enable) { fl::g_linear_decode.store(enable != 0 ? 1 : 0); }
 
 const char* fl_status_string(int status) {
   switch (status) {

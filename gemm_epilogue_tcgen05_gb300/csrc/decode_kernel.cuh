@@ -75,16 +75,6 @@ __host__ __device__ inline int dec_cta_of(int u, int units, int grid) {
 }
 
 // Four bf16 values [n, n+4) of a vector as fp32 (8-byte load when fully in range); zeros at or past `limit`.
-__device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* base, int n, int limit, float (&v)[4]) {
-  if (n + 4 <= limit) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(base + n));
-    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = n + j < limit ? __bfloat162float(base[n + j]) : 0.f;
-  }
-}
-
 __device__ __forceinline__ bool spin_until(const unsigned* ctr, unsigned need, const int* status,
                                            unsigned long long timeout_ns, int* status_w, int where, int detail) {
   const uint64_t t0 = global_timer_ns();

@@ -1,0 +1,325 @@
+// Decode-shaped (M <= 32 tokens) Linear layers with element-wise epilogues: bias + GELU, SwiGLU,
+// and the fused QKV projection with RoPE.
+//
+// With a few dozen tokens the GEMM is a stream over W ("GEMM Epilogue 完全拆解"
+// (pinghaoyang.com.cn), §边界五), and a 256-row output tile would spend its tensor-core time on
+// rows that do not exist.  The kernel therefore swaps the operands like the RMSNorm decode
+// kernel: D^T[128 W rows x 32 tokens] = W_tile * X^T on tcgen05 (MMA M = 128, N = 32), one
+// thread-block cluster of C CTAs per tile of W rows, CTA r streaming the k blocks
+// [r K/C, (r+1) K/C).  No row statistic couples the tiles, so the tail stays inside the cluster:
+// the C partial tiles are summed through distributed shared memory in rank order (deterministic),
+// each CTA finishing its share of the tile's outputs: bias, then GELU (§GELU激活融合 of "Triton
+// 算子融合: Linear 与 Attention"), SiLU(g) u (§模式 C of the epilogue page), or the rotation of
+// adjacent feature pairs (Q and K; §模式 B), written as bf16 with 16-byte stores.
+//
+// A tile of W rows is
+//   GELU:   128 output features;
+//   QKV:    one head (128 rows) of the Q, K or V section of the stacked W_qkv;
+//   SwiGLU: 64 gate rows and the 64 up rows of the same 64 output features (two TMA boxes), so the
+//           gate and up values of a feature sit in the same tile.
+// Every CTA passes both cluster barriers whatever happens (errors only skip work).
+#pragma once
+#include "gemm_kernel.cuh"
+
+namespace fl {
+
+enum LinearDecodeKind : int { LD_GELU_TANH = 0, LD_GELU_ERF = 1, LD_SWIGLU = 2, LD_QKV_ROPE = 3 };
+
+constexpr int kLdTokens = 32;                   // MMA N: the tokens
+constexpr int kLdStages = 10;
+constexpr int kLdABytes = 128 * kBK * 2;        // W rows of the tile
+constexpr int kLdStageBytes = kLdABytes + kLdTokens * kBK * 2;
+constexpr int kLdL2PrefetchUnits = 16;          // W k blocks pulled into L2 before griddepcontrol.wait
+
+struct alignas(128) LinearDecodeParams {
+  CUtensorMap map_w;   // W [rows, K] bf16, box {64, 128}; SwiGLU: W_gate, box {64, 64}
+  CUtensorMap map_w2;  // SwiGLU: W_up, box {64, 64}
+  CUtensorMap map_x;   // X [M, K] bf16, box {64, 32}
+  int M, K;
+  int n_out;           // output features: GELU N, SwiGLU d_ff, QKV d_model (per section)
+  int num_f, num_kb;   // W-row tiles, 64-wide k blocks
+  const __nv_bfloat16* bias;   // [W rows] or null (SwiGLU: b_gate [d_ff])
+  const __nv_bfloat16* bias2;  // SwiGLU: b_up [d_ff] or null
+  __nv_bfloat16* out[3];       // GELU, SwiGLU: out[0]; QKV: Q, K, V
+  long long ldo;
+  const int* positions;        // QKV: token positions [M], or null for m % seq_len
+  int seq_len;
+  double log2_theta;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+constexpr int kLdSmallBytes = 1024;  // RoPE frequencies (128 floats), flags
+constexpr int kLdSmemBytes = kLdStages * kLdStageBytes + kLdSmallBytes + 1024 /*bars*/ + 1024 /*align*/;
+
+template <int C, int KIND>
+__global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid_constant__ LinearDecodeParams p) {
+  static_assert(C == 1 || C == 2 || C == 4 || C == 8, "cluster size");
+  constexpr bool kSwiglu = KIND == LD_SWIGLU;
+  constexpr int kOut = kSwiglu ? 64 : 128;    // output features per tile
+  constexpr int kRows = kOut / C;             // output features this CTA finishes
+  constexpr int kGroups = kRows / 8;          // groups of 8 features per token
+  constexpr int kItems = 32 * kGroups;        // (token, group) items
+  constexpr int kIpt = (kItems + 127) / 128;  // items per epilogue thread
+  static_assert(kGroups >= 1, "at least 8 features per CTA");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_mem = smem;
+  float* P = reinterpret_cast<float*>(stage_mem);  // [32 tokens][128 W rows] after the stream
+  uint8_t* small = smem + kLdStages * kLdStageBytes;
+  float* inv_freq = reinterpret_cast<float*>(small);            // QKV: [64] hi, [64] lo
+  volatile int* flags = reinterpret_cast<volatile int*>(inv_freq + 128);  // [0] this CTA ok
+  uint64_t* bars = reinterpret_cast<uint64_t*>(small + kLdSmallBytes);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + kLdStages;
+  uint64_t* tfull_bar = bars + 2 * kLdStages;
+  uint64_t* drain_bar = tfull_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtx wctx{abort_flag, p.status, p.timeout_ns};
+  const uint32_t rank = C > 1 ? cluster_ctarank() : 0u;
+  const int f = static_cast<int>(blockIdx.x) / C;  // W-row tile of this cluster
+  const int kb0 = static_cast<int>(rank) * p.num_kb / C;
+  const int kb1 = (static_cast<int>(rank) + 1) * p.num_kb / C;
+  // first W row of the tile (SwiGLU: of its gate half, and of its up half in W_up)
+  const int wrow = f * (kSwiglu ? 64 : 128);
+
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLdStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    flags[0] = 1;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.map_w);
+    tma_prefetch_desc(&p.map_x);
+    if (kSwiglu) tma_prefetch_desc(&p.map_w2);
+    // the weights do not depend on earlier work on the stream: first tiles into L2 before the wait
+    for (int kb = kb0; kb < kb1 && kb < kb0 + kLdL2PrefetchUnits; ++kb) {
+      tma_prefetch_l2_2d(&p.map_w, kb * kBK, wrow);
+      if (kSwiglu) tma_prefetch_l2_2d(&p.map_w2, kb * kBK, wrow);
+    }
+  }
+  if (KIND == LD_QKV_ROPE && threadIdx.x >= 64 && threadIdx.x < 128) {
+    const int i = threadIdx.x - 64;  // pair index within the head
+    const double fr = exp2(-(2.0 * i / 128.0) * p.log2_theta);  // theta^(-2i/128)
+    const float hi = static_cast<float>(fr);
+    inv_freq[i] = hi;
+    inv_freq[64 + i] = static_cast<float>(fr - static_cast<double>(hi));
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // X, the biases and the positions may be written by the preceding kernel
+
+  // this thread's items: token t = item / kGroups, output features kRows * rank + 8 g .. + 7 of the tile
+  const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
+  float bs[kIpt][8], b2s[kIpt][8];
+
+  // ---------------------------------------------------------------- phase 1: stream W, partial tile
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued_mask = 0, issued_phase = 0;
+      bool ok = true;
+      const uint64_t w_policy = l2_policy_evict_first();
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wctx, W_PRODUCER_EMPTY)) { ok = false; break; }
+        uint8_t* a_dst = stage_mem + stage * kLdStageBytes;
+        mbar_arrive_expect_tx(&full_bar[stage], kLdStageBytes);
+        if (kSwiglu) {
+          // gate rows 0..63, up rows 64..127 of the A tile (8 KB each in the 128-byte swizzle)
+          tma_load_2d_hint(&p.map_w, &full_bar[stage], a_dst, kb * kBK, wrow, w_policy);
+          tma_load_2d_hint(&p.map_w2, &full_bar[stage], a_dst + 64 * kBK * 2, kb * kBK, wrow, w_policy);
+        } else {
+          tma_load_2d_hint(&p.map_w, &full_bar[stage], a_dst, kb * kBK, wrow, w_policy);
+        }
+        tma_load_2d(&p.map_x, &full_bar[stage], a_dst + kLdABytes, kb * kBK, 0);
+        issued_mask |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == kLdStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) {
+        flags[0] = 0;
+        for (int s = 0; s < kLdStages; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_quiet(&full_bar[s], (issued_phase >> s) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kLdTokens);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, wctx, W_MMA_FULL)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(stage_mem + stage * kLdStageBytes);
+        const uint64_t adesc = sdesc_k_sw128(a_addr);
+        const uint64_t bdesc = sdesc_k_sw128(a_addr + kLdABytes);
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k)
+          mma_bf16(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        mma_commit(&empty_bar[stage]);
+        if (++stage == kLdStages) { stage = 0; phase ^= 1u; }
+      }
+      if (ok) mma_commit(tfull_bar);
+      else flags[0] = 0;
+      mma_commit(drain_bar);
+      mbar_wait_quiet(drain_bar, 0, p.timeout_ns);
+    }
+  } else {
+    // The biases of this thread's items, loaded while the weights stream.
+#pragma unroll
+    for (int it = 0; it < kIpt; ++it) {
+      const int item = ti + 128 * it;
+      const int g = item % kGroups;
+      const bool in = item < kItems;
+      const int j = static_cast<int>(rank) * kRows + g * 8;  // feature within the tile
+      const int n = (kSwiglu ? f * 64 : f * 128) + j;        // W row (SwiGLU: output feature)
+      const int lim = KIND == LD_QKV_ROPE ? p.num_f * 128 : p.n_out;  // entries of the bias vectors
+      const int bl = in && p.bias ? lim : 0, b2l = in && p.bias2 ? lim : 0;
+      load_bf16x4(p.bias, n, bl, *reinterpret_cast<float(*)[4]>(bs[it]));
+      load_bf16x4(p.bias, n + 4, bl, *reinterpret_cast<float(*)[4]>(bs[it] + 4));
+      if (kSwiglu) {
+        load_bf16x4(p.bias2, n, b2l, *reinterpret_cast<float(*)[4]>(b2s[it]));
+        load_bf16x4(p.bias2, n + 4, b2l, *reinterpret_cast<float(*)[4]>(b2s[it] + 4));
+      }
+    }
+    // TMEM lane quarter q = W rows 32 q .. 32 q + 31 of the tile; each thread one row, 32 tokens.
+    const int q = warp & 3;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar, 0, wctx, W_EPI_TMEM_FULL));
+    if (ok) {
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16), acc);
+      tmem_ld_wait();
+      const int r = q * 32 + lane;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) P[t * 128 + r] = __uint_as_float(acc[t]);
+    } else if (lane == 0) {
+      flags[0] = 0;
+    }
+  }
+  // Cluster barrier A: every CTA of the cluster has its partial tile in P.
+  __syncwarp();
+  if (C > 1) cluster_sync_all();
+  else __syncthreads();
+
+  // ---------------------------------------------------------------- phase 2: reduce, epilogue, store
+  int fv[C];
+  if constexpr (C > 1) {
+#pragma unroll
+    for (int j = 0; j < C; ++j)
+      fv[j] = ld_dsmem_s32(mapa_shared(smem_u32(const_cast<int*>(flags)), static_cast<uint32_t>(j)));
+  } else {
+    fv[0] = flags[0];
+  }
+  int all = 1;
+#pragma unroll
+  for (int j = 0; j < C; ++j) all &= fv[j] != 0 ? 1 : 0;
+  if (ti >= 0 && all != 0) {
+    // QKV: section and head of the tile (a tile is one head of one section)
+    const int d = p.n_out;
+    const int sec = KIND == LD_QKV_ROPE ? (f * 128) / d : 0;
+    const int col_base = KIND == LD_QKV_ROPE ? f * 128 - sec * d : f * kOut;
+    __nv_bfloat16* out = p.out[sec];
+#pragma unroll
+    for (int it = 0; it < kIpt; ++it) {
+      const int item = ti + 128 * it;
+      if (item >= kItems) continue;
+      const int t = item / kGroups, g = item % kGroups;
+      const int j = static_cast<int>(rank) * kRows + g * 8;  // first output feature within the tile
+      // sums of the C partials in rank order (SwiGLU: the gate rows j.., and the up rows 64 + j..)
+      float s[8], s2[8];
+      {
+        const uint32_t la = smem_u32(P + t * 128 + j);
+        float4 xa[C], xb[C], ya[C], yb[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          const uint32_t ra = C > 1 ? mapa_shared(la, static_cast<uint32_t>(c)) : la;
+          xa[c] = C > 1 ? ld_dsmem_f4(ra) : *reinterpret_cast<const float4*>(P + t * 128 + j);
+          xb[c] = C > 1 ? ld_dsmem_f4(ra + 16) : *reinterpret_cast<const float4*>(P + t * 128 + j + 4);
+          if (kSwiglu) {
+            ya[c] = C > 1 ? ld_dsmem_f4(ra + 256) : *reinterpret_cast<const float4*>(P + t * 128 + 64 + j);
+            yb[c] = C > 1 ? ld_dsmem_f4(ra + 272) : *reinterpret_cast<const float4*>(P + t * 128 + 68 + j);
+          }
+        }
+        float4 a = xa[0], b = xb[0], u = ya[0], v = yb[0];
+#pragma unroll
+        for (int c = 1; c < C; ++c) {
+          a.x += xa[c].x; a.y += xa[c].y; a.z += xa[c].z; a.w += xa[c].w;
+          b.x += xb[c].x; b.y += xb[c].y; b.z += xb[c].z; b.w += xb[c].w;
+          if (kSwiglu) {
+            u.x += ya[c].x; u.y += ya[c].y; u.z += ya[c].z; u.w += ya[c].w;
+            v.x += yb[c].x; v.y += yb[c].y; v.z += yb[c].z; v.w += yb[c].w;
+          }
+        }
+        s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w; s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+        s2[0] = u.x; s2[1] = u.y; s2[2] = u.z; s2[3] = u.w; s2[4] = v.x; s2[5] = v.y; s2[6] = v.z; s2[7] = v.w;
+      }
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float h = s[e] + bs[it][e];
+        if (KIND == LD_GELU_TANH) y[e] = gelu_tanh_f(h);
+        else if (KIND == LD_GELU_ERF) y[e] = gelu_erf_f(h);
+        else if (KIND == LD_SWIGLU) y[e] = silu_f(h) * (s2[e] + b2s[it][e]);
+        else y[e] = h;
+      }
+      if (KIND == LD_QKV_ROPE && sec < 2) {
+        // adjacent pairs (2i, 2i + 1) of the head: i = (j + e) / 2
+        const float pos = static_cast<float>(p.positions != nullptr ? (t < p.M ? p.positions[t] : 0)
+                                                                     : t % p.seq_len);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int i = (j + e) >> 1;
+          float sn, cs;
+          rope_sincos(pos, inv_freq[i], inv_freq[64 + i], sn, cs);
+          const float x0 = y[e], x1 = y[e + 1];
+          y[e] = x0 * cs - x1 * sn;
+          y[e + 1] = fmaf(x0, sn, x1 * cs);
+        }
+      }
+      const int col = col_base + j;
+      if (t < p.M && col < p.n_out) {
+        __nv_bfloat16* dst = out + static_cast<size_t>(t) * p.ldo + col;
+        if (col + 8 <= p.n_out) {  // 16-byte aligned: ldo % 8 == 0, col % 8 == 0
+          uint4 w;
+          w.x = pack_bf16x2(y[0], y[1]);
+          w.y = pack_bf16x2(y[2], y[3]);
+          w.z = pack_bf16x2(y[4], y[5]);
+          w.w = pack_bf16x2(y[6], y[7]);
+          *reinterpret_cast<uint4*>(dst) = w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (col + e < p.n_out) dst[e] = __float2bfloat16_rn(y[e]);
+        }
+      }
+    }
+  }
+  // Cluster barrier B: every read of a peer's P is done before any CTA of the cluster leaves.
+  __syncwarp();
+  if (C > 1) cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 32);
+  }
+}
+
+}  // namespace fl

@@ -198,6 +198,17 @@ __device__ __forceinline__ void unpack32(const uint4 (&w)[4], float (&v)[32]) {
   }
 }
 
+// Four bf16 values base[n .. n + 3] as floats; entries at or past `limit` read as zero.
+__device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* base, int n, int limit, float (&v)[4]) {
+  if (n + 4 <= limit) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(base + n));
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = n + j < limit ? __bfloat162float(base[n + j]) : 0.f;
+  }
+}
+
 __device__ __forceinline__ void tmem_load32f(uint32_t taddr, bool zero, float (&v)[32]) {
   if (zero) {
 #pragma unroll

@@ -41,6 +41,17 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Process-wide switch for the two-CTA (cta_group::2) mainloop: 1 = use it when
 // M spans at least two 128-row blocks (default), 0 = always one CTA per tile.
 int cta_pairing_mode();
+int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU and QKV + RoPE run the decode kernels
+// Decode-shaped (M <= 32) GELU, SwiGLU and QKV + RoPE (k_linear_decode.cu).  Returns FL_OK, an
+// error, or kDecodeNotTaken when the call should run on the GEMM kernel instead.
+constexpr int kDecodeNotTaken = -2;
+int linear_decode_gelu(const void* X, const void* W, const void* b, void* Y, int M, int N, int K, int64_t ldx,
+                       int64_t ldw, int64_t ldy, int mode, const DeviceInfo& di, cudaStream_t s);
+int linear_decode_swiglu(const void* X, const void* Wg, const void* Wu, const void* bg, const void* bu, void* Y, int M,
+                         int N, int K, int64_t ldx, int64_t ldw, int64_t ldy, const DeviceInfo& di, cudaStream_t s);
+int linear_decode_qkv(const void* X, const void* Wqkv, const void* bqkv, void* const outs[3], const int32_t* positions,
+                      int M, int K, int d_model, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldo,
+                      const DeviceInfo& di, cudaStream_t s);
 // CTAs per cluster for a problem with M rows.
 inline int choose_cg(int M) { return (cta_pairing_mode() != 0 && M > kBM) ? 2 : 1; }
 

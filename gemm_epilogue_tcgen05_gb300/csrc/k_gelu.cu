@@ -197,6 +197,11 @@ extern "C" int fused_linear_gelu(const void* X, const void* W, const void* b, vo
   int st = current_device(&di);
   if (st != FL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == FL_BF16) {
+    // a few tokens: the swap-AB decode kernel streams W instead of padding a 256-row tile
+    st = linear_decode_gelu(X, W, b, Y, M, N, K, ldx, ldw, ldy, mode, di, s);
+    if (st != kDecodeNotTaken) return st;
+  }
 
   if (dtype == FL_F32) {
     Tf32Params p;

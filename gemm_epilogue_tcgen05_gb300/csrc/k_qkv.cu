@@ -89,6 +89,13 @@ extern "C" int fused_qkv_rope(const void* X, const void* Wqkv, const void* bqkv,
     return FL_ERR_ALIGNMENT;
   if (!pitch_ok(ldo, 2) || (K > 0 && (!pitch_ok(ldx, 2) || !pitch_ok(ldw, 2)))) return FL_ERR_ALIGNMENT;
   void* const outs[3] = {Q, Kout, V};
+  DeviceInfo di;
+  st = current_device(&di);
+  if (st != FL_OK) return st;
+  // a few tokens: the swap-AB decode kernel streams W instead of padding a 256-row tile
+  st = linear_decode_qkv(X, Wqkv, bqkv, outs, positions, M, K, d_model, seq_len, theta, ldx, ldw, ldo, di,
+                         static_cast<cudaStream_t>(stream));
+  if (st != kDecodeNotTaken) return st;
   return launch_qkv<EPI_QKV_ROPE>(X, Wqkv, bqkv, outs, positions, M, K, d_model, kv_width, head_dim, seq_len,
                                   theta, ldx, ldw, ldo, ldo, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream));
 }

@@ -19,6 +19,10 @@ extern "C" int fused_swiglu(const void* X, const void* Wgate, const void* Wup, c
   DeviceInfo di;
   int st = current_device(&di);
   if (st != FL_OK) return st;
+  // a few tokens: the swap-AB decode kernel streams W instead of padding a 256-row tile
+  st = linear_decode_swiglu(X, Wgate, Wup, bgate, bup, Y, M, N, K, ldx, ldw, ldy, di,
+                            static_cast<cudaStream_t>(stream));
+  if (st != kDecodeNotTaken) return st;
 
   auto setup = [&](int cg, GemmParams& p) -> bool {
     init_params(p, M, N, K, 128, cg);

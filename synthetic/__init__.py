@@ -260,6 +260,10 @@ WORKLOADS = {
                                                quant="int4_g32"),
     "quant_nvfp4_g16_8192x16384x4096": Workload("quant_nvfp4_g16_8192x16384x4096", "quant", 8192, 16384, 4096,
                                                 quant="nvfp4_g16"),
+    # decode shapes (32 tokens) of the up projection with GELU and of the fused QKV projection
+    "gelu_decode_32x16384x4096": Workload("gelu_decode_32x16384x4096", "gelu_tanh", 32, 16384, 4096),
+    "qkv_decode_32x12288x4096": Workload("qkv_decode_32x12288x4096", "qkv_rope", 32, 12288, 4096,
+                                         has_bias=False, n_heads=32, head_dim=128, seq_len=2048),
 }
 
 

@@ -203,6 +203,68 @@ def test_qkv_rope_full_workload_sampled():
     assert_bf16_close(got, ref, "qkv full")
 
 
+# ------------------------------------------------------------------ decode shapes (M <= 32) of GELU, SwiGLU, QKV
+@pytest.mark.parametrize("decode", [True, False])
+@pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (5, 4096, 512), (17, 8000, 320), (1, 16384, 256),
+                                   (32, 1000, 200), (9, 136, 64)])
+def test_gelu_decode_shapes(decode, M, N, K):
+    """Swap-AB decode kernel (clusters of 8, 4, 2 and 1 CTAs across these shapes; ragged N and K)
+    and, with the decode path off, the GEMM kernel on the same small M."""
+    fl.set_linear_decode(decode)
+    try:
+        X = _draw((M, K), syn.STREAM_X, seed=M)
+        W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=M)
+        b = _draw((N,), syn.STREAM_B, 0.3, seed=M)
+        for mode, bias in (("tanh", b), ("erf", None)):
+            Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), None if bias is None else dev_bf16(bias), mode=mode)
+            m = oracle.GELU_TANH if mode == "tanh" else oracle.GELU_ERF
+            assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), None if bias is None else f64(bias), m),
+                              f"gelu decode={decode} {mode} {M}x{N}x{K}")
+    finally:
+        fl.set_linear_decode(True)
+
+
+@pytest.mark.parametrize("decode", [True, False])
+@pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (9, 5000, 768), (3, 2000, 136), (32, 200, 64)])
+def test_swiglu_decode_shapes(decode, M, N, K):
+    fl.set_linear_decode(decode)
+    try:
+        X = _draw((M, K), syn.STREAM_X, seed=M)
+        Wg, Wu = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=M), _draw((N, K), syn.STREAM_WUP, K ** -0.5, seed=M)
+        bg, bu = _draw((N,), syn.STREAM_B, 0.1, seed=M), _draw((N,), syn.STREAM_BUP, 0.1, seed=M)
+        Y = fl.fused_swiglu(dev_bf16(X), dev_bf16(Wg), dev_bf16(Wu), dev_bf16(bg), dev_bf16(bu))
+        assert_bf16_close(host(Y), oracle.swiglu(f64(X), f64(Wg), f64(Wu), f64(bg), f64(bu)),
+                          f"swiglu decode={decode} {M}x{N}x{K}")
+        Y = fl.fused_swiglu(dev_bf16(X), dev_bf16(Wg), dev_bf16(Wu), None, None)
+        assert_bf16_close(host(Y), oracle.swiglu(f64(X), f64(Wg), f64(Wu), None, None),
+                          f"swiglu decode={decode} no bias {M}x{N}x{K}")
+    finally:
+        fl.set_linear_decode(True)
+
+
+@pytest.mark.parametrize("decode", [True, False])
+@pytest.mark.parametrize("M,H,K", [(32, 4, 1024), (7, 16, 512), (1, 32, 256), (20, 2, 200)])
+def test_qkv_rope_decode_shapes(decode, M, H, K):
+    fl.set_linear_decode(decode)
+    try:
+        D = 128
+        X = _draw((M, K), syn.STREAM_X, seed=M)
+        Wq = _draw((3 * H * D, K), syn.STREAM_W, K ** -0.5, seed=M)
+        bq = _draw((3 * H * D,), syn.STREAM_B, 0.02, seed=M)
+        d = H * D
+        q, k, v = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), dev_bf16(bq), n_heads=H, head_dim=D, seq_len=5)
+        ref = _qkv_ref(X, Wq, bq, H, D, np.arange(M) % 5)
+        assert_bf16_close(host(torch.cat([q, k, v], 1)), ref, f"qkv decode={decode} M={M} H={H} K={K}")
+        # decode positions deep into a long context (the angle reduction matters there)
+        pos = np.random.default_rng(M).integers(0, 1 << 20, size=M).astype(np.int32)
+        q, k, v = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, head_dim=D,
+                                    positions=torch.from_numpy(pos).cuda())
+        ref = _qkv_ref(X, Wq, None, H, D, pos)
+        assert_bf16_close(host(torch.cat([q, k, v], 1)), ref, f"qkv decode={decode} positions M={M} H={H}")
+    finally:
+        fl.set_linear_decode(True)
+
+
 # ------------------------------------------------------------------ SwiGLU
 def test_swiglu_small_ragged_with_bias():
     M, N, K = 300, 200, 136
