@@ -227,7 +227,7 @@ class Case:
             self.flops = 2.0 * w.M * w.N * w.K
         self.bytes = self.algorithmic_bytes()
         # decode shapes (32 tokens): the weight stream bounds them
-        self.hbm_bound = w.M <= 32 and w.kind in ("rmsnorm_fp8", "gelu_tanh", "qkv_rope")
+        self.hbm_bound = w.M <= 32 and w.kind in ("rmsnorm_fp8", "gelu_tanh", "qkv_rope", "qkv_fp8kv")
 
     def algorithmic_bytes(self) -> float:
         """Each operand read once and each output written once (bytes)."""
@@ -260,23 +260,23 @@ class Case:
                               seq_len=w.seq_len, theta=w.theta, out=out, stream=stream)
         elif w.kind == "qkv_fp8kv":
             fl.fused_qkv_rope_fp8kv(d["X"], d["W"], d.get("b"), n_heads=w.n_heads, n_kv_heads=w.n_kv_heads,
-                                    head_dim=w.head_dim, seq_len=w.seq_len, theta=w.theta, out=self.out, stream=stream)
+                                    head_dim=w.head_dim, seq_len=w.seq_len, theta=w.theta, out=out, stream=stream)
         elif w.kind == "swiglu":
-            fl.fused_swiglu(d["X"], d["Wgate"], d["Wup"], d.get("bgate"), d.get("bup"), Y=self.out, stream=stream)
+            fl.fused_swiglu(d["X"], d["Wgate"], d["Wup"], d.get("bgate"), d.get("bup"), Y=out, stream=stream)
         elif w.kind == "cross_entropy":
-            fl.fused_linear_cross_entropy(d["X"], d["W"], d.get("b"), self.labels, loss=self.out, workspace=self.ws,
+            fl.fused_linear_cross_entropy(d["X"], d["W"], d.get("b"), self.labels, loss=out, workspace=self.ws,
                                           stream=stream)
         elif w.kind == "gelu_bwd":
-            fl.fused_dgrad_gelu(d["dZ"], d["W"], d["H"], mode="tanh", dH=self.out, stream=stream)
+            fl.fused_dgrad_gelu(d["dZ"], d["W"], d["H"], mode="tanh", dH=out, stream=stream)
         elif w.kind == "swiglu_bwd":
-            fl.fused_swiglu_bwd(d["dO"], d["Wd"], d["G"], d["U"], dGU=self.out, stream=stream)
+            fl.fused_swiglu_bwd(d["dO"], d["Wd"], d["G"], d["U"], dGU=out, stream=stream)
         elif w.kind == "quant":
-            fl.fused_linear_quant(d["X"], d["W"], d.get("b"), self.fmt, Yq=self.out[0], scales=self.out[1],
+            fl.fused_linear_quant(d["X"], d["W"], d.get("b"), self.fmt, Yq=out[0], scales=out[1],
                                   stream=stream)
         elif w.kind == "rms_chain":
             fl.fused_linear_residual_gamma(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], store_h1=False, H2=self.h2,
                                            rms_partials=self.part, stream=stream)
-            fl.fused_linear_rms_rowscale(self.h2, d["W2"], None, self.part, w.N, w.eps, Y=self.out, stream=stream)
+            fl.fused_linear_rms_rowscale(self.h2, d["W2"], None, self.part, w.N, w.eps, Y=out, stream=stream)
         else:
             fl.fused_linear_residual_rmsnorm_fp8(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], w.eps,
                                                  Yq=out[0], row_scale=out[1], workspace=ws, stream=stream)
@@ -643,6 +643,7 @@ def main():
     if args.rows == "all":
         for name in ("qkv_rope_8192x12288x4096", "qkv_fp8kv_8192x6144x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
                      "rmsnorm_fp8_decode_32x4096x14336", "gelu_decode_32x16384x4096", "qkv_decode_32x12288x4096",
+                     "qkv_fp8kv_decode_32x6144x4096",
                      "rms_chain_8192x4096x4096_to_14336",
                      "lm_head_ce_8192x32768x4096", "gelu_bwd_8192x16384x4096", "swiglu_bwd_8192x14336x4096",
                      "quant_fp8_1x128_8192x16384x4096",

@@ -513,6 +513,6 @@ def set_cta_pairing(enable: bool) -> None:
 
 
 def set_linear_decode(enable: bool) -> None:
-    """Decode kernels for M <= 32 calls of fused_linear_gelu (bf16), fused_swiglu and fused_qkv_rope
-    on (default) or off (the prefill GEMM kernel then takes them)."""
+    """Decode kernels for M <= 32 calls of fused_linear_gelu (bf16), fused_swiglu, fused_qkv_rope and
+    fused_qkv_rope_fp8kv on (default) or off (the prefill GEMM kernel then takes them)."""
     load().fl_set_linear_decode(1 if enable else 0)

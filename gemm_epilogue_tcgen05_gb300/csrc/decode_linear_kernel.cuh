@@ -1,5 +1,5 @@
 // Decode-shaped (M <= 32 tokens) Linear layers with element-wise epilogues: bias + GELU, SwiGLU,
-// and the fused QKV projection with RoPE.
+// the fused QKV projection with RoPE, and its grouped-query form with the K/V cache entry in FP8.
 //
 // With a few dozen tokens the GEMM is a stream over W ("GEMM Epilogue 完全拆解"
 // (pinghaoyang.com.cn), §边界五), and a 256-row output tile would spend its tensor-core time on
@@ -14,7 +14,9 @@
 //
 // A tile of W rows is
 //   GELU:   128 output features;
-//   QKV:    one head (128 rows) of the Q, K or V section of the stacked W_qkv;
+//   QKV:    one head (128 rows) of the Q, K or V section of the stacked W_qkv (the FP8 K/V form:
+//           K rotated, then K and V as E4M3 with one scale per token and head, max|.|/448 over the
+//           head's 128 values, which takes one more exchange between the cluster's CTAs);
 //   SwiGLU: 64 gate rows and the 64 up rows of the same 64 output features (two TMA boxes), so the
 //           gate and up values of a feature sit in the same tile.
 // Every CTA passes both cluster barriers whatever happens (errors only skip work).
@@ -23,7 +25,7 @@
 
 namespace fl {
 
-enum LinearDecodeKind : int { LD_GELU_TANH = 0, LD_GELU_ERF = 1, LD_SWIGLU = 2, LD_QKV_ROPE = 3 };
+enum LinearDecodeKind : int { LD_GELU_TANH = 0, LD_GELU_ERF = 1, LD_SWIGLU = 2, LD_QKV_ROPE = 3, LD_QKV_FP8KV = 4 };
 
 constexpr int kLdTokens = 32;                   // MMA N: the tokens
 constexpr int kLdStages = 10;
@@ -36,12 +38,17 @@ struct alignas(128) LinearDecodeParams {
   CUtensorMap map_w2;  // SwiGLU: W_up, box {64, 64}
   CUtensorMap map_x;   // X [M, K] bf16, box {64, 32}
   int M, K;
-  int n_out;           // output features: GELU N, SwiGLU d_ff, QKV d_model (per section)
+  int n_out;           // output features: GELU N, SwiGLU d_ff, QKV d_model (the Q section)
+  int kv_width;        // QKV: width of the K and V sections (= n_out for the plain QKV)
   int num_f, num_kb;   // W-row tiles, 64-wide k blocks
   const __nv_bfloat16* bias;   // [W rows] or null (SwiGLU: b_gate [d_ff])
   const __nv_bfloat16* bias2;  // SwiGLU: b_up [d_ff] or null
-  __nv_bfloat16* out[3];       // GELU, SwiGLU: out[0]; QKV: Q, K, V
+  __nv_bfloat16* out[3];       // GELU, SwiGLU: out[0]; QKV: Q, K, V (FP8 K/V form: Q only)
   long long ldo;
+  uint8_t* out_kv[2];          // FP8 K/V form: K and V codes [M, kv_width]
+  long long ldkv;
+  float* kv_scale[2];          // FP8 K/V form: K and V scales [M][lds], one per head
+  long long lds;
   const int* positions;        // QKV: token positions [M], or null for m % seq_len
   int seq_len;
   double log2_theta;
@@ -49,7 +56,7 @@ struct alignas(128) LinearDecodeParams {
   unsigned long long timeout_ns;
 };
 
-constexpr int kLdSmallBytes = 1024;  // RoPE frequencies (128 floats), flags
+constexpr int kLdSmallBytes = 1024;  // RoPE frequencies (128 floats), per-token maxima (32), flags
 constexpr int kLdSmemBytes = kLdStages * kLdStageBytes + kLdSmallBytes + 1024 /*bars*/ + 1024 /*align*/;
 
 template <int C, int KIND>
@@ -68,7 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
   float* P = reinterpret_cast<float*>(stage_mem);  // [32 tokens][128 W rows] after the stream
   uint8_t* small = smem + kLdStages * kLdStageBytes;
   float* inv_freq = reinterpret_cast<float*>(small);            // QKV: [64] hi, [64] lo
-  volatile int* flags = reinterpret_cast<volatile int*>(inv_freq + 128);  // [0] this CTA ok
+  float* pmax = inv_freq + 128;                                 // FP8 K/V: [32] this CTA's per-token max
+  volatile int* flags = reinterpret_cast<volatile int*>(pmax + 32);  // [0] this CTA ok
   uint64_t* bars = reinterpret_cast<uint64_t*>(small + kLdSmallBytes);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + kLdStages;
@@ -109,7 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
       if (kSwiglu) tma_prefetch_l2_2d(&p.map_w2, kb * kBK, wrow);
     }
   }
-  if (KIND == LD_QKV_ROPE && threadIdx.x >= 64 && threadIdx.x < 128) {
+  constexpr bool kQkv = KIND == LD_QKV_ROPE || KIND == LD_QKV_FP8KV;
+  if (kQkv && threadIdx.x >= 64 && threadIdx.x < 128) {
     const int i = threadIdx.x - 64;  // pair index within the head
     const double fr = exp2(-(2.0 * i / 128.0) * p.log2_theta);  // theta^(-2i/128)
     const float hi = static_cast<float>(fr);
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
       const bool in = item < kItems;
       const int j = static_cast<int>(rank) * kRows + g * 8;  // feature within the tile
       const int n = (kSwiglu ? f * 64 : f * 128) + j;        // W row (SwiGLU: output feature)
-      const int lim = KIND == LD_QKV_ROPE ? p.num_f * 128 : p.n_out;  // entries of the bias vectors
+      const int lim = kQkv ? p.num_f * 128 : p.n_out;  // entries of the bias vectors
       const int bl = in && p.bias ? lim : 0, b2l = in && p.bias2 ? lim : 0;
       load_bf16x4(p.bias, n, bl, *reinterpret_cast<float(*)[4]>(bs[it]));
       load_bf16x4(p.bias, n + 4, bl, *reinterpret_cast<float(*)[4]>(bs[it] + 4));
@@ -232,21 +241,25 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
   int all = 1;
 #pragma unroll
   for (int j = 0; j < C; ++j) all &= fv[j] != 0 ? 1 : 0;
-  if (ti >= 0 && all != 0) {
-    // QKV: section and head of the tile (a tile is one head of one section)
-    const int d = p.n_out;
-    const int sec = KIND == LD_QKV_ROPE ? (f * 128) / d : 0;
-    const int col_base = KIND == LD_QKV_ROPE ? f * 128 - sec * d : f * kOut;
-    __nv_bfloat16* out = p.out[sec];
+  // QKV: section (0 Q, 1 K, 2 V) of the tile (a tile is one head of one section) and its first column
+  const int sec = !kQkv ? 0 : (f * 128 < p.n_out ? 0 : (f * 128 < p.n_out + p.kv_width ? 1 : 2));
+  const int col_base = !kQkv ? f * kOut : f * 128 - (sec == 0 ? 0 : (sec == 1 ? p.n_out : p.n_out + p.kv_width));
+  const int width = !kQkv || sec == 0 ? p.n_out : p.kv_width;
+  const bool fp8 = KIND == LD_QKV_FP8KV && sec > 0;  // the same for every CTA of the cluster
+  const bool ok = all != 0;
+  float y[kIpt][8];
+  if (ti >= 0) {
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
       const int item = ti + 128 * it;
-      if (item >= kItems) continue;
+      const bool has = item < kItems;  // the same across a warp: kItems is a multiple of 32
       const int t = item / kGroups, g = item % kGroups;
       const int j = static_cast<int>(rank) * kRows + g * 8;  // first output feature within the tile
-      // sums of the C partials in rank order (SwiGLU: the gate rows j.., and the up rows 64 + j..)
-      float s[8], s2[8];
-      {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[it][e] = 0.f;
+      if (has && ok) {
+        // sums of the C partials in rank order (SwiGLU: the gate rows j.., and the up rows 64 + j..)
+        float s[8], s2[8];
         const uint32_t la = smem_u32(P + t * 128 + j);
         float4 xa[C], xb[C], ya[C], yb[C];
 #pragma unroll
@@ -271,44 +284,95 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
         }
         s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w; s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
         s2[0] = u.x; s2[1] = u.y; s2[2] = u.z; s2[3] = u.w; s2[4] = v.x; s2[5] = v.y; s2[6] = v.z; s2[7] = v.w;
-      }
-      float y[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float h = s[e] + bs[it][e];
-        if (KIND == LD_GELU_TANH) y[e] = gelu_tanh_f(h);
-        else if (KIND == LD_GELU_ERF) y[e] = gelu_erf_f(h);
-        else if (KIND == LD_SWIGLU) y[e] = silu_f(h) * (s2[e] + b2s[it][e]);
-        else y[e] = h;
-      }
-      if (KIND == LD_QKV_ROPE && sec < 2) {
-        // adjacent pairs (2i, 2i + 1) of the head: i = (j + e) / 2
-        const float pos = static_cast<float>(p.positions != nullptr ? (t < p.M ? p.positions[t] : 0)
-                                                                     : t % p.seq_len);
+        for (int e = 0; e < 8; ++e) {
+          const float h = s[e] + bs[it][e];
+          if (KIND == LD_GELU_TANH) y[it][e] = gelu_tanh_f(h);
+          else if (KIND == LD_GELU_ERF) y[it][e] = gelu_erf_f(h);
+          else if (KIND == LD_SWIGLU) y[it][e] = silu_f(h) * (s2[e] + b2s[it][e]);
+          else y[it][e] = h;
+        }
+        if (kQkv && sec < 2) {
+          // adjacent pairs (2i, 2i + 1) of the head: i = (j + e) / 2
+          const float pos = static_cast<float>(p.positions != nullptr ? (t < p.M ? p.positions[t] : 0)
+                                                                       : t % p.seq_len);
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int i = (j + e) >> 1;
-          float sn, cs;
-          rope_sincos(pos, inv_freq[i], inv_freq[64 + i], sn, cs);
-          const float x0 = y[e], x1 = y[e + 1];
-          y[e] = x0 * cs - x1 * sn;
-          y[e + 1] = fmaf(x0, sn, x1 * cs);
+          for (int e = 0; e < 8; e += 2) {
+            const int i = (j + e) >> 1;
+            float sn, cs;
+            rope_sincos(pos, inv_freq[i], inv_freq[64 + i], sn, cs);
+            const float x0 = y[it][e], x1 = y[it][e + 1];
+            y[it][e] = x0 * cs - x1 * sn;
+            y[it][e + 1] = x0 * sn + x1 * cs;
+          }
         }
       }
-      const int col = col_base + j;
-      if (t < p.M && col < p.n_out) {
-        __nv_bfloat16* dst = out + static_cast<size_t>(t) * p.ldo + col;
-        if (col + 8 <= p.n_out) {  // 16-byte aligned: ldo % 8 == 0, col % 8 == 0
-          uint4 w;
-          w.x = pack_bf16x2(y[0], y[1]);
-          w.y = pack_bf16x2(y[2], y[3]);
-          w.z = pack_bf16x2(y[4], y[5]);
-          w.w = pack_bf16x2(y[6], y[7]);
-          *reinterpret_cast<uint4*>(dst) = w;
-        } else {
+      if (fp8) {
+        // this CTA's max |y| of token t over its features: a butterfly over the token's lanes
+        float am = 0.f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (col + e < p.n_out) dst[e] = __float2bfloat16_rn(y[e]);
+        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(y[it][e]));
+#pragma unroll
+        for (int o = kGroups / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (has && g == 0) pmax[t] = am;
+      }
+      if (!fp8 && has && ok) {
+        const int col = col_base + j;
+        __nv_bfloat16* out = p.out[sec];
+        if (t < p.M && col < width) {
+          __nv_bfloat16* dst = out + static_cast<size_t>(t) * p.ldo + col;
+          if (col + 8 <= width) {  // 16-byte aligned: ldo % 8 == 0, col % 8 == 0
+            uint4 w;
+            w.x = pack_bf16x2(y[it][0], y[it][1]);
+            w.y = pack_bf16x2(y[it][2], y[it][3]);
+            w.z = pack_bf16x2(y[it][4], y[it][5]);
+            w.w = pack_bf16x2(y[it][6], y[it][7]);
+            *reinterpret_cast<uint4*>(dst) = w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (col + e < width) dst[e] = __float2bfloat16_rn(y[it][e]);
+          }
+        }
+      }
+    }
+  }
+  if (KIND == LD_QKV_FP8KV && fp8) {
+    // FP8 K/V: the head's max over every CTA of the cluster, then scale and codes
+    __syncwarp();
+    if (C > 1) cluster_sync_all();
+    else __syncthreads();
+    if (ti >= 0 && ok) {
+#pragma unroll
+      for (int it = 0; it < kIpt; ++it) {
+        const int item = ti + 128 * it;
+        if (item >= kItems) continue;
+        const int t = item / kGroups, g = item % kGroups;
+        const int j = static_cast<int>(rank) * kRows + g * 8;
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+          amax = fmaxf(amax, C > 1 ? ld_dsmem_f32(mapa_shared(smem_u32(pmax + t), static_cast<uint32_t>(c))) : pmax[t]);
+        const float qs = amax > 0.f ? 448.f / amax : 0.f;
+        const int col = col_base + j;
+        if (t < p.M) {
+          if (rank == 0 && g == 0)
+            p.kv_scale[sec - 1][static_cast<size_t>(t) * p.lds + col_base / 128] = amax * (1.f / 448.f);
+          if (col < width) {
+            uint32_t w[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              w[k] = f32x2_to_e4m3x2(fmaf(y[it][4 * k], qs, 0.f), fmaf(y[it][4 * k + 1], qs, 0.f)) |
+                     (f32x2_to_e4m3x2(fmaf(y[it][4 * k + 2], qs, 0.f), fmaf(y[it][4 * k + 3], qs, 0.f)) << 16);
+            uint8_t* dst = p.out_kv[sec - 1] + static_cast<size_t>(t) * p.ldkv + col;
+            if (col + 8 <= width) {  // 8-byte aligned: ldkv % 16 == 0, col % 8 == 0
+              *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (col + e < width) dst[e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+            }
+          }
         }
       }
     }

@@ -41,7 +41,7 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Process-wide switch for the two-CTA (cta_group::2) mainloop: 1 = use it when
 // M spans at least two 128-row blocks (default), 0 = always one CTA per tile.
 int cta_pairing_mode();
-int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU and QKV + RoPE run the decode kernels
+int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU and QKV + RoPE (both forms) run the decode kernels
 // Decode-shaped (M <= 32) GELU, SwiGLU and QKV + RoPE (k_linear_decode.cu).  Returns FL_OK, an
 // error, or kDecodeNotTaken when the call should run on the GEMM kernel instead.
 constexpr int kDecodeNotTaken = -2;
@@ -52,6 +52,10 @@ int linear_decode_swiglu(const void* X, const void* Wg, const void* Wu, const vo
 int linear_decode_qkv(const void* X, const void* Wqkv, const void* bqkv, void* const outs[3], const int32_t* positions,
                       int M, int K, int d_model, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldo,
                       const DeviceInfo& di, cudaStream_t s);
+int linear_decode_qkv_fp8kv(const void* X, const void* Wqkv, const void* bqkv, void* Q, void* Kq, void* Vq,
+                            float* k_scale, float* v_scale, const int32_t* positions, int M, int K, int d_model,
+                            int kv_width, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldq, int64_t ldkv,
+                            int64_t lds, const DeviceInfo& di, cudaStream_t s);
 // CTAs per cluster for a problem with M rows.
 inline int choose_cg(int M) { return (cta_pairing_mode() != 0 && M > kBM) ? 2 : 1; }
 

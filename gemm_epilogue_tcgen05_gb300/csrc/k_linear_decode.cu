@@ -1,4 +1,4 @@
-// Decode-shaped (M <= 32 tokens) GELU, SwiGLU and QKV + RoPE: parameters, cluster size and launch of
+// Decode-shaped (M <= 32 tokens) GELU, SwiGLU, QKV + RoPE and its FP8 K/V form: parameters, cluster size and launch of
 // linear_decode_kernel (decode_linear_kernel.cuh).  The entry points in k_gelu.cu, k_swiglu.cu and
 // k_qkv.cu call these first; kDecodeNotTaken sends the call to the GEMM kernel instead.
 #include <cmath>
@@ -145,6 +145,7 @@ int linear_decode_qkv(const void* X, const void* Wqkv, const void* bqkv, void* c
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return FL_ERR_CUDA;
   p.n_out = d_model;
+  p.kv_width = d_model;
   p.num_f = 3 * d_model / 128;  // one head of one section per tile
   p.bias = static_cast<const __nv_bfloat16*>(bqkv);
   for (int i = 0; i < 3; ++i) p.out[i] = static_cast<__nv_bfloat16*>(outs[i]);
@@ -153,6 +154,35 @@ int linear_decode_qkv(const void* X, const void* Wqkv, const void* bqkv, void* c
   p.seq_len = seq_len;
   p.log2_theta = std::log2(static_cast<double>(theta));
   return ld_run<LD_QKV_ROPE>(p, di, s);
+}
+
+int linear_decode_qkv_fp8kv(const void* X, const void* Wqkv, const void* bqkv, void* Q, void* Kq, void* Vq,
+                            float* k_scale, float* v_scale, const int32_t* positions, int M, int K, int d_model,
+                            int kv_width, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldq, int64_t ldkv,
+                            int64_t lds, const DeviceInfo& di, cudaStream_t s) {
+  if (!ld_taken(M, K) || d_model % 128 != 0 || kv_width % 128 != 0) return kDecodeNotTaken;
+  const int rows = d_model + 2 * kv_width;
+  LinearDecodeParams p;
+  if (!ld_common(p, X, M, K, ldx, di) ||
+      !encode_2d(&p.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wqkv, K, rows, ldw, kBK, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return FL_ERR_CUDA;
+  p.n_out = d_model;
+  p.kv_width = kv_width;
+  p.num_f = rows / 128;  // one head of one section per tile
+  p.bias = static_cast<const __nv_bfloat16*>(bqkv);
+  p.out[0] = static_cast<__nv_bfloat16*>(Q);
+  p.ldo = ldq;
+  p.out_kv[0] = static_cast<uint8_t*>(Kq);
+  p.out_kv[1] = static_cast<uint8_t*>(Vq);
+  p.ldkv = ldkv;
+  p.kv_scale[0] = k_scale;
+  p.kv_scale[1] = v_scale;
+  p.lds = lds;
+  p.positions = positions;
+  p.seq_len = seq_len;
+  p.log2_theta = std::log2(static_cast<double>(theta));
+  return ld_run<LD_QKV_FP8KV>(p, di, s);
 }
 
 }  // namespace fl

@@ -121,6 +121,13 @@ extern "C" int fused_qkv_rope_fp8kv(const void* X, const void* Wqkv, const void*
     return FL_ERR_ALIGNMENT;
   if (!pitch_ok(ldq, 2) || !pitch_ok(ldkv, 1) || (K > 0 && (!pitch_ok(ldx, 2) || !pitch_ok(ldw, 2))))
     return FL_ERR_ALIGNMENT;
+  DeviceInfo di;
+  st = current_device(&di);
+  if (st != FL_OK) return st;
+  // a few tokens: the swap-AB decode kernel streams W instead of padding a 256-row tile
+  st = linear_decode_qkv_fp8kv(X, Wqkv, bqkv, Q, Kq, Vq, k_scale, v_scale, positions, M, K, d_model, kv_width,
+                               seq_len, theta, ldx, ldw, ldq, ldkv, lds, di, static_cast<cudaStream_t>(stream));
+  if (st != kDecodeNotTaken) return st;
   void* const outs[3] = {Q, Kq, Vq};
   return launch_qkv<EPI_QKV_FP8KV>(X, Wqkv, bqkv, outs, positions, M, K, d_model, kv_width, head_dim, seq_len,
                                    theta, ldx, ldw, ldq, ldkv, k_scale, v_scale, lds,

@@ -312,8 +312,8 @@ FL_API void fl_set_max_ctas(int n);
  * same either way.  Process-wide; intended for tests and diagnostics. */
 FL_API void fl_set_cta_pairing(int enable);
 
-/* Decode-shaped calls: with 1 (the default) fused_linear_gelu (bf16), fused_swiglu and
- * fused_qkv_rope with M <= 32 rows run a swap-AB kernel that streams W once (tiles of W rows
+/* Decode-shaped calls: with 1 (the default) fused_linear_gelu (bf16), fused_swiglu,
+ * fused_qkv_rope and fused_qkv_rope_fp8kv with M <= 32 rows run a swap-AB kernel that streams W once (tiles of W rows
  * on the tensor cores' M side, the tokens on N, split-K across a thread-block cluster) whenever
  * its tiles (128 output features; SwiGLU 64) fit on the SMs at once; with 0 they run on the
  * prefill GEMM kernel.  Results agree within rounding (the split-K sums in a different order).

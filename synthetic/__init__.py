@@ -264,6 +264,9 @@ WORKLOADS = {
     "gelu_decode_32x16384x4096": Workload("gelu_decode_32x16384x4096", "gelu_tanh", 32, 16384, 4096),
     "qkv_decode_32x12288x4096": Workload("qkv_decode_32x12288x4096", "qkv_rope", 32, 12288, 4096,
                                          has_bias=False, n_heads=32, head_dim=128, seq_len=2048),
+    "qkv_fp8kv_decode_32x6144x4096": Workload("qkv_fp8kv_decode_32x6144x4096", "qkv_fp8kv", 32, 6144, 4096,
+                                              has_bias=False, n_heads=32, n_kv_heads=8, head_dim=128,
+                                              seq_len=2048),
 }
 
 

@@ -628,6 +628,31 @@ def test_qkv_fp8kv_small(pairing, H, Hkv):
         assert torch.equal(q, out[0])
 
 
+@pytest.mark.parametrize("decode", [True, False])
+@pytest.mark.parametrize("M,H,Hkv,K", [(32, 4, 2, 1024), (7, 32, 8, 512), (1, 16, 4, 256), (20, 2, 2, 200)])
+def test_qkv_fp8kv_decode_shapes(decode, M, H, Hkv, K):
+    """Decode shapes of the FP8 K/V form (clusters of 8, 2, 4 and 4 CTAs: the head's max spans the
+    cluster), and the GEMM kernel on the same shapes with the decode path off."""
+    fl.set_linear_decode(decode)
+    try:
+        D = 128
+        X = _draw((M, K), syn.STREAM_X, seed=M + 1)
+        Wq = _draw(((H + 2 * Hkv) * D, K), syn.STREAM_W, K ** -0.5, seed=M + 1)
+        bq = _draw(((H + 2 * Hkv) * D,), syn.STREAM_B, 0.5, seed=M + 1)
+        zero = M // 2
+        X[zero] = 0  # without bias this token's K and V heads are all zero -> scale 0, codes 0
+        pos = np.random.default_rng(M).integers(0, 1 << 20, size=M).astype(np.int32)
+        for bias in (bq, None):
+            out = fl.fused_qkv_rope_fp8kv(dev_bf16(X), dev_bf16(Wq), None if bias is None else dev_bf16(bias),
+                                          n_heads=H, n_kv_heads=Hkv, head_dim=D,
+                                          positions=torch.from_numpy(pos).cuda())
+            ref = oracle.qkv_rope_kv_fp8(f64(X), f64(Wq), None if bias is None else f64(bias), H, Hkv, D, 1e4, pos)
+            _check_kv_fp8(out, ref, f"qkv fp8kv decode={decode} M={M} H={H} Hkv={Hkv} bias={bias is not None}")
+        assert torch.count_nonzero(out[1][zero]) == 0 and torch.count_nonzero(out[4][zero]) == 0
+    finally:
+        fl.set_linear_decode(True)
+
+
 def test_qkv_fp8kv_rejects_odd_heads():
     X = dev_bf16(_draw((8, 64), syn.STREAM_X))
     W = dev_bf16(_draw(((2 + 2) * 128, 64), syn.STREAM_W))
