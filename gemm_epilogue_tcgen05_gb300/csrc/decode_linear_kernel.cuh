@@ -9,8 +9,9 @@
 // [r K/C, (r+1) K/C).  No row statistic couples the tiles, so the tail stays inside the cluster:
 // the C partial tiles are summed through distributed shared memory in rank order (deterministic),
 // each CTA finishing its share of the tile's outputs: bias, then GELU (§GELU激活融合 of "Triton
-// 算子融合: Linear 与 Attention"), SiLU(g) u (§模式 C of the epilogue page), or the rotation of
-// adjacent feature pairs (Q and K; §模式 B), written as bf16 with 16-byte stores.
+// 算子融合: Linear 与 Attention"), SiLU(g) u (§模式 B of the epilogue page), or the rotation of
+// adjacent feature pairs of Q and K (§QKV投影融合 of the Triton page; §模式 B), written as bf16
+// with 16-byte stores.
 //
 // A tile of W rows is
 //   GELU:   128 output features;
