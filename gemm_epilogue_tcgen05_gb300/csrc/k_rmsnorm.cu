@@ -74,13 +74,14 @@ int max_active_clusters(const DeviceInfo& di) {
 }
 
 // Cluster size for the cluster decode kernel, or 0 to run the flat split-K kernel: every
-// feature tile gets a resident cluster of C CTAs, each CTA streams at least one k block, and
-// at least three quarters of the SMs take part in the weight stream.
+// feature tile gets a resident cluster of C CTAs and each CTA streams at least one k block.
+// The cluster kernel wins whenever it fits, even on few SMs (measured, 20 back-to-back calls:
+// 32 x 14336 x 4096 on 112 SMs 27.1 us against 33.3 us flat; 32 x 1024 x 14336 on 64 SMs 14.6
+// against 18.7 us), so the flat kernel serves only more tiles than SMs, or a CTA cap.
 int pick_decode_cluster(const DeviceInfo& di, int num_f, int num_kb, int sms) {
   const int cs[4] = {8, 4, 2, 1};
   for (int C : cs) {
     if (C > num_kb || static_cast<long long>(num_f) * C > sms) continue;
-    if (4LL * num_f * C < 3LL * sms) return 0;  // too few SMs would stream: the flat kernel uses them all
     const int fit = C == 8   ? max_active_clusters<8>(di)
                     : C == 4 ? max_active_clusters<4>(di)
                     : C == 2 ? max_active_clusters<2>(di)

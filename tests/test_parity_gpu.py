@@ -332,7 +332,7 @@ def test_rmsnorm_fp8_decode_flat_kernel_under_cta_cap():
     M, N, K = 24, 4096, 768
     X, W, b, Z, g = _rms_case(M, N, K, True, seed=5)
     q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), f64(b), f64(Z), f64(g), 1e-6)
-    for cap in (0, 100, 40):
+    for cap in (0, 24, 16):  # 32 feature tiles: one cluster each needs 32 SMs or more
         fl.set_max_ctas(cap)
         ws = fl.rmsnorm_fp8_workspace(M, N, K)
         q, s = _rms_run(X, W, b, Z, g, workspace=ws)
@@ -416,13 +416,14 @@ def test_rmsnorm_fp8_decode_full_workload():
     assert_fp8_close(q, s, q_ref, s_ref, "decode full")
 
 
-@pytest.mark.parametrize("M,N", [(256, 1024), (16, 1024), (16, 4096)])
-def test_rmsnorm_fp8_wait_timeout_reports_status(M, N):
+@pytest.mark.parametrize("M,N,cap", [(256, 1024, 0), (16, 1024, 4), (16, 4096, 0)])
+def test_rmsnorm_fp8_wait_timeout_reports_status(M, N, cap):
     # A counter that never reaches its target makes the exchange wait run out:
     # the kernel records FL_ERR_TIMEOUT, drains and returns; the context stays usable.
-    # (M = 16: N = 1024 runs the flat decode kernel, N = 4096 the cluster one; both keep
-    # their grid-wide count at counters[N / 128].)
+    # (M = 16: under a cap of 4 CTAs N = 1024 runs the flat decode kernel, N = 4096 the cluster
+    # one; both keep their grid-wide count at counters[N / 128].)
     K = 512
+    fl.set_max_ctas(cap)
     X, W, b, Z, g = _rms_case(M, N, K, False)
     ws = fl.rmsnorm_fp8_workspace(M, N, K)
     ws[:4] = torch.tensor([100, 0, 0, 0], dtype=torch.uint8)  # counters[0] = 100: never equals its target
@@ -437,6 +438,7 @@ def test_rmsnorm_fp8_wait_timeout_reports_status(M, N):
     ws.zero_()
     q, s = _rms_run(X, W, b, Z, g, workspace=ws)
     assert fl.device_status() == fl.FL_OK
+    fl.set_max_ctas(0)
     q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None, f64(Z), f64(g), 1e-6)
     assert_fp8_close(q, s, q_ref, s_ref, "after timeout")
 
@@ -840,7 +842,7 @@ def test_every_entry_point_is_deterministic_across_calls():
         "swiglu_bwd": lambda: [fl.fused_swiglu_bwd(X, Wt, G, Z)],
     }
     first = {k: [t.clone() for t in f()] for k, f in calls.items()}
-    fl.set_max_ctas(40)  # decode on the flat split-K kernel, the GEMMs on fewer CTAs
+    fl.set_max_ctas(24)  # decode on the flat split-K kernel (32 feature tiles), the GEMMs on fewer CTAs
     capped = {k: [t.clone() for t in calls[k]()] for k in ("rmsnorm_decode", "gelu", "swiglu_bwd")}
     for i, (a, c) in enumerate(zip(capped["rmsnorm_decode"], calls["rmsnorm_decode"]())):
         assert torch.equal(a, c), f"flat decode kernel: output {i} differs between two calls"
