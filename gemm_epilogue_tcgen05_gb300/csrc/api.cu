@@ -104,6 +104,11 @@ bool ensure_smem_attr(const void* kernel, int device, int smem_bytes) {
       return true;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
     return false;
+  // All of the unified L1/shared storage as shared memory, so that the carveout leaves room for a
+  // second CTA of the decode variant that runs two per SM (103 KB each).
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+      cudaSuccess)
+    return false;
   if (g_smem_attr_n < 256) g_smem_attr[g_smem_attr_n++] = SmemAttr{kernel, device, smem_bytes};
   return true;
 }

@@ -58,30 +58,39 @@ struct alignas(128) LinearDecodeParams {
 };
 
 constexpr int kLdSmallBytes = 1024;  // RoPE frequencies (128 floats), per-token maxima (32), flags
-constexpr int kLdSmemBytes = kLdStages * kLdStageBytes + kLdSmallBytes + 1024 /*bars*/ + 1024 /*align*/;
+// S stages of 20 KB: 10 with one CTA per SM, 5 with two (for more clusters than SMs hold singly)
+__host__ __device__ constexpr int ld_smem_bytes(int S) {
+  return S * kLdStageBytes + kLdSmallBytes + 1024 /*bars*/ + 1024 /*align*/;
+}
+constexpr int kLdStagesPair = 5;
+__host__ __device__ constexpr int ld_pow2_at_least(int x) { return x <= 1 ? 1 : 2 * ld_pow2_at_least((x + 1) / 2); }
 
-template <int C, int KIND>
-__global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid_constant__ LinearDecodeParams p) {
-  static_assert(C == 1 || C == 2 || C == 4 || C == 8, "cluster size");
+// C CTAs per cluster (1 to 8) split K; the tile's groups of 8 output features are shared out
+// as evenly as 8-feature groups allow (rank r finishes groups [r G / C, (r + 1) G / C)).
+template <int C, int KIND, int S>
+__global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
+    linear_decode_kernel(const __grid_constant__ LinearDecodeParams p) {
+  static_assert(C >= 1 && C <= 8, "cluster size");
+  static_assert(S == kLdStages || S == kLdStagesPair, "stages");
   constexpr bool kSwiglu = KIND == LD_SWIGLU;
   constexpr int kOut = kSwiglu ? 64 : 128;    // output features per tile
-  constexpr int kRows = kOut / C;             // output features this CTA finishes
-  constexpr int kGroups = kRows / 8;          // groups of 8 features per token
-  constexpr int kItems = 32 * kGroups;        // (token, group) items
+  constexpr int kG = kOut / 8;                // groups of 8 features per tile
+  constexpr int kGmax = (kG + C - 1) / C;     // groups per CTA, at most
+  constexpr int kP2 = ld_pow2_at_least(kGmax);  // lanes per token: a power of two for the butterflies
+  constexpr int kItems = 32 * kP2;            // (token, group slot) items
   constexpr int kIpt = (kItems + 127) / 128;  // items per epilogue thread
-  static_assert(kGroups >= 1, "at least 8 features per CTA");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_mem = smem;
   float* P = reinterpret_cast<float*>(stage_mem);  // [32 tokens][128 W rows] after the stream
-  uint8_t* small = smem + kLdStages * kLdStageBytes;
+  uint8_t* small = smem + S * kLdStageBytes;
   float* inv_freq = reinterpret_cast<float*>(small);            // QKV: [64] hi, [64] lo
   float* pmax = inv_freq + 128;                                 // FP8 K/V: [32] this CTA's per-token max
   volatile int* flags = reinterpret_cast<volatile int*>(pmax + 32);  // [0] this CTA ok
   uint64_t* bars = reinterpret_cast<uint64_t*>(small + kLdSmallBytes);
   uint64_t* full_bar = bars;
-  uint64_t* empty_bar = bars + kLdStages;
-  uint64_t* tfull_bar = bars + 2 * kLdStages;
+  uint64_t* empty_bar = bars + S;
+  uint64_t* tfull_bar = bars + 2 * S;
   uint64_t* drain_bar = tfull_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -93,12 +102,15 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
   const int f = static_cast<int>(blockIdx.x) / C;  // W-row tile of this cluster
   const int kb0 = static_cast<int>(rank) * p.num_kb / C;
   const int kb1 = (static_cast<int>(rank) + 1) * p.num_kb / C;
+  // this CTA's groups of 8 output features in the tile: [g0, g0 + ng)
+  const int g0 = static_cast<int>(rank) * kG / C;
+  const int ng = (static_cast<int>(rank) + 1) * kG / C - g0;
   // first W row of the tile (SwiGLU: of its gate half, and of its up half in W_up)
   const int wrow = f * (kSwiglu ? 64 : 128);
 
   griddep_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kLdStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -136,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();  // X, the biases and the positions may be written by the preceding kernel
 
-  // this thread's items: token t = item / kGroups, output features kRows * rank + 8 g .. + 7 of the tile
+  // this thread's items: token t = item / kP2, output features 8 (g0 + gl) .. + 7 of the tile for slot
+  // gl = item % kP2 < ng
   const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
   float bs[kIpt][8], b2s[kIpt][8];
 
@@ -161,11 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
         tma_load_2d(&p.map_x, &full_bar[stage], a_dst + kLdABytes, kb * kBK, 0);
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == kLdStages) { stage = 0; phase ^= 1u; }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
       }
       if (!ok) {
         flags[0] = 0;
-        for (int s = 0; s < kLdStages; ++s)
+        for (int s = 0; s < S; ++s)
           if (issued_mask & (1u << s)) mbar_wait_quiet(&full_bar[s], (issued_phase >> s) & 1u, p.timeout_ns);
       }
     }
@@ -185,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
         for (int k = 0; k < kBK / kUmmaK; ++k)
           mma_bf16(tmem_base, adesc + 2 * k, bdesc + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
         mma_commit(&empty_bar[stage]);
-        if (++stage == kLdStages) { stage = 0; phase ^= 1u; }
+        if (++stage == S) { stage = 0; phase ^= 1u; }
       }
       if (ok) mma_commit(tfull_bar);
       else flags[0] = 0;
@@ -197,9 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
       const int item = ti + 128 * it;
-      const int g = item % kGroups;
-      const bool in = item < kItems;
-      const int j = static_cast<int>(rank) * kRows + g * 8;  // feature within the tile
+      const int gl = item % kP2;
+      const bool in = item < kItems && gl < ng;
+      const int j = (g0 + (gl < ng ? gl : 0)) * 8;  // feature within the tile
       const int n = (kSwiglu ? f * 64 : f * 128) + j;        // W row (SwiGLU: output feature)
       const int lim = kQkv ? p.num_f * 128 : p.n_out;  // entries of the bias vectors
       const int bl = in && p.bias ? lim : 0, b2l = in && p.bias2 ? lim : 0;
@@ -253,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
       const int item = ti + 128 * it;
-      const bool has = item < kItems;  // the same across a warp: kItems is a multiple of 32
-      const int t = item / kGroups, g = item % kGroups;
-      const int j = static_cast<int>(rank) * kRows + g * 8;  // first output feature within the tile
+      const int t = item / kP2, gl = item % kP2;
+      const bool has = item < kItems && gl < ng;  // item < kItems is the same across a warp
+      const int j = (g0 + (gl < ng ? gl : 0)) * 8;  // first output feature within the tile
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[it][e] = 0.f;
       if (has && ok) {
@@ -309,13 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
         }
       }
       if (fp8) {
-        // this CTA's max |y| of token t over its features: a butterfly over the token's lanes
+        // this CTA's max |y| of token t over its features: a butterfly over the token's kP2 lanes
+        // (slots past ng hold zeros)
         float am = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(y[it][e]));
 #pragma unroll
-        for (int o = kGroups / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        if (has && g == 0) pmax[t] = am;
+        for (int o = kP2 / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (item < kItems && gl == 0) pmax[t] = am;
       }
       if (!fp8 && has && ok) {
         const int col = col_base + j;
@@ -347,9 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
 #pragma unroll
       for (int it = 0; it < kIpt; ++it) {
         const int item = ti + 128 * it;
-        if (item >= kItems) continue;
-        const int t = item / kGroups, g = item % kGroups;
-        const int j = static_cast<int>(rank) * kRows + g * 8;
+        const int t = item / kP2, gl = item % kP2;
+        if (item >= kItems || gl >= ng) continue;
+        const int j = (g0 + gl) * 8;
         float amax = 0.f;
 #pragma unroll
         for (int c = 0; c < C; ++c)
@@ -357,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_decode_kernel(const __grid
         const float qs = amax > 0.f ? 448.f / amax : 0.f;
         const int col = col_base + j;
         if (t < p.M) {
-          if (rank == 0 && g == 0)
+          if (rank == 0 && gl == 0)
             p.kv_scale[sec - 1][static_cast<size_t>(t) * p.lds + col_base / 128] = amax * (1.f / 448.f);
           if (col < width) {
             uint32_t w[2];

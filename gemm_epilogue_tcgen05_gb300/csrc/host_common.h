@@ -42,7 +42,7 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // M spans at least two 128-row blocks (default), 0 = always one CTA per tile.
 int cta_pairing_mode();
 int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU and QKV + RoPE (both forms) run the decode kernels
-// Decode-shaped (M <= 32) GELU, SwiGLU and QKV + RoPE (k_linear_decode.cu).  Returns FL_OK, an
+// Decode-shaped (M <= 32) GELU, SwiGLU and QKV + RoPE (k_linear_decode_*.cu).  Returns FL_OK, an
 // error, or kDecodeNotTaken when the call should run on the GEMM kernel instead.
 constexpr int kDecodeNotTaken = -2;
 int linear_decode_gelu(const void* X, const void* W, const void* b, void* Y, int M, int N, int K, int64_t ldx,

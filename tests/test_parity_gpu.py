@@ -206,10 +206,11 @@ def test_qkv_rope_full_workload_sampled():
 # ------------------------------------------------------------------ decode shapes (M <= 32) of GELU, SwiGLU, QKV
 @pytest.mark.parametrize("decode", [True, False])
 @pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (5, 4096, 512), (17, 8000, 320), (1, 16384, 256),
-                                   (32, 1000, 200), (9, 136, 64)])
+                                   (32, 1000, 200), (9, 136, 64), (12, 3072, 512), (32, 11000, 200)])
 def test_gelu_decode_shapes(decode, M, N, K):
-    """Swap-AB decode kernel (clusters of 8, 4, 2 and 1 CTAs across these shapes; ragged N and K)
-    and, with the decode path off, the GEMM kernel on the same small M."""
+    """Swap-AB decode kernel (clusters of 8, 4, 2, 1, 4, 1, 6 and 3 CTAs across these shapes; the 6 and
+    3 with uneven shares of the tile, the 3 with two CTAs per SM; ragged N and K) and, with the
+    decode path off, the GEMM kernel on the same small M."""
     fl.set_linear_decode(decode)
     try:
         X = _draw((M, K), syn.STREAM_X, seed=M)
@@ -225,7 +226,8 @@ def test_gelu_decode_shapes(decode, M, N, K):
 
 
 @pytest.mark.parametrize("decode", [True, False])
-@pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (9, 5000, 768), (3, 2000, 136), (32, 200, 64)])
+@pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (9, 5000, 768), (3, 2000, 136), (32, 200, 64),
+                                   (4, 3000, 256), (6, 6000, 512)])  # 47 tiles: clusters of 3; 94: 3 on 2 CTAs per SM
 def test_swiglu_decode_shapes(decode, M, N, K):
     fl.set_linear_decode(decode)
     try:
@@ -631,10 +633,12 @@ def test_qkv_fp8kv_small(pairing, H, Hkv):
 
 
 @pytest.mark.parametrize("decode", [True, False])
-@pytest.mark.parametrize("M,H,Hkv,K", [(32, 4, 2, 1024), (7, 32, 8, 512), (1, 16, 4, 256), (20, 2, 2, 200)])
+@pytest.mark.parametrize("M,H,Hkv,K", [(32, 4, 2, 1024), (7, 32, 8, 512), (1, 16, 4, 256), (20, 2, 2, 200),
+                                       (5, 16, 4, 512)])
 def test_qkv_fp8kv_decode_shapes(decode, M, H, Hkv, K):
-    """Decode shapes of the FP8 K/V form (clusters of 8, 2, 4 and 4 CTAs: the head's max spans the
-    cluster), and the GEMM kernel on the same shapes with the decode path off."""
+    """Decode shapes of the FP8 K/V form (clusters of 8, 3, 4, 4 and 6 CTAs, the 3 and 6 with uneven
+    shares of the head: its max spans the cluster), and the GEMM kernel on the same shapes with the
+    decode path off."""
     fl.set_linear_decode(decode)
     try:
         D = 128
