@@ -722,6 +722,12 @@ def single_workload(args, world, rank, local, barrier, dist):
             "roofline": {"bound": "hbm" if c.hbm_bound else "tensor", "achieved": val, "peak": pkv,
                          "unit": unit, "frac": val / pkv, "traffic": recorded_traffic(args.workload)},
             "gpu_launches": args.steps, "clocks": clk.summary()}
+    if c.hbm_bound:
+        # decode shapes: also back to back, as a decode loop issues them
+        g_ms, g_kind = time_graph_rotating(c)
+        g_ach = c.bytes / (g_ms * 1e-3) / 1e9
+        line["back_to_back"] = {"us_per_call": g_ms * 1e3, "GB/s": g_ach, "frac": g_ach / pkv,
+                                "timing": f"{g_kind} of 20 back-to-back calls over 3 rotating operand copies (> L2)"}
     if dist is not None:
         dist.destroy_process_group()
     if rank == 0:

@@ -2,13 +2,14 @@
 // GEMM and the copies out overlapped.
 //   The operation is fused_linear_gelu's ("Triton 算子融合: Linear 与 Attention", §Linear算子剖析
 //   and §GELU激活融合).  The pipeline is this library's own: X is cut into row blocks and W into
-//   blocks of output columns, uploaded in an interleaved order (X0, W0, X1, ..., X(R-1), W1, ...,
-//   W(C-1)); the GEMM of output block (r, c) starts as soon as X_r and W_c have landed, and the
-//   block goes back to the host (one 2-D copy of a strided region of the row-major array) on a
-//   second copy stream while later blocks are still uploading or computing.  The first output
-//   leaves after one row block of X and one column block of W, and from then on every column
-//   block of W unlocks R output blocks, so the copy engines in both directions and the tensor
-//   cores run at once.
+//   blocks of output columns, uploaded alternately (X0, W0, X1, W1, ..., then the rest of the
+//   longer list); the GEMM of output block (r, c) starts as soon as X_r and W_c have landed, and
+//   the block goes back to the host (one 2-D copy of a strided region of the row-major array) on
+//   a second copy stream while later blocks are still uploading or computing.  The first output
+//   leaves after one row block of X and one column block of W; alternating keeps the landed row
+//   and column blocks balanced, so each upload completes as many output blocks as it can and the
+//   copies back (more bytes than the copies in, over a link each direction of which is slower
+//   than the GEMMs) start early and do not run dry.
 #include <mutex>
 
 #include "host_common.h"
@@ -122,31 +123,43 @@ extern "C" int fused_linear_gelu_host(const void* X, const void* W, const void* 
       return false;
     return cudaEventRecord(hp.w_ready[c], hp.in) == cudaSuccess;
   };
-  // upload order: b, X0, W0, X1 .. X(R-1), W1 .. W(C-1)
-  bool ok = b == nullptr ||
-            cudaMemcpyAsync(db, b, static_cast<size_t>(N) * 2, cudaMemcpyHostToDevice, hp.in) == cudaSuccess;
-  ok = ok && up_x(0) && up_w(0);
-  for (int r = 1; r < rows && ok; ++r) ok = up_x(r);
-  for (int c = 1; c < cols && ok; ++c) ok = up_w(c);
-  if (!ok) return FL_ERR_CUDA;
-  // output blocks in the order their inputs arrive: column 0 for every row block, then column by column
-  for (int c = 0; c < cols; ++c) {
+  // output block (r, c) on the caller's stream once X_r and W_c have landed, then back to the host
+  bool x_waited[kHostMaxRow] = {}, w_waited[kHostMaxCol] = {};
+  auto emit = [&](int r, int c) -> int {
+    if (!x_waited[r] && cudaStreamWaitEvent(s, hp.x_ready[r], 0) != cudaSuccess) return FL_ERR_CUDA;
+    if (!w_waited[c] && cudaStreamWaitEvent(s, hp.w_ready[c], 0) != cudaSuccess) return FL_ERR_CUDA;
+    x_waited[r] = w_waited[c] = true;
+    const int m0 = r * mr, mrr = M - m0 < mr ? M - m0 : mr;
     const int n0 = c * nc, ncc = N - n0 < nc ? N - n0 : nc;
-    if (cudaStreamWaitEvent(s, hp.w_ready[c], 0) != cudaSuccess) return FL_ERR_CUDA;
-    for (int r = 0; r < rows; ++r) {
-      const int m0 = r * mr, mrr = M - m0 < mr ? M - m0 : mr;
-      if (c == 0 && cudaStreamWaitEvent(s, hp.x_ready[r], 0) != cudaSuccess) return FL_ERR_CUDA;
-      st = fused_linear_gelu(dX + static_cast<size_t>(m0) * K, dW + static_cast<size_t>(n0) * K,
-                             b != nullptr ? db + n0 : nullptr, dY + static_cast<size_t>(m0) * N + n0, mrr, ncc, K, K,
-                             K, N, FL_BF16, mode, s);
-      if (st != FL_OK) return st;
-      cudaEvent_t e = hp.y_ready[r * kHostMaxCol + c];
-      if (cudaEventRecord(e, s) != cudaSuccess || cudaStreamWaitEvent(hp.out, e, 0) != cudaSuccess ||
-          cudaMemcpy2DAsync(static_cast<__nv_bfloat16*>(Y) + static_cast<size_t>(m0) * N + n0,
-                            static_cast<size_t>(N) * 2, dY + static_cast<size_t>(m0) * N + n0,
-                            static_cast<size_t>(N) * 2, static_cast<size_t>(ncc) * 2, mrr, cudaMemcpyDeviceToHost,
-                            hp.out) != cudaSuccess)
-        return FL_ERR_CUDA;
+    const int rc = fused_linear_gelu(dX + static_cast<size_t>(m0) * K, dW + static_cast<size_t>(n0) * K,
+                                     b != nullptr ? db + n0 : nullptr, dY + static_cast<size_t>(m0) * N + n0, mrr, ncc,
+                                     K, K, K, N, FL_BF16, mode, s);
+    if (rc != FL_OK) return rc;
+    cudaEvent_t e = hp.y_ready[r * kHostMaxCol + c];
+    if (cudaEventRecord(e, s) != cudaSuccess || cudaStreamWaitEvent(hp.out, e, 0) != cudaSuccess ||
+        cudaMemcpy2DAsync(static_cast<__nv_bfloat16*>(Y) + static_cast<size_t>(m0) * N + n0,
+                          static_cast<size_t>(N) * 2, dY + static_cast<size_t>(m0) * N + n0,
+                          static_cast<size_t>(N) * 2, static_cast<size_t>(ncc) * 2, mrr, cudaMemcpyDeviceToHost,
+                          hp.out) != cudaSuccess)
+      return FL_ERR_CUDA;
+    return FL_OK;
+  };
+  // upload order: b, then X0, W0, X1, W1, ... and the rest of the longer list; after each upload,
+  // the output blocks it completes (every landed column block for a row block, and vice versa)
+  if (b != nullptr && cudaMemcpyAsync(db, b, static_cast<size_t>(N) * 2, cudaMemcpyHostToDevice, hp.in) != cudaSuccess)
+    return FL_ERR_CUDA;
+  int xr = 0, wc = 0;  // row and column blocks uploaded so far
+  while (xr < rows || wc < cols) {
+    if (xr < rows && (wc == cols || xr <= wc)) {
+      if (!up_x(xr)) return FL_ERR_CUDA;
+      for (int c = 0; c < wc; ++c)
+        if ((st = emit(xr, c)) != FL_OK) return st;
+      ++xr;
+    } else {
+      if (!up_w(wc)) return FL_ERR_CUDA;
+      for (int r = 0; r < xr; ++r)
+        if ((st = emit(r, wc)) != FL_OK) return st;
+      ++wc;
     }
   }
   // the caller's stream resumes once every column block is back on the host

@@ -3,6 +3,7 @@
 // Each entry point lives in its own translation unit (k_linear_decode_*.cu), so the kernel
 // variants of the kinds compile in parallel.  kDecodeNotTaken sends a call to the GEMM kernel.
 #pragma once
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -73,25 +74,34 @@ int ld_launch(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s)
   return FL_OK;
 }
 
-// One launch shape: C CTAs per tile, and one CTA per SM (10 stages) or two (5 stages each).  Of
-// the two-per-SM shapes only C = 3 ever wins the choice below outright (77 to 101 tiles on 152
-// SMs, e.g. the 96 head tiles of a 32-head QKV); the others tie with a one-per-SM shape.
+// One launch shape: C CTAs per tile, and one CTA per SM (10 stages) or two (5 stages each).  The
+// list is in the order of preference between shapes that stream equally many k blocks per CTA.
 struct LdShape {
   int C;
   bool pair;
 };
-constexpr LdShape kLdShapes[] = {{1, false}, {2, false}, {3, false}, {4, false}, {6, false}, {8, false}, {3, true}};
+constexpr LdShape kLdShapes[] = {{1, false}, {2, false}, {2, true}, {3, true},
+                                 {4, false}, {4, true},  {8, false}, {8, true}};
 
 template <int KIND>
-int ld_fit_of(const LdShape& c, const DeviceInfo& di) {
-  switch (c.C) {  // one CTA per SM
+int ld_fit_single(int C, const DeviceInfo& di) {
+  switch (C) {
     case 1: return ld_fit<1, KIND, kLdStages>(di);
     case 2: return ld_fit<2, KIND, kLdStages>(di);
-    case 3: return ld_fit<3, KIND, kLdStages>(di);
     case 4: return ld_fit<4, KIND, kLdStages>(di);
-    case 6: return ld_fit<6, KIND, kLdStages>(di);
     default: return ld_fit<8, KIND, kLdStages>(di);
   }
+}
+
+// Clusters of this shape the device holds at once.  A cluster of an even C at two CTAs per SM
+// occupies C/2 SMs, the footprint of a one-per-SM cluster of C/2 (measured: 48 clusters of 6 at two
+// per SM ran in two waves, and one-per-SM clusters of 3 fit 46).  The occupancy query itself
+// reports one block per SM for the two-per-SM kernel although the hardware runs two, so it is not
+// asked.  Clusters of 3 are bounded by their CTA count (measured: 96 clusters, 288 CTAs, at once).
+template <int KIND>
+int ld_fit_of(const LdShape& c, const DeviceInfo& di, int sms) {
+  if (!c.pair) return ld_fit_single<KIND>(c.C, di);
+  return c.C == 3 ? 2 * sms / 3 : ld_fit_single<KIND>(c.C / 2, di);
 }
 
 template <int KIND>
@@ -100,40 +110,52 @@ int ld_launch_of(const LdShape& c, const LinearDecodeParams& p, const DeviceInfo
     switch (c.C) {
       case 1: return ld_launch<1, KIND, kLdStages>(p, di, s);
       case 2: return ld_launch<2, KIND, kLdStages>(p, di, s);
-      case 3: return ld_launch<3, KIND, kLdStages>(p, di, s);
       case 4: return ld_launch<4, KIND, kLdStages>(p, di, s);
-      case 6: return ld_launch<6, KIND, kLdStages>(p, di, s);
       default: return ld_launch<8, KIND, kLdStages>(p, di, s);
     }
   }
-  return ld_launch<3, KIND, kLdStagesPair>(p, di, s);
+  switch (c.C) {
+    case 2: return ld_launch<2, KIND, kLdStagesPair>(p, di, s);
+    case 3: return ld_launch<3, KIND, kLdStagesPair>(p, di, s);
+    case 4: return ld_launch<4, KIND, kLdStagesPair>(p, di, s);
+    default: return ld_launch<8, KIND, kLdStagesPair>(p, di, s);
+  }
 }
 
-// Launch shape: every cluster resident at once, each CTA with at least one k block, and the
-// fewest W bytes on the busiest SM: ceil(tiles C / SMs) CTAs there, each streaming 1/C of a tile.
-// Ties go to one CTA per SM, then to the smaller C.  The resident-cluster count of the one-per-SM
-// shapes comes from the occupancy query; for the two-per-SM shape the query reports one block per
-// SM although the hardware runs two (measured, 20 back-to-back calls: QKV 32 x 12288 x 4096 on 288
-// CTAs 18.2 us against 23.5 us on 96), so that shape relies on its per-SM bound alone; a cluster
-// that did not fit would only wait for a later wave, as the tiles are independent.  With more tiles than SMs the stream would run
-// in two uneven waves (measured: SwiGLU 32 x 14336 x 4096, 224 tiles, 45.0 us against 42.9 us
-// on the GEMM kernel), so the GEMM kernel takes those calls.
+// k blocks a CTA streams below which a further split of the tile no longer pays: 16 blocks are
+// 256 KB of W (measured on 32 tiles of K = 4096, 20 back-to-back calls: clusters of 4 9.3-9.4 us,
+// of 8 9.6 us, of 6 9.7 us).
+constexpr int kLdMinKbPerCta = 16;
+
+// Launch shape.  When one CTA per tile already engages 3/4 of the SMs, W streams close to the HBM
+// rate and a split would add only its reduction (measured: 128 tiles of K = 4096, 21.9 us on one
+// CTA per tile, 22.4-22.9 us on clusters of 2 at two per SM).  Otherwise the per-CTA stream is the
+// limit (each CTA keeps at most its ring of stages in flight), so the shape with the fewest k blocks
+// per CTA wins, counting no fewer than kLdMinKbPerCta; ties go to the smaller C, then to one CTA per
+// SM (the order of kLdShapes).  Every cluster must be resident at once (a cluster that did not fit would run in a later wave),
+// at most one (10 stages) or two (5 stages) CTAs per SM, each CTA with at least one k block.
+// Measured (K = 4096, 20 back-to-back calls per point): 48 tiles 12.6 us on clusters of 4 at two per
+// SM against 13.4 on clusters of 3 and 14.9 on clusters of 2; 64 tiles 13.2 against 14.1 on clusters
+// of 2; 80 and 96 tiles on clusters of 3 at two per SM (15.6 and 18.7 us) against 17.0 and 20.2 on
+// clusters of 2.  With more tiles than SMs the stream would run in two uneven waves (measured:
+// SwiGLU 32 x 14336 x 4096, 224 tiles, 45.0 us against 42.9 us on the GEMM kernel), so the GEMM
+// kernel takes those calls.
 template <int KIND>
 int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
   const int cap = max_ctas_override();
   const int sms = cap > 0 && cap < di.num_sms ? cap : di.num_sms;
   if (p.num_f > sms) return kDecodeNotTaken;
+  if (4 * p.num_f >= 3 * sms) return ld_launch_of<KIND>(LdShape{1, false}, p, di, s);
   const LdShape* best = nullptr;
-  long long best_per_sm = 0;  // CTAs on the busiest SM
+  int best_kb = 0;
   for (const LdShape& c : kLdShapes) {
     const long long ctas = static_cast<long long>(p.num_f) * c.C;
-    const long long per_sm = (ctas + sms - 1) / sms;
-    if (c.C > p.num_kb || per_sm > (c.pair ? 2 : 1)) continue;
-    // per-SM load per_sm / C: compare per_sm * best.C against best_per_sm * C
-    if (best != nullptr && per_sm * best->C >= best_per_sm * c.C) continue;
-    if (!c.pair && ld_fit_of<KIND>(c, di) < p.num_f) continue;
+    if (c.C > p.num_kb || ctas > static_cast<long long>(c.pair ? 2 : 1) * sms) continue;
+    const int kb = std::max(cdiv(p.num_kb, c.C), kLdMinKbPerCta);
+    if (best != nullptr && kb >= best_kb) continue;
+    if (ld_fit_of<KIND>(c, di, sms) < p.num_f) continue;
     best = &c;
-    best_per_sm = per_sm;
+    best_kb = kb;
   }
   if (best == nullptr) return kDecodeNotTaken;
   return ld_launch_of<KIND>(*best, p, di, s);

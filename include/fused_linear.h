@@ -267,10 +267,11 @@ FL_API int fused_swiglu_bwd(const void* dO, const void* Wd, const void* G, const
 /* fused_linear_gelu (bf16) on HOST buffers: copies in, GEMM + epilogue, copies out.
  *   X [M,K], W [N,K], b [N] (nullable) and Y [M,N] are contiguous bf16 arrays in host
  *   memory (page-locked for the copies to overlap; pageable memory works, serialised).
- *   The pipeline is this library's: X and b are uploaded first, then W in blocks of
- *   whole 256-column output tiles (about N/8 columns each); each block's GEMM starts as
- *   soon as its rows of W have landed, and its columns of Y return to the host (one 2-D
- *   copy) on a second copy stream while later blocks upload and compute.
+ *   The pipeline is this library's: X is cut into about 4 blocks of whole 128-row tiles
+ *   and W into about 8 blocks of whole 256-column output tiles, uploaded alternately (b,
+ *   X0, W0, X1, W1, ..., then the rest of W); output block (r, c) is computed as soon as
+ *   X_r and W_c have landed, and returns to the host (one 2-D copy) on a second copy
+ *   stream while later blocks upload and compute.
  * dev_buf: caller-owned device memory of fl_linear_gelu_host_buffer_bytes(M, N, K)
  *   bytes, 256-byte aligned (holds X, W, b and Y on the device; no allocation per call).
  * Asynchronous with respect to the host: the call enqueues everything and returns; the

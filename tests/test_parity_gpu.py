@@ -206,11 +206,15 @@ def test_qkv_rope_full_workload_sampled():
 # ------------------------------------------------------------------ decode shapes (M <= 32) of GELU, SwiGLU, QKV
 @pytest.mark.parametrize("decode", [True, False])
 @pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (5, 4096, 512), (17, 8000, 320), (1, 16384, 256),
-                                   (32, 1000, 200), (9, 136, 64), (12, 3072, 512), (32, 11000, 200)])
+                                   (32, 1000, 200), (9, 136, 64), (32, 4096, 2048), (32, 4096, 4096),
+                                   (7, 6100, 4000), (3, 2048, 8192), (32, 3072, 8192), (32, 13312, 2048),
+                                   (17, 11200, 4096)])
 def test_gelu_decode_shapes(decode, M, N, K):
-    """Swap-AB decode kernel (clusters of 8, 4, 2, 1, 4, 1, 6 and 3 CTAs across these shapes; the 6 and
-    3 with uneven shares of the tile, the 3 with two CTAs per SM; ragged N and K) and, with the
-    decode path off, the GEMM kernel on the same small M."""
+    """Swap-AB decode kernel and, with the decode path off, the GEMM kernel on the same small M.  On
+    152 SMs the decode shapes take one CTA per tile (the first six: few k blocks, or 128 tiles),
+    clusters of 2, of 4, of 4 at two CTAs per SM (48 ragged tiles, ragged K), of 8 at two per SM
+    (16 and 24 tiles), of 2 at two per SM, and of 3 at two per SM (uneven shares of the tile, ragged
+    N)."""
     fl.set_linear_decode(decode)
     try:
         X = _draw((M, K), syn.STREAM_X, seed=M)
@@ -227,7 +231,8 @@ def test_gelu_decode_shapes(decode, M, N, K):
 
 @pytest.mark.parametrize("decode", [True, False])
 @pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (9, 5000, 768), (3, 2000, 136), (32, 200, 64),
-                                   (4, 3000, 256), (6, 6000, 512)])  # 47 tiles: clusters of 3; 94: 3 on 2 CTAs per SM
+                                   (4, 3000, 4096), (6, 6000, 4096)])  # 47 tiles: clusters of 4, 94: of 3,
+                                                                      # both at two CTAs per SM
 def test_swiglu_decode_shapes(decode, M, N, K):
     fl.set_linear_decode(decode)
     try:
@@ -245,8 +250,10 @@ def test_swiglu_decode_shapes(decode, M, N, K):
 
 
 @pytest.mark.parametrize("decode", [True, False])
-@pytest.mark.parametrize("M,H,K", [(32, 4, 1024), (7, 16, 512), (1, 32, 256), (20, 2, 200)])
+@pytest.mark.parametrize("M,H,K", [(32, 4, 1024), (7, 16, 4096), (1, 32, 4096), (20, 2, 200), (2, 4, 8192)])
 def test_qkv_rope_decode_shapes(decode, M, H, K):
+    """Head tiles on one CTA each, on clusters of 4 and of 3 at two CTAs per SM (48 and 96 tiles) and
+    on clusters of 8 (12 tiles of K = 8192); the GEMM kernel with the decode path off."""
     fl.set_linear_decode(decode)
     try:
         D = 128
@@ -633,12 +640,12 @@ def test_qkv_fp8kv_small(pairing, H, Hkv):
 
 
 @pytest.mark.parametrize("decode", [True, False])
-@pytest.mark.parametrize("M,H,Hkv,K", [(32, 4, 2, 1024), (7, 32, 8, 512), (1, 16, 4, 256), (20, 2, 2, 200),
-                                       (5, 16, 4, 512)])
+@pytest.mark.parametrize("M,H,Hkv,K", [(32, 4, 2, 1024), (7, 32, 8, 4096), (3, 64, 8, 4096), (20, 2, 2, 200),
+                                       (5, 16, 4, 2048), (2, 8, 2, 8192)])
 def test_qkv_fp8kv_decode_shapes(decode, M, H, Hkv, K):
-    """Decode shapes of the FP8 K/V form (clusters of 8, 3, 4, 4 and 6 CTAs, the 3 and 6 with uneven
-    shares of the head: its max spans the cluster), and the GEMM kernel on the same shapes with the
-    decode path off."""
+    """Decode shapes of the FP8 K/V form (one CTA per head tile; clusters of 4 and of 3 at two CTAs
+    per SM, the 3 with uneven shares of the head, so its max spans the cluster; clusters of 2 and of
+    8), and the GEMM kernel on the same shapes with the decode path off."""
     fl.set_linear_decode(decode)
     try:
         D = 128
@@ -737,10 +744,12 @@ def test_backward_full_workload_sampled(name):
 
 
 # ------------------------------------------------------------------ host-buffer pipeline
-@pytest.mark.parametrize("M,N,K,bias", [(300, 520, 200, True), (1024, 4096, 512, False), (5, 8, 8, True)])
+@pytest.mark.parametrize("M,N,K,bias", [(300, 520, 200, True), (1024, 4096, 512, False), (5, 8, 8, True),
+                                        (1024, 256, 64, False)])
 def test_linear_gelu_host_pipeline(M, N, K, bias):
-    """Host buffers in and out, column blocks overlapped: the same values as the device
-    entry point bit for bit (same kernel, same accumulation order), and the oracle."""
+    """Host buffers in and out, row and column blocks overlapped (3 x 3, 4 x 8, 1 x 1 and 4 x 1
+    blocks): the same values as the device entry point bit for bit (same kernel, same
+    accumulation order), and the oracle."""
     X = _draw((M, K), syn.STREAM_X)
     W = _draw((N, K), syn.STREAM_W, K ** -0.5)
     b = _draw((N,), syn.STREAM_B, 0.5) if bias else None
