@@ -93,15 +93,50 @@ int ld_fit_single(int C, const DeviceInfo& di) {
   }
 }
 
-// Clusters of this shape the device holds at once.  A cluster of an even C at two CTAs per SM
-// occupies C/2 SMs, the footprint of a one-per-SM cluster of C/2 (measured: 48 clusters of 6 at two
-// per SM ran in two waves, and one-per-SM clusters of 3 fit 46).  The occupancy query itself
-// reports one block per SM for the two-per-SM kernel although the hardware runs two, so it is not
-// asked.  Clusters of 3 are bounded by their CTA count (measured: 96 clusters, 288 CTAs, at once).
+// Stand-in with the block size and shared memory of the two-per-SM decode kernel; never launched.
+__global__ void __launch_bounds__(kThreads, 2) ld_pair_stand_in_kernel() {}
+
+// Clusters of C CTAs at two per SM the device holds at once (cached per device).  The occupancy
+// query reports one block per SM for the two-per-SM decode kernel itself, although the hardware runs
+// two (measured: the 288 CTAs of QKV 32 x 12288 x 4096 in one wave; Nsight's occupancy analysis
+// gives two), so it is asked about the stand-in.  Its counts match what ran on 152 SMs: 97 clusters
+// of 3 (96 ran in one wave, 100 in two) and 46 of 6 (48 ran in two waves).
+int ld_fit_pair(int C, const DeviceInfo& di) {
+  static std::mutex mu;
+  static int cache[64][9];
+  static bool known[64][9];
+  if (di.device < 0 || di.device >= 64 || C < 1 || C > 8) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!known[di.device][C]) {
+    int n = 0;
+    const void* kfn = reinterpret_cast<const void*>(&ld_pair_stand_in_kernel);
+    if (ensure_smem_attr(kfn, di.device, ld_smem_bytes(kLdStagesPair))) {
+      cudaLaunchConfig_t cfg;
+      std::memset(&cfg, 0, sizeof(cfg));
+      cudaLaunchAttribute attr[1];
+      cfg.gridDim = dim3(C * (2 * di.num_sms / C));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = ld_smem_bytes(kLdStagesPair);
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = C;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kfn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+    }
+    cache[di.device][C] = n;
+    known[di.device][C] = true;
+  }
+  return cache[di.device][C];
+}
+
 template <int KIND>
-int ld_fit_of(const LdShape& c, const DeviceInfo& di, int sms) {
-  if (!c.pair) return ld_fit_single<KIND>(c.C, di);
-  return c.C == 3 ? 2 * sms / 3 : ld_fit_single<KIND>(c.C / 2, di);
+int ld_fit_of(const LdShape& c, const DeviceInfo& di) {
+  return c.pair ? ld_fit_pair(c.C, di) : ld_fit_single<KIND>(c.C, di);
 }
 
 template <int KIND>
@@ -153,7 +188,7 @@ int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
     if (c.C > p.num_kb || ctas > static_cast<long long>(c.pair ? 2 : 1) * sms) continue;
     const int kb = std::max(cdiv(p.num_kb, c.C), kLdMinKbPerCta);
     if (best != nullptr && kb >= best_kb) continue;
-    if (ld_fit_of<KIND>(c, di, sms) < p.num_f) continue;
+    if (ld_fit_of<KIND>(c, di) < p.num_f) continue;
     best = &c;
     best_kb = kb;
   }

@@ -208,13 +208,13 @@ def test_qkv_rope_full_workload_sampled():
 @pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (5, 4096, 512), (17, 8000, 320), (1, 16384, 256),
                                    (32, 1000, 200), (9, 136, 64), (32, 4096, 2048), (32, 4096, 4096),
                                    (7, 6100, 4000), (3, 2048, 8192), (32, 3072, 8192), (32, 13312, 2048),
-                                   (17, 11200, 4096)])
+                                   (17, 11200, 4096), (5, 12800, 4096)])
 def test_gelu_decode_shapes(decode, M, N, K):
     """Swap-AB decode kernel and, with the decode path off, the GEMM kernel on the same small M.  On
     152 SMs the decode shapes take one CTA per tile (the first six: few k blocks, or 128 tiles),
     clusters of 2, of 4, of 4 at two CTAs per SM (48 ragged tiles, ragged K), of 8 at two per SM
-    (16 and 24 tiles), of 2 at two per SM, and of 3 at two per SM (uneven shares of the tile, ragged
-    N)."""
+    (16 and 24 tiles), of 2 at two per SM, of 3 at two per SM (uneven shares of the tile, ragged N),
+    and of 2 at two per SM again (100 tiles: more clusters of 3 than fit at once)."""
     fl.set_linear_decode(decode)
     try:
         X = _draw((M, K), syn.STREAM_X, seed=M)
