@@ -150,6 +150,7 @@ int ld_launch_of(const LdShape& c, const LinearDecodeParams& p, const DeviceInfo
     }
   }
   switch (c.C) {
+    case 1: return ld_launch<1, KIND, kLdStagesPair>(p, di, s);
     case 2: return ld_launch<2, KIND, kLdStagesPair>(p, di, s);
     case 3: return ld_launch<3, KIND, kLdStagesPair>(p, di, s);
     case 4: return ld_launch<4, KIND, kLdStagesPair>(p, di, s);
@@ -172,14 +173,18 @@ constexpr int kLdMinKbPerCta = 16;
 // Measured (K = 4096, 20 back-to-back calls per point): 48 tiles 12.6 us on clusters of 4 at two per
 // SM against 13.4 on clusters of 3 and 14.9 on clusters of 2; 64 tiles 13.2 against 14.1 on clusters
 // of 2; 80 and 96 tiles on clusters of 3 at two per SM (15.6 and 18.7 us) against 17.0 and 20.2 on
-// clusters of 2.  With more tiles than SMs the stream would run in two uneven waves (measured:
-// SwiGLU 32 x 14336 x 4096, 224 tiles, 45.0 us against 42.9 us on the GEMM kernel), so the GEMM
-// kernel takes those calls.
+// clusters of 2.  With more tiles than SMs, one CTA per tile at two per SM keeps every tile resident
+// at once (measured, K = 4096: SwiGLU 32 x 14336 x 4096, 224 tiles, 37.8 us against 45.3 in two
+// waves of one per SM and 45.9 on the GEMM kernel; GELU 32 x 20480 x 4096, 160 tiles, 28.3 us
+// against 42.8 and 37.2); with more tiles than that holds, the GEMM kernel takes the call.
 template <int KIND>
 int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
   const int cap = max_ctas_override();
   const int sms = cap > 0 && cap < di.num_sms ? cap : di.num_sms;
-  if (p.num_f > sms) return kDecodeNotTaken;
+  if (p.num_f > sms) {
+    if (p.num_f > 2 * sms || ld_fit_pair(1, di) < p.num_f) return kDecodeNotTaken;
+    return ld_launch_of<KIND>(LdShape{1, true}, p, di, s);
+  }
   if (4 * p.num_f >= 3 * sms) return ld_launch_of<KIND>(LdShape{1, false}, p, di, s);
   const LdShape* best = nullptr;
   int best_kb = 0;

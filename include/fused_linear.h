@@ -300,7 +300,9 @@ FL_API int fl_device_status(void* stream);
 FL_API void fl_set_wait_timeout_ns(uint64_t ns);
 
 /* Caps the number of CTAs of the persistent kernels and of the decode kernels
- * (0 = one per SM).  Used by tests to make each CTA walk many tiles, or to run the
+ * (0 = one per SM; the decode kernels of fused_linear_gelu, fused_swiglu and the QKV
+ * calls take it as the number of SMs, and their two-per-SM shapes launch up to twice
+ * as many CTAs).  Used by tests to make each CTA walk many tiles, or to run the
  * flat split-K decode kernel where the cluster one would not fit under the cap; the
  * RMSNorm workspace size depends on it, so size the workspace under the same cap.
  * Process-wide. */
@@ -316,8 +318,9 @@ FL_API void fl_set_cta_pairing(int enable);
 /* Decode-shaped calls: with 1 (the default) fused_linear_gelu (bf16), fused_swiglu,
  * fused_qkv_rope and fused_qkv_rope_fp8kv with M <= 32 rows run a swap-AB kernel that streams W once (tiles of W rows
  * on the tensor cores' M side, the tokens on N, split-K across a thread-block cluster) whenever
- * its tiles (128 output features; SwiGLU 64) fit on the SMs at once; with 0 they run on the
- * prefill GEMM kernel.  Results agree within rounding (the split-K sums in a different order).
+ * its tiles (128 output features; SwiGLU 64) fit on the SMs at once, at up to two per SM; with 0
+ * they run on the prefill GEMM kernel.  Results agree within rounding (the split-K sums in a
+ * different order).
  * Process-wide; intended for tests and diagnostics. */
 FL_API void fl_set_linear_decode(int enable);
 

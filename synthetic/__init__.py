@@ -267,6 +267,8 @@ WORKLOADS = {
     "qkv_fp8kv_decode_32x6144x4096": Workload("qkv_fp8kv_decode_32x6144x4096", "qkv_fp8kv", 32, 6144, 4096,
                                               has_bias=False, n_heads=32, n_kv_heads=8, head_dim=128,
                                               seq_len=2048),
+    "swiglu_decode_32x14336x4096": Workload("swiglu_decode_32x14336x4096", "swiglu", 32, 14336, 4096,
+                                            has_bias=False),
 }
 
 

@@ -208,13 +208,14 @@ def test_qkv_rope_full_workload_sampled():
 @pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (5, 4096, 512), (17, 8000, 320), (1, 16384, 256),
                                    (32, 1000, 200), (9, 136, 64), (32, 4096, 2048), (32, 4096, 4096),
                                    (7, 6100, 4000), (3, 2048, 8192), (32, 3072, 8192), (32, 13312, 2048),
-                                   (17, 11200, 4096), (5, 12800, 4096)])
+                                   (17, 11200, 4096), (5, 12800, 4096), (3, 20480, 512)])
 def test_gelu_decode_shapes(decode, M, N, K):
     """Swap-AB decode kernel and, with the decode path off, the GEMM kernel on the same small M.  On
     152 SMs the decode shapes take one CTA per tile (the first six: few k blocks, or 128 tiles),
     clusters of 2, of 4, of 4 at two CTAs per SM (48 ragged tiles, ragged K), of 8 at two per SM
     (16 and 24 tiles), of 2 at two per SM, of 3 at two per SM (uneven shares of the tile, ragged N),
-    and of 2 at two per SM again (100 tiles: more clusters of 3 than fit at once)."""
+    of 2 at two per SM again (100 tiles: more clusters of 3 than fit at once), and one CTA per tile at
+    two per SM (160 tiles, more than SMs)."""
     fl.set_linear_decode(decode)
     try:
         X = _draw((M, K), syn.STREAM_X, seed=M)
@@ -231,8 +232,8 @@ def test_gelu_decode_shapes(decode, M, N, K):
 
 @pytest.mark.parametrize("decode", [True, False])
 @pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (9, 5000, 768), (3, 2000, 136), (32, 200, 64),
-                                   (4, 3000, 4096), (6, 6000, 4096)])  # 47 tiles: clusters of 4, 94: of 3,
-                                                                      # both at two CTAs per SM
+                                   (4, 3000, 4096), (6, 6000, 4096), (5, 10000, 256)])
+# 47 tiles: clusters of 4, 94: of 3, both at two CTAs per SM; 157 tiles: one CTA per tile, two per SM
 def test_swiglu_decode_shapes(decode, M, N, K):
     fl.set_linear_decode(decode)
     try:
@@ -250,10 +251,12 @@ def test_swiglu_decode_shapes(decode, M, N, K):
 
 
 @pytest.mark.parametrize("decode", [True, False])
-@pytest.mark.parametrize("M,H,K", [(32, 4, 1024), (7, 16, 4096), (1, 32, 4096), (20, 2, 200), (2, 4, 8192)])
+@pytest.mark.parametrize("M,H,K", [(32, 4, 1024), (7, 16, 4096), (1, 32, 4096), (20, 2, 200), (2, 4, 8192),
+                                   (1, 64, 256)])
 def test_qkv_rope_decode_shapes(decode, M, H, K):
-    """Head tiles on one CTA each, on clusters of 4 and of 3 at two CTAs per SM (48 and 96 tiles) and
-    on clusters of 8 (12 tiles of K = 8192); the GEMM kernel with the decode path off."""
+    """Head tiles on one CTA each, on clusters of 4 and of 3 at two CTAs per SM (48 and 96 tiles), on
+    clusters of 8 (12 tiles of K = 8192) and on one CTA each at two per SM (192 tiles); the GEMM
+    kernel with the decode path off."""
     fl.set_linear_decode(decode)
     try:
         D = 128
@@ -423,6 +426,36 @@ def test_rmsnorm_fp8_decode_full_workload():
     q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(ops["X"]), f64(ops["W"]), None, f64(ops["Z"]), f64(ops["gamma"]),
                                          w.eps)
     assert_fp8_close(q, s, q_ref, s_ref, "decode full")
+
+
+@pytest.mark.parametrize("name", ["gelu_decode_32x16384x4096", "qkv_decode_32x12288x4096",
+                                  "qkv_fp8kv_decode_32x6144x4096", "swiglu_decode_32x14336x4096"])
+def test_linear_decode_full_workloads(name):
+    """The decode rows of bench.py at full size, in the launch shapes bench.py times (one CTA per
+    tile; clusters of 3 and of 4 at two per SM; one CTA per tile at two per SM for SwiGLU's 224
+    tiles), against the oracle on every output."""
+    w = syn.WORKLOADS[name]
+    ops = syn.make_operands(w)
+    d = {k: dev_bf16(v) for k, v in ops.items()}
+    if w.kind == "gelu_tanh":
+        Y = fl.fused_linear_gelu(d["X"], d["W"], d.get("b"), mode="tanh")
+        ref = oracle.linear_gelu(f64(ops["X"]), f64(ops["W"]), f64(ops["b"]) if "b" in ops else None,
+                                 oracle.GELU_TANH)
+        assert_bf16_close(host(Y), ref, name)
+    elif w.kind == "qkv_rope":
+        q, k, v = fl.fused_qkv_rope(d["X"], d["W"], None, n_heads=w.n_heads, head_dim=w.head_dim,
+                                    seq_len=w.seq_len, theta=w.theta)
+        ref = _qkv_ref(ops["X"], ops["W"], None, w.n_heads, w.head_dim, np.arange(w.M) % w.seq_len, w.theta)
+        assert_bf16_close(host(torch.cat([q, k, v], 1)), ref, name)
+    elif w.kind == "qkv_fp8kv":
+        out = fl.fused_qkv_rope_fp8kv(d["X"], d["W"], None, n_heads=w.n_heads, n_kv_heads=w.n_kv_heads,
+                                      head_dim=w.head_dim, seq_len=w.seq_len, theta=w.theta)
+        ref = oracle.qkv_rope_kv_fp8(f64(ops["X"]), f64(ops["W"]), None, w.n_heads, w.n_kv_heads, w.head_dim,
+                                     w.theta, np.arange(w.M) % w.seq_len)
+        _check_kv_fp8(out, ref, name)
+    else:
+        Y = fl.fused_swiglu(d["X"], d["Wgate"], d["Wup"], None, None)
+        assert_bf16_close(host(Y), oracle.swiglu(f64(ops["X"]), f64(ops["Wgate"]), f64(ops["Wup"]), None, None), name)
 
 
 @pytest.mark.parametrize("M,N,cap", [(256, 1024, 0), (16, 1024, 4), (16, 4096, 0)])
@@ -641,11 +674,12 @@ def test_qkv_fp8kv_small(pairing, H, Hkv):
 
 @pytest.mark.parametrize("decode", [True, False])
 @pytest.mark.parametrize("M,H,Hkv,K", [(32, 4, 2, 1024), (7, 32, 8, 4096), (3, 64, 8, 4096), (20, 2, 2, 200),
-                                       (5, 16, 4, 2048), (2, 8, 2, 8192)])
+                                       (5, 16, 4, 2048), (2, 8, 2, 8192), (2, 128, 16, 256)])
 def test_qkv_fp8kv_decode_shapes(decode, M, H, Hkv, K):
     """Decode shapes of the FP8 K/V form (one CTA per head tile; clusters of 4 and of 3 at two CTAs
     per SM, the 3 with uneven shares of the head, so its max spans the cluster; clusters of 2 and of
-    8), and the GEMM kernel on the same shapes with the decode path off."""
+    8; one CTA per tile at two per SM for 160 tiles), and the GEMM kernel on the same shapes with the
+    decode path off."""
     fl.set_linear_decode(decode)
     try:
         D = 128
