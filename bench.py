@@ -73,12 +73,39 @@ NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 7900.0
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and with whitespace runs collapsed, so that a change
+    to comments alone keeps the hash (string and character literals are kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the library's source code (comments and layout excluded): the key under which the
+    committed ncu traffic figures are looked up."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_epilogue_tcgen05_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -163,20 +163,22 @@ int ld_launch_of(const LdShape& c, const LinearDecodeParams& p, const DeviceInfo
 // of 8 9.6 us, of 6 9.7 us).
 constexpr int kLdMinKbPerCta = 16;
 
-// Launch shape.  When one CTA per tile already engages 3/4 of the SMs, W streams close to the HBM
-// rate and a split would add only its reduction (measured: 128 tiles of K = 4096, 21.9 us on one
-// CTA per tile, 22.4-22.9 us on clusters of 2 at two per SM).  Otherwise the per-CTA stream is the
-// limit (each CTA keeps at most its ring of stages in flight), so the shape with the fewest k blocks
-// per CTA wins, counting no fewer than kLdMinKbPerCta; ties go to the smaller C, then to one CTA per
-// SM (the order of kLdShapes).  Every cluster must be resident at once (a cluster that did not fit would run in a later wave),
-// at most one (10 stages) or two (5 stages) CTAs per SM, each CTA with at least one k block.
-// Measured (K = 4096, 20 back-to-back calls per point): 48 tiles 12.6 us on clusters of 4 at two per
-// SM against 13.4 on clusters of 3 and 14.9 on clusters of 2; 64 tiles 13.2 against 14.1 on clusters
-// of 2; 80 and 96 tiles on clusters of 3 at two per SM (15.6 and 18.7 us) against 17.0 and 20.2 on
-// clusters of 2.  With more tiles than SMs, one CTA per tile at two per SM keeps every tile resident
-// at once (measured, K = 4096: SwiGLU 32 x 14336 x 4096, 224 tiles, 37.8 us against 45.3 in two
-// waves of one per SM and 45.9 on the GEMM kernel; GELU 32 x 20480 x 4096, 160 tiles, 28.3 us
-// against 42.8 and 37.2); with more tiles than that holds, the GEMM kernel takes the call.
+// Launch shape.  Every cluster must be resident at once (a cluster that did not fit would run in a
+// later wave), with at most one (10 stages) or two (5 stages) CTAs per SM and at least one k block
+// per CTA.  Measured per point: 20 back-to-back calls, K = 4096.
+// - More tiles than SMs: one CTA per tile at two per SM keeps every tile resident at once (SwiGLU
+//   32 x 14336 x 4096, 224 tiles, 37.8 us against 45.3 in two waves of one per SM and 45.9 on the
+//   GEMM kernel; GELU 32 x 20480 x 4096, 160 tiles, 28.3 us against 42.8 and 37.2).  With more tiles
+//   than that holds, the GEMM kernel takes the call.
+// - One CTA per tile already engaging 3/4 of the SMs: W streams close to the HBM rate and a split
+//   would add only its reduction (128 tiles: 21.9 us on one CTA per tile and SM, 24.6 at two per SM,
+//   22.4-22.9 on clusters of 2 at two per SM).
+// - Otherwise the per-CTA stream is the limit (each CTA keeps at most its ring of stages in flight):
+//   the shape with the fewest k blocks per CTA wins, counting no fewer than kLdMinKbPerCta; ties go
+//   to the smaller C, then to one CTA per SM (the order of kLdShapes).  48 tiles: 12.6 us on clusters
+//   of 4 at two per SM against 13.4 on clusters of 3 and 14.9 on clusters of 2; 64 tiles: 13.2
+//   against 14.1 on clusters of 2; 80 and 96 tiles on clusters of 3 at two per SM (15.6 and 18.7 us)
+//   against 17.0 and 20.2 on clusters of 2.
 template <int KIND>
 int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
   const int cap = max_ctas_override();
