@@ -42,6 +42,7 @@ struct alignas(128) LinearDecodeParams {
   int n_out;           // output features: GELU N, SwiGLU d_ff, QKV d_model (the Q section)
   int kv_width;        // QKV: width of the K and V sections (= n_out for the plain QKV)
   int num_f, num_kb;   // W-row tiles, 64-wide k blocks
+  int f0;              // first tile of this launch (a call with more tiles than fit at once takes several)
   const __nv_bfloat16* bias;   // [W rows] or null (SwiGLU: b_gate [d_ff])
   const __nv_bfloat16* bias2;  // SwiGLU: b_up [d_ff] or null
   __nv_bfloat16* out[3];       // GELU, SwiGLU: out[0]; QKV: Q, K, V (FP8 K/V form: Q only)
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   const int lane = threadIdx.x & 31;
   const WaitCtx wctx{abort_flag, p.status, p.timeout_ns};
   const uint32_t rank = C > 1 ? cluster_ctarank() : 0u;
-  const int f = static_cast<int>(blockIdx.x) / C;  // W-row tile of this cluster
+  const int f = p.f0 + static_cast<int>(blockIdx.x) / C;  // W-row tile of this cluster
   const int kb0 = static_cast<int>(rank) * p.num_kb / C;
   const int kb1 = (static_cast<int>(rank) + 1) * p.num_kb / C;
   // this CTA's groups of 8 output features in the tile: [g0, g0 + ng)

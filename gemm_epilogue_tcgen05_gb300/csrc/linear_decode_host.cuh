@@ -60,13 +60,14 @@ int ld_fit(const DeviceInfo& di) {
   return cache[di.device];
 }
 
+// Launches tiles [p.f0, p.f0 + tiles) (the whole call unless it takes several launches).
 template <int C, int KIND, int S>
-int ld_launch(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
+int ld_launch(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s, int tiles) {
   const void* kfn = reinterpret_cast<const void*>(&linear_decode_kernel<C, KIND, S>);
   if (!ensure_smem_attr(kfn, di.device, ld_smem_bytes(S))) return kDecodeNotTaken;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  ld_config<C, KIND, S>(cfg, attr, p.num_f * C, s);
+  ld_config<C, KIND, S>(cfg, attr, tiles * C, s);
   if (cudaLaunchKernelEx(&cfg, linear_decode_kernel<C, KIND, S>, p) != cudaSuccess) {
     cudaGetLastError();  // a refused launch configuration: the GEMM kernel takes the call
     return kDecodeNotTaken;
@@ -140,21 +141,22 @@ int ld_fit_of(const LdShape& c, const DeviceInfo& di) {
 }
 
 template <int KIND>
-int ld_launch_of(const LdShape& c, const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
+int ld_launch_of(const LdShape& c, const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s,
+                 int tiles) {
   if (!c.pair) {
     switch (c.C) {
-      case 1: return ld_launch<1, KIND, kLdStages>(p, di, s);
-      case 2: return ld_launch<2, KIND, kLdStages>(p, di, s);
-      case 4: return ld_launch<4, KIND, kLdStages>(p, di, s);
-      default: return ld_launch<8, KIND, kLdStages>(p, di, s);
+      case 1: return ld_launch<1, KIND, kLdStages>(p, di, s, tiles);
+      case 2: return ld_launch<2, KIND, kLdStages>(p, di, s, tiles);
+      case 4: return ld_launch<4, KIND, kLdStages>(p, di, s, tiles);
+      default: return ld_launch<8, KIND, kLdStages>(p, di, s, tiles);
     }
   }
   switch (c.C) {
-    case 1: return ld_launch<1, KIND, kLdStagesPair>(p, di, s);
-    case 2: return ld_launch<2, KIND, kLdStagesPair>(p, di, s);
-    case 3: return ld_launch<3, KIND, kLdStagesPair>(p, di, s);
-    case 4: return ld_launch<4, KIND, kLdStagesPair>(p, di, s);
-    default: return ld_launch<8, KIND, kLdStagesPair>(p, di, s);
+    case 1: return ld_launch<1, KIND, kLdStagesPair>(p, di, s, tiles);
+    case 2: return ld_launch<2, KIND, kLdStagesPair>(p, di, s, tiles);
+    case 3: return ld_launch<3, KIND, kLdStagesPair>(p, di, s, tiles);
+    case 4: return ld_launch<4, KIND, kLdStagesPair>(p, di, s, tiles);
+    default: return ld_launch<8, KIND, kLdStagesPair>(p, di, s, tiles);
   }
 }
 
@@ -168,8 +170,8 @@ constexpr int kLdMinKbPerCta = 16;
 // per CTA.  Measured per point: 20 back-to-back calls, K = 4096.
 // - More tiles than SMs: one CTA per tile at two per SM keeps every tile resident at once (SwiGLU
 //   32 x 14336 x 4096, 224 tiles, 37.8 us against 45.3 in two waves of one per SM and 45.9 on the
-//   GEMM kernel; GELU 32 x 20480 x 4096, 160 tiles, 28.3 us against 42.8 and 37.2).  With more tiles
-//   than that holds, the GEMM kernel takes the call.
+//   GEMM kernel; GELU 32 x 20480 x 4096, 160 tiles, 28.3 us against 42.8 and 37.2).  More tiles
+//   than that holds run as several such launches of equal shares, back to back on the stream.
 // - One CTA per tile already engaging 3/4 of the SMs: W streams close to the HBM rate and a split
 //   would add only its reduction (128 tiles: 21.9 us on one CTA per tile and SM, 24.6 at two per SM,
 //   22.4-22.9 on clusters of 2 at two per SM).
@@ -184,10 +186,19 @@ int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
   const int cap = max_ctas_override();
   const int sms = cap > 0 && cap < di.num_sms ? cap : di.num_sms;
   if (p.num_f > sms) {
-    if (p.num_f > 2 * sms || ld_fit_pair(1, di) < p.num_f) return kDecodeNotTaken;
-    return ld_launch_of<KIND>(LdShape{1, true}, p, di, s);
+    const int per_launch = std::min(2 * sms, ld_fit_pair(1, di));  // tiles resident at once
+    if (per_launch < 1) return kDecodeNotTaken;
+    const int launches = cdiv(p.num_f, per_launch);
+    const int share = cdiv(p.num_f, launches);
+    LinearDecodeParams q = p;
+    for (q.f0 = 0; q.f0 < p.num_f; q.f0 += share) {
+      const int st = ld_launch_of<KIND>(LdShape{1, true}, q, di, s, std::min(share, p.num_f - q.f0));
+      // a refused first launch leaves the call to the GEMM kernel; a later one cannot
+      if (st != FL_OK) return q.f0 == 0 ? st : FL_ERR_CUDA;
+    }
+    return FL_OK;
   }
-  if (4 * p.num_f >= 3 * sms) return ld_launch_of<KIND>(LdShape{1, false}, p, di, s);
+  if (4 * p.num_f >= 3 * sms) return ld_launch_of<KIND>(LdShape{1, false}, p, di, s, p.num_f);
   const LdShape* best = nullptr;
   int best_kb = 0;
   for (const LdShape& c : kLdShapes) {
@@ -200,7 +211,7 @@ int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
     best_kb = kb;
   }
   if (best == nullptr) return kDecodeNotTaken;
-  return ld_launch_of<KIND>(*best, p, di, s);
+  return ld_launch_of<KIND>(*best, p, di, s, p.num_f);
 }
 
 inline bool ld_common(LinearDecodeParams& p, const void* X, int M, int K, int64_t ldx, const DeviceInfo& di) {

@@ -317,10 +317,10 @@ FL_API void fl_set_cta_pairing(int enable);
 
 /* Decode-shaped calls: with 1 (the default) fused_linear_gelu (bf16), fused_swiglu,
  * fused_qkv_rope and fused_qkv_rope_fp8kv with M <= 32 rows run a swap-AB kernel that streams W once (tiles of W rows
- * on the tensor cores' M side, the tokens on N, split-K across a thread-block cluster) whenever
- * its tiles (128 output features; SwiGLU 64) fit on the SMs at once, at up to two per SM; with 0
- * they run on the prefill GEMM kernel.  Results agree within rounding (the split-K sums in a
- * different order).
+ * on the tensor cores' M side, the tokens on N, split-K across a thread-block cluster; tiles of
+ * 128 output features, SwiGLU 64; more tiles than fit at once, at two CTAs per SM, in several
+ * launches); with 0 they run on the prefill GEMM kernel.  Results agree within rounding (the
+ * split-K sums in a different order).
  * Process-wide; intended for tests and diagnostics. */
 FL_API void fl_set_linear_decode(int enable);
 

@@ -428,6 +428,38 @@ def test_rmsnorm_fp8_decode_full_workload():
     assert_fp8_close(q, s, q_ref, s_ref, "decode full")
 
 
+@pytest.mark.parametrize("cap", [8, 0])
+def test_linear_decode_several_launches(cap):
+    """More tiles than fit at once (two CTAs per SM) run as several launches of equal shares of the
+    tiles: under a cap of 8 SMs (16 tiles per launch) and on the whole device (304 on 152 SMs).  GELU
+    40 / 320 tiles, SwiGLU 47 / 313, QKV 48 / 384 head tiles, QKV + FP8 K/V 40 / 320."""
+    fl.set_max_ctas(cap)
+    big = cap == 0
+    M, K = 3, 136
+    N = 40960 if big else 5000
+    X = _draw((M, K), syn.STREAM_X, seed=11)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=11)
+    b = _draw((N,), syn.STREAM_B, 0.3, seed=11)
+    Y = fl.fused_linear_gelu(dev_bf16(X), dev_bf16(W), dev_bf16(b), mode="tanh")
+    assert_bf16_close(host(Y), oracle.linear_gelu(f64(X), f64(W), f64(b), oracle.GELU_TANH), f"gelu launches N={N}")
+    Nsw = 20000 if big else 3000
+    Wg, Wu = _draw((Nsw, K), syn.STREAM_W, K ** -0.5, seed=12), _draw((Nsw, K), syn.STREAM_WUP, K ** -0.5, seed=12)
+    Y = fl.fused_swiglu(dev_bf16(X), dev_bf16(Wg), dev_bf16(Wu), None, None)
+    assert_bf16_close(host(Y), oracle.swiglu(f64(X), f64(Wg), f64(Wu), None, None), f"swiglu launches N={Nsw}")
+    D = 128
+    H = 128 if big else 16
+    Wq = _draw((3 * H * D, K), syn.STREAM_W, K ** -0.5, seed=13)
+    q, k, v = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, head_dim=D, seq_len=7)
+    assert_bf16_close(host(torch.cat([q, k, v], 1)), _qkv_ref(X, Wq, None, H, D, np.arange(M) % 7),
+                      f"qkv launches H={H}")
+    H, Hkv = (256, 32) if big else (32, 4)
+    Wq = _draw(((H + 2 * Hkv) * D, K), syn.STREAM_W, K ** -0.5, seed=14)
+    pos = np.array([5, 900, 77], dtype=np.int32)
+    out = fl.fused_qkv_rope_fp8kv(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, n_kv_heads=Hkv, head_dim=D,
+                                  positions=torch.from_numpy(pos).cuda())
+    _check_kv_fp8(out, oracle.qkv_rope_kv_fp8(f64(X), f64(Wq), None, H, Hkv, D, 1e4, pos), f"fp8kv launches H={H}")
+
+
 @pytest.mark.parametrize("name", ["gelu_decode_32x16384x4096", "qkv_decode_32x12288x4096",
                                   "qkv_fp8kv_decode_32x6144x4096", "swiglu_decode_32x14336x4096"])
 def test_linear_decode_full_workloads(name):
