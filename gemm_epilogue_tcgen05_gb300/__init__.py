@@ -88,6 +88,8 @@ def load() -> ctypes.CDLL:
     lib.fl_set_cta_pairing.restype = None
     lib.fl_set_linear_decode.argtypes = [I]
     lib.fl_set_linear_decode.restype = None
+    lib.fl_linear_decode_shape.argtypes = [I, I, I, I, P, P, P]
+    lib.fl_linear_decode_shape.restype = I
     lib.fl_status_string.argtypes = [I]
     lib.fl_status_string.restype = ctypes.c_char_p
     lib.fl_version.argtypes = []
@@ -510,6 +512,18 @@ def set_max_ctas(n: int) -> None:
 def set_cta_pairing(enable: bool) -> None:
     """Two-CTA (cta_group::2) prefill tiles on (default) or off; results are the same."""
     load().fl_set_cta_pairing(1 if enable else 0)
+
+
+DECODE_GELU, DECODE_SWIGLU, DECODE_QKV, DECODE_QKV_FP8KV = 0, 1, 2, 3
+
+
+def linear_decode_shape(kind: int, M: int, N: int, K: int) -> tuple[int, int, int]:
+    """(CTAs per W-row tile, CTAs per SM, launches) that a decode-shaped call would use on the current
+    device; (0, 0, 0) when it would run on the GEMM kernel.  N: the rows of W (SwiGLU: d_ff; QKV:
+    3 * d_model; QKV + FP8 K/V: (n_heads + 2 * n_kv_heads) * head_dim)."""
+    out = [ctypes.c_int(0) for _ in range(3)]
+    _check("fl_linear_decode_shape", load().fl_linear_decode_shape(kind, M, N, K, *(ctypes.byref(o) for o in out)))
+    return tuple(o.value for o in out)
 
 
 def set_linear_decode(enable: bool) -> None:

@@ -52,6 +52,15 @@ int linear_decode_swiglu(const void* X, const void* Wg, const void* Wu, const vo
 int linear_decode_qkv(const void* X, const void* Wqkv, const void* bqkv, void* const outs[3], const int32_t* positions,
                       int M, int K, int d_model, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldo,
                       const DeviceInfo& di, cudaStream_t s);
+// The decode launch plan of a call with num_f W-row tiles and num_kb k blocks (see fl_linear_decode_shape).
+void linear_decode_plan_gelu(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                             int* launches);
+void linear_decode_plan_swiglu(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                               int* launches);
+void linear_decode_plan_qkv(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                            int* launches);
+void linear_decode_plan_qkv_fp8kv(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                                  int* launches);
 int linear_decode_qkv_fp8kv(const void* X, const void* Wqkv, const void* bqkv, void* Q, void* Kq, void* Vq,
                             float* k_scale, float* v_scale, const int32_t* positions, int M, int K, int d_model,
                             int kv_width, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldq, int64_t ldkv,

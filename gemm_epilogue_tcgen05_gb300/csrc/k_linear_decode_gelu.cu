@@ -18,4 +18,9 @@ int linear_decode_gelu(const void* X, const void* W, const void* b, void* Y, int
   return mode == FL_GELU_TANH ? ld_run<LD_GELU_TANH>(p, di, s) : ld_run<LD_GELU_ERF>(p, di, s);
 }
 
+void linear_decode_plan_gelu(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                         int* launches) {
+  ld_plan_out<LD_GELU_TANH>(num_f, num_kb, di, cluster, ctas_per_sm, launches);
+}
+
 }  // namespace fl

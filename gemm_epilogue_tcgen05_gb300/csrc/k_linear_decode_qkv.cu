@@ -24,4 +24,9 @@ int linear_decode_qkv(const void* X, const void* Wqkv, const void* bqkv, void* c
   return ld_run<LD_QKV_ROPE>(p, di, s);
 }
 
+void linear_decode_plan_qkv(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                         int* launches) {
+  ld_plan_out<LD_QKV_ROPE>(num_f, num_kb, di, cluster, ctas_per_sm, launches);
+}
+
 }  // namespace fl

@@ -33,4 +33,9 @@ int linear_decode_qkv_fp8kv(const void* X, const void* Wqkv, const void* bqkv, v
   return ld_run<LD_QKV_FP8KV>(p, di, s);
 }
 
+void linear_decode_plan_qkv_fp8kv(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                         int* launches) {
+  ld_plan_out<LD_QKV_FP8KV>(num_f, num_kb, di, cluster, ctas_per_sm, launches);
+}
+
 }  // namespace fl

@@ -20,4 +20,9 @@ int linear_decode_swiglu(const void* X, const void* Wg, const void* Wu, const vo
   return ld_run<LD_SWIGLU>(p, di, s);
 }
 
+void linear_decode_plan_swiglu(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                         int* launches) {
+  ld_plan_out<LD_SWIGLU>(num_f, num_kb, di, cluster, ctas_per_sm, launches);
+}
+
 }  // namespace fl

@@ -165,6 +165,14 @@ int ld_launch_of(const LdShape& c, const LinearDecodeParams& p, const DeviceInfo
 // of 8 9.6 us, of 6 9.7 us).
 constexpr int kLdMinKbPerCta = 16;
 
+// The launches of one call: shape, and the tiles of each launch (launches = 0: the call goes to the
+// GEMM kernel).
+struct LdPlan {
+  LdShape shape;
+  int launches;
+  int share;  // tiles per launch (the last takes the rest)
+};
+
 // Launch shape.  Every cluster must be resident at once (a cluster that did not fit would run in a
 // later wave), with at most one (10 stages) or two (5 stages) CTAs per SM and at least one k block
 // per CTA.  Measured per point: 20 back-to-back calls, K = 4096.
@@ -182,36 +190,53 @@ constexpr int kLdMinKbPerCta = 16;
 //   against 14.1 on clusters of 2; 80 and 96 tiles on clusters of 3 at two per SM (15.6 and 18.7 us)
 //   against 17.0 and 20.2 on clusters of 2.
 template <int KIND>
-int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
+LdPlan ld_plan(int num_f, int num_kb, const DeviceInfo& di) {
   const int cap = max_ctas_override();
   const int sms = cap > 0 && cap < di.num_sms ? cap : di.num_sms;
-  if (p.num_f > sms) {
+  LdPlan none{{1, false}, 0, 0};
+  if (num_f < 1 || num_kb < 1) return none;
+  if (num_f > sms) {
     const int per_launch = std::min(2 * sms, ld_fit_pair(1, di));  // tiles resident at once
-    if (per_launch < 1) return kDecodeNotTaken;
-    const int launches = cdiv(p.num_f, per_launch);
-    const int share = cdiv(p.num_f, launches);
-    LinearDecodeParams q = p;
-    for (q.f0 = 0; q.f0 < p.num_f; q.f0 += share) {
-      const int st = ld_launch_of<KIND>(LdShape{1, true}, q, di, s, std::min(share, p.num_f - q.f0));
-      // a refused first launch leaves the call to the GEMM kernel; a later one cannot
-      if (st != FL_OK) return q.f0 == 0 ? st : FL_ERR_CUDA;
-    }
-    return FL_OK;
+    if (per_launch < 1) return none;
+    const int launches = cdiv(num_f, per_launch);
+    return LdPlan{{1, true}, launches, cdiv(num_f, launches)};
   }
-  if (4 * p.num_f >= 3 * sms) return ld_launch_of<KIND>(LdShape{1, false}, p, di, s, p.num_f);
+  if (4 * num_f >= 3 * sms) return LdPlan{{1, false}, 1, num_f};
   const LdShape* best = nullptr;
   int best_kb = 0;
   for (const LdShape& c : kLdShapes) {
-    const long long ctas = static_cast<long long>(p.num_f) * c.C;
-    if (c.C > p.num_kb || ctas > static_cast<long long>(c.pair ? 2 : 1) * sms) continue;
-    const int kb = std::max(cdiv(p.num_kb, c.C), kLdMinKbPerCta);
+    const long long ctas = static_cast<long long>(num_f) * c.C;
+    if (c.C > num_kb || ctas > static_cast<long long>(c.pair ? 2 : 1) * sms) continue;
+    const int kb = std::max(cdiv(num_kb, c.C), kLdMinKbPerCta);
     if (best != nullptr && kb >= best_kb) continue;
-    if (ld_fit_of<KIND>(c, di) < p.num_f) continue;
+    if (ld_fit_of<KIND>(c, di) < num_f) continue;
     best = &c;
     best_kb = kb;
   }
-  if (best == nullptr) return kDecodeNotTaken;
-  return ld_launch_of<KIND>(*best, p, di, s, p.num_f);
+  if (best == nullptr) return none;
+  return LdPlan{*best, 1, num_f};
+}
+
+template <int KIND>
+int ld_run(const LinearDecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
+  const LdPlan pl = ld_plan<KIND>(p.num_f, p.num_kb, di);
+  if (pl.launches == 0) return kDecodeNotTaken;
+  LinearDecodeParams q = p;
+  for (q.f0 = 0; q.f0 < p.num_f; q.f0 += pl.share) {
+    const int st = ld_launch_of<KIND>(pl.shape, q, di, s, std::min(pl.share, p.num_f - q.f0));
+    // a refused first launch leaves the call to the GEMM kernel; a later one cannot
+    if (st != FL_OK) return q.f0 == 0 ? st : FL_ERR_CUDA;
+  }
+  return FL_OK;
+}
+
+// The plan as the query entry point reports it.
+template <int KIND>
+void ld_plan_out(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm, int* launches) {
+  const LdPlan pl = ld_plan<KIND>(num_f, num_kb, di);
+  *cluster = pl.launches > 0 ? pl.shape.C : 0;
+  *ctas_per_sm = pl.launches > 0 ? (pl.shape.pair ? 2 : 1) : 0;
+  *launches = pl.launches;
 }
 
 inline bool ld_common(LinearDecodeParams& p, const void* X, int M, int K, int64_t ldx, const DeviceInfo& di) {

@@ -324,6 +324,18 @@ FL_API void fl_set_cta_pairing(int enable);
  * Process-wide; intended for tests and diagnostics. */
 FL_API void fl_set_linear_decode(int enable);
 
+/* The launches a decode-shaped call would make on the current device, without making them.
+ * kind: FL_DECODE_GELU (fused_linear_gelu, N output features), FL_DECODE_SWIGLU (fused_swiglu,
+ * N = d_ff), FL_DECODE_QKV (fused_qkv_rope, N = 3 * n_heads * head_dim) or FL_DECODE_QKV_FP8KV
+ * (fused_qkv_rope_fp8kv, N = (n_heads + 2 * n_kv_heads) * head_dim).  On FL_OK: *cluster = CTAs
+ * per W-row tile (0 when the call runs on the GEMM kernel instead: M outside 1..32, the decode
+ * path off, or no shape fits), *ctas_per_sm = 1 or 2 (the kernel variant with 10 or 5 stages),
+ * *launches = consecutive launches of equal tile shares (more tiles than fit at once).
+ * Takes fl_set_max_ctas and fl_set_linear_decode into account.  FL_ERR_INVALID_ARG for a null
+ * output pointer, a negative size or an unknown kind. */
+enum { FL_DECODE_GELU = 0, FL_DECODE_SWIGLU = 1, FL_DECODE_QKV = 2, FL_DECODE_QKV_FP8KV = 3 };
+FL_API int fl_linear_decode_shape(int kind, int M, int N, int K, int* cluster, int* ctas_per_sm, int* launches);
+
 /* Static text for a status code. */
 FL_API const char* fl_status_string(int status);
 

@@ -121,3 +121,19 @@ def test_host_pipeline_rejects_bad_arguments_on_host(lib):
     assert lib.fused_linear_gelu_host(a, a, None, a, 64, 256, 64, 1, a, need - 1, None) == fl.FL_ERR_WORKSPACE
     assert lib.fused_linear_gelu_host(a, a, None, a, 64, 256, 64, 1, P(0x10010), need, None) == fl.FL_ERR_ALIGNMENT
     assert lib.fused_linear_gelu_host(None, None, None, None, 0, 256, 64, 1, None, 0, None) == fl.FL_OK
+
+
+def test_decode_shape_query_on_host(lib):
+    out = [ctypes.c_int(7) for _ in range(3)]
+    refs = [ctypes.byref(o) for o in out]
+    # unknown kind, negative size, null output: rejected before the device is touched
+    assert lib.fl_linear_decode_shape(4, 8, 4096, 4096, *refs) == fl.FL_ERR_INVALID_ARG
+    assert lib.fl_linear_decode_shape(fl.DECODE_GELU, -1, 4096, 4096, *refs) == fl.FL_ERR_INVALID_ARG
+    assert lib.fl_linear_decode_shape(fl.DECODE_GELU, 8, 4096, 4096, None, refs[1], refs[2]) == fl.FL_ERR_INVALID_ARG
+    # not a decode call (M outside 1..32, or nothing to do): FL_OK and all zeros, no device needed
+    for M, N, K in ((33, 4096, 4096), (0, 4096, 4096), (8, 0, 4096), (8, 4096, 0)):
+        for o in out:
+            o.value = 7
+        assert lib.fl_linear_decode_shape(fl.DECODE_SWIGLU, M, N, K, *refs) == fl.FL_OK
+        assert [o.value for o in out] == [0, 0, 0]
+    assert fl.linear_decode_shape(fl.DECODE_QKV, 64, 12288, 4096) == (0, 0, 0)

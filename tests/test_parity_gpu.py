@@ -230,6 +230,49 @@ def test_gelu_decode_shapes(decode, M, N, K):
         fl.set_linear_decode(True)
 
 
+_DECODE_SHAPES = [  # (kind, M, N = rows of W, K) -> (CTAs per tile, CTAs per SM, launches) on 152 SMs
+    (fl.DECODE_GELU, 32, 1024, 1024, (1, 1, 1)), (fl.DECODE_GELU, 5, 4096, 512, (1, 1, 1)),
+    (fl.DECODE_GELU, 17, 8000, 320, (1, 1, 1)), (fl.DECODE_GELU, 1, 16384, 256, (1, 1, 1)),
+    (fl.DECODE_GELU, 32, 1000, 200, (1, 1, 1)), (fl.DECODE_GELU, 9, 136, 64, (1, 1, 1)),
+    (fl.DECODE_GELU, 32, 4096, 2048, (2, 1, 1)), (fl.DECODE_GELU, 32, 4096, 4096, (4, 1, 1)),
+    (fl.DECODE_GELU, 7, 6100, 4000, (4, 2, 1)), (fl.DECODE_GELU, 3, 2048, 8192, (8, 2, 1)),
+    (fl.DECODE_GELU, 32, 3072, 8192, (8, 2, 1)), (fl.DECODE_GELU, 32, 13312, 2048, (2, 2, 1)),
+    (fl.DECODE_GELU, 17, 11200, 4096, (3, 2, 1)), (fl.DECODE_GELU, 5, 12800, 4096, (2, 2, 1)),
+    (fl.DECODE_GELU, 3, 20480, 512, (1, 2, 1)), (fl.DECODE_GELU, 3, 40960, 136, (1, 2, 2)),
+    (fl.DECODE_GELU, 32, 16384, 4096, (1, 1, 1)),
+    (fl.DECODE_SWIGLU, 32, 1024, 1024, (1, 1, 1)), (fl.DECODE_SWIGLU, 9, 5000, 768, (1, 1, 1)),
+    (fl.DECODE_SWIGLU, 4, 3000, 4096, (4, 2, 1)), (fl.DECODE_SWIGLU, 6, 6000, 4096, (3, 2, 1)),
+    (fl.DECODE_SWIGLU, 5, 10000, 256, (1, 2, 1)), (fl.DECODE_SWIGLU, 3, 20000, 136, (1, 2, 2)),
+    (fl.DECODE_SWIGLU, 32, 14336, 4096, (1, 2, 1)),
+    (fl.DECODE_QKV, 32, 1536, 1024, (1, 1, 1)), (fl.DECODE_QKV, 7, 6144, 4096, (4, 2, 1)),
+    (fl.DECODE_QKV, 1, 12288, 4096, (3, 2, 1)), (fl.DECODE_QKV, 2, 1536, 8192, (8, 1, 1)),
+    (fl.DECODE_QKV, 1, 24576, 256, (1, 2, 1)), (fl.DECODE_QKV, 3, 49152, 136, (1, 2, 2)),
+    (fl.DECODE_QKV_FP8KV, 7, 6144, 4096, (4, 2, 1)), (fl.DECODE_QKV_FP8KV, 3, 10240, 4096, (3, 2, 1)),
+    (fl.DECODE_QKV_FP8KV, 5, 3072, 2048, (2, 1, 1)), (fl.DECODE_QKV_FP8KV, 2, 1536, 8192, (8, 1, 1)),
+    (fl.DECODE_QKV_FP8KV, 2, 20480, 256, (1, 2, 1)), (fl.DECODE_QKV_FP8KV, 3, 40960, 136, (1, 2, 2)),
+    (fl.DECODE_QKV, 64, 12288, 4096, (0, 0, 0)),
+]
+
+
+def test_linear_decode_launch_shapes():
+    """The launch shape of every decode case the parity tests run (and of the bench rows), as the
+    library reports it: on a 152-SM GB300 the cases cover one CTA per tile, clusters of 2, 4 and 8 at
+    one CTA per SM, of 1, 2, 3, 4 and 8 at two per SM, and several launches; under a cap of 8 SMs a
+    40-tile call takes three launches."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the expected shapes are those of a 152-SM GB300")
+    for kind, M, N, K, want in _DECODE_SHAPES:
+        assert fl.linear_decode_shape(kind, M, N, K) == want, (kind, M, N, K)
+    fl.set_max_ctas(8)
+    assert fl.linear_decode_shape(fl.DECODE_GELU, 3, 5000, 136) == (1, 2, 3)
+    fl.set_max_ctas(0)
+    fl.set_linear_decode(False)
+    try:
+        assert fl.linear_decode_shape(fl.DECODE_GELU, 32, 4096, 4096) == (0, 0, 0)
+    finally:
+        fl.set_linear_decode(True)
+
+
 @pytest.mark.parametrize("decode", [True, False])
 @pytest.mark.parametrize("M,N,K", [(32, 1024, 1024), (9, 5000, 768), (3, 2000, 136), (32, 200, 64),
                                    (4, 3000, 4096), (6, 6000, 4096), (5, 10000, 256)])
