@@ -69,6 +69,7 @@ enum { FL_GELU_ERF = 0, FL_GELU_TANH = 1 };
  * TF32 products per term, hi*hi + hi*lo + lo*hi with x = hi + lo split exactly, fp32
  * accumulate: within ~2^-21 of each product, where one TF32 product would miss fp32 accuracy).
  * mode: FL_GELU_ERF or FL_GELU_TANH.  Y must not alias X, W or b.
+ * bf16 with M <= 32 runs the decode kernel (fl_set_linear_decode, fl_linear_decode_shape).
  */
 FL_API int fused_linear_gelu(const void* X, const void* W, const void* b, void* Y,
                       int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldy,
@@ -88,6 +89,7 @@ FL_API int fused_linear_gelu(const void* X, const void* W, const void* b, void* 
  * (nullable).  positions: nullable device int32 [M]; when NULL row m has
  * position m % seq_len (rows are sequences of seq_len tokens laid end to end).
  * Positions must lie in [0, 2^24).  head_dim must be 128 and d a multiple of 256.
+ * M <= 32 runs the decode kernel, one head per W-row tile (fl_set_linear_decode).
  */
 FL_API int fused_qkv_rope(const void* X, const void* Wqkv, const void* bqkv,
                    void* Q, void* Kout, void* V, const int32_t* positions,
@@ -105,7 +107,8 @@ FL_API int fused_qkv_rope(const void* X, const void* Wqkv, const void* bqkv,
  * Kq, Vq [M, n_kv_heads*head_dim] E4M3 bytes (K rotated, V not; pitch ldkv bytes, a
  * multiple of 16); k_scale, v_scale [M, lds] fp32, one per (token, kv head).
  * Positions as in fused_qkv_rope.  head_dim must be 128 and n_heads, n_kv_heads even
- * and non-zero (FL_ERR_UNSUPPORTED otherwise). */
+ * and non-zero (FL_ERR_UNSUPPORTED otherwise).  M <= 32 runs the decode kernel, whose
+ * clusters exchange each head's per-token maximum in distributed shared memory. */
 FL_API int fused_qkv_rope_fp8kv(const void* X, const void* Wqkv, const void* bqkv, void* Q, void* Kq, void* Vq,
                                 float* k_scale, float* v_scale, const int32_t* positions, int M, int K,
                                 int n_heads, int n_kv_heads, int head_dim, int seq_len, float theta,
@@ -118,6 +121,7 @@ FL_API int fused_qkv_rope_fp8kv(const void* X, const void* Wqkv, const void* bqk
  * bgate, bup [N] bf16 (each nullable); Y [M,N] bf16.  The gate and up rows
  * that feed the same output columns are loaded side by side into one
  * shared-memory stage, so no host-side repacking of the weights is needed.
+ * M <= 32 runs the decode kernel: 64 gate and the 64 matching up rows per W-row tile.
  */
 FL_API int fused_swiglu(const void* X, const void* Wgate, const void* Wup,
                  const void* bgate, const void* bup, void* Y,
