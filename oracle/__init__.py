@@ -53,7 +53,7 @@ def _lib():
         "orc_rope_rotate": [D, D, D, P, P],
         "orc_residual_rmsnorm_linear": [P, L, P, P, P, P, L, L, D, P, P, L, P, P],
         "orc_linear_cross_entropy": [P, L, P, P, L, L, P, P],
-        "orc_linear_quant": [P, L, P, P, L, L, I, P, P, P],
+        "orc_linear_quant": [P, L, P, P, L, L, I, P, P, P, P],
         "orc_qkv_rope_kv_fp8": [P, L, P, P, L, L, L, L, D, P, P, P, P, P, P, P],
         "orc_dgrad_gelu": [P, L, P, L, L, P, I, P, L, P],
         "orc_swiglu_bwd": [P, L, P, L, L, P, P, P, L, P],
@@ -230,9 +230,12 @@ def e2m1_encode(y: float) -> int:
     return _lib().orc_e2m1_encode(float(y))
 
 
-def linear_quant(X, W, b, fmt):
-    """(codes uint8 [r, qbytes], scales [r, nblocks], y fp64 [r, N]) of the block-scaled Linear output."""
-    X, W, b = _f64(X), _f64(W), _f64(b)
+def linear_quant(X, W, b, fmt, inv_smooth=None):
+    """(codes uint8 [r, qbytes], scales [r, nblocks], y fp64 [r, N]) of the block-scaled Linear output.
+
+    inv_smooth: optional per-column factor [N] applied to the Linear output before the
+    block maxima (step 3 of the five-step quantised write-back); y is the corrected output."""
+    X, W, b, inv_smooth = _f64(X), _f64(W), _f64(b), _f64(inv_smooth)
     r, K = X.shape
     N = W.shape[0]
     bs = QUANT_BLOCK[fmt]
@@ -241,7 +244,10 @@ def linear_quant(X, W, b, fmt):
     q = np.empty((r, qbytes), dtype=np.uint8)
     sc = np.empty((r, nb), dtype=np.float64)
     y = np.empty((r, N), dtype=np.float64)
-    _lib().orc_linear_quant(_ptr(X), r, _ptr(W), _ptr(b), N, K, int(fmt), _ptr(q), _ptr(sc), _ptr(y))
+    if inv_smooth is not None and inv_smooth.shape != (N,):
+        raise ValueError("inv_smooth must have N entries")
+    _lib().orc_linear_quant(_ptr(X), r, _ptr(W), _ptr(b), N, K, int(fmt), _ptr(inv_smooth), _ptr(q), _ptr(sc),
+                            _ptr(y))
     return q, sc, y
 
 

@@ -288,6 +288,12 @@ int orc_e2m1_encode(double y) {
 }
 
 /* Linear followed by block-scaled quantisation of every row.
+ * Step 3 of [E] §仿射量化与尾声的五步 (optional scale-factor correction): when the
+ * activation leaves a SmoothQuant/QuaRot-style smoothed layer, the epilogue multiplies it
+ * by the inverse smoothing coefficient before quantising, so the codes hold what the next
+ * kernel expects.  Here that is a per-output-column factor: y[n] <- y[n] * inv_smooth[n]
+ * (NULL: no correction), applied before the block maximum of step 1, since the codes and
+ * the scale must describe the corrected values.
  * fmt 0: FP8 E4M3, blocks of 128 columns, fp32 scale = amax / 448, codes 1 byte each.
  * fmt 1: INT4 symmetric, groups of 32, fp32 scale = amax / 7, code = round-half-even(y / s)
  *        clamped to [-7, 7], two's-complement nibble; column 2j in the low nibble of byte j.
@@ -295,9 +301,9 @@ int orc_e2m1_encode(double y) {
  *        codes are divided by), values E2M1, column 2j in the low nibble of byte j.
  * Outputs: q [nrows, qbytes_per_row] (qbytes = N for fmt 0, N/2 otherwise),
  *          scale [nrows, nblocks] as fp64 (fmt 0, 1) or as E4M3 codes widened to fp64 (fmt 2),
- *          y [nrows, N] the unquantised Linear output. */
+ *          y [nrows, N] the unquantised (corrected) Linear output. */
 void orc_linear_quant(const double* X, long nrows, const double* W, const double* b, long N, long K, int fmt,
-                      uint8_t* q, double* scale, double* y) {
+                      const double* inv_smooth, uint8_t* q, double* scale, double* y) {
     const long bs = fmt == 0 ? 128 : (fmt == 1 ? 32 : 16);
     const long nblocks = (N + bs - 1) / bs;
     const long qbytes = fmt == 0 ? N : (N + 1) / 2;
@@ -306,6 +312,8 @@ void orc_linear_quant(const double* X, long nrows, const double* W, const double
         double* yi = y + (size_t)i * (size_t)N;
 #pragma omp parallel for schedule(static)
         for (long n = 0; n < N; ++n) yi[n] = linear_at(x, W, b, K, n);
+        if (inv_smooth)
+            for (long n = 0; n < N; ++n) yi[n] *= inv_smooth[n];
         uint8_t* qi = q + (size_t)i * (size_t)qbytes;
         for (long n = 0; n < qbytes; ++n) qi[n] = 0;
         for (long blk = 0; blk < nblocks; ++blk) {

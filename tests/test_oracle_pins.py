@@ -397,6 +397,78 @@ def test_quant_formats_round_trip_and_layout():
     assert not q0.any() and not s0.any()
 
 
+def test_quant_smoothing_factor_of_ones_changes_nothing():
+    """Step 3 of the five-step quantised write-back with every factor 1 is the plain
+    block-scaled output, in all three formats."""
+    rng = np.random.default_rng(21)
+    X = rng.standard_normal((2, 40))
+    W = rng.standard_normal((96, 40)) / math.sqrt(40)
+    for fmt in (oracle.QUANT_FP8_1X128, oracle.QUANT_INT4_G32, oracle.QUANT_NVFP4_G16):
+        q0, s0, y0 = oracle.linear_quant(X, W, None, fmt)
+        q1, s1, y1 = oracle.linear_quant(X, W, None, fmt, inv_smooth=np.ones(96))
+        assert np.array_equal(q0, q1) and np.array_equal(s0, s1) and np.array_equal(y0, y1)
+
+
+def test_quant_smoothing_undoes_a_per_column_weight_scale():
+    """Scaling output column n of the Linear (row n of W and b[n]) by c_n and correcting
+    with the inverse factor 1/c_n gives back the unscaled codes and scales exactly (c_n
+    powers of two, so every product is exact).  A factor that divided instead of
+    multiplying, or that was indexed by anything but the output column, fails this."""
+    rng = np.random.default_rng(22)
+    N, K = 160, 48
+    X = rng.standard_normal((3, K))
+    W = rng.standard_normal((N, K)) / math.sqrt(K)
+    b = rng.standard_normal(N) * 0.1
+    c = 2.0 ** rng.integers(-3, 4, size=N)
+    for fmt in (oracle.QUANT_FP8_1X128, oracle.QUANT_INT4_G32, oracle.QUANT_NVFP4_G16):
+        q0, s0, y0 = oracle.linear_quant(X, W, b, fmt)
+        q1, s1, y1 = oracle.linear_quant(X, W * c[:, None], b * c, fmt, inv_smooth=1.0 / c)
+        assert np.array_equal(q0, q1) and np.array_equal(s0, s1)
+        assert np.array_equal(y0, y1)
+    # a correction that is not undone moves the codes
+    q2, _, _ = oracle.linear_quant(X, W * c[:, None], b * c, oracle.QUANT_FP8_1X128)
+    assert not np.array_equal(oracle.linear_quant(X, W, b, oracle.QUANT_FP8_1X128)[0], q2)
+
+
+def test_quant_smoothing_hand_computed_nvfp4_block():
+    """One 1 x 16 NVFP4 group worked by hand.  X = [1], W[n] = n + 1, so the Linear output
+    is 1, 2, ..., 16; the inverse smoothing factor is 1/2 on even columns and 1 on odd ones,
+    so the corrected values are 0.5, 2, 1.5, 4, 2.5, 6, 3.5, 8, 4.5, 10, 5.5, 12, 6.5, 14,
+    7.5, 16.  Their maximum 16 gives 16 / 6 = 2.667, whose nearest E4M3 value is 2.75 =
+    1.375 * 2^1 (exponent field 8, mantissa 3: code 0x43).  Divided by 2.75 the values are
+    0.18, 0.73, 0.55, 1.45, 0.91, 2.18, 1.27, 2.91, 1.64, 3.64, 2.0, 4.36, 2.36, 5.09, 2.73,
+    5.82, and the nearest E2M1 values 0, 0.5, 0.5, 1.5, 1, 2, 1.5, 3, 1.5, 4, 2, 4, 2, 6, 3, 6
+    are codes 0 1 1 3 2 4 3 5 3 6 4 6 4 7 5 7, packed low nibble first."""
+    X = np.ones((1, 1))
+    W = np.arange(1.0, 17.0)[:, None]
+    inv = np.where(np.arange(16) % 2 == 0, 0.5, 1.0)
+    q, s, y = oracle.linear_quant(X, W, None, oracle.QUANT_NVFP4_G16, inv_smooth=inv)
+    assert np.array_equal(y[0], [0.5, 2, 1.5, 4, 2.5, 6, 3.5, 8, 4.5, 10, 5.5, 12, 6.5, 14, 7.5, 16])
+    assert int(s[0, 0]) == 0x43
+    assert list(q[0]) == [0x10, 0x31, 0x42, 0x53, 0x63, 0x64, 0x74, 0x75]
+    # without the correction column 0 is 1 / 2.75 = 0.36, which rounds to 0.5 (code 1)
+    q_plain, s_plain, _ = oracle.linear_quant(X, W, None, oracle.QUANT_NVFP4_G16)
+    assert int(s_plain[0, 0]) == 0x43 and q_plain[0, 0] & 15 == 1
+
+
+def test_quant_smoothing_block_maximum_maps_to_the_top_code():
+    """FP8 1x128 with a correction: the block maximum is taken after the correction, so the
+    corrected maximum codes to +-448 (0x7E / 0xFE) and the scale is that maximum / 448."""
+    rng = np.random.default_rng(23)
+    X = rng.standard_normal((4, 32))
+    W = rng.standard_normal((256, 32)) / math.sqrt(32)
+    inv = rng.uniform(0.25, 4.0, size=256)
+    q, s, y = oracle.linear_quant(X, W, None, oracle.QUANT_FP8_1X128, inv_smooth=inv)
+    ref = (X @ W.T) * inv
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-13)
+    for blk in range(2):
+        seg = ref[:, blk * 128:(blk + 1) * 128]
+        assert np.allclose(s[:, blk], np.abs(seg).max(axis=1) / 448, rtol=1e-13)
+        top = np.argmax(np.abs(seg), axis=1)
+        codes = q[np.arange(4), blk * 128 + top]
+        assert set(codes.tolist()) <= {0x7E, 0xFE}
+
+
 def test_qkv_rope_kv_fp8_against_complex_rotation_and_e4m3_bounds():
     """GQA widths (4 query heads, 2 kv heads): Q and K against RoPE as complex
     multiplication of a numpy projection, V against the projection alone; each
