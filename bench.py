@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 import synthetic as syn  # noqa: E402
 
 HEADLINE = "gelu_tanh_8192x16384x4096"
+DECODE = "rmsnorm_fp8_decode_32x4096x14336"  # the decode half of the metric (HBM GB/s)
 METRIC = "fused GEMM+epilogue TFLOP/s & % bf16 tensor peak; decode-shape HBM GB/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -195,6 +196,13 @@ def dev_bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
 
 
+def dev_operand(a):
+    """A host operand on the device: bf16 bit patterns (uint16) as bf16, fp32 as fp32."""
+    if a.dtype == np.float32:
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return dev_bf16(a)
+
+
 class Case:
     """Device operands of one workload plus the call that runs it through the C ABI."""
 
@@ -204,7 +212,7 @@ class Case:
         self.w = syn.WORKLOADS[name]
         self.name = name
         self.host = syn.make_operands(self.w)
-        self.dev = {k: dev_bf16(v) for k, v in self.host.items()}
+        self.dev = {k: dev_operand(v) for k, v in self.host.items()}
         w = self.w
         d = self.dev
         if w.kind in ("gelu_tanh", "gelu_erf"):
@@ -299,7 +307,7 @@ class Case:
             fl.fused_swiglu_bwd(d["dO"], d["Wd"], d["G"], d["U"], dGU=out, stream=stream)
         elif w.kind == "quant":
             fl.fused_linear_quant(d["X"], d["W"], d.get("b"), self.fmt, Yq=out[0], scales=out[1],
-                                  stream=stream)
+                                  inv_smooth=d.get("inv_smooth"), stream=stream)
         elif w.kind == "rms_chain":
             fl.fused_linear_residual_gamma(d["X"], d["W"], d.get("b"), d["Z"], d["gamma"], store_h1=False, H2=self.h2,
                                            rms_partials=self.part, stream=stream)
@@ -310,6 +318,13 @@ class Case:
 
     def outputs(self):
         return self.out if isinstance(self.out, tuple) else (self.out,)
+
+    def status(self, ws=None) -> int:
+        """Device-side failures of the calls so far: the workspace's record and the device-wide word."""
+        ws = getattr(self, "ws", None) if ws is None else ws
+        st = self.fl.check_device_status(ws) if ws is not None else self.fl.FL_OK
+        dev = self.fl.device_status()
+        return st if st != self.fl.FL_OK else dev
 
 
 def time_device(case: Case, steps: int, warmup: int, flush: torch.Tensor, barrier):
@@ -333,15 +348,17 @@ def time_device(case: Case, steps: int, warmup: int, flush: torch.Tensor, barrie
     wall = time.perf_counter() - t0
     barrier()
     torch.cuda.synchronize()
-    if case.fl.device_status() != case.fl.FL_OK:
+    if case.status() != case.fl.FL_OK:
         raise RuntimeError(f"{case.name}: device-side failure reported")
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
 
 
-def unfused_fn(case: Case):
-    """The same computation as separate torch / cuBLAS kernels (comparison baseline, not our path)."""
+def unfused_fn(case: Case, d=None):
+    """The same computation as separate torch / cuBLAS kernels (comparison baseline, not our path);
+    `d` replaces the case's own operands."""
     import torch.nn.functional as F
-    w, d = case.w, case.dev
+    w = case.w
+    d = case.dev if d is None else d
     if w.kind in ("gelu_tanh", "gelu_erf"):
         approx = "tanh" if w.kind == "gelu_tanh" else "none"
         return lambda: F.gelu(F.linear(d["X"], d["W"], d.get("b")), approximate=approx)
@@ -397,6 +414,8 @@ def unfused_fn(case: Case):
             return torch.stack((dy * u * s * (1 + g * (1 - s)), dy * g * s), dim=-1).reshape(w.M, -1).bfloat16()
         return swiglu_bwd
     if w.kind == "quant":
+        if "inv_smooth" in d:
+            return lambda: unfused_quant(F.linear(d["X"], d["W"], d.get("b")).float() * d["inv_smooth"], case.fmt)
         return lambda: unfused_quant(F.linear(d["X"], d["W"], d.get("b")).float(), case.fmt)
     if w.kind == "rms_chain":
         return lambda: F.linear(F.rms_norm(F.linear(d["X"], d["W"]) + d["Z"], (w.N,), weight=d["gamma"], eps=w.eps),
@@ -453,10 +472,21 @@ def time_fn(fn, steps: int, warmup: int, flush: torch.Tensor):
     return statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
 
 
-def time_graph_rotating(case: Case, calls: int = 20, copies: int = 3, replays: int = 20):
+def standin_kernel(nbytes: int = 8 << 20):
+    """A few-microsecond kernel that is not a decode call: an in-place scale of an 8 MiB bf16
+    buffer (torch's elementwise kernel, 16 MiB of traffic), standing in for the other work a
+    decode step puts between two calls of the same layer kind."""
+    buf = torch.ones(nbytes // 2, dtype=torch.bfloat16, device="cuda")
+    return lambda: buf.mul_(1.0)
+
+
+def time_graph_rotating(case: Case, calls: int = 20, copies: int = 3, replays: int = 20, mode: str = "fused",
+                        between=None):
     """Per-call time (ms) of `calls` back-to-back calls captured in one CUDA graph, cycling through
     `copies` separate copies of every operand (together larger than L2, so each call reads its
-    operands from HBM), as a decode loop would issue them."""
+    operands from HBM), as a decode loop would issue them.
+    mode "fused": the library call; "unfused": the torch/cuBLAS sequence of the same workload.
+    between: an optional callable enqueued after every call (the interleaved measurement)."""
     import gemm_epilogue_tcgen05_gb300 as fl
     w = case.w
     sets = [case.dev] + [{k: v.clone() for k, v in case.dev.items()} for _ in range(copies - 1)]
@@ -464,11 +494,17 @@ def time_graph_rotating(case: Case, calls: int = 20, copies: int = 3, replays: i
     single = not isinstance(case.out, tuple)
     wss = [getattr(case, "ws", None)] + [fl.rmsnorm_fp8_workspace(w.M, w.N, w.K) if w.kind == "rmsnorm_fp8" else None
                                          for _ in range(copies - 1)]
+    unf = [unfused_fn(case, d) for d in sets] if mode == "unfused" else None
 
     def seq(stream):
         for i in range(calls):
-            o = outs[i % copies]
-            case.run(stream, d=sets[i % copies], out=o[0] if single else o, ws=wss[i % copies])
+            if unf is not None:
+                unf[i % copies]()
+            else:
+                o = outs[i % copies]
+                case.run(stream, d=sets[i % copies], out=o[0] if single else o, ws=wss[i % copies])
+            if between is not None:
+                between()
 
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
@@ -497,9 +533,70 @@ def time_graph_rotating(case: Case, calls: int = 20, copies: int = 3, replays: i
         run()
     e.record()
     torch.cuda.synchronize()
-    if fl.device_status() != fl.FL_OK:
+    if any(case.status(ws) != fl.FL_OK for ws in wss):
         raise RuntimeError("decode graph: device-side failure reported")
     return s.elapsed_time(e) / (replays * calls), kind
+
+
+def time_graph_standin(between, calls: int = 20, replays: int = 20) -> float:
+    """Per-call time (ms) of the stand-in kernel alone, captured and replayed like the decode graphs."""
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(calls):
+            between()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            between()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(replays):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / (replays * calls)
+
+
+def host_enqueue_us(case: Case, calls: int = 200) -> dict:
+    """Host time to enqueue one decode call, through the C ABI directly (the arguments marshalled
+    once beforehand) and through the Python binding, with the tensor-map descriptor cache on and
+    off.  The calls run on the GPU meanwhile; the host never waits inside the timed loop."""
+    import ctypes
+    fl, w, d = case.fl, case.w, case.dev
+    lib = fl.load()
+    P = ctypes.c_void_p
+    q, rs = case.out
+    ws = case.ws
+    stream = torch.cuda.current_stream()
+    args = (P(d["X"].data_ptr()), P(d["W"].data_ptr()), None, P(d["Z"].data_ptr()), P(d["gamma"].data_ptr()),
+            ctypes.c_float(w.eps), P(q.data_ptr()), P(rs.data_ptr()), None, w.M, w.N, w.K, d["X"].stride(0),
+            d["W"].stride(0), d["Z"].stride(0), q.stride(0), P(ws.data_ptr()), ws.numel(), P(stream.cuda_stream))
+    out = {}
+    for cache in (True, False):
+        fl.set_descriptor_cache(cache)
+        for label, fn in (("c_abi", lambda: lib.fused_linear_residual_rmsnorm_fp8(*args)), ("python", case.run)):
+            for _ in range(20):
+                fn()
+            torch.cuda.synchronize()
+            best = float("inf")
+            for _ in range(3):
+                t0 = time.perf_counter()
+                for _ in range(calls):
+                    fn()
+                best = min(best, (time.perf_counter() - t0) / calls * 1e6)
+                torch.cuda.synchronize()
+            out[f"{label}_us_{'cached' if cache else 'uncached'}"] = best
+    fl.set_descriptor_cache(True)
+    if case.status() != fl.FL_OK:
+        raise RuntimeError("host enqueue timing: device-side failure reported")
+    out["what"] = (f"host wall time per call of {calls} back-to-back enqueues (best of 3), "
+                   "validation + tensor-map encodes (or cache hits) + launch")
+    return out
 
 
 def time_e2e(case: Case, steps: int, warmup: int, barrier):
@@ -571,7 +668,7 @@ def oracle_sample(w, rows: int, f: dict | None = None):
         oracle.qkv_rope_kv_fp8(f["X"], f["W"], f.get("b"), w.n_heads, w.n_kv_heads, w.head_dim, w.theta,
                                np.arange(rows) % w.seq_len)
     elif w.kind == "quant":
-        oracle.linear_quant(f["X"], f["W"], f.get("b"), QUANT_FMT[w.quant])
+        oracle.linear_quant(f["X"], f["W"], f.get("b"), QUANT_FMT[w.quant], inv_smooth=f.get("inv_smooth"))
     elif w.kind == "cross_entropy":
         oracle.linear_cross_entropy(f["X"], f["W"], f.get("b"), syn.make_labels(w)[:rows])
     elif w.kind == "rms_chain":
@@ -604,6 +701,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(syn.WORKLOADS),
                     help="workload timed as the step (default: the headline); used for profiling runs")
+    ap.add_argument("--no-cooperative", action="store_true",
+                    help="launch the RMSNorm prefill kernel without the cooperative attribute (same grid); "
+                         "for kernel profilers that refuse cooperative launches of clusters")
     ap.add_argument("--unfused", action="store_true",
                     help="with --workload: time the unfused torch/cuBLAS sequence of that workload instead "
                          "(comparison baseline); one extra call runs inside the NVTX range 'unfused_step'")
@@ -634,6 +734,9 @@ def main():
 
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    if args.no_cooperative:
+        import gemm_epilogue_tcgen05_gb300 as fl
+        fl.set_cooperative_launch(False)
     if args.unfused:
         return unfused_workload(args, world, rank, local, dist)
     if args.workload != HEADLINE:
@@ -667,6 +770,7 @@ def main():
     del head
 
     rows = []
+    decode = None
     if args.rows == "all":
         for name in ("qkv_rope_8192x12288x4096", "qkv_fp8kv_8192x6144x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
                      "rmsnorm_fp8_decode_32x4096x14336", "gelu_decode_32x16384x4096", "qkv_decode_32x12288x4096",
@@ -674,7 +778,8 @@ def main():
                      "rms_chain_8192x4096x4096_to_14336",
                      "lm_head_ce_8192x32768x4096", "gelu_bwd_8192x16384x4096", "swiglu_bwd_8192x14336x4096",
                      "quant_fp8_1x128_8192x16384x4096",
-                     "quant_int4_g32_8192x16384x4096", "quant_nvfp4_g16_8192x16384x4096"):
+                     "quant_int4_g32_8192x16384x4096", "quant_nvfp4_g16_8192x16384x4096",
+                     "quant_fp8_1x128_smooth_8192x16384x4096"):
             c = Case(name)
             row_steps = min(args.steps, 200)
             ts, _ = time_device(c, row_steps, args.warmup, flush, barrier)
@@ -684,15 +789,35 @@ def main():
                 ach = c.bytes / (m * 1e-3) / 1e9
                 g_ms, g_kind = time_graph_rotating(c)
                 g_ach = c.bytes / (g_ms * 1e-3) / 1e9
-                rows.append({"workload": name, "value": g_ach, "unit": "GB/s", "us_per_call": g_ms * 1e3,
-                             "timing": f"{g_kind} of 20 back-to-back calls over 3 rotating operand copies (> L2)",
-                             "single_launch": {"us": m * 1e3, "GB/s": ach, "frac": ach / pk["hbm_gbs"],
-                                               "timing": "one launch, L2 flushed before it"},
-                             "roofline": {"bound": "hbm", "achieved": g_ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                          "frac": g_ach / pk["hbm_gbs"], "traffic": recorded_traffic(name),
-                                          "frac_of_nominal": g_ach / NOMINAL_HBM_GBS,
-                                          "algorithmic_bytes": c.bytes},
-                             "unfused_torch_us": unf * 1e3, "speedup_vs_unfused": unf / m})
+                u_ms, _ = time_graph_rotating(c, mode="unfused")
+                row = {"workload": name, "value": g_ach, "unit": "GB/s", "us_per_call": g_ms * 1e3,
+                       "timing": f"{g_kind} of 20 back-to-back calls over 3 rotating operand copies (> L2)",
+                       "single_launch": {"us": m * 1e3, "GB/s": ach, "frac": ach / pk["hbm_gbs"],
+                                         "timing": "one launch, L2 flushed before it"},
+                       "roofline": {"bound": "hbm", "achieved": g_ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                    "frac": g_ach / pk["hbm_gbs"], "traffic": recorded_traffic(name),
+                                    "frac_of_nominal": g_ach / NOMINAL_HBM_GBS,
+                                    "algorithmic_bytes": c.bytes},
+                       "unfused_torch_us": u_ms * 1e3, "speedup_vs_unfused": u_ms / g_ms,
+                       "unfused_timing": "the same graph form (20 calls, 3 rotating copies)",
+                       "unfused_single_launch_us": unf * 1e3, "speedup_vs_unfused_single_launch": unf / m}
+                if name == DECODE:
+                    standin = standin_kernel()
+                    i_ms, _ = time_graph_rotating(c, between=standin)
+                    s_ms = time_graph_standin(standin)
+                    per = i_ms - s_ms
+                    i_ach = c.bytes / (per * 1e-3) / 1e9
+                    decode = {"workload": name, "GB/s": g_ach, "frac": g_ach / pk["hbm_gbs"],
+                              "us_per_call": g_ms * 1e3, "timing": row["timing"],
+                              "interleaved": {"us_per_call": per * 1e3, "GB/s": i_ach, "frac": i_ach / pk["hbm_gbs"],
+                                              "us_per_pair": i_ms * 1e3, "standin_us": s_ms * 1e3,
+                                              "timing": "graph of 20 (decode call, stand-in kernel) pairs over 3 "
+                                                        "rotating operand copies, minus a graph of 20 stand-ins; "
+                                                        "stand-in: in-place scale of an 8 MiB bf16 buffer"},
+                              "single_launch": row["single_launch"], "peak_gbs": pk["hbm_gbs"],
+                              "host_enqueue": host_enqueue_us(c)}
+                    row["interleaved"] = decode["interleaved"]
+                rows.append(row)
             else:
                 ach = c.flops / (m * 1e-3) / 1e12
                 rows.append({"workload": name, "value": ach, "unit": "TFLOP/s", "ms_per_launch": m,
@@ -714,7 +839,7 @@ def main():
         "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
         "unfused_baseline": {"ms_per_step": head_unfused, "speedup": head_unfused / ms,
                              "what": "torch F.gelu(F.linear(X, W, b), approximate='tanh'): cuBLAS GEMM + separate GELU"},
-        "rows": rows, "wall_s_timed_region": wall,
+        "decode": decode, "rows": rows, "wall_s_timed_region": wall,
         # numbers the source pages print, for context only (other hardware, other kernels)
         "pages_context": {
             "unfused_layernorm_gelu_8x4096x4096_fp16_a100_ms": 0.5,

@@ -49,7 +49,7 @@ def load() -> ctypes.CDLL:
     lib.fused_linear_gelu.argtypes = [P, P, P, P, I, I, I, I64, I64, I64, I, I, P]
     lib.fused_qkv_rope.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, I64, I64, I64, P]
     lib.fused_swiglu.argtypes = [P, P, P, P, P, P, I, I, I, I64, I64, I64, P]
-    lib.fused_linear_residual_rmsnorm_fp8.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I64, I64, I64, I64,
+    lib.fused_linear_residual_rmsnorm_fp8.argtypes = [P, P, P, P, P, F, P, P, P, I, I, I, I64, I64, I64, I64,
                                                       P, SZ, P]
     for f in (lib.fused_linear_gelu, lib.fused_qkv_rope, lib.fused_swiglu,
               lib.fused_linear_residual_rmsnorm_fp8):
@@ -70,7 +70,7 @@ def load() -> ctypes.CDLL:
     lib.fused_linear_gelu_host.restype = I
     lib.fl_linear_gelu_host_buffer_bytes.argtypes = [I, I, I]
     lib.fl_linear_gelu_host_buffer_bytes.restype = SZ
-    lib.fused_linear_quant.argtypes = [P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, P]
+    lib.fused_linear_quant.argtypes = [P, P, P, P, P, P, I, I, I, I64, I64, I64, I64, I, P]
     lib.fused_linear_quant.restype = I
     lib.fl_cross_entropy_workspace_bytes.argtypes = [I, I]
     lib.fl_cross_entropy_workspace_bytes.restype = SZ
@@ -80,6 +80,14 @@ def load() -> ctypes.CDLL:
     lib.fl_rmsnorm_fp8_workspace_bytes.restype = SZ
     lib.fl_device_status.argtypes = [P]
     lib.fl_device_status.restype = I
+    lib.fl_check_device_status.argtypes = [P, P]
+    lib.fl_check_device_status.restype = I
+    lib.fl_set_cooperative_launch.argtypes = [I]
+    lib.fl_set_cooperative_launch.restype = None
+    lib.fl_set_descriptor_cache.argtypes = [I]
+    lib.fl_set_descriptor_cache.restype = None
+    lib.fl_descriptor_cache_stats.argtypes = [P, P]
+    lib.fl_descriptor_cache_stats.restype = None
     lib.fl_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.fl_set_wait_timeout_ns.restype = None
     lib.fl_set_max_ctas.argtypes = [I]
@@ -307,8 +315,11 @@ def rmsnorm_fp8_workspace(M: int, N: int, K: int, device=None) -> torch.Tensor:
 
 
 def fused_linear_residual_rmsnorm_fp8(X, W, b, Z, gamma, eps: float = 1e-6, Yq=None, row_scale=None,
-                                      workspace=None, stream=None):
-    """Returns (Yq, row_scale): E4M3 codes as uint8 [M, N] and fp32 scales [M]."""
+                                      workspace=None, h_out=None, stream=None):
+    """Returns (Yq, row_scale): E4M3 codes as uint8 [M, N] and fp32 scales [M].
+
+    h_out: None (default), True (allocate one) or a bf16 [M, N] tensor with Z's row pitch;
+    when given, h = X W^T + b + Z is written there too and (Yq, row_scale, h_out) is returned."""
     M, K = X.shape
     N = W.shape[0]
     _mat(X, "X", torch.bfloat16)
@@ -324,14 +335,21 @@ def fused_linear_residual_rmsnorm_fp8(X, W, b, Z, gamma, eps: float = 1e-6, Yq=N
     if row_scale is None:
         row_scale = torch.empty(M, dtype=torch.float32, device=X.device)
     _vec(row_scale, "row_scale", torch.float32, M)
+    want_h = h_out is not None
+    if h_out is True:
+        h_out = torch.empty_strided((M, N), (_ld(Z, N, N), 1), dtype=torch.bfloat16, device=X.device)
+    if want_h:
+        _mat(h_out, "h_out", torch.bfloat16)
+        if tuple(h_out.shape) != (M, N) or (M > 1 and h_out.stride(0) != Z.stride(0)):
+            raise ValueError("h_out must be [M, N] with Z's row pitch")
     if workspace is None:
         workspace = rmsnorm_fp8_workspace(M, N, K, X.device)
     st = load().fused_linear_residual_rmsnorm_fp8(
-        _ptr(X), _ptr(W), _ptr(b), _ptr(Z), _ptr(gamma), float(eps), _ptr(Yq), _ptr(row_scale), M, N, K,
-        _ld(X, K, K), _ld(W, K, K), _ld(Z, N, N), _ld(Yq, N, N), _ptr(workspace), workspace.numel(),
-        _stream(stream))
+        _ptr(X), _ptr(W), _ptr(b), _ptr(Z), _ptr(gamma), float(eps), _ptr(Yq), _ptr(row_scale),
+        _ptr(h_out) if want_h else None, M, N, K, _ld(X, K, K), _ld(W, K, K), _ld(Z, N, N), _ld(Yq, N, N),
+        _ptr(workspace), workspace.numel(), _stream(stream))
     _check("fused_linear_residual_rmsnorm_fp8", st)
-    return Yq, row_scale
+    return (Yq, row_scale, h_out) if want_h else (Yq, row_scale)
 
 
 def rms_partials_per_row(n_norm: int) -> int:
@@ -421,9 +439,12 @@ QUANT_FP8_1X128, QUANT_INT4_G32, QUANT_NVFP4_G16 = 0, 1, 2
 QUANT_BLOCK = {QUANT_FP8_1X128: 128, QUANT_INT4_G32: 32, QUANT_NVFP4_G16: 16}
 
 
-def fused_linear_quant(X, W, b=None, fmt: int = QUANT_FP8_1X128, Yq=None, scales=None, stream=None):
+def fused_linear_quant(X, W, b=None, fmt: int = QUANT_FP8_1X128, Yq=None, scales=None, inv_smooth=None,
+                       stream=None):
     """Block-scaled quantised Linear output; returns (codes uint8, scales).
 
+    inv_smooth: optional fp32 [N] inverse smoothing factor, multiplied into each output
+    column before the block maxima (the optional correction step of the quantised write-back).
     FP8 1x128: codes [M, N] E4M3, scales fp32 [M, ceil(N/128)].
     INT4 g32:  codes [M, N/2] (column 2j in the low nibble of byte j), scales fp32 [M, ceil(N/32)].
     NVFP4 g16: codes [M, N/2] E2M1 pairs, scales E4M3 bytes (uint8) [M, ceil(N/16)].
@@ -435,6 +456,7 @@ def fused_linear_quant(X, W, b=None, fmt: int = QUANT_FP8_1X128, Yq=None, scales
     _mat(X, "X", torch.bfloat16)
     _mat(W, "W", torch.bfloat16)
     _vec(b, "b", torch.bfloat16, N)
+    _vec(inv_smooth, "inv_smooth", torch.float32, N)
     qbytes = N if fmt == QUANT_FP8_1X128 else N // 2
     nblocks = -(-N // QUANT_BLOCK[fmt])
     sdt = torch.uint8 if fmt == QUANT_NVFP4_G16 else torch.float32
@@ -444,7 +466,8 @@ def fused_linear_quant(X, W, b=None, fmt: int = QUANT_FP8_1X128, Yq=None, scales
         scales = torch.empty((M, nblocks), dtype=sdt, device=X.device)
     _mat(Yq, "Yq", torch.uint8)
     _mat(scales, "scales", sdt)
-    st = load().fused_linear_quant(_ptr(X), _ptr(W), _ptr(b), _ptr(Yq), _ptr(scales), M, N, K, _ld(X, K, K),
+    st = load().fused_linear_quant(_ptr(X), _ptr(W), _ptr(b), _ptr(inv_smooth), _ptr(Yq), _ptr(scales), M, N, K,
+                                   _ld(X, K, K),
                                    _ld(W, K, K), _ld(Yq, qbytes, qbytes), _ld(scales, nblocks, nblocks), int(fmt),
                                    _stream(stream))
     _check("fused_linear_quant", st)
@@ -497,8 +520,32 @@ def fused_swiglu_bwd(dO, Wd, G, U, dGU=None, stream=None):
 
 
 def device_status(stream=None) -> int:
-    """Synchronises the stream; returns (and clears) the device-side failure code."""
+    """Synchronises the stream; returns (and clears) the device-wide failure code."""
     return load().fl_device_status(_stream(stream))
+
+
+def check_device_status(workspace=None, stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the failure code recorded in `workspace`
+    (a workspace of the RMSNorm + FP8 or cross-entropy calls); None: the device-wide word."""
+    return load().fl_check_device_status(_ptr(workspace), _stream(stream))
+
+
+def set_cooperative_launch(enable: bool) -> None:
+    """Cooperative attribute on the RMSNorm prefill launch (default on); off only for profilers
+    that refuse cooperative launches of clusters."""
+    load().fl_set_cooperative_launch(1 if enable else 0)
+
+
+def set_descriptor_cache(enable: bool) -> None:
+    """Tensor-map descriptor cache on (default) or off (and emptied)."""
+    load().fl_set_descriptor_cache(1 if enable else 0)
+
+
+def descriptor_cache_stats() -> tuple[int, int]:
+    """(hits, misses) of the tensor-map descriptor cache since the process started."""
+    h, m = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    load().fl_descriptor_cache_stats(ctypes.byref(h), ctypes.byref(m))
+    return h.value, m.value
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -1,9 +1,9 @@
 // Library-wide host state: device query cache, the per-device status word,
-// wait limits, tensor-map encoding and the small exported utility calls.
+// wait limits, tensor-map encoding (with its descriptor cache) and the small
+// exported utility calls.
 #include <cudaTypedefs.h>
 
 #include <atomic>
-#include <cstdlib>
 #include <mutex>
 
 #include "host_common.h"
@@ -25,6 +25,7 @@ std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_max_ctas{0};
 std::atomic<int> g_pairing{1};
 std::atomic<int> g_linear_decode{1};
+std::atomic<int> g_cooperative{1};
 
 struct SmemAttr {
   const void* fn;
@@ -89,13 +90,7 @@ int max_ctas_override() { return g_max_ctas.load(); }
 int cta_pairing_mode() { return g_pairing.load(); }
 int linear_decode_mode() { return g_linear_decode.load(); }
 
-bool launch_tool_attached() {
-  // Nsight tools announce their injection through these variables in the target process.
-  static const bool attached = std::getenv("CUDA_INJECTION64_PATH") != nullptr ||
-                               std::getenv("NV_NSIGHT_INJECTION_TRANSPORT_TYPE") != nullptr ||
-                               std::getenv("NV_TPS_LAUNCH_TOKEN") != nullptr;
-  return attached;
-}
+int cooperative_launch_mode() { return g_cooperative.load(); }
 
 bool ensure_smem_attr(const void* kernel, int device, int smem_bytes) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -113,18 +108,72 @@ bool ensure_smem_attr(const void* kernel, int device, int smem_bytes) {
   return true;
 }
 
-bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
-               uint64_t outer, uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+namespace {
+// Descriptor cache.  A tensor map is a pure function of its arguments (address, extents, pitch,
+// box, element type, swizzle): it holds no device state, so an entry stays valid for as long as
+// its key is unchanged, even across frees and reallocations, and any change of pointer or shape
+// is a different key.  Decode-shaped calls re-encode the same few maps on every call; the cache
+// takes that work off the enqueue path.  Fixed size, round-robin replacement, one mutex.
+struct MapKey {
+  const void* base;
+  uint64_t inner, outer, ld_elems;
+  uint32_t box_inner, box_outer;
+  int dt, elem_bytes, sw;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && ld_elems == o.ld_elems &&
+           box_inner == o.box_inner && box_outer == o.box_outer && dt == o.dt && elem_bytes == o.elem_bytes &&
+           sw == o.sw;
+  }
+};
+constexpr int kMapCacheSize = 128;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCacheSize];
+CUtensorMap g_map_val[kMapCacheSize];
+int g_map_n = 0, g_map_next = 0;
+std::atomic<int> g_map_cache_on{1};
+std::atomic<unsigned long long> g_map_hits{0}, g_map_misses{0};
+
+bool encode_uncached(CUtensorMap* map, const MapKey& k) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld_elems * static_cast<uint64_t>(elem_bytes)};
-  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint64_t dims[2] = {k.inner, k.outer};
+  cuuint64_t strides[1] = {k.ld_elems * static_cast<uint64_t>(k.elem_bytes)};
+  cuuint32_t box[2] = {k.box_inner, k.box_outer};
   cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, static_cast<CUtensorMapDataType>(k.dt), 2, const_cast<void*>(k.base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(k.sw),
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  const MapKey k{base, inner, outer, ld_elems, box_inner, box_outer, static_cast<int>(dt), elem_bytes,
+                 static_cast<int>(sw)};
+  if (g_map_cache_on.load() == 0) return encode_uncached(map, k);
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < g_map_n; ++i)
+      if (g_map_key[i] == k) {
+        *map = g_map_val[i];
+        g_map_hits.fetch_add(1);
+        return true;
+      }
+  }
+  if (!encode_uncached(map, k)) return false;  // failures are not cached
+  g_map_misses.fetch_add(1);
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  int slot;
+  if (g_map_n < kMapCacheSize) {
+    slot = g_map_n++;
+  } else {
+    slot = g_map_next;
+    g_map_next = (g_map_next + 1) % kMapCacheSize;
+  }
+  g_map_key[slot] = k;
+  g_map_val[slot] = *map;
+  return true;
 }
 
 }  // namespace fl
@@ -144,6 +193,34 @@ int fl_device_status(void* stream) {
   if (words[ST_CODE] == 0) return FL_OK;
   if (cudaMemset(dptr, 0, sizeof(words)) != cudaSuccess) return FL_ERR_CUDA;
   return words[ST_CODE];
+}
+
+int fl_check_device_status(void* workspace, void* stream) {
+  using namespace fl;
+  if (workspace == nullptr) return fl_device_status(stream);
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kWsStatusBytes - 1)) != 0) return FL_ERR_ALIGNMENT;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FL_ERR_CUDA;
+  int words[ST_WORDS];
+  if (cudaMemcpy(words, workspace, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return FL_ERR_CUDA;
+  if (words[ST_CODE] == 0) return FL_OK;
+  if (cudaMemset(workspace, 0, sizeof(words)) != cudaSuccess) return FL_ERR_CUDA;
+  return words[ST_CODE];
+}
+
+void fl_set_cooperative_launch(int enable) { fl::g_cooperative.store(enable != 0 ? 1 : 0); }
+
+void fl_set_descriptor_cache(int enable) {
+  fl::g_map_cache_on.store(enable != 0 ? 1 : 0);
+  if (enable == 0) {
+    std::lock_guard<std::mutex> lk(fl::g_map_mu);
+    fl::g_map_n = 0;
+    fl::g_map_next = 0;
+  }
+}
+
+void fl_descriptor_cache_stats(unsigned long long* hits, unsigned long long* misses) {
+  if (hits != nullptr) *hits = fl::g_map_hits.load();
+  if (misses != nullptr) *misses = fl::g_map_misses.load();
 }
 
 void fl_set_wait_timeout_ns(uint64_t ns) { fl::g_timeout_ns.store(ns == 0 ? fl::kDefaultTimeoutNs : ns); }
@@ -187,6 +264,6 @@ const char* fl_status_string(int status) {
   }
 }
 
-int fl_version(void) { return 100; }
+int fl_version(void) { return 200; }
 
 }  // extern "C"

@@ -258,6 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
           ss += hv[e] * hv[e];
           am = fmaxf(am, fabsf(hv[e] * gs[it][e]));
         }
+        if (p.hout != nullptr && t < p.M) {  // h leaves in bf16 as well (the residual stream after the add)
+          __nv_bfloat16* hrow = p.hout + static_cast<size_t>(t) * p.ldh;
+          store_h4(hrow, f * 128 + row, p.N, make_float4(hv[0], hv[1], hv[2], hv[3]));
+          store_h4(hrow, f * 128 + row + 4, p.N, make_float4(hv[4], hv[5], hv[6], hv[7]));
+        }
         // h to the leader's H[t][row ..]
         const uint32_t hl = smem_u32(H + t * 128 + row);
         if constexpr (C > 1) {

@@ -55,6 +55,8 @@ struct alignas(128) DecodeParams {
   uint8_t* yq;
   long long ldq;
   float* row_scale;
+  __nv_bfloat16* hout;  // nullable [M][ldh]: h = X W^T + b + z in bf16 (the residual stream after the add)
+  long long ldh;
   float* partials;    // [grid][seg_max][128 features][32 tokens]
   float* hbuf;        // [num_f][32 tokens][128 features]
   float2* stats;      // [num_f][32 tokens]
@@ -74,7 +76,19 @@ __host__ __device__ inline int dec_cta_of(int u, int units, int grid) {
                           static_cast<unsigned>(units));
 }
 
-// Four bf16 values [n, n+4) of a vector as fp32 (8-byte load when fully in range); zeros at or past `limit`.
+// h[n .. n+3] of one token's row as bf16 (one 8-byte store when all four lie below `limit`;
+// the row is 16-byte aligned and n a multiple of 4).
+__device__ __forceinline__ void store_h4(__nv_bfloat16* row, int n, int limit, const float4& h) {
+  if (n + 4 <= limit) {
+    *reinterpret_cast<uint2*>(row + n) = make_uint2(pack_bf16x2(h.x, h.y), pack_bf16x2(h.z, h.w));
+  } else {
+    const float e[4] = {h.x, h.y, h.z, h.w};
+    for (int j = 0; j < 4 && n + j < limit; ++j) row[n + j] = __float2bfloat16_rn(e[j]);
+  }
+}
+
+// Bounded spin until *ctr == need.  Gives up when `status` already holds a failure (the count can
+// then never complete) or after timeout_ns, recording the failure in status_w.
 __device__ __forceinline__ bool spin_until(const unsigned* ctr, unsigned need, const int* status,
                                            unsigned long long timeout_ns, int* status_w, int where, int detail) {
   const uint64_t t0 = global_timer_ns();
@@ -415,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
           am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
         }
         if (lane == 0) __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + t, make_float2(ss, am));
+        if (p.hout != nullptr && t < p.M) store_h4(p.hout + static_cast<size_t>(t) * p.ldh, f * 128 + fq * 4, p.N, hv);
       }
       named_bar_sync(1, kEpiThreads);
       if (leader) p.counters[f] = 0u;  // every contributor has arrived; ready for the next call

@@ -70,7 +70,8 @@ struct alignas(128) GemmParams {
   float* row_scale;
   float2* partials;        // [num_m_blocks][num_n_blocks][128] (sum h^2, max |h*gamma|)
   float* rms_partials;     // [ceil(n/256)][M] per-row partial sums of squares (GEMM -> RMSNorm -> GEMM chain)
-  int n_partials, n_norm, store_h1;
+  int n_partials, n_norm;
+  int store_h1;            // RESID_GAMMA and RMSNORM_FP8: also store h (bf16) through map_out[1]
   // LM-head cross-entropy
   const int* labels;       // [M]; negative = ignored row
   float* loss;             // [M]
@@ -81,6 +82,7 @@ struct alignas(128) GemmParams {
   int quant_fmt;
   void* qscale;            // fp32 [M][lds] (FP8, INT4) or E4M3 bytes [M][lds] (NVFP4)
   long long lds;
+  const float* smooth;     // nullable fp32 [N]: inverse smoothing factor per output column
   // QKV with an FP8 K/V cache: K/V section width (n_kv_heads * head_dim) and their scales [M][lds]
   int kv_width;
   float* kscale;
@@ -152,6 +154,22 @@ __device__ __forceinline__ void load_vec32(const __nv_bfloat16* ptr, int col0, i
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = (col0 + j < n_limit) ? __bfloat162float(ptr[col0 + j]) : 0.f;
+  }
+}
+
+// 32 fp32 values [col0, col0+32) of a vector (the inverse smoothing factors); zeros past n_limit.
+// `ptr` is 16-byte aligned and col0 a multiple of 32.
+__device__ __forceinline__ void load_f32x32(const float* ptr, int col0, int n_limit, float (&v)[32]) {
+  if (col0 + 32 <= n_limit) {
+    const float4* q = reinterpret_cast<const float4*>(ptr + col0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 w = __ldg(q + i);
+      v[4 * i + 0] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = (col0 + j < n_limit) ? __ldg(ptr + col0 + j) : 0.f;
   }
 }
 
@@ -1076,6 +1094,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
         // of one thread, so no cross-thread reduction is needed.
         if (!ok) break;
         const int n0 = nb * 256;
+        // Step 3 (optional scale-factor correction): the output of a smoothed layer is multiplied
+        // per column by the inverse smoothing factor before the block maximum and the rounding.
+        const bool has_sm = p.smooth != nullptr;
         if (p.quant_fmt == QF_FP8_1X128) {
 #pragma unroll 1
           for (int blk = 0; blk < 2; ++blk) {
@@ -1086,7 +1107,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
               tmem_load32f(tacc + blk * 128 + u * 32, k_empty, v);
               load_vec32(p.bias, n0 + blk * 128 + u * 32, p.N, b);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j] + b[j]));
+              for (int j = 0; j < 32; ++j) v[j] += b[j];
+              if (has_sm) {
+                load_f32x32(p.smooth, n0 + blk * 128 + u * 32, p.N, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= b[j];
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
             }
             const float qs = amax > 0.f ? 448.f / amax : 0.f;
             if (row_ok && n0 + blk * 128 < p.N)
@@ -1098,7 +1126,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
               tmem_load32f(tacc + blk * 128 + u * 32, k_empty, v);
               load_vec32(p.bias, n0 + blk * 128 + u * 32, p.N, b);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = (v[j] + b[j]) * qs;
+              for (int j = 0; j < 32; ++j) v[j] += b[j];
+              if (has_sm) {
+                load_f32x32(p.smooth, n0 + blk * 128 + u * 32, p.N, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= b[j];
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] *= qs;
               stage_fp8_32(buf, lane, u, v);
             }
             ring.commit(&p.map_out[0], buf, lane, n0 + blk * 128, y_box);
@@ -1115,6 +1150,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             load_vec32(p.bias, col0, p.N, b);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] += b[j];
+            if (has_sm) {
+              load_f32x32(p.smooth, col0, p.N, b);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] *= b[j];
+            }
             uint32_t w[4];
             if (p.quant_fmt == QF_INT4_G32) {
               float amax = 0.f;
@@ -1178,8 +1218,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
         const int n0 = nb * 256;
         const __nv_bfloat16* zrow = p.resid + static_cast<long long>(row_ok ? m : 0) * p.ldz;
         // Pass 1: h = acc + b + z; partial sum of h^2 and partial max |h * gamma| over this tile's columns.
+        // With h_out, h also leaves in bf16 (the residual stream after the add, [E] §模式 A), two
+        // 32-column units per staging buffer, while the row exchange is still ahead.
         float ss = 0.f, am = 0.f;
         if (ok) {
+          uint32_t hbuf = 0;
 #pragma unroll 1
           for (int u = 0; u < 8; ++u) {
             const int col0 = n0 + u * 32;
@@ -1193,6 +1236,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
               const float h = v[j] + b[j] + z[j];
               ss = fmaf(h, h, ss);
               am = fmaxf(am, fabsf(h * g[j]));
+              v[j] = h;
+            }
+            if (p.store_h1) {
+              if ((u & 1) == 0) hbuf = ring.acquire(lane);
+              stage_bf16_32(hbuf, lane, u & 1, v);
+              if (u & 1) ring.commit(&p.map_out[1], hbuf, lane, n0 + (u >> 1) * 64, y_box);
             }
           }
           p.partials[static_cast<size_t>(mb * p.num_n_blocks + nb) * kBM + row_in_tile] = make_float2(ss, am);

@@ -24,8 +24,9 @@ int current_device(DeviceInfo* out);
 int* device_status_ptr(int device);
 uint64_t wait_timeout_ns();
 int max_ctas_override();
-// True when a launch-intercepting CUDA tool (e.g. a profiler) is injected into the process.
-bool launch_tool_attached();
+// 1 (default): kernels whose CTAs wait on one another launch with the cooperative attribute;
+// 0: without it (fl_set_cooperative_launch).
+int cooperative_launch_mode();
 // Makes sure the kernel may use `smem_bytes` of dynamic shared memory on `device`.
 bool ensure_smem_attr(const void* kernel, int device, int smem_bytes);
 
@@ -35,6 +36,25 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const v
                uint64_t outer, uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every workspace the library takes starts with its status record: kWsStatusBytes bytes, of
+// which the first ST_WORDS ints are written by a kernel that gives up a bounded wait and read
+// back by fl_check_device_status.  The layout proper follows it.
+constexpr size_t kWsStatusBytes = 256;
+
+// Device memory to clear (cudaMemsetAsync on the launch stream) right before the kernel is
+// enqueued, once every check has passed; bytes == 0: nothing.  Cleared at most once.
+struct PreLaunchClear {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  bool done = false;
+};
+inline int run_clear(PreLaunchClear* c, cudaStream_t s) {
+  if (c == nullptr || c->bytes == 0 || c->done) return FL_OK;
+  if (cudaMemsetAsync(c->ptr, 0, c->bytes, s) != cudaSuccess) return FL_ERR_CUDA;
+  c->done = true;
+  return FL_OK;
+}
 inline bool pitch_ok(int64_t ld, int elem_bytes) { return ((ld * elem_bytes) & 15) == 0; }
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -91,12 +111,14 @@ constexpr int kRetryUnpaired = -1;
 // override, but never fewer than `min_units` (tiles that must run at once).
 // With `cooperative` the launch fails instead of starting if not every CTA can
 // be resident at once (needed when CTAs wait on one another).
+// p.status: where a timed-out wait is recorded; null selects the device-wide status word.
 template <int EPI, int CG>
-int launch_gemm_cg(GemmParams& p, const DeviceInfo& di, cudaStream_t stream, bool cooperative, int min_units) {
+int launch_gemm_cg(GemmParams& p, const DeviceInfo& di, cudaStream_t stream, bool cooperative, int min_units,
+                   PreLaunchClear* clear) {
   using T = EpiTraits<EPI, CG>;
   const void* kfn = reinterpret_cast<const void*>(&fused_gemm_kernel<EPI, CG>);
   if (!ensure_smem_attr(kfn, di.device, T::kSmemBytes)) return CG == 2 ? kRetryUnpaired : FL_ERR_CUDA;
-  p.status = device_status_ptr(di.device);
+  if (p.status == nullptr) p.status = device_status_ptr(di.device);
   if (p.status == nullptr) return FL_ERR_CUDA;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -128,16 +150,17 @@ int launch_gemm_cg(GemmParams& p, const DeviceInfo& di, cudaStream_t stream, boo
   if (units < min_units) units = min_units;
   if (units > max_units) return CG == 2 ? kRetryUnpaired : FL_ERR_UNSUPPORTED;
   cfg.gridDim = dim3(CG * units);
-  // Launch-intercepting tools (Nsight Compute) refuse cooperative launches of
-  // clusters; under such a tool the grid stays within the resident-cluster count
-  // computed above, so every pair is still placed at once on the serialised device.
-  if (cooperative && !(CG == 2 && launch_tool_attached())) {
+  // The grid never exceeds what can be resident at once (computed above); the cooperative
+  // attribute makes the driver guarantee it.  fl_set_cooperative_launch(0) drops the attribute
+  // for tools that refuse cooperative launches of clusters (a profiler serialising the device).
+  if (cooperative && cooperative_launch_mode() != 0) {
     attr[nattr].id = cudaLaunchAttributeCooperative;
     attr[nattr].val.cooperative = 1;
     ++nattr;
   }
   cfg.attrs = nattr ? attr : nullptr;
   cfg.numAttrs = nattr;
+  if (run_clear(clear, stream) != FL_OK) return FL_ERR_CUDA;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_gemm_kernel<EPI, CG>, p);
   if (e == cudaSuccess) return FL_OK;
   if (CG == 2) {
@@ -149,19 +172,28 @@ int launch_gemm_cg(GemmParams& p, const DeviceInfo& di, cudaStream_t stream, boo
 
 // Runs `setup(cg, params)` (which fills the tensor maps and epilogue fields for
 // tiles of cg x 128 rows) and launches; a refused pair launch is retried with
-// one CTA per tile.
+// one CTA per tile.  `clear`, if given, is enqueued right before the first launch.
 template <int EPI, class Setup>
 int run_gemm(int M, Setup&& setup, const DeviceInfo& di, cudaStream_t stream, bool cooperative,
-             int min_units) {
+             int min_units, PreLaunchClear* clear = nullptr) {
   GemmParams p;
   int cg = choose_cg(M);
   if (cg == 2) {
     if (!setup(2, p)) return FL_ERR_CUDA;
-    const int st = launch_gemm_cg<EPI, 2>(p, di, stream, cooperative, min_units);
+    const int st = launch_gemm_cg<EPI, 2>(p, di, stream, cooperative, min_units, clear);
     if (st != kRetryUnpaired) return st;
   }
   if (!setup(1, p)) return FL_ERR_CUDA;
-  return launch_gemm_cg<EPI, 1>(p, di, stream, cooperative, min_units);
+  return launch_gemm_cg<EPI, 1>(p, di, stream, cooperative, min_units, clear);
 }
+
+// fused_linear_residual_rmsnorm_fp8 after its argument checks, over a given workspace
+// (k_rmsnorm.cu).  scratch_mode (the no-allocation entry point): failures go to the device-wide
+// status word instead of the workspace's record, and the workspace's counters are cleared on
+// `s` right before the launch, after every check has passed.
+int rmsnorm_fp8_enqueue(const void* X, const void* W, const void* b, const void* Z, const void* gamma, float eps,
+                        void* Yq, float* row_scale, void* h_out, int M, int N, int K, int64_t ldx, int64_t ldw,
+                        int64_t ldz, int64_t ldq, void* workspace, size_t workspace_bytes, cudaStream_t s,
+                        bool scratch_mode);
 
 }  // namespace fl

@@ -10,14 +10,14 @@ namespace {
 constexpr size_t kCeAlign = 256;
 inline size_t ce_align(size_t x) { return (x + kCeAlign - 1) / kCeAlign * kCeAlign; }
 struct CeLayout {
-  size_t counters, partials, label_logit, total;
+  size_t counters, partials, label_logit, total;  // byte offsets; the status record is at 0
 };
 CeLayout ce_layout(int M, int V) {
   CeLayout l{};
   if (M <= 0 || V <= 0) return l;
   const size_t num_m = cdiv(M, kBM), num_n = cdiv(V, 256);
-  l.counters = 0;
-  l.partials = ce_align(num_m * sizeof(unsigned));
+  l.counters = kWsStatusBytes;
+  l.partials = l.counters + ce_align(num_m * sizeof(unsigned));
   l.label_logit = l.partials + ce_align(num_n * static_cast<size_t>(M) * sizeof(float2));
   l.total = l.label_logit + ce_align(static_cast<size_t>(M) * sizeof(float));
   return l;
@@ -61,6 +61,7 @@ extern "C" int fused_linear_cross_entropy(const void* X, const void* W, const vo
     p.bias = static_cast<const __nv_bfloat16*>(b);
     p.labels = labels;
     p.loss = loss;
+    p.status = reinterpret_cast<int*>(ws);  // this workspace's status record
     p.counters = reinterpret_cast<unsigned*>(ws + wl.counters);
     p.ce_partials = reinterpret_cast<float2*>(ws + wl.partials);
     p.label_logit = reinterpret_cast<float*>(ws + wl.label_logit);

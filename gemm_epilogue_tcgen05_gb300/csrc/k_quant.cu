@@ -1,12 +1,14 @@
 // fused_linear_quant: Linear (+ bias) with a block-scaled quantised write-back.
-//   "GEMM Epilogue 完全拆解" (pinghaoyang.com.cn), §仿射量化与尾声的五步 (steps 1, 2, 4, 5):
-//   per block the maximum gives the scale, the values are rounded to the target format,
-//   packed compactly (two 4-bit codes per byte) and the scale array is written by the
-//   same epilogue.
+//   "GEMM Epilogue 完全拆解" (pinghaoyang.com.cn), §仿射量化与尾声的五步: optionally the
+//   output is first multiplied per column by an inverse smoothing factor (step 3, for a
+//   layer fed by SmoothQuant/QuaRot-style smoothing), then per block the maximum gives the
+//   scale, the values are rounded to the target format, packed compactly (two 4-bit codes
+//   per byte) and the scale array is written by the same epilogue.
 #include "host_common.h"
 
-extern "C" int fused_linear_quant(const void* X, const void* W, const void* b, void* Yq, void* scales, int M, int N,
-                                  int K, int64_t ldx, int64_t ldw, int64_t ldq, int64_t lds, int fmt, void* stream) {
+extern "C" int fused_linear_quant(const void* X, const void* W, const void* b, const float* inv_smooth, void* Yq,
+                                  void* scales, int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldq,
+                                  int64_t lds, int fmt, void* stream) {
   using namespace fl;
   if (M < 0 || N < 0 || K < 0) return FL_ERR_INVALID_ARG;
   if (fmt != FL_QUANT_FP8_1X128 && fmt != FL_QUANT_INT4_G32 && fmt != FL_QUANT_NVFP4_G16) return FL_ERR_INVALID_ARG;
@@ -16,7 +18,9 @@ extern "C" int fused_linear_quant(const void* X, const void* W, const void* b, v
   const int block = fmt == FL_QUANT_FP8_1X128 ? 128 : (fmt == FL_QUANT_INT4_G32 ? 32 : 16);
   const int64_t qbytes = fmt == FL_QUANT_FP8_1X128 ? N : N / 2;
   if (ldq < qbytes || lds < cdiv(N, block) || (K > 0 && (ldx < K || ldw < K))) return FL_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(W) || !aligned16(b) || !aligned16(Yq) || !aligned16(scales)) return FL_ERR_ALIGNMENT;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(b) || !aligned16(inv_smooth) || !aligned16(Yq) ||
+      !aligned16(scales))
+    return FL_ERR_ALIGNMENT;
   if (!pitch_ok(ldq, 1) || (K > 0 && (!pitch_ok(ldx, 2) || !pitch_ok(ldw, 2)))) return FL_ERR_ALIGNMENT;
   DeviceInfo di;
   int st = current_device(&di);
@@ -33,6 +37,7 @@ extern "C" int fused_linear_quant(const void* X, const void* W, const void* b, v
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return false;
     p.bias = static_cast<const __nv_bfloat16*>(b);
+    p.smooth = inv_smooth;
     p.quant_fmt = fmt;
     p.qscale = scales;
     p.lds = lds;

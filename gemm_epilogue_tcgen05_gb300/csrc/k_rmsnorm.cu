@@ -20,7 +20,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
   bool decode;
-  size_t counters, partials, hbuf, stats, total;  // byte offsets (total = size)
+  size_t counters, partials, hbuf, stats, total;  // byte offsets (total = size); the status record is at 0
   int grid, seg_max;                              // decode only
   bool units_ok;                                  // decode unit indices fit 32-bit arithmetic
 };
@@ -92,12 +92,13 @@ int pick_decode_cluster(const DeviceInfo& di, int num_f, int num_kb, int sms) {
 }
 
 template <int C>
-int launch_decode_cluster(const DecodeParams& p, const DeviceInfo& di, cudaStream_t s) {
+int launch_decode_cluster(const DecodeParams& p, const DeviceInfo& di, cudaStream_t s, PreLaunchClear* clear) {
   const void* kfn = reinterpret_cast<const void*>(&rmsnorm_fp8_decode_cluster_kernel<C>);
   if (!ensure_smem_attr(kfn, di.device, kDcSmemBytes)) return FL_ERR_CUDA;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
   cluster_cfg<C>(cfg, attr, p.num_f * C, s);
+  if (run_clear(clear, s) != FL_OK) return FL_ERR_CUDA;
   return cudaLaunchKernelEx(&cfg, rmsnorm_fp8_decode_cluster_kernel<C>, p) == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
@@ -126,35 +127,32 @@ WsLayout layout(int M, int N, int K, int num_sms) {
         if (segs > w.seg_max) w.seg_max = segs;
       }
     }
-    w.counters = 0;
-    w.partials = align_up(static_cast<size_t>(num_f + 2) * sizeof(unsigned));
+    w.counters = kWsStatusBytes;
+    w.partials = w.counters + align_up(static_cast<size_t>(num_f + 2) * sizeof(unsigned));
     w.hbuf = w.partials + align_up(static_cast<size_t>(w.grid) * w.seg_max * 128 * kDecTokens * sizeof(float));
     w.stats = w.hbuf + align_up(static_cast<size_t>(num_f) * kDecTokens * 128 * sizeof(float));
     w.total = w.stats + align_up(static_cast<size_t>(num_f) * kDecTokens * sizeof(float2));
   } else {
     const int num_m = cdiv(M, kBM), num_n = cdiv(N, 256);
-    w.counters = 0;
-    w.partials = align_up(static_cast<size_t>(2 * num_m) * sizeof(unsigned));
+    w.counters = kWsStatusBytes;
+    w.partials = w.counters + align_up(static_cast<size_t>(2 * num_m) * sizeof(unsigned));
     w.total = w.partials + align_up(static_cast<size_t>(num_m) * num_n * kBM * sizeof(float2));
   }
   return w;
 }
 
-}  // namespace
-}  // namespace fl
-
-extern "C" size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K) {
-  using namespace fl;
-  DeviceInfo di;
-  if (current_device(&di) == FL_ERR_CUDA) return 0;
-  return layout(M, N, K, decode_sms(di)).total;
+// Byte ranges [a, a + na) and [b, b + nb) overlap.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
 }
 
-extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const void* b, const void* Z,
-                                                 const void* gamma, float eps, void* Yq, float* row_scale, int M,
-                                                 int N, int K, int64_t ldx, int64_t ldw, int64_t ldz, int64_t ldq,
-                                                 void* workspace, size_t workspace_bytes, void* stream) {
-  using namespace fl;
+}  // namespace
+
+int rmsnorm_fp8_enqueue(const void* X, const void* W, const void* b, const void* Z, const void* gamma, float eps,
+                        void* Yq, float* row_scale, void* h_out, int M, int N, int K, int64_t ldx, int64_t ldw,
+                        int64_t ldz, int64_t ldq, void* workspace, size_t workspace_bytes, cudaStream_t s,
+                        bool scratch_mode) {
   if (M < 0 || N < 0 || K < 0) return FL_ERR_INVALID_ARG;
   if (!(eps >= 0.f)) return FL_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FL_OK;
@@ -162,8 +160,12 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
       (K > 0 && (X == nullptr || W == nullptr)))
     return FL_ERR_INVALID_ARG;
   if (ldz < N || ldq < N || (K > 0 && (ldx < K || ldw < K))) return FL_ERR_INVALID_ARG;
+  // h_out shares the residual's layout (pitch ldz) and must not overlap it: both passes of the
+  // prefill epilogue read Z after the first one has started writing h.
+  const size_t zbytes = (static_cast<size_t>(M - 1) * static_cast<size_t>(ldz) + static_cast<size_t>(N)) * 2;
+  if (h_out != nullptr && overlaps(h_out, zbytes, Z, zbytes)) return FL_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(W) || !aligned16(b) || !aligned16(Z) || !aligned16(gamma) || !aligned16(Yq) ||
-      !aligned16(row_scale))
+      !aligned16(row_scale) || !aligned16(h_out))
     return FL_ERR_ALIGNMENT;
   if (!pitch_ok(ldz, 2) || !pitch_ok(ldq, 1) || (K > 0 && (!pitch_ok(ldx, 2) || !pitch_ok(ldw, 2))))
     return FL_ERR_ALIGNMENT;
@@ -174,7 +176,16 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
   if (workspace == nullptr || workspace_bytes < wl.total) return FL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return FL_ERR_ALIGNMENT;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // A caller-owned workspace records failures in its own status record, so concurrent calls
+  // on different workspaces never see each other's; the no-allocation entry point's shared
+  // scratch uses the device-wide word instead, and clears its counters before the launch.
+  int* status = scratch_mode ? device_status_ptr(di.device) : reinterpret_cast<int*>(ws);
+  if (status == nullptr) return FL_ERR_CUDA;
+  PreLaunchClear clear;
+  if (scratch_mode) {
+    clear.ptr = ws;
+    clear.bytes = wl.partials;  // status record and counters
+  }
 
   if (wl.decode) {
     if (!wl.units_ok || wl.seg_max > kDecMaxSeg) return FL_ERR_UNSUPPORTED;
@@ -200,18 +211,19 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
     p.yq = static_cast<uint8_t*>(Yq);
     p.ldq = ldq;
     p.row_scale = row_scale;
+    p.hout = static_cast<__nv_bfloat16*>(h_out);
+    p.ldh = ldz;
     p.counters = reinterpret_cast<unsigned*>(ws + wl.counters);
     p.partials = reinterpret_cast<float*>(ws + wl.partials);
     p.hbuf = reinterpret_cast<float*>(ws + wl.hbuf);
     p.stats = reinterpret_cast<float2*>(ws + wl.stats);
-    p.status = device_status_ptr(di.device);
+    p.status = status;
     p.timeout_ns = wait_timeout_ns();
-    if (p.status == nullptr) return FL_ERR_CUDA;
     switch (pick_decode_cluster(di, p.num_f, p.num_kb, decode_sms(di))) {
-      case 8: return launch_decode_cluster<8>(p, di, s);
-      case 4: return launch_decode_cluster<4>(p, di, s);
-      case 2: return launch_decode_cluster<2>(p, di, s);
-      case 1: return launch_decode_cluster<1>(p, di, s);
+      case 8: return launch_decode_cluster<8>(p, di, s, &clear);
+      case 4: return launch_decode_cluster<4>(p, di, s, &clear);
+      case 2: return launch_decode_cluster<2>(p, di, s, &clear);
+      case 1: return launch_decode_cluster<1>(p, di, s, &clear);
       default: break;
     }
     const void* kfn = reinterpret_cast<const void*>(&rmsnorm_fp8_decode_kernel);
@@ -231,6 +243,7 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (run_clear(&clear, s) != FL_OK) return FL_ERR_CUDA;
     return cudaLaunchKernelEx(&cfg, rmsnorm_fp8_decode_kernel, p) == cudaSuccess ? FL_OK : FL_ERR_CUDA;
   }
 
@@ -248,6 +261,11 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
     if (!encode_2d(&p.map_out[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Yq, N, M, ldq, 128, 32,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return false;
+    if (h_out != nullptr && !encode_2d(&p.map_out[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h_out, N, M, ldz, 64, 32,
+                                       CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+    p.store_h1 = h_out != nullptr;
+    p.status = status;
     p.bias = static_cast<const __nv_bfloat16*>(b);
     p.resid = static_cast<const __nv_bfloat16*>(Z);
     p.ldz = ldz;
@@ -260,5 +278,23 @@ extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, c
   };
   // Every tile of a row block must be resident together: at least one row block's
   // worth of tiles runs at once and all CTAs are co-scheduled (cooperative launch).
-  return run_gemm<EPI_RMSNORM_FP8>(M, setup, di, s, true, num_n);
+  return run_gemm<EPI_RMSNORM_FP8>(M, setup, di, s, true, num_n, &clear);
+}
+
+}  // namespace fl
+
+extern "C" size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K) {
+  using namespace fl;
+  DeviceInfo di;
+  if (current_device(&di) == FL_ERR_CUDA) return 0;
+  return layout(M, N, K, decode_sms(di)).total;
+}
+
+extern "C" int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const void* b, const void* Z,
+                                                 const void* gamma, float eps, void* Yq, float* row_scale,
+                                                 void* h_out, int M, int N, int K, int64_t ldx, int64_t ldw,
+                                                 int64_t ldz, int64_t ldq, void* workspace, size_t workspace_bytes,
+                                                 void* stream) {
+  return fl::rmsnorm_fp8_enqueue(X, W, b, Z, gamma, eps, Yq, row_scale, h_out, M, N, K, ldx, ldw, ldz, ldq,
+                                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false);
 }

@@ -16,7 +16,9 @@
  *   - Calls are asynchronous: they validate the arguments on the host, enqueue
  *     one kernel on `stream` (a cudaStream_t; NULL = legacy default stream) and
  *     return.  Device-side failures (a bounded wait that ran out) are recorded
- *     in a library status word and reported by fl_device_status().
+ *     in the status record at the start of the call's workspace (calls that take
+ *     one: fl_check_device_status(workspace, stream)) or else in a device-wide
+ *     status word (fl_device_status(stream)).
  *   - Alignment (a requirement of the tensor-memory-access copies): every base
  *     pointer must be 16-byte aligned and every leading dimension times the
  *     element size must be a multiple of 16 bytes.
@@ -139,40 +141,48 @@ FL_API int fused_swiglu(const void* X, const void* Wgate, const void* Wup,
  * leading dimension ldz, gamma [N] bf16.  Yq [M,N] E4M3 bytes (leading dimension
  * ldq, a multiple of 16), row_scale [M] fp32 (dequantise with Yq * row_scale).
  * A row whose maximum is 0 gets scale 0 and zero codes.
+ * h_out: nullable bf16 [M,N] with the residual's leading dimension ldz: when given,
+ * h = X W^T + b + Z (the residual stream after the add, which the next block of a
+ * model reads) is also written, rounded once to bf16; NULL writes nothing extra.
+ * h_out must not overlap Z (FL_ERR_INVALID_ARG).
  * workspace: device memory of at least fl_rmsnorm_fp8_workspace_bytes(M, N, K)
- * bytes, 256-byte aligned and ZERO-FILLED before its first use.  The kernels
+ * bytes, 256-byte aligned and ZERO-FILLED before its first use.  Its first 256 bytes
+ * are this call's status record: a device-side wait that runs out is recorded there
+ * (read and clear it with fl_check_device_status(workspace, stream)).  The kernels
  * reset the counters they keep there before they return, so the same workspace
  * serves later calls on the same stream without clearing; after FL_ERR_TIMEOUT
  * it must be zero-filled again.  Calls that may run concurrently must not share
  * a workspace.  M <= 32 with K > 0 runs the split-K decode kernel (one CTA per
  * SM, each streaming an equal share of W); larger M runs the persistent
- * prefill kernel.  Both launch cooperatively (all CTAs resident at once) and
- * fail with FL_ERR_CUDA if that is impossible.  N must not exceed
- * 256 * (number of SMs) on the prefill path.
+ * prefill kernel.  Both keep every CTA resident at once (the prefill kernel
+ * launches cooperatively) and fail with FL_ERR_CUDA if that is impossible.
+ * N must not exceed 256 * (number of SMs) on the prefill path.
  */
 FL_API int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const void* b,
                                       const void* Z, const void* gamma, float eps,
-                                      void* Yq, float* row_scale,
+                                      void* Yq, float* row_scale, void* h_out,
                                       int M, int N, int K,
                                       int64_t ldx, int64_t ldw, int64_t ldz, int64_t ldq,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
-/* Same computation as fused_linear_residual_rmsnorm_fp8, for callers that
- * cannot allocate device memory and so cannot supply a workspace: a decode
- * step recorded into a CUDA graph (allocating during capture breaks it), a
- * serving loop that must not stall in the allocator, or a plugin whose host
- * framework owns all device memory.  The pages have no counterpart of this
- * call; it exists only for such callers.
+/* Same computation as fused_linear_residual_rmsnorm_fp8 (without h_out), for callers
+ * that cannot allocate device memory and so cannot supply a workspace: a serving loop
+ * that must not stall in the allocator (cudaMalloc can synchronise the device), or a
+ * plugin whose host framework owns all device memory and hands it none.  The pages have
+ * no counterpart of this call; it exists only for such callers.
  * Scratch: one FL_NOALLOC_SCRATCH_BYTES array compiled into the library and
  * held by every GPU that loads it until the process exits.  A shape whose
  * fl_rmsnorm_fp8_workspace_bytes(M, N, K) exceeds that size is rejected with
- * FL_ERR_WORKSPACE.  The array is shared by every call: calls that can overlap
- * on the GPU (streams with no ordering between them) race and must not be
- * issued.  Each call clears the counters the kernels wait on with an
- * asynchronous memset on `stream` before its launch; nothing is allocated.
- * The first call on a device looks up the array's device address, so make it
- * before any stream capture that records later calls.  Other arguments,
- * layouts and errors are those of fused_linear_residual_rmsnorm_fp8. */
+ * FL_ERR_WORKSPACE.  The array is shared by every call and keeps the last call's
+ * contents: calls that can overlap on the GPU (streams with no ordering between
+ * them) race and must not be issued.  A call that passes every check enqueues an
+ * asynchronous memset on `stream` that clears the counters the kernels wait on, then
+ * the kernel; a rejected call enqueues nothing.  Nothing is allocated.  The first
+ * call on a device looks up the array's device address with that device current (a
+ * one-time set-up); make that first call before any stream capture.  The address is
+ * kept for the life of the process, so cudaDeviceReset is not supported with this
+ * call.  Device-side failures go to the device-wide status word (fl_device_status).
+ * Other arguments, layouts and errors are those of fused_linear_residual_rmsnorm_fp8. */
 #define FL_NOALLOC_SCRATCH_BYTES (8u << 20)
 FL_API int fused_linear_residual_rmsnorm_fp8_noalloc(const void* X, const void* W, const void* b,
                                                      const void* Z, const void* gamma, float eps,
@@ -220,7 +230,8 @@ FL_API int fl_rms_partials_per_row(int n_norm);
  * row, loss 0; >= V: loss NaN), loss [M] fp32 out.  logits: nullable bf16 [M,V] copy of
  * the logits (leading dimension ldl), e.g. kept for a backward pass.
  * workspace: fl_cross_entropy_workspace_bytes(M, V) bytes, 256-byte aligned and
- * zero-filled before first use; the kernel resets its counters, so it can be reused
+ * zero-filled before first use; its first 256 bytes are the call's status record
+ * (fl_check_device_status).  The kernel resets its counters, so it can be reused
  * by later calls on the same stream (re-zero it after FL_ERR_TIMEOUT). */
 FL_API int fused_linear_cross_entropy(const void* X, const void* W, const void* b, const int32_t* labels,
                                       float* loss, void* logits, int M, int V, int K,
@@ -233,6 +244,10 @@ FL_API size_t fl_cross_entropy_workspace_bytes(int M, int V);
  *   of a row, scale = max|y| / qmax, codes = y / scale rounded to the format (nearest
  *   even, saturating), packed compactly, and the scale array written beside them.
  *   A block whose maximum is 0 gets scale 0 and zero codes.
+ *   Step 3 (optional scale-factor correction): inv_smooth, a nullable fp32 [N] vector
+ *   (16-byte aligned), is the inverse smoothing coefficient of a layer fed by
+ *   SmoothQuant/QuaRot-style smoothing; when given, y[m,n] = (X W^T + b)[m,n] *
+ *   inv_smooth[n] is what the blocks' maxima, scales and codes describe.
  * fmt FL_QUANT_FP8_1X128: E4M3 codes, one byte per value (Yq [M,N], ldq >= N bytes);
  *     blocks of 128 columns, fp32 scales [M][lds] = max / 448.
  * fmt FL_QUANT_INT4_G32: signed 4-bit codes in [-7, 7] (two's complement), two per byte
@@ -244,9 +259,9 @@ FL_API size_t fl_cross_entropy_workspace_bytes(int M, int V);
  * X [M,K] bf16, W [N,K] bf16, b [N] bf16 (nullable); ldq in bytes (multiple of 16),
  * lds in scale elements (>= number of blocks per row). */
 enum { FL_QUANT_FP8_1X128 = 0, FL_QUANT_INT4_G32 = 1, FL_QUANT_NVFP4_G16 = 2 };
-FL_API int fused_linear_quant(const void* X, const void* W, const void* b, void* Yq, void* scales,
-                              int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldq, int64_t lds,
-                              int fmt, void* stream);
+FL_API int fused_linear_quant(const void* X, const void* W, const void* b, const float* inv_smooth,
+                              void* Yq, void* scales, int M, int N, int K, int64_t ldx, int64_t ldw,
+                              int64_t ldq, int64_t lds, int fmt, void* stream);
 
 /* Backward of Linear -> GELU, fused into the dgrad GEMM.
  *   "GEMM Epilogue 完全拆解", §模式 D: dH = (dZ W) * GELU'(H).  dZ [M,K] bf16 is the
@@ -292,10 +307,24 @@ FL_API size_t fl_linear_gelu_host_buffer_bytes(int M, int N, int K);
 FL_API size_t fl_rmsnorm_fp8_workspace_bytes(int M, int N, int K);
 
 /* Synchronises `stream`, then returns FL_OK if no kernel of this library
- * recorded a device-side failure on the current device since the previous
- * call, else the recorded code (FL_ERR_TIMEOUT), and clears the record.
- * Returns FL_ERR_CUDA if the synchronisation itself fails. */
+ * recorded a device-side failure in the device-wide status word of the current
+ * device since the previous call, else the recorded code (FL_ERR_TIMEOUT), and
+ * clears the record.  Calls that take a workspace record their failures in it
+ * instead (fl_check_device_status).  Returns FL_ERR_CUDA if the synchronisation
+ * itself fails. */
 FL_API int fl_device_status(void* stream);
+
+/* The status of the calls that used `workspace` (a workspace of
+ * fused_linear_residual_rmsnorm_fp8 or fused_linear_cross_entropy).
+ *   "GEMM Epilogue 完全拆解", §边界三 (布局即约定): the error contract travels with the
+ *   buffer layout, so a failure is reported against the workspace the call used.
+ * Synchronises `stream`, reads the status record in the workspace's first 256 bytes,
+ * returns FL_OK if it is clear, else the recorded code (FL_ERR_TIMEOUT) after clearing
+ * it.  Concurrent calls on other streams with other workspaces neither see nor clear
+ * this record.  workspace NULL: the same as fl_device_status(stream).
+ * FL_ERR_ALIGNMENT if workspace is not 256-byte aligned; FL_ERR_CUDA if the
+ * synchronisation or the read fails. */
+FL_API int fl_check_device_status(void* workspace, void* stream);
 
 /* Upper bound, in nanoseconds, on every device-side wait of later launches
  * (default 2e9).  A wait that runs out sets the status word, makes the kernel
@@ -318,6 +347,24 @@ FL_API void fl_set_max_ctas(int n);
  * blocks; with 0 every CTA computes its own 128-row tile.  Results are the
  * same either way.  Process-wide; intended for tests and diagnostics. */
 FL_API void fl_set_cta_pairing(int enable);
+
+/* Cooperative launch of the kernels whose CTAs wait on one another (the RMSNorm prefill
+ * kernel's row exchange): with 1 (the default) the launch carries the cooperative attribute,
+ * so the driver refuses it rather than start a grid that cannot be resident at once; with 0
+ * the same grid (sized to what is resident at once) launches without it.  Only for tools
+ * that refuse cooperative launches of clusters, such as a kernel profiler serialising the
+ * device.  Process-wide; intended for diagnostics. */
+FL_API void fl_set_cooperative_launch(int enable);
+
+/* Tensor-map descriptor cache: every call encodes the TMA descriptors of its operands; with
+ * 1 (the default) an encoded descriptor is kept, keyed by (address, extents, pitch, box,
+ * element type, swizzle), and reused when a later call passes the same key (a descriptor
+ * holds nothing else, so reuse is exact; a new pointer or shape is a new key).  128 entries,
+ * round-robin replacement, guarded by a mutex.  0 disables and empties it.
+ * fl_descriptor_cache_stats returns the hits and misses counted since the process started
+ * (either pointer may be NULL).  Process-wide. */
+FL_API void fl_set_descriptor_cache(int enable);
+FL_API void fl_descriptor_cache_stats(unsigned long long* hits, unsigned long long* misses);
 
 /* Decode-shaped calls: with 1 (the default) fused_linear_gelu (bf16), fused_swiglu,
  * fused_qkv_rope and fused_qkv_rope_fp8kv with M <= 32 rows run a swap-AB kernel that streams W once (tiles of W rows

@@ -22,8 +22,11 @@ Recipe (one element):
    bf16 (round to nearest even).
 
 Streams within a workload: X = 0, W = 1, b = 2, Z = 3, gamma = 4,
-W_up = 5, b_up = 6, W2 (second GEMM of a chain) = 7, labels = 8.
+W_up = 5, b_up = 6, W2 (second GEMM of a chain) = 7, labels = 8,
+inverse smoothing factors = 9.
 Labels are uniform integers: (top 53 bits of counter i) mod V.
+Inverse smoothing factors are log-normal with median 1: exp(0.5 z) for a
+standard normal z of stream 9 (fp64), rounded to fp32.
 """
 from __future__ import annotations
 
@@ -41,7 +44,8 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 21  # elements per vectorised chunk (bounds host memory)
 
-STREAM_X, STREAM_W, STREAM_B, STREAM_Z, STREAM_GAMMA, STREAM_WUP, STREAM_BUP, STREAM_W2, STREAM_LABEL = range(9)
+STREAM_X, STREAM_W, STREAM_B, STREAM_Z, STREAM_GAMMA, STREAM_WUP, STREAM_BUP, STREAM_W2, STREAM_LABEL, \
+    STREAM_SMOOTH = range(10)
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -144,6 +148,12 @@ def draw_labels(seed: int, stream: int, count: int, vocab: int) -> np.ndarray:
     return ((z >> np.uint64(11)) % np.uint64(vocab)).astype(np.int32)
 
 
+def draw_inv_smooth(seed: int, count: int) -> np.ndarray:
+    """Per-column inverse smoothing factors, fp32: exp(0.5 z), z standard normal (stream 9)."""
+    z = normal_f64(seed, STREAM_SMOOTH, 0, count)
+    return np.exp(0.5 * z).astype(np.float32)
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (nearest even); returns uint16 bit patterns."""
     bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
@@ -223,6 +233,7 @@ class Workload:
     N2: int = 0          # rms_chain: output features of the second GEMM (its K is N)
     quant: str = ""      # quant: "fp8_1x128" | "int4_g32" | "nvfp4_g16"
     n_kv_heads: int = 0  # qkv_fp8kv: key/value heads (grouped-query attention)
+    smooth: bool = False  # quant: per-column inverse smoothing factors (fp32 [N], "inv_smooth")
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
 
@@ -260,6 +271,9 @@ WORKLOADS = {
                                                quant="int4_g32"),
     "quant_nvfp4_g16_8192x16384x4096": Workload("quant_nvfp4_g16_8192x16384x4096", "quant", 8192, 16384, 4096,
                                                 quant="nvfp4_g16"),
+    # the same with the output of a smoothed layer: inverse smoothing factor per column first
+    "quant_fp8_1x128_smooth_8192x16384x4096": Workload("quant_fp8_1x128_smooth_8192x16384x4096", "quant", 8192,
+                                                       16384, 4096, quant="fp8_1x128", smooth=True),
     # decode shapes (32 tokens) of the up projection with GELU and of the fused QKV projection
     "gelu_decode_32x16384x4096": Workload("gelu_decode_32x16384x4096", "gelu_tanh", 32, 16384, 4096),
     "qkv_decode_32x12288x4096": Workload("qkv_decode_32x12288x4096", "qkv_rope", 32, 12288, 4096,
@@ -320,12 +334,15 @@ def make_operands(w: Workload, rows: tuple[int, int] | None = None) -> dict:
             out[name] = draw(w.seed, stream, shape, mean, std, dt, rows[0], rows[1])
         else:
             out[name] = draw(w.seed, stream, shape, mean, std, dt)
+    if w.smooth:
+        out["inv_smooth"] = draw_inv_smooth(w.seed, w.N)
     return out
 
 
 def to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact fp64 copy of an operand produced by :func:`draw`."""
-    if dtype == "bf16":
+    """Exact fp64 copy of an operand produced by :func:`draw` (fp32 arrays are widened as they
+    are, whatever the workload's dtype: the inverse smoothing factors are always fp32)."""
+    if dtype == "bf16" and a.dtype != np.float32:
         return bf16_bits_to_f64(a)
     return a.astype(np.float64)
 

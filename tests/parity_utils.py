@@ -69,11 +69,14 @@ def assert_fp8_close(codes: np.ndarray, scale: np.ndarray, q_ref: np.ndarray, s_
     assert np.mean(d != 0) < 0.02, f"{what}: {np.mean(d != 0):.3%} of codes differ"
 
 
-def sample_rows(M: int, extra: int = 4, seed: int = 0) -> np.ndarray:
-    """Rows that cover tile edges (first/last of 128-row blocks) plus a few random ones."""
+def sample_rows(M: int, seed: int = 0) -> np.ndarray:
+    """Rows of a full-size workload to compare: one random row in every 32-row slice, so every
+    128-row block, both halves of every 256-row pair tile and the rows of every epilogue warp of
+    every tile are checked (256 rows at M = 8192), plus the edges of the first blocks and the last
+    row."""
     rng = np.random.default_rng(seed)
-    rows = {0, 1, 127, 128, M - 1, M // 2, min(M - 1, 129)}
-    rows |= set(rng.integers(0, M, size=extra).tolist())
+    rows = {0, 1, 127, 128, 129, 255, 256, M - 1}
+    rows |= {s + int(rng.integers(0, min(32, M - s))) for s in range(0, M, 32)}
     return np.array(sorted(r for r in rows if 0 <= r < M), dtype=np.int64)
 
 

@@ -24,7 +24,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert fl.version() == 100
+    assert fl.version() == 200
     assert fl.status_string(fl.FL_OK) == "ok"
     assert "timed out" in fl.status_string(fl.FL_ERR_TIMEOUT)
     assert fl.status_string(99) == "unknown status"
@@ -64,23 +64,33 @@ def test_other_entry_points_reject_bad_arguments_on_host(lib):
     assert lib.fused_swiglu(a, a, P(0x10008), None, None, a, 8, 8, 8, 8, 8, 8, None) == fl.FL_ERR_ALIGNMENT
     # RMSNorm: missing gamma, negative eps, FP8 pitch not a multiple of 16
     f = ctypes.c_float
-    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, None, f(1e-6), a, a, 8, 16, 8, 8, 8, 16, 16,
+    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, None, f(1e-6), a, a, None, 8, 16, 8, 8, 8, 16, 16,
                                                  a, 1 << 20, None) == fl.FL_ERR_INVALID_ARG
-    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, a, f(-1.0), a, a, 8, 16, 8, 8, 8, 16, 16,
+    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, a, f(-1.0), a, a, None, 8, 16, 8, 8, 8, 16, 16,
                                                  a, 1 << 20, None) == fl.FL_ERR_INVALID_ARG
-    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, a, f(1e-6), a, a, 8, 24, 8, 8, 8, 24, 24,
+    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, a, a, f(1e-6), a, a, None, 8, 24, 8, 8, 8, 24, 24,
                                                  a, 1 << 20, None) == fl.FL_ERR_ALIGNMENT
+    # h_out: may not overlap the residual Z (same pitch), must be 16-byte aligned
+    z = 0x100000
+    for h in (z, z + 16 * 2 * 7, z - 16):  # same base, inside the last row, one row-end before the start
+        assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, P(z), a, f(1e-6), a, a, P(h), 8, 16, 8, 8, 8, 16,
+                                                     16, a, 1 << 20, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_residual_rmsnorm_fp8(a, a, None, P(z), a, f(1e-6), a, a, P(z + 4096 + 8), 8, 16, 8, 8,
+                                                 8, 16, 16, a, 1 << 20, None) == fl.FL_ERR_ALIGNMENT
 
 
 def test_quant_rejects_bad_arguments_on_host(lib):
     a = P(0x10000)
     # unknown format, odd N for a 4-bit format, short scale pitch, code pitch not a multiple of 16
-    assert lib.fused_linear_quant(a, a, None, a, a, 8, 32, 16, 16, 16, 32, 4, 3, None) == fl.FL_ERR_INVALID_ARG
-    assert lib.fused_linear_quant(a, a, None, a, a, 8, 33, 16, 16, 16, 32, 4, 1, None) == fl.FL_ERR_UNSUPPORTED
-    assert lib.fused_linear_quant(a, a, None, a, a, 8, 256, 16, 16, 16, 128, 7, 1, None) == fl.FL_ERR_INVALID_ARG
-    assert lib.fused_linear_quant(a, a, None, a, a, 8, 264, 16, 16, 16, 264, 3, 0, None) == fl.FL_ERR_ALIGNMENT
-    assert lib.fused_linear_quant(a, a, None, a, None, 8, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_ERR_INVALID_ARG
-    assert lib.fused_linear_quant(None, None, None, None, None, 0, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_OK
+    assert lib.fused_linear_quant(a, a, None, None, a, a, 8, 32, 16, 16, 16, 32, 4, 3, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_quant(a, a, None, None, a, a, 8, 33, 16, 16, 16, 32, 4, 1, None) == fl.FL_ERR_UNSUPPORTED
+    assert lib.fused_linear_quant(a, a, None, None, a, a, 8, 256, 16, 16, 16, 128, 7, 1, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_quant(a, a, None, None, a, a, 8, 264, 16, 16, 16, 264, 3, 0, None) == fl.FL_ERR_ALIGNMENT
+    assert lib.fused_linear_quant(a, a, None, None, a, None, 8, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_ERR_INVALID_ARG
+    assert lib.fused_linear_quant(None, None, None, None, None, None, 0, 32, 16, 16, 16, 32, 1, 0, None) == fl.FL_OK
+    # the inverse smoothing vector must be 16-byte aligned like every other operand
+    assert lib.fused_linear_quant(a, a, None, P(0x10004), a, a, 8, 32, 16, 16, 16, 32, 1, 0,
+                                  None) == fl.FL_ERR_ALIGNMENT
 
 
 def test_qkv_fp8kv_rejects_bad_arguments_on_host(lib):
@@ -137,3 +147,27 @@ def test_decode_shape_query_on_host(lib):
         assert lib.fl_linear_decode_shape(fl.DECODE_SWIGLU, M, N, K, *refs) == fl.FL_OK
         assert [o.value for o in out] == [0, 0, 0]
     assert fl.linear_decode_shape(fl.DECODE_QKV, 64, 12288, 4096) == (0, 0, 0)
+
+
+def test_workspace_status_check_and_diagnostic_switches_on_host(lib):
+    # a workspace that is not 256-byte aligned cannot hold a status record
+    assert lib.fl_check_device_status(P(0x10010), None) == fl.FL_ERR_ALIGNMENT
+    # the diagnostic switches take any int and need no device
+    for f in (lib.fl_set_cooperative_launch, lib.fl_set_descriptor_cache):
+        f(0)
+        f(1)
+    h, m = ctypes.c_ulonglong(7), ctypes.c_ulonglong(7)
+    lib.fl_descriptor_cache_stats(ctypes.byref(h), ctypes.byref(m))
+    assert h.value >= 0 and m.value >= 0
+    lib.fl_descriptor_cache_stats(None, None)
+
+
+def test_noalloc_rejects_bad_arguments_before_any_device_work(lib):
+    f = lib.fused_linear_residual_rmsnorm_fp8_noalloc
+    I64 = ctypes.c_int64
+    f.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, I64, I64, I64, I64,
+                  P]
+    a = P(0x10000)
+    assert f(a, a, None, a, a, 1e-6, a, a, -1, 16, 8, 8, 8, 16, 16, None) == fl.FL_ERR_INVALID_ARG
+    assert f(a, a, None, a, a, -1.0, a, a, 8, 16, 8, 8, 8, 16, 16, None) == fl.FL_ERR_INVALID_ARG
+    assert f(None, None, None, None, None, 1e-6, None, None, 0, 16, 8, 8, 8, 16, 16, None) == fl.FL_OK
