@@ -191,6 +191,87 @@ def job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
     return world * units_per_rank / seconds_max
 
 
+# ----------------------------------------------------------------------------- byte model
+def _nbytes(shape, dt: str) -> int:
+    return math.prod(shape) * (2 if dt == "bf16" else 4)
+
+
+def operand_bytes(w) -> dict:
+    """Bytes of every input of one call, each read once (weights included)."""
+    out = {name: _nbytes(shape, dt) for name, _, shape, _, _, dt in syn.operand_specs(w)}
+    if w.smooth:
+        out["inv_smooth"] = 4 * w.N
+    if w.kind == "cross_entropy":
+        out["labels"] = 4 * w.M
+    return out
+
+
+def output_bytes(w, store_h: bool = False) -> dict:
+    """Bytes of every output of one call, each written once.  store_h: the RMSNorm call also writes
+    h_out, and the chain's first GEMM also writes H1 (the residual stream after the add)."""
+    M, N = w.M, w.N
+    if w.kind in ("gelu_tanh", "gelu_erf", "swiglu", "gelu_bwd"):
+        return {"Y": 2 * M * N}
+    if w.kind == "swiglu_bwd":
+        return {"dGU": 2 * M * 2 * N}
+    if w.kind == "qkv_rope":
+        dm = w.n_heads * w.head_dim
+        return {"Q": 2 * M * dm, "K": 2 * M * dm, "V": 2 * M * dm}
+    if w.kind == "qkv_fp8kv":
+        dq, dkv = w.n_heads * w.head_dim, w.n_kv_heads * w.head_dim
+        return {"Q": 2 * M * dq, "Kq": M * dkv, "Vq": M * dkv, "k_scale": 4 * M * w.n_kv_heads,
+                "v_scale": 4 * M * w.n_kv_heads}
+    if w.kind == "cross_entropy":
+        return {"loss": 4 * M}
+    if w.kind == "quant":
+        bs = {"fp8_1x128": 128, "int4_g32": 32, "nvfp4_g16": 16}[w.quant]
+        codes = M * N if w.quant == "fp8_1x128" else M * (N // 2)
+        return {"codes": codes, "scales": M * -(-N // bs) * (1 if w.quant == "nvfp4_g16" else 4)}
+    if w.kind == "rms_chain":
+        # H2 is written by the first GEMM and read back by the second (counted as its output traffic)
+        out = {"H2_write": 2 * M * N, "H2_read": 2 * M * N, "Y": 2 * M * w.N2}
+        if store_h:
+            out["H1"] = 2 * M * N
+        return out
+    out = {"Yq": M * N, "row_scale": 4 * M}  # residual + RMSNorm + FP8
+    if store_h:
+        out["h_out"] = 2 * M * N
+    return out
+
+
+def algorithmic_bytes(w, store_h: bool = False) -> float:
+    """The roofline numerator of an HBM-bound call: each operand read once, each output written once."""
+    return float(sum(operand_bytes(w).values()) + sum(output_bytes(w, store_h).values()))
+
+
+def unfused_activation_bytes(w) -> dict:
+    """Activation bytes per call that the unfused sequence moves between the GEMM and its consumer,
+    in the accounting of the end-to-end ledger of "GEMM Epilogue 完全拆解" (§端到端账本): weights,
+    the first GEMM's input and the last output are left out, since both forms move them alike.
+      chain (output projection -> residual -> RMSNorm -> gate/up GEMM): the projection writes d;
+        the residual add reads d + d and writes d; RMSNorm reads d and gamma (d, counted per token
+        as the page does) and writes d; the next GEMM reads d: 3d written + 5d read;
+      SwiGLU: the GEMM writes gate and up (2 d_ff), the elementwise kernel reads them and writes
+        d_ff: 5 d_ff."""
+    if w.kind == "rms_chain":
+        return {"written": 3 * 2 * w.M * w.N, "read": 5 * 2 * w.M * w.N}
+    if w.kind == "swiglu":
+        return {"written": 3 * 2 * w.M * w.N, "read": 2 * 2 * w.M * w.N}
+    raise ValueError(f"no unfused ledger for {w.kind}")
+
+
+def fused_activation_bytes(w, store_h: bool = True) -> dict:
+    """The same ledger for the fused kernels: chain, the first epilogue reads the residual (d) and
+    writes H2 (d) and H1 (d, the residual stream kept for the next block), the second GEMM reads H2
+    (d): 4d; SwiGLU: only its d_ff output leaves the epilogue."""
+    if w.kind == "rms_chain":
+        out = output_bytes(w, store_h)
+        return {"written": out["H2_write"] + out.get("H1", 0), "read": operand_bytes(w)["Z"] + out["H2_read"]}
+    if w.kind == "swiglu":
+        return {"written": output_bytes(w)["Y"], "read": 0}
+    raise ValueError(f"no fused ledger for {w.kind}")
+
+
 # ----------------------------------------------------------------------------- workloads
 def dev_bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
@@ -260,26 +341,9 @@ class Case:
                         torch.empty(w.M, dtype=torch.float32, device="cuda"))
             self.ws = fl.rmsnorm_fp8_workspace(w.M, w.N, w.K)
             self.flops = 2.0 * w.M * w.N * w.K
-        self.bytes = self.algorithmic_bytes()
+        self.bytes = algorithmic_bytes(w)
         # decode shapes (32 tokens): the weight stream bounds them
         self.hbm_bound = w.M <= 32 and w.kind in ("rmsnorm_fp8", "gelu_tanh", "qkv_rope", "qkv_fp8kv", "swiglu")
-
-    def algorithmic_bytes(self) -> float:
-        """Each operand read once and each output written once (bytes)."""
-        w = self.w
-        b = sum(v.nbytes for v in self.host.values())
-        if w.kind == "rmsnorm_fp8":
-            return float(b + w.M * w.N + 4 * w.M)
-        if w.kind == "qkv_rope":
-            return float(b + 2 * w.M * w.N)
-        if w.kind == "cross_entropy":
-            return float(b + 4 * w.M + 4 * w.M)  # + labels in, loss out
-        if w.kind in ("quant", "qkv_fp8kv", "gelu_bwd", "swiglu_bwd"):
-            return float(b + sum(t.numel() * t.element_size() for t in self.out))
-        if w.kind == "rms_chain":
-            # h2 is written by the first GEMM and read by the second; y is written once
-            return float(b + 2 * (2 * w.M * w.N) + 2 * w.M * w.N2)
-        return float(b + 2 * w.M * w.N)
 
     def run(self, stream=None, d=None, out=None, ws=None):
         """One call; `d`, `out` and `ws` replace the case's own operands, outputs and workspace."""
@@ -826,6 +890,13 @@ def main():
                                           "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS,
                                           "traffic": recorded_traffic(name), "algorithmic_bytes": c.bytes},
                              "unfused_torch_ms": unf, "speedup_vs_unfused": unf / m})
+                if c.w.kind in ("rms_chain", "swiglu"):
+                    one = syn.scaled(c.w, M=1)
+                    rows[-1]["activation_bytes_per_token"] = {
+                        "fused": sum(fused_activation_bytes(one, store_h=False).values()),
+                        "unfused": sum(unfused_activation_bytes(one).values()),
+                        "what": "activation traffic between the GEMM and its consumer per token, weights and "
+                                "the first input / last output excluded (the end-to-end ledger's accounting)"}
             del c
             torch.cuda.empty_cache()
 
