@@ -17,7 +17,8 @@
 //   GELU:   128 output features;
 //   QKV:    one head (128 rows) of the Q, K or V section of the stacked W_qkv (the FP8 K/V form:
 //           K rotated, then K and V as E4M3 with one scale per token and head, max|.|/448 over the
-//           head's 128 values, which takes one more exchange between the cluster's CTAs);
+//           head's 128 values; there each CTA finishes whole tokens, all 128 features of the head,
+//           so the maximum is a shuffle inside the CTA and needs no exchange between the CTAs);
 //   SwiGLU: 64 gate rows and the 64 up rows of the same 64 output features (two TMA boxes), so the
 //           gate and up values of a feature sit in the same tile.
 // Every CTA passes both cluster barriers whatever happens (errors only skip work).
@@ -67,7 +68,8 @@ constexpr int kLdStagesPair = 5;
 __host__ __device__ constexpr int ld_pow2_at_least(int x) { return x <= 1 ? 1 : 2 * ld_pow2_at_least((x + 1) / 2); }
 
 // C CTAs per cluster (1 to 8) split K; the tile's groups of 8 output features are shared out
-// as evenly as 8-feature groups allow (rank r finishes groups [r G / C, (r + 1) G / C)).
+// as evenly as 8-feature groups allow (rank r finishes groups [r G / C, (r + 1) G / C)), except in
+// the FP8 K/V form, where rank r finishes tokens [32 r / C, 32 (r + 1) / C) over every group.
 template <int C, int KIND, int S>
 __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
     linear_decode_kernel(const __grid_constant__ LinearDecodeParams p) {
@@ -78,7 +80,10 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   constexpr int kG = kOut / 8;                // groups of 8 features per tile
   constexpr int kGmax = (kG + C - 1) / C;     // groups per CTA, at most
   constexpr int kP2 = ld_pow2_at_least(kGmax);  // lanes per token: a power of two for the butterflies
-  constexpr int kItems = 32 * kP2;            // (token, group slot) items
+  // FP8 K/V form: (token, group) items of this rank's tokens, a token's 16 groups in 16 lanes
+  constexpr bool kTokSplit = KIND == LD_QKV_FP8KV;
+  constexpr int kTokMax = (32 + C - 1) / C;   // tokens per CTA, at most
+  constexpr int kItems = kTokSplit ? kTokMax * kG : 32 * kP2;  // (token, group slot) items
   constexpr int kIpt = (kItems + 127) / 128;  // items per epilogue thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -86,8 +91,7 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   float* P = reinterpret_cast<float*>(stage_mem);  // [32 tokens][128 W rows] after the stream
   uint8_t* small = smem + S * kLdStageBytes;
   float* inv_freq = reinterpret_cast<float*>(small);            // QKV: [64] hi, [64] lo
-  float* pmax = inv_freq + 128;                                 // FP8 K/V: [32] this CTA's per-token max
-  volatile int* flags = reinterpret_cast<volatile int*>(pmax + 32);  // [0] this CTA ok
+  volatile int* flags = reinterpret_cast<volatile int*>(inv_freq + 160);  // [0] this CTA ok
   uint64_t* bars = reinterpret_cast<uint64_t*>(small + kLdSmallBytes);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + S;
@@ -103,9 +107,12 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   const int f = p.f0 + static_cast<int>(blockIdx.x) / C;  // W-row tile of this cluster
   const int kb0 = static_cast<int>(rank) * p.num_kb / C;
   const int kb1 = (static_cast<int>(rank) + 1) * p.num_kb / C;
-  // this CTA's groups of 8 output features in the tile: [g0, g0 + ng)
-  const int g0 = static_cast<int>(rank) * kG / C;
-  const int ng = (static_cast<int>(rank) + 1) * kG / C - g0;
+  // this CTA's groups of 8 output features in the tile: [g0, g0 + ng) (token split: all of them)
+  const int g0 = kTokSplit ? 0 : static_cast<int>(rank) * kG / C;
+  const int ng = kTokSplit ? kG : (static_cast<int>(rank) + 1) * kG / C - g0;
+  // this CTA's tokens (token split): [tk0, tk1)
+  const int tk0 = kTokSplit ? static_cast<int>(rank) * 32 / C : 0;
+  const int tk1 = kTokSplit ? (static_cast<int>(rank) + 1) * 32 / C : 32;
   // first W row of the tile (SwiGLU: of its gate half, and of its up half in W_up)
   const int wrow = f * (kSwiglu ? 64 : 128);
 
@@ -150,8 +157,20 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   griddep_wait();  // X, the biases and the positions may be written by the preceding kernel
 
   // this thread's items: token t = item / kP2, output features 8 (g0 + gl) .. + 7 of the tile for slot
-  // gl = item % kP2 < ng
+  // gl = item % kP2 < ng; token split: token tk0 + item / kG, features 8 (item % kG) .. + 7
   const int ti = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127, or negative
+  auto item_tg = [&](int item, int& t, int& gl) {
+    if (kTokSplit) {
+      t = tk0 + item / kG;
+      gl = item % kG;
+    } else {
+      t = item / kP2;
+      gl = item % kP2;
+    }
+  };
+  // item < kItems, the token inside this CTA's range, a feature group inside its share; the same
+  // across a warp's lanes of one token (kG and kP2 are powers of two dividing 32)
+  auto item_has = [&](int item, int t, int gl) { return item < kItems && t < tk1 && gl < ng; };
   float bs[kIpt][8], b2s[kIpt][8];
 
   // ---------------------------------------------------------------- phase 1: stream W, partial tile
@@ -211,8 +230,9 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
       const int item = ti + 128 * it;
-      const int gl = item % kP2;
-      const bool in = item < kItems && gl < ng;
+      int t, gl;
+      item_tg(item, t, gl);
+      const bool in = item_has(item, t, gl);
       const int j = (g0 + (gl < ng ? gl : 0)) * 8;  // feature within the tile
       const int n = (kSwiglu ? f * 64 : f * 128) + j;        // W row (SwiGLU: output feature)
       const int lim = kQkv ? p.num_f * 128 : p.n_out;  // entries of the bias vectors
@@ -262,39 +282,74 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   const int width = !kQkv || sec == 0 ? p.n_out : p.kv_width;
   const bool fp8 = KIND == LD_QKV_FP8KV && sec > 0;  // the same for every CTA of the cluster
   const bool ok = all != 0;
+  // The C partials of item `it` (token t, features j..j+7 of the tile) from every rank's P, in
+  // flight at once (SwiGLU: the gate rows j.., and the up rows 64 + j..).
+  constexpr int kCu = kSwiglu ? C : 1;
+  float4 xa[kIpt][C], xb[kIpt][C], ya[kIpt][kCu], yb[kIpt][kCu];
+  auto load_item = [&](int it, int t, int j) {
+    const uint32_t la = smem_u32(P + t * 128 + j);
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const uint32_t ra = C > 1 ? mapa_shared(la, static_cast<uint32_t>(c)) : la;
+      xa[it][c] = C > 1 ? ld_dsmem_f4(ra) : *reinterpret_cast<const float4*>(P + t * 128 + j);
+      xb[it][c] = C > 1 ? ld_dsmem_f4(ra + 16) : *reinterpret_cast<const float4*>(P + t * 128 + j + 4);
+      if constexpr (kSwiglu) {
+        ya[it][c] = C > 1 ? ld_dsmem_f4(ra + 256) : *reinterpret_cast<const float4*>(P + t * 128 + 64 + j);
+        yb[it][c] = C > 1 ? ld_dsmem_f4(ra + 272) : *reinterpret_cast<const float4*>(P + t * 128 + 68 + j);
+      }
+    }
+  };
+  // FP8 K/V form: cluster barrier B is split.  Every item's partials are loaded first; the
+  // barrier's first half then says this CTA has read everything it needs from its peers' P (the
+  // loads have returned before the release), and its second half, before the CTA leaves, keeps
+  // its own P alive until every peer has read it, with the epilogue and the stores in between.
+  // The other kinds load each item's partials just before its epilogue and keep the whole barrier
+  // at the end.  (Measured, 20 back-to-back calls, 5 alternating runs on one box: FP8 K/V
+  // 32 x 6144 x 4096 12.06 us against 12.60 with the feature split and one barrier more; QKV
+  // 32 x 12288 x 4096 is slower split, 21.0 against 19.4, and 19.3 against 19.0 with the loads
+  // of both its items ahead of the epilogue.)
+  constexpr bool kSplitB = kTokSplit && C > 1;
+  if constexpr (kSplitB) {
+    if (ti >= 0 && ok) {
+#pragma unroll
+      for (int it = 0; it < kIpt; ++it) {
+        const int item = ti + 128 * it;
+        int t, gl;
+        item_tg(item, t, gl);
+        if (item_has(item, t, gl)) load_item(it, t, (g0 + gl) * 8);
+      }
+    }
+    __syncwarp();
+    cluster_arrive_release();
+  }
+
+  // Sums in rank order, epilogue, stores.
   float y[kIpt][8];
   if (ti >= 0) {
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
       const int item = ti + 128 * it;
-      const int t = item / kP2, gl = item % kP2;
-      const bool has = item < kItems && gl < ng;  // item < kItems is the same across a warp
+      int t, gl;
+      item_tg(item, t, gl);
+      const bool has = item_has(item, t, gl);
       const int j = (g0 + (gl < ng ? gl : 0)) * 8;  // first output feature within the tile
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[it][e] = 0.f;
       if (has && ok) {
-        // sums of the C partials in rank order (SwiGLU: the gate rows j.., and the up rows 64 + j..)
+        if constexpr (!kSplitB) load_item(it, t, j);
         float s[8], s2[8];
-        const uint32_t la = smem_u32(P + t * 128 + j);
-        float4 xa[C], xb[C], ya[C], yb[C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-          const uint32_t ra = C > 1 ? mapa_shared(la, static_cast<uint32_t>(c)) : la;
-          xa[c] = C > 1 ? ld_dsmem_f4(ra) : *reinterpret_cast<const float4*>(P + t * 128 + j);
-          xb[c] = C > 1 ? ld_dsmem_f4(ra + 16) : *reinterpret_cast<const float4*>(P + t * 128 + j + 4);
-          if (kSwiglu) {
-            ya[c] = C > 1 ? ld_dsmem_f4(ra + 256) : *reinterpret_cast<const float4*>(P + t * 128 + 64 + j);
-            yb[c] = C > 1 ? ld_dsmem_f4(ra + 272) : *reinterpret_cast<const float4*>(P + t * 128 + 68 + j);
-          }
+        float4 a = xa[it][0], b = xb[it][0], u = make_float4(0.f, 0.f, 0.f, 0.f), v = u;
+        if constexpr (kSwiglu) {
+          u = ya[it][0];
+          v = yb[it][0];
         }
-        float4 a = xa[0], b = xb[0], u = ya[0], v = yb[0];
 #pragma unroll
         for (int c = 1; c < C; ++c) {
-          a.x += xa[c].x; a.y += xa[c].y; a.z += xa[c].z; a.w += xa[c].w;
-          b.x += xb[c].x; b.y += xb[c].y; b.z += xb[c].z; b.w += xb[c].w;
-          if (kSwiglu) {
-            u.x += ya[c].x; u.y += ya[c].y; u.z += ya[c].z; u.w += ya[c].w;
-            v.x += yb[c].x; v.y += yb[c].y; v.z += yb[c].z; v.w += yb[c].w;
+          a.x += xa[it][c].x; a.y += xa[it][c].y; a.z += xa[it][c].z; a.w += xa[it][c].w;
+          b.x += xb[it][c].x; b.y += xb[it][c].y; b.z += xb[it][c].z; b.w += xb[it][c].w;
+          if constexpr (kSwiglu) {
+            u.x += ya[it][c].x; u.y += ya[it][c].y; u.z += ya[it][c].z; u.w += ya[it][c].w;
+            v.x += yb[it][c].x; v.y += yb[it][c].y; v.z += yb[it][c].z; v.w += yb[it][c].w;
           }
         }
         s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w; s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
@@ -323,14 +378,33 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
         }
       }
       if (fp8) {
-        // this CTA's max |y| of token t over its features: a butterfly over the token's kP2 lanes
-        // (slots past ng hold zeros)
-        float am = 0.f;
+        // the head's max |y| of token t: a butterfly over the token's kG lanes, which hold all 128
+        // features of the head (lanes without an item hold zeros); then scale and codes
+        float amax = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(y[it][e]));
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[it][e]));
 #pragma unroll
-        for (int o = kP2 / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        if (item < kItems && gl == 0) pmax[t] = am;
+        for (int o = kG / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float qs = amax > 0.f ? 448.f / amax : 0.f;
+        const int col = col_base + j;
+        if (has && ok && t < p.M) {
+          if (gl == 0) p.kv_scale[sec - 1][static_cast<size_t>(t) * p.lds + col_base / 128] = amax * (1.f / 448.f);
+          if (col < width) {
+            uint32_t w[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              w[k] = f32x2_to_e4m3x2(fmaf(y[it][4 * k], qs, 0.f), fmaf(y[it][4 * k + 1], qs, 0.f)) |
+                     (f32x2_to_e4m3x2(fmaf(y[it][4 * k + 2], qs, 0.f), fmaf(y[it][4 * k + 3], qs, 0.f)) << 16);
+            uint8_t* dst = p.out_kv[sec - 1] + static_cast<size_t>(t) * p.ldkv + col;
+            if (col + 8 <= width) {  // 8-byte aligned: ldkv % 16 == 0, col % 8 == 0
+              *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (col + e < width) dst[e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+            }
+          }
+        }
       }
       if (!fp8 && has && ok) {
         const int col = col_base + j;
@@ -353,49 +427,11 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
       }
     }
   }
-  if (KIND == LD_QKV_FP8KV && fp8) {
-    // FP8 K/V: the head's max over every CTA of the cluster, then scale and codes
-    __syncwarp();
-    if (C > 1) cluster_sync_all();
-    else __syncthreads();
-    if (ti >= 0 && ok) {
-#pragma unroll
-      for (int it = 0; it < kIpt; ++it) {
-        const int item = ti + 128 * it;
-        const int t = item / kP2, gl = item % kP2;
-        if (item >= kItems || gl >= ng) continue;
-        const int j = (g0 + gl) * 8;
-        float amax = 0.f;
-#pragma unroll
-        for (int c = 0; c < C; ++c)
-          amax = fmaxf(amax, C > 1 ? ld_dsmem_f32(mapa_shared(smem_u32(pmax + t), static_cast<uint32_t>(c))) : pmax[t]);
-        const float qs = amax > 0.f ? 448.f / amax : 0.f;
-        const int col = col_base + j;
-        if (t < p.M) {
-          if (rank == 0 && gl == 0)
-            p.kv_scale[sec - 1][static_cast<size_t>(t) * p.lds + col_base / 128] = amax * (1.f / 448.f);
-          if (col < width) {
-            uint32_t w[2];
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              w[k] = f32x2_to_e4m3x2(fmaf(y[it][4 * k], qs, 0.f), fmaf(y[it][4 * k + 1], qs, 0.f)) |
-                     (f32x2_to_e4m3x2(fmaf(y[it][4 * k + 2], qs, 0.f), fmaf(y[it][4 * k + 3], qs, 0.f)) << 16);
-            uint8_t* dst = p.out_kv[sec - 1] + static_cast<size_t>(t) * p.ldkv + col;
-            if (col + 8 <= width) {  // 8-byte aligned: ldkv % 16 == 0, col % 8 == 0
-              *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (col + e < width) dst[e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
-            }
-          }
-        }
-      }
-    }
-  }
-  // Cluster barrier B: every read of a peer's P is done before any CTA of the cluster leaves.
+  // Cluster barrier B (its second half in the FP8 K/V form): every peer has read this CTA's P
+  // before it leaves.
   __syncwarp();
-  if (C > 1) cluster_sync_all();
+  if (kSplitB) cluster_wait_acquire();
+  else if (C > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 32);

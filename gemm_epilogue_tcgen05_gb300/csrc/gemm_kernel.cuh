@@ -326,7 +326,6 @@ struct SavedRing {
     const uint32_t b = issued & 1u;
     fence_async_smem();  // the warp's reads of this buffer come before the copy's writes
     mbar_arrive_expect_tx(&bar[b], NS * kSavedBoxBytes);
-#pragma unroll
     const uint64_t pol = l2_policy_evict_first();
 #pragma unroll
     for (int t = 0; t < NS; ++t) tma_load_2d_to_hint(&maps[t], &bar[b], box(issued, t), x, y, pol);
