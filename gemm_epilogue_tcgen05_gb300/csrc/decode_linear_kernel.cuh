@@ -33,7 +33,13 @@ constexpr int kLdTokens = 32;                   // MMA N: the tokens
 constexpr int kLdStages = 10;
 constexpr int kLdABytes = 128 * kBK * 2;        // W rows of the tile
 constexpr int kLdStageBytes = kLdABytes + kLdTokens * kBK * 2;
-constexpr int kLdL2PrefetchUnits = 16;          // W k blocks pulled into L2 before griddepcontrol.wait
+// W k blocks a CTA pulls into L2 before griddepcontrol.wait.  Measured per call (3 alternating runs on
+// one box, us; back to back in a graph / interleaved with another kernel / single launch), window 8
+// against 16: QKV + FP8 K/V 32 x 6144 x 4096 12.15 / 12.88 / 20.1 against 12.02 / 13.72 / 20.8, QKV
+// 32 x 12288 x 4096 18.4 / 20.6 / 29.1 against 19.0 / 22.5 / 30.4, GELU 32 x 16384 x 4096 22.6 / 23.3
+// / 31.4 against 22.3 / 23.8 / 31.7, SwiGLU 32 x 14336 x 4096 35.6 / 38.7 / 48.1 against 37.4 / 39.8 /
+// 48.5.  A deep window competes with the call's own stream when no earlier call is left to overlap.
+constexpr int kLdL2PrefetchUnits = 8;
 
 struct alignas(128) LinearDecodeParams {
   CUtensorMap map_w;   // W [rows, K] bf16, box {64, 128}; SwiGLU: W_gate, box {64, 64}
