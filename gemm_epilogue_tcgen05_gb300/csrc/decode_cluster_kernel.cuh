@@ -12,10 +12,12 @@
 //     to the cluster leader's shared memory, and every other CTA of the cluster leaves, so
 //     the SMs free up for the next kernel on the stream;
 //   * the leaders publish their cluster's per-token partials ("GEMM Epilogue 完全拆解",
-//     §模式 A: the tile-local half of the two-level row reduction), wait for a grid-wide
-//     count (bounded spin; every cluster is resident, the host checks), merge the num_f
-//     partials per token and write the E4M3 codes and the per-token scale
-//     (§仿射量化与尾声的五步).
+//     §模式 A: the tile-local half of the two-level row reduction), each value in a 64-bit word
+//     tagged with the call's epoch, and count themselves on a grid-wide counter; every leader
+//     polls all num_f partials of its tokens and the count at once (bounded; every cluster is
+//     resident, the host checks) until each carries this call's epoch and the count is full, so
+//     the wait and the loads are one round trip, then merges them per token in a fixed order and
+//     writes the E4M3 codes and the per-token scale (§仿射量化与尾声的五步).
 // Every CTA passes the cluster barriers it shares with its peers whatever happens (errors only
 // skip work), so a timed-out wait can never leave a peer blocked at a barrier.
 #pragma once
@@ -103,6 +105,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();  // X, Z, gamma, b and the workspace may be written by the preceding kernel
+  // this call's epoch (leaders): one more than the previous call's, which the last leader of that
+  // call stored after every leader had read it
+  const unsigned epoch = rank == 0 && threadIdx.x >= 32 ? ld_relaxed_u32(p.epoch) + 1u : 0u;
 
   // Residual, bias and gamma of the epilogue threads' reduce items (phase 2): loaded by the
   // epilogue warps while the weights stream, so none of their latency is left for the tail.
@@ -305,48 +310,72 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
 #pragma unroll
       for (int k = 0; k < 8; ++k) load_bf16x4(p.gamma, n + 4 * k, p.N, *reinterpret_cast<float(*)[4]>(gq + 4 * k));
     }
+    const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
     if (warp == 1 && cl_ok) {
-      // the MMA warp is idle now: it merges the ranks' partials (lane = token), publishes them
-      // and waits for the grid-wide count while the epilogue warps load gamma
+      // the MMA warp is idle now: it merges the ranks' partials (lane = token) and publishes
+      // them, each value with the epoch in the same 64-bit word, while the epilogue warps load gamma
       float ss = 0.f, am = 0.f;
       for (int j = 0; j < C; ++j) {  // rank order: deterministic
         const float2 v = Sall[j * 32 + lane];
         ss += v.x;
         am = fmaxf(am, v.y);
       }
-      __stcg(p.stats + static_cast<size_t>(f) * kDecTokens + lane, make_float2(ss, am));
+      unsigned long long* rec = p.recs + (static_cast<size_t>(f) * kDecTokens + lane) * 2;
+      st_relaxed_u64(rec, tag | __float_as_uint(ss));
+      st_relaxed_u64(rec + 1, tag | __float_as_uint(am));
       __syncwarp();
-      if (lane == 0) {
-        // the warp's stores are ordered before this release by the warp barrier, so the count
-        // publishes them
-        red_release_add_u32(p.counters + p.num_f, 1u);
-        flags[1] = spin_until(p.counters + p.num_f, static_cast<unsigned>(p.num_f), p.status, p.timeout_ns,
-                              p.status, W_DECODE_ROWS, p.num_f)
-                       ? 1
-                       : 0;
-      }
+      if (lane == 0) red_release_add_u32(p.counters + p.num_f, 1u);
     }
-    __syncthreads();
-    const bool finish = flags[1] != 0;
 
     // ---------------------------------------------------------------- phase 4: merge statistics, quantise (leader)
-    if (finish && ti >= 0) {
-      // The four threads of token tq each merge every fourth cluster's partial (fixed order),
-      // then combine by a butterfly, so all four hold the same bits.
-      float SS = 0.f, A = 0.f;
-      for (int cb = ti & 3; cb < p.num_f; cb += 32) {  // 8 loads in flight
-        float2 w[8];
+    // The four threads of token tq each merge every fourth cluster's partial (fixed order), then
+    // combine by a butterfly, so all four hold the same bits.  Each group of 8 partials, and the
+    // count, is polled until all carry this call's epoch and the count is full (a cluster that
+    // failed publishes nothing, and every wait gives up once a failure is recorded).
+    float SS = 0.f, A = 0.f;
+    bool ready = true;
+    if (ti >= 0) {
+      ready = cl_ok;
+      const uint64_t t0 = global_timer_ns();
+      for (int cb = ti & 3; cb < p.num_f && ready; cb += 32) {
+        for (uint32_t i = 0;; ++i) {
+          unsigned long long w[8][2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c = cb + 4 * j;
-          w[j] = c < p.num_f ? __ldcg(p.stats + static_cast<size_t>(c) * kDecTokens + tq) : make_float2(0.f, 0.f);
-        }
+          for (int j = 0; j < 8; ++j) {
+            const int c = cb + 4 * j;
+            const unsigned long long* rec = p.recs + (static_cast<size_t>(c) * kDecTokens + tq) * 2;
+            w[j][0] = c < p.num_f ? ld_relaxed_u64(rec) : tag;
+            w[j][1] = c < p.num_f ? ld_relaxed_u64(rec + 1) : tag;
+          }
+          bool all = ld_relaxed_u32(p.counters + p.num_f) == static_cast<unsigned>(p.num_f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          SS += w[j].x;
-          A = fmaxf(A, w[j].y);
+          for (int j = 0; j < 8; ++j) all = all && (w[j][0] >> 32) == epoch && (w[j][1] >> 32) == epoch;
+          if (all) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (cb + 4 * j >= p.num_f) continue;  // past the last tile: contributes nothing
+              SS += __uint_as_float(static_cast<uint32_t>(w[j][0]));
+              A = fmaxf(A, __uint_as_float(static_cast<uint32_t>(w[j][1])));
+            }
+            break;
+          }
+          if ((i & 15u) == 15u) {
+            if (*reinterpret_cast<const volatile int*>(p.status + ST_CODE) != 0) {
+              ready = false;
+              break;
+            }
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+              record_failure(p.status, W_DECODE_ROWS, p.num_f);
+              ready = false;
+              break;
+            }
+          }
+          __nanosleep(32);
         }
       }
+    }
+    const bool finish = __syncthreads_and(ready ? 1 : 0) != 0;
+    if (finish && ti >= 0) {
 #pragma unroll
       for (int o = 1; o < 4; o <<= 1) {
         SS += __shfl_xor_sync(0xffffffffu, SS, o);
@@ -376,12 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
       }
     }
     if (threadIdx.x == 64 && finish) {
-      // the last leader to leave resets the counters for the next call (this thread passed the
-      // count itself, so every leader has read it once the leavers are complete)
+      // the last leader to leave resets the counters for the next call and stores this call's
+      // epoch (every leader has read the count and the previous epoch once the leavers are complete)
       const unsigned old = atomicAdd(p.counters + p.num_f + 1, 1u);
       if (old + 1u == static_cast<unsigned>(p.num_f)) {
         p.counters[p.num_f] = 0u;
         p.counters[p.num_f + 1] = 0u;
+        *p.epoch = epoch;
       }
     }
   }

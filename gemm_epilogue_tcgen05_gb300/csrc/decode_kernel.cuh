@@ -59,8 +59,13 @@ struct alignas(128) DecodeParams {
   long long ldh;
   float* partials;    // [grid][seg_max][128 features][32 tokens]
   float* hbuf;        // [num_f][32 tokens][128 features]
-  float2* stats;      // [num_f][32 tokens]
+  float2* stats;      // [num_f][32 tokens] (flat kernel)
   unsigned* counters; // [num_f] k-block arrivals, then finished tiles, then finishers that left
+  // Cluster kernel: per (feature tile, token) the tile's sum of h^2 and max |h * gamma|, each in a
+  // 64-bit word whose high half is the call's epoch ([num_f][32 tokens][2]), and the workspace's
+  // epoch word (the previous call's epoch; this call's is one more).
+  unsigned long long* recs;
+  unsigned* epoch;
   int* status;
   unsigned long long timeout_ns;
 };

@@ -18,9 +18,13 @@ namespace {
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Byte offset, inside the status area at the workspace's start, of the decode epoch word (a fixed
+// place whatever the shape, past the status words that fl_check_device_status reads and clears).
+constexpr size_t kEpochOffset = 128;
+
 struct WsLayout {
   bool decode;
-  size_t counters, partials, hbuf, stats, total;  // byte offsets (total = size); the status record is at 0
+  size_t counters, recs, partials, hbuf, stats, total;  // byte offsets (total = size); the status record is at 0
   int grid, seg_max;                              // decode only
   bool units_ok;                                  // decode unit indices fit 32-bit arithmetic
 };
@@ -128,7 +132,8 @@ WsLayout layout(int M, int N, int K, int num_sms) {
       }
     }
     w.counters = kWsStatusBytes;
-    w.partials = w.counters + align_up(static_cast<size_t>(num_f + 2) * sizeof(unsigned));
+    w.recs = w.counters + align_up(static_cast<size_t>(num_f + 2) * sizeof(unsigned));
+    w.partials = w.recs + align_up(static_cast<size_t>(num_f) * kDecTokens * 2 * sizeof(unsigned long long));
     w.hbuf = w.partials + align_up(static_cast<size_t>(w.grid) * w.seg_max * 128 * kDecTokens * sizeof(float));
     w.stats = w.hbuf + align_up(static_cast<size_t>(num_f) * kDecTokens * 128 * sizeof(float));
     w.total = w.stats + align_up(static_cast<size_t>(num_f) * kDecTokens * sizeof(float2));
@@ -184,7 +189,7 @@ int rmsnorm_fp8_enqueue(const void* X, const void* W, const void* b, const void*
   PreLaunchClear clear;
   if (scratch_mode) {
     clear.ptr = ws;
-    clear.bytes = wl.partials;  // status record and counters
+    clear.bytes = wl.partials;  // status area (with the decode epoch word), counters and decode records
   }
 
   if (wl.decode) {
@@ -217,6 +222,8 @@ int rmsnorm_fp8_enqueue(const void* X, const void* W, const void* b, const void*
     p.partials = reinterpret_cast<float*>(ws + wl.partials);
     p.hbuf = reinterpret_cast<float*>(ws + wl.hbuf);
     p.stats = reinterpret_cast<float2*>(ws + wl.stats);
+    p.recs = reinterpret_cast<unsigned long long*>(ws + wl.recs);
+    p.epoch = reinterpret_cast<unsigned*>(ws + kEpochOffset);
     p.status = status;
     p.timeout_ns = wait_timeout_ns();
     switch (pick_decode_cluster(di, p.num_f, p.num_kb, decode_sms(di))) {

@@ -350,6 +350,14 @@ def _rms_case(M, N, K, bias, seed=0):
     return X, W, b, Z, g
 
 
+def _assert_ws_reset(ws, M, N):
+    """After a call the workspace's status words and the counters the kernels wait on are zero
+    again (the decode kernels' epoch word, at byte 128 of the status area, counts calls)."""
+    assert torch.count_nonzero(ws[:32]) == 0, "status record set"
+    n = 4 * (-(-N // 128) + 2) if M <= 32 else 8 * -(-M // 128)
+    assert torch.count_nonzero(ws[256:256 + n]) == 0, "counters not reset"
+
+
 def _rms_run(X, W, b, Z, g, ldq=None, workspace=None):
     M, N = Z.shape
     Yq = None
@@ -392,7 +400,7 @@ def test_rmsnorm_fp8_decode_flat_kernel_under_cta_cap():
         ws = fl.rmsnorm_fp8_workspace(M, N, K)
         q, s = _rms_run(X, W, b, Z, g, workspace=ws)
         assert_fp8_close(q, s, q_ref, s_ref, f"cap {cap}")
-        assert torch.count_nonzero(ws[:512]) == 0, "status or counters not reset"
+        _assert_ws_reset(ws, M, N)
     fl.set_max_ctas(0)
 
 
@@ -407,7 +415,7 @@ def test_rmsnorm_fp8_workspace_reuse_and_few_ctas():
         q2, s2 = _rms_run(X, W, b, Z, g, workspace=ws)
         fl.set_max_ctas(0)
         assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
-        assert torch.count_nonzero(ws[:512]) == 0, "status or counters not reset"
+        _assert_ws_reset(ws, M, 2048)
         q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), f64(b), f64(Z), f64(g), 1e-6)
         assert_fp8_close(q1, s1, q_ref, s_ref, f"reuse M={M}")
 
@@ -449,7 +457,31 @@ def test_rmsnorm_fp8_decode_back_to_back_shared_workspace(graph):
     for i, ((Yq, rs), j) in enumerate(zip(outs, order)):
         q_ref, s_ref, _ = refs[j]
         assert_fp8_close(Yq.cpu().numpy(), rs.cpu().numpy().astype(np.float64), q_ref, s_ref, f"call {i} (set {j})")
-    assert torch.count_nonzero(ws[:512]) == 0, "status or counters not reset"
+    _assert_ws_reset(ws, M, N)
+
+
+def test_rmsnorm_fp8_decode_workspace_shared_across_shapes_and_kernels():
+    """One workspace serves decode calls of different widths (so different numbers of feature
+    tiles, whose per-tile statistics share the same records) and of both decode kernels (the
+    flat one under a CTA cap), in an order where a stale record of an earlier call sits where the
+    next call looks: every call's codes and scales match its own oracle result."""
+    M, K = 24, 512
+    cases = {N: _rms_case(M, N, K, True, seed=20 + N // 1024) for N in (4096, 2048, 3072)}
+    refs = {N: oracle.rmsnorm_fp8(f64(X), f64(W), f64(b), f64(Z), f64(g), 1e-6) for N, (X, W, b, Z, g) in cases.items()}
+    fl.set_max_ctas(16)
+    size = max(fl.rmsnorm_fp8_workspace_bytes(M, N, K) for N in cases)
+    fl.set_max_ctas(0)
+    size = max([size] + [fl.rmsnorm_fp8_workspace_bytes(M, N, K) for N in cases])
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for N, cap in ((4096, 0), (2048, 0), (4096, 0), (3072, 16), (2048, 0), (4096, 16), (3072, 0), (4096, 0)):
+        fl.set_max_ctas(cap)
+        X, W, b, Z, g = cases[N]
+        q, s = _rms_run(X, W, b, Z, g, workspace=ws)
+        q_ref, s_ref, _ = refs[N]
+        assert_fp8_close(q, s, q_ref, s_ref, f"N={N} cap={cap}")
+        assert fl.check_device_status(ws) == fl.FL_OK
+        _assert_ws_reset(ws, M, N)
+    fl.set_max_ctas(0)
 
 
 def test_rmsnorm_fp8_prefill_full_workload_sampled():
