@@ -1132,7 +1132,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
                 for (int j = 0; j < 32; ++j) v[j] *= b[j];
               }
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] *= qs;
+              for (int j = 0; j < 32; ++j) v[j] = fmaf(v[j], qs, 0.f);  // + 0: a zero block codes as +0
               stage_fp8_32(buf, lane, u, v);
             }
             ring.commit(&p.map_out[0], buf, lane, n0 + blk * 128, y_box);
@@ -1190,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
 #pragma unroll
                   for (int e = 0; e < 4; ++e) {
                     const int j = 16 * h + 8 * i + 2 * e;
-                    word |= f32x2_to_e2m1x2(v[j] * inv, v[j + 1] * inv) << (8 * e);
+                    word |= f32x2_to_e2m1x2(fmaf(v[j], inv, 0.f), fmaf(v[j + 1], inv, 0.f)) << (8 * e);  // +0 as above
                   }
                   w[2 * h + i] = word;
                 }

@@ -1,0 +1,129 @@
+"""Degenerate inputs the method defines, on the GPU, through the C ABI, against the fp64 oracle:
+rows, heads and blocks whose maximum is zero (scale 0 and zero codes), K = 0 (the Linear output is
+the bias alone), and empty problems (M = 0 or N = 0) for every entry point (nothing is written)."""
+import numpy as np
+import pytest
+import torch
+
+import gemm_epilogue_tcgen05_gb300 as fl
+import oracle
+import synthetic as syn
+from parity_utils import assert_bf16_close, assert_fp8_close, assert_quant_close, dev_bf16, f64, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    fl.set_max_ctas(0)
+    fl.set_cta_pairing(True)
+    yield
+    fl.set_max_ctas(0)
+    fl.set_cta_pairing(True)
+    assert fl.device_status() == fl.FL_OK
+
+
+def _draw(shape, stream, std=1.0, mean=0.0, seed=0):
+    return syn.draw(seed, stream, shape, mean, std, "bf16")
+
+
+@pytest.mark.parametrize("M,N,K,cap", [(300, 1024, 256, 0), (24, 4096, 512, 0), (24, 4096, 512, 16)])
+def test_rmsnorm_fp8_zero_row_gets_zero_scale_and_codes(M, N, K, cap):
+    """A row whose h = X W^T + Z is all zero has maximum 0: scale 0 and all codes 0 (prefill, the
+    cluster decode kernel and, under a CTA cap, the flat one); the other rows are the oracle's."""
+    fl.set_max_ctas(cap)
+    X = _draw((M, K), syn.STREAM_X, seed=8)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=8)
+    Z = _draw((M, N), syn.STREAM_Z, seed=8)
+    g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0, seed=8)
+    zr = [0, M // 2, M - 1]
+    X[zr] = 0
+    Z[zr] = 0
+    q, s = fl.fused_linear_residual_rmsnorm_fp8(dev_bf16(X), dev_bf16(W), None, dev_bf16(Z), dev_bf16(g), 1e-6,
+                                                workspace=fl.rmsnorm_fp8_workspace(M, N, K))
+    q, s = q.cpu().numpy(), s.cpu().numpy().astype(np.float64)
+    assert not q[zr].any() and not s[zr].any()
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(f64(X), f64(W), None, f64(Z), f64(g), 1e-6)
+    assert_fp8_close(q, s, q_ref, s_ref, f"zero rows {M}x{N}x{K} cap {cap}")
+
+
+@pytest.mark.parametrize("M", [40, 5])
+def test_rmsnorm_fp8_and_h_out_with_k_zero(M):
+    """K = 0: h = b + Z; codes, scales and h_out against the oracle."""
+    N = 512
+    b = _draw((N,), syn.STREAM_B, 0.5, seed=9)
+    Z = _draw((M, N), syn.STREAM_Z, seed=9)
+    g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0, seed=9)
+    Xe = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
+    We = torch.empty((N, 0), dtype=torch.bfloat16, device="cuda")
+    q, s, h = fl.fused_linear_residual_rmsnorm_fp8(Xe, We, dev_bf16(b), dev_bf16(Z), dev_bf16(g), 1e-6, h_out=True)
+    h_ref = f64(b)[None, :] + f64(Z)
+    assert_bf16_close(host(h), h_ref, f"h_out K=0 M={M}")
+    q_ref, s_ref, _ = oracle.rmsnorm_fp8(np.zeros((M, 0)), np.zeros((N, 0)), f64(b), f64(Z), f64(g), 1e-6)
+    assert_fp8_close(q.cpu().numpy(), s.cpu().numpy().astype(np.float64), q_ref, s_ref, f"K=0 M={M}")
+
+
+@pytest.mark.parametrize("M", [257, 7])
+def test_qkv_fp8kv_zero_token_gets_zero_scales_and_codes(M):
+    """A token whose projection is all zero (zero input row, no bias) has head maxima 0: every K and
+    V scale 0 and every code 0, prefill and decode."""
+    H, Hkv, D, K = 4, 2, 128, 256
+    X = _draw((M, K), syn.STREAM_X, seed=10)
+    X[[0, M - 1]] = 0
+    Wq = _draw(((H + 2 * Hkv) * D, K), syn.STREAM_W, K ** -0.5, seed=10)
+    Q, Kq, Vq, ks, vs = fl.fused_qkv_rope_fp8kv(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, n_kv_heads=Hkv,
+                                                head_dim=D, seq_len=64)
+    for t in (Kq, Vq, ks, vs, Q):
+        assert torch.count_nonzero(t[0]) == 0 and torch.count_nonzero(t[M - 1]) == 0
+    ref = oracle.qkv_rope_kv_fp8(f64(X), f64(Wq), None, H, Hkv, D, 10000.0, np.arange(M) % 64)
+    assert_fp8_close(Kq.cpu().numpy(), ks.cpu().numpy().astype(np.float64), ref["kq"], ref["ks"], f"K M={M}")
+    assert_fp8_close(Vq.cpu().numpy(), vs.cpu().numpy().astype(np.float64), ref["vq"], ref["vs"], f"V M={M}")
+    assert_bf16_close(host(Q), ref["q"], f"Q M={M}")
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_quant_smoothing_zero_factors_give_zero_blocks(fmt):
+    """Inverse smoothing factors that are zero over a whole block make that block's maximum 0: scale
+    0 and zero codes; partly zero blocks keep the oracle's scale and codes."""
+    M, N, K = 130, 512, 96
+    X = _draw((M, K), syn.STREAM_X, seed=11)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=11)
+    b = _draw((N,), syn.STREAM_B, 0.5, seed=11)
+    inv = syn.draw_inv_smooth(11, N)
+    bs = {0: 128, 1: 32, 2: 16}[fmt]
+    inv[:bs] = 0.0          # the first block of every row: all zero
+    inv[bs + 3:bs + 7] = 0  # part of the second block
+    Yq, S = fl.fused_linear_quant(dev_bf16(X), dev_bf16(W), dev_bf16(b), fmt, inv_smooth=torch.from_numpy(inv).cuda())
+    Yq, S = Yq.cpu().numpy(), S.cpu().numpy()
+    assert not S[:, 0].any()
+    assert not Yq[:, :bs if fmt == 0 else bs // 2].any()
+    q_ref, s_ref, y_ref = oracle.linear_quant(f64(X), f64(W), f64(b), fmt, inv_smooth=inv.astype(np.float64))
+    e2m1 = np.array([oracle.e2m1_decode(c) for c in range(16)])
+    dec = {"scale": lambda c: oracle.e4m3_decode(c)}
+    dec["value"] = (lambda c: oracle.e4m3_decode(c)) if fmt == 0 else (
+        (lambda c: np.where(c & 8, c.astype(np.int32) - 16, c).astype(np.float64)) if fmt == 1 else (lambda c: e2m1[c]))
+    assert_quant_close(fmt, Yq, S, q_ref, s_ref, y_ref, dec, f"zero smoothing block fmt {fmt}")
+
+
+def test_every_entry_point_accepts_empty_problems():
+    """M = 0 (or N = 0 where the call has one) returns FL_OK and writes nothing."""
+    dev = "cuda"
+    lib = fl.load()
+    sentinel = torch.full((64,), 7, dtype=torch.uint8, device=dev)
+    p = sentinel.data_ptr()
+    a = None
+    # M = 0 through the C ABI, with real (untouched) output pointers
+    st = [
+        lib.fused_linear_gelu(a, a, a, p, 0, 64, 64, 64, 64, 64, fl.FL_BF16, fl.FL_GELU_TANH, None),
+        lib.fused_swiglu(a, a, a, a, a, p, 0, 64, 64, 64, 64, 64, None),
+        lib.fused_linear_quant(a, a, a, a, p, p, 0, 64, 64, 64, 64, 64, 1, 0, None),
+        lib.fused_dgrad_gelu(a, a, a, p, 0, 64, 64, 64, 64, 64, 64, fl.FL_GELU_TANH, None),
+        lib.fused_swiglu_bwd(a, a, a, a, p, 0, 64, 64, 64, 64, 64, 128, None),
+        lib.fused_linear_residual_rmsnorm_fp8(a, a, a, a, a, 1e-6, p, p, p, 0, 64, 64, 64, 64, 64, 64, a, 0, None),
+        lib.fused_linear_residual_rmsnorm_fp8(a, a, a, a, a, 1e-6, p, p, p, 8, 0, 64, 64, 64, 64, 64, a, 0, None),
+        lib.fused_linear_cross_entropy(a, a, a, a, p, a, 0, 64, 64, 64, 64, 0, a, 0, None),
+        lib.fused_qkv_rope(a, a, a, p, p, p, a, 0, 64, 2, 128, 16, 1e4, 64, 64, 256, None),
+    ]
+    assert st == [fl.FL_OK] * len(st), st
+    torch.cuda.synchronize()
+    assert torch.all(sentinel == 7)
