@@ -390,8 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
         for (int k = 0; k < 8; ++k) {
           const float4 hv = *reinterpret_cast<const float4*>(H + tq * 128 + c0 + 4 * k);
           const float* gg = gq + 4 * k;
-          w[k] = f32x2_to_e4m3x2(hv.x * gg[0] * qs, hv.y * gg[1] * qs) |
-                 (f32x2_to_e4m3x2(hv.z * gg[2] * qs, hv.w * gg[3] * qs) << 16);
+          // + 0: a zero row codes as +0 whatever the sign of gamma
+          w[k] = f32x2_to_e4m3x2(fmaf(hv.x * gg[0], qs, 0.f), fmaf(hv.y * gg[1], qs, 0.f)) |
+                 (f32x2_to_e4m3x2(fmaf(hv.z * gg[2], qs, 0.f), fmaf(hv.w * gg[3], qs, 0.f)) << 16);
         }
         uint8_t* dst = p.yq + static_cast<size_t>(tq) * p.ldq + n;
         if (n + 32 <= p.N) {  // 16-byte aligned: ldq % 16 == 0, n % 32 == 0

@@ -500,8 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_kernel(const _
           const int t = (ti >> 5) + 4 * k;
           if (t >= p.M) continue;
           const float qs = qs_s[t];
-          const uint32_t w = f32x2_to_e4m3x2(hv[k].x * g4[0] * qs, hv[k].y * g4[1] * qs) |
-                             (f32x2_to_e4m3x2(hv[k].z * g4[2] * qs, hv[k].w * g4[3] * qs) << 16);
+          // + 0: a zero row codes as +0 whatever the sign of gamma
+          const uint32_t w = f32x2_to_e4m3x2(fmaf(hv[k].x * g4[0], qs, 0.f), fmaf(hv[k].y * g4[1], qs, 0.f)) |
+                             (f32x2_to_e4m3x2(fmaf(hv[k].z * g4[2], qs, 0.f), fmaf(hv[k].w * g4[3], qs, 0.f)) << 16);
           uint8_t* dst = p.yq + static_cast<size_t>(t) * p.ldq + n;
           if (n + 4 <= p.N) {
             *reinterpret_cast<uint32_t*>(dst) = w;

@@ -1294,7 +1294,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemm_kernel(const __grid_co
             load_vec32(p.gamma, col0, p.N, g);
             load_vec32(p.bias, col0, p.N, b);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = (v[j] + b[j] + z[j]) * g[j] * qs;
+            for (int j = 0; j < 32; ++j) v[j] = fmaf((v[j] + b[j] + z[j]) * g[j], qs, 0.f);  // + 0: a zero row codes as +0
             stage_fp8_32(buf, lane, u, v);
           }
           ring.commit(&p.map_out[0], buf, lane, n0 + c * 128, y_box);

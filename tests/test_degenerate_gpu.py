@@ -36,6 +36,7 @@ def test_rmsnorm_fp8_zero_row_gets_zero_scale_and_codes(M, N, K, cap):
     W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=8)
     Z = _draw((M, N), syn.STREAM_Z, seed=8)
     g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0, seed=8)
+    g[1::3] ^= 0x8000  # a third of gamma negative (bf16 sign bit): a zero row must still code as +0
     zr = [0, M // 2, M - 1]
     X[zr] = 0
     Z[zr] = 0
