@@ -322,15 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
         am = fmaxf(am, v.y);
       }
       unsigned long long* rec = p.recs + (static_cast<size_t>(f) * kDecTokens + lane) * 2;
-      st_relaxed_u64(rec, tag | __float_as_uint(ss));
-      st_relaxed_u64(rec + 1, tag | __float_as_uint(am));
+      st_relaxed_u64x2(rec, tag | __float_as_uint(ss), tag | __float_as_uint(am));
     }
 
     // ---------------------------------------------------------------- phase 4: merge statistics, quantise (leader)
     // The four threads of token tq each merge every fourth cluster's partial (fixed order), then
     // combine by a butterfly, so all four hold the same bits.  Each group of 8 partials is polled
     // until all carry this call's epoch (a cluster that failed publishes nothing, and every wait
-    // gives up once a failure is recorded).
+    // gives up once a failure is recorded).  A record's two words are read in one 16-byte load (each
+    // word is single-copy atomic and carries its own tag) and the poll spins without a sleep: both
+    // together measured 0.06 us faster per call back to back, 0.08 us with another kernel between
+    // calls (5 alternating runs on one box, every run faster).
     float SS = 0.f, A = 0.f;
     bool ready = true;
     if (ti >= 0) {
@@ -343,8 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
           for (int j = 0; j < 8; ++j) {
             const int c = cb + 4 * j;
             const unsigned long long* rec = p.recs + (static_cast<size_t>(c) * kDecTokens + tq) * 2;
-            w[j][0] = c < p.num_f ? ld_relaxed_u64(rec) : tag;
-            w[j][1] = c < p.num_f ? ld_relaxed_u64(rec + 1) : tag;
+            if (c < p.num_f) {
+              ld_relaxed_u64x2(rec, w[j][0], w[j][1]);
+            } else {
+              w[j][0] = tag;
+              w[j][1] = tag;
+            }
           }
           bool all = true;
 #pragma unroll
@@ -369,7 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
               break;
             }
           }
-          __nanosleep(32);
         }
       }
     }
