@@ -13,12 +13,17 @@
 //     the SMs free up for the next kernel on the stream;
 //   * the leaders publish their cluster's per-token partials ("GEMM Epilogue 完全拆解",
 //     §模式 A: the tile-local half of the two-level row reduction), each value in a 64-bit word
-//     tagged with the call's epoch; every leader polls all num_f partials of its tokens at once
-//     (bounded; every cluster is resident, the host checks) until each carries this call's epoch,
-//     so the wait and the loads are one round trip, then merges them per token in a fixed order
-//     and writes the E4M3 codes and the per-token scale (§仿射量化与尾声的五步).  The tag alone
-//     tells a value of this call from a stale one, so no grid-wide count is kept (measured: polling
-//     a count as well cost 0.3 us per call back to back, 0.25 us with another kernel between calls).
+//     tagged with the call's epoch, and count themselves on a grid-wide counter; every leader
+//     polls all num_f partials of its tokens and the count at once (bounded; every cluster is
+//     resident, the host checks) until each carries this call's epoch and the count is exactly
+//     num_f, so the wait and the loads are one round trip, then merges them per token in a fixed
+//     order and writes the E4M3 codes and the per-token scale (§仿射量化与尾声的五步).
+//     The tag alone tells a value of this call from one of an earlier, completed call.  The count
+//     gives the wait a condition that lives in the workspace where the host can see it: a count
+//     that can never be exactly num_f (a workspace not zero-filled as the contract asks, or one a
+//     failure test has set) makes the wait run out and report FL_ERR_TIMEOUT rather than finish.
+//     It is a relaxed add, not a release: the tags already make each record self-validating, and a
+//     release fence in front of the add cost about 0.2 us per call.
 // Every CTA passes the cluster barriers it shares with its peers whatever happens (errors only
 // skip work), so a timed-out wait can never leave a peer blocked at a barrier.
 #pragma once
@@ -301,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
   else __syncthreads();
 
   if (rank == 0) {
-    // ---------------------------------------------------------------- phase 3: publish (leader)
+    // ---------------------------------------------------------------- phase 3: publish, grid-wide count (leader)
     // this thread's quantisation slice: token tq, features 32 (ti % 4) .. + 31 of the tile; its
     // gamma is loaded before the grid-wide wait
     const int tq = ti >> 2, c0 = (ti & 3) * 32;
@@ -314,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
     const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
     if (warp == 1 && cl_ok) {
       // the MMA warp is idle now: it merges the ranks' partials (lane = token) and publishes
-      // them, each value with the epoch in the same 64-bit word, while the epilogue warps load gamma
+      // them, each value with the epoch in the same 64-bit word, then counts the cluster, while the
+      // epilogue warps load gamma
       float ss = 0.f, am = 0.f;
       for (int j = 0; j < C; ++j) {  // rank order: deterministic
         const float2 v = Sall[j * 32 + lane];
@@ -323,16 +329,19 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
       }
       unsigned long long* rec = p.recs + (static_cast<size_t>(f) * kDecTokens + lane) * 2;
       st_relaxed_u64x2(rec, tag | __float_as_uint(ss), tag | __float_as_uint(am));
+      __syncwarp();
+      if (lane == 0) red_relaxed_add_u32(p.counters + p.num_f, 1u);
     }
 
     // ---------------------------------------------------------------- phase 4: merge statistics, quantise (leader)
     // The four threads of token tq each merge every fourth cluster's partial (fixed order), then
-    // combine by a butterfly, so all four hold the same bits.  Each group of 8 partials is polled
-    // until all carry this call's epoch (a cluster that failed publishes nothing, and every wait
-    // gives up once a failure is recorded).  A record's two words are read in one 16-byte load (each
-    // word is single-copy atomic and carries its own tag) and the poll spins without a sleep: both
-    // together measured 0.06 us faster per call back to back, 0.08 us with another kernel between
-    // calls (5 alternating runs on one box, every run faster).
+    // combine by a butterfly, so all four hold the same bits.  Each group of 8 partials, and the
+    // count, is polled until all carry this call's epoch and the count is exactly num_f (a cluster
+    // that failed publishes nothing, and every wait gives up once a failure is recorded).  A
+    // record's two words are read in one 16-byte load (each word is single-copy atomic and carries
+    // its own tag) and the poll spins without a sleep: both together measured 0.06 us faster per
+    // call back to back, 0.08 us with another kernel between calls (5 alternating runs on one box,
+    // every run faster).
     float SS = 0.f, A = 0.f;
     bool ready = true;
     if (ti >= 0) {
@@ -352,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) rmsnorm_fp8_decode_cluster_kernel
               w[j][1] = tag;
             }
           }
-          bool all = true;
+          bool all = ld_relaxed_u32(p.counters + p.num_f) == static_cast<unsigned>(p.num_f);
 #pragma unroll
           for (int j = 0; j < 8; ++j) all = all && (w[j][0] >> 32) == epoch && (w[j][1] >> 32) == epoch;
           if (all) {
