@@ -176,6 +176,21 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const v
   return true;
 }
 
+namespace {
+// Reads the status words at `rec` and clears them if a failure is recorded.  The read and the
+// clear are ordered on `stream` (the caller's, already synchronised), so neither can overtake work
+// the caller enqueues there later; the clear is complete when this returns.
+int read_and_clear_status(void* rec, cudaStream_t stream) {
+  int words[ST_WORDS];
+  if (cudaMemcpyAsync(words, rec, sizeof(words), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return FL_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FL_ERR_CUDA;
+  if (words[ST_CODE] == 0) return FL_OK;
+  if (cudaMemsetAsync(rec, 0, sizeof(words), stream) != cudaSuccess) return FL_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FL_ERR_CUDA;
+  return words[ST_CODE];
+}
+}  // namespace
+
 }  // namespace fl
 
 extern "C" {
@@ -188,11 +203,7 @@ int fl_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FL_ERR_CUDA;
   int* dptr = device_status_ptr(di.device);
   if (dptr == nullptr) return FL_ERR_CUDA;
-  int words[ST_WORDS];
-  if (cudaMemcpy(words, dptr, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return FL_ERR_CUDA;
-  if (words[ST_CODE] == 0) return FL_OK;
-  if (cudaMemset(dptr, 0, sizeof(words)) != cudaSuccess) return FL_ERR_CUDA;
-  return words[ST_CODE];
+  return read_and_clear_status(dptr, static_cast<cudaStream_t>(stream));
 }
 
 int fl_check_device_status(void* workspace, void* stream) {
@@ -200,11 +211,7 @@ int fl_check_device_status(void* workspace, void* stream) {
   if (workspace == nullptr) return fl_device_status(stream);
   if ((reinterpret_cast<uintptr_t>(workspace) & (kWsStatusBytes - 1)) != 0) return FL_ERR_ALIGNMENT;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FL_ERR_CUDA;
-  int words[ST_WORDS];
-  if (cudaMemcpy(words, workspace, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return FL_ERR_CUDA;
-  if (words[ST_CODE] == 0) return FL_OK;
-  if (cudaMemset(workspace, 0, sizeof(words)) != cudaSuccess) return FL_ERR_CUDA;
-  return words[ST_CODE];
+  return read_and_clear_status(workspace, static_cast<cudaStream_t>(stream));
 }
 
 void fl_set_cooperative_launch(int enable) { fl::g_cooperative.store(enable != 0 ? 1 : 0); }
