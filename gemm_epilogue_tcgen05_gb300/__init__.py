@@ -6,9 +6,15 @@ pointers, leading dimensions and a stream handle, and calls the C ABI of
 kernels do every step of the computation.  There is no other code path: if
 the library is not built or cannot be loaded, every call raises.
 
-Functions carry the C names: :func:`fused_linear_gelu`,
-:func:`fused_qkv_rope`, :func:`fused_swiglu` and
-:func:`fused_linear_residual_rmsnorm_fp8`.
+Functions carry the C names: :func:`fused_linear_gelu` (and its host-buffer
+form :func:`fused_linear_gelu_host`), :func:`fused_qkv_rope`,
+:func:`fused_qkv_rope_fp8kv`, :func:`fused_swiglu`,
+:func:`fused_linear_residual_rmsnorm_fp8` (and
+:func:`fused_linear_residual_rmsnorm_fp8_noalloc`, which takes no workspace),
+the deferred-scale chain :func:`fused_linear_residual_gamma` and
+:func:`fused_linear_rms_rowscale`, :func:`fused_linear_cross_entropy`,
+:func:`fused_linear_quant`, and the backward epilogues
+:func:`fused_dgrad_gelu` and :func:`fused_swiglu_bwd`.
 """
 from __future__ import annotations
 
@@ -76,6 +82,9 @@ def load() -> ctypes.CDLL:
     lib.fl_cross_entropy_workspace_bytes.restype = SZ
     lib.fl_rms_partials_per_row.argtypes = [I]
     lib.fl_rms_partials_per_row.restype = I
+    lib.fused_linear_residual_rmsnorm_fp8_noalloc.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I64, I64, I64,
+                                                              I64, P]
+    lib.fused_linear_residual_rmsnorm_fp8_noalloc.restype = I
     lib.fl_rmsnorm_fp8_workspace_bytes.argtypes = [I, I, I]
     lib.fl_rmsnorm_fp8_workspace_bytes.restype = SZ
     lib.fl_device_status.argtypes = [P]
@@ -350,6 +359,28 @@ def fused_linear_residual_rmsnorm_fp8(X, W, b, Z, gamma, eps: float = 1e-6, Yq=N
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check("fused_linear_residual_rmsnorm_fp8", st)
     return (Yq, row_scale, h_out) if want_h else (Yq, row_scale)
+
+
+def fused_linear_residual_rmsnorm_fp8_noalloc(X, W, b, Z, gamma, Yq, row_scale, eps: float = 1e-6,
+                                              stream=None):
+    """The same codes and scales as :func:`fused_linear_residual_rmsnorm_fp8`, through the entry point
+    that needs no workspace (it uses a scratch array built into the library; calls that may overlap
+    on the GPU must not be issued).  Yq (uint8 [M, N]) and row_scale (fp32 [M]) are the caller's:
+    the call allocates nothing.  Returns (Yq, row_scale)."""
+    M, K = X.shape
+    N = W.shape[0]
+    _mat(X, "X", torch.bfloat16)
+    _mat(W, "W", torch.bfloat16)
+    _mat(Z, "Z", torch.bfloat16)
+    _vec(b, "b", torch.bfloat16, N)
+    _vec(gamma, "gamma", torch.bfloat16, N)
+    _mat(Yq, "Yq", torch.uint8)
+    _vec(row_scale, "row_scale", torch.float32, M)
+    st = load().fused_linear_residual_rmsnorm_fp8_noalloc(
+        _ptr(X), _ptr(W), _ptr(b), _ptr(Z), _ptr(gamma), float(eps), _ptr(Yq), _ptr(row_scale), M, N, K,
+        _ld(X, K, K), _ld(W, K, K), _ld(Z, N, N), _ld(Yq, N, N), _stream(stream))
+    _check("fused_linear_residual_rmsnorm_fp8_noalloc", st)
+    return Yq, row_scale
 
 
 def rms_partials_per_row(n_norm: int) -> int:

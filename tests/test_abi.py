@@ -23,6 +23,15 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} declared in include/fused_linear.h but not exported"
 
 
+def test_every_compute_entry_point_has_a_binding_of_the_same_name(lib):
+    """Each computing call the header declares (the fl_* names are queries and switches) has a
+    function of the same name in the Python binding."""
+    compute = [n for n in fl.header_symbols() if not n.startswith("fl_")]
+    assert len(compute) >= 12
+    missing = [n for n in compute if not callable(getattr(fl, n, None))]
+    assert not missing, f"no binding for {missing}"
+
+
 def test_status_strings_and_version(lib):
     assert fl.version() == 200
     assert fl.status_string(fl.FL_OK) == "ok"

@@ -61,6 +61,11 @@ def test_noalloc_matches_workspace_entry_point_and_oracle_twice(M, N, K, bias):
         q, s = Yq.cpu().numpy(), sc.cpu().numpy().astype(np.float64)
         assert_fp8_close(q, s, q_ws, s_ws, f"noalloc {M}x{N}x{K} call {call} vs workspace entry point")
         assert_fp8_close(q, s, q_or, s_or, f"noalloc {M}x{N}x{K} call {call} vs oracle")
+    # the Python binding of the same entry point: the same call, bit for bit
+    Yb = torch.zeros((M, N), dtype=torch.uint8, device="cuda")
+    sb = torch.zeros(M, dtype=torch.float32, device="cuda")
+    fl.fused_linear_residual_rmsnorm_fp8_noalloc(X, W, b, Z, g, Yb, sb, 1e-6)
+    assert torch.equal(Yb, Yq) and torch.equal(sb, sc)
 
 
 def test_noalloc_rejects_shapes_it_cannot_serve():
