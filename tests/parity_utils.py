@@ -143,3 +143,52 @@ def assert_quant_close(fmt: int, codes, scales, q_ref, s_ref, y_ref, decode, wha
     err = np.abs(deq - y_ref)
     slack = 1e-5 * np.abs(y_ref).max(initial=0) + 1e-12
     assert np.all(err <= bound + slack), f"{what}: dequantised error {np.max(err - bound):.3g} over the bound"
+
+
+# ------------------------------------------------------------------ cases and checks shared by the GPU test files
+def rms_case(M: int, N: int, K: int, bias: bool, seed: int = 0):
+    """Seeded operands of a residual + RMSNorm + FP8 call: X, W, b (or None), Z, gamma."""
+    X = syn.draw(seed, syn.STREAM_X, (M, K), 0.0, 1.0, "bf16")
+    W = syn.draw(seed, syn.STREAM_W, (N, K), 0.0, K ** -0.5, "bf16")
+    b = syn.draw(seed, syn.STREAM_B, (N,), 0.0, 0.02, "bf16") if bias else None
+    Z = syn.draw(seed, syn.STREAM_Z, (M, N), 0.0, 1.0, "bf16")
+    g = syn.draw(seed, syn.STREAM_GAMMA, (N,), 1.0, 0.1, "bf16")
+    return X, W, b, Z, g
+
+
+def qkv_ref(X, Wq, bq, H, D, pos, theta=10000.0):
+    """The oracle's QKV + RoPE output [Q | K | V] for bf16 host operands."""
+    import oracle
+    return oracle.qkv_rope(f64(X), f64(Wq), None if bq is None else f64(bq), H, D, theta, pos)
+
+
+def assert_loss_close(got, ref, what):
+    """The fp32 loss within the fp32 output bound, max |gpu - oracle| <= 1e-4 (recorded)."""
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan), f"{what}: NaN pattern differs"
+    assert_f32_close(got[~nan], ref[~nan], f"{what}: loss")
+
+
+def check_kv_fp8(out, ref, what):
+    """Q in bf16, and the K and V codes and scales of the FP8 cache form, against the oracle; the
+    dequantised K and V also within half an E4M3 step of the exact values."""
+    import oracle
+    Q, Kq, Vq, ks, vs = out
+    assert_bf16_close(host(Q), ref["q"], f"{what}: Q")
+    hd = 128
+    for codes, scale, r_codes, r_scale, exact, nm in ((Kq, ks, ref["kq"], ref["ks"], ref["kv"][:, :Kq.shape[1]], "K"),
+                                                      (Vq, vs, ref["vq"], ref["vs"], ref["kv"][:, Kq.shape[1]:], "V")):
+        c, s = codes.cpu().numpy(), scale.cpu().numpy().astype(np.float64)
+        assert_fp8_close(c, s, r_codes, r_scale, f"{what}: {nm}")
+        heads = np.arange(c.shape[1]) // hd
+        deq = oracle.e4m3_decode(c) * s[:, heads]
+        bound = 2.0 ** -4 * np.abs(exact) + 2.0 ** -10 * s[:, heads] + 1e-5 * np.abs(exact).max()
+        assert np.all(np.abs(deq - exact) <= bound), f"{what}: {nm} dequantised outside the E4M3 half-step"
+
+
+def assert_ws_reset(ws, M, N):
+    """After a call the workspace's status words and the counters the kernels wait on are zero
+    again (the decode kernels' epoch word, at byte 128 of the status area, counts calls)."""
+    assert torch.count_nonzero(ws[:32]) == 0, "status record set"
+    n = 4 * (-(-N // 128) + 2) if M <= 32 else 8 * -(-M // 128)
+    assert torch.count_nonzero(ws[256:256 + n]) == 0, "counters not reset"

@@ -14,6 +14,11 @@ import oracle
 import synthetic as syn
 from parity_utils import (assert_bf16_close, assert_f32_close, assert_fp8_close, assert_quant_close, dev_bf16,
                           dev_f32, f64, host, sample_rows)
+from parity_utils import assert_loss_close as _assert_loss_close
+from parity_utils import check_kv_fp8 as _check_kv_fp8
+from parity_utils import qkv_ref as _qkv_ref
+from parity_utils import assert_ws_reset as _assert_ws_reset
+from parity_utils import rms_case as _rms_case
 
 pytestmark = pytest.mark.gpu
 
@@ -169,10 +174,6 @@ def test_gelu_many_tiles_per_cta_both_modes(pairing):
 
 
 # ------------------------------------------------------------------ QKV + RoPE
-def _qkv_ref(X, Wq, bq, H, D, pos, theta=10000.0):
-    return oracle.qkv_rope(f64(X), f64(Wq), None if bq is None else f64(bq), H, D, theta, pos)
-
-
 def test_qkv_rope_small_bias_and_positions():
     M, K, H, D = 300, 192, 2, 128
     X = _draw((M, K), syn.STREAM_X)
@@ -341,23 +342,6 @@ def test_swiglu_full_workload_sampled():
 
 
 # ------------------------------------------------------------------ residual + RMSNorm + FP8
-def _rms_case(M, N, K, bias, seed=0):
-    X = _draw((M, K), syn.STREAM_X, seed=seed)
-    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=seed)
-    b = _draw((N,), syn.STREAM_B, 0.02, seed=seed) if bias else None
-    Z = _draw((M, N), syn.STREAM_Z, seed=seed)
-    g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0, seed=seed)
-    return X, W, b, Z, g
-
-
-def _assert_ws_reset(ws, M, N):
-    """After a call the workspace's status words and the counters the kernels wait on are zero
-    again (the decode kernels' epoch word, at byte 128 of the status area, counts calls)."""
-    assert torch.count_nonzero(ws[:32]) == 0, "status record set"
-    n = 4 * (-(-N // 128) + 2) if M <= 32 else 8 * -(-M // 128)
-    assert torch.count_nonzero(ws[256:256 + n]) == 0, "counters not reset"
-
-
 def _rms_run(X, W, b, Z, g, ldq=None, workspace=None):
     M, N = Z.shape
     Yq = None
@@ -718,13 +702,6 @@ def test_rms_chain_full_workload_sampled():
 
 
 # ------------------------------------------------------------------ LM-head cross-entropy
-def _assert_loss_close(got, ref, what):
-    """The fp32 loss within the fp32 output bound, max |gpu - oracle| <= 1e-4 (recorded)."""
-    nan = np.isnan(ref)
-    assert np.array_equal(np.isnan(got), nan), f"{what}: NaN pattern differs"
-    assert_f32_close(got[~nan], ref[~nan], f"{what}: loss")
-
-
 @pytest.mark.parametrize("pairing", [True, False])
 def test_cross_entropy_small_with_logits(pairing):
     fl.set_cta_pairing(pairing)
@@ -845,20 +822,6 @@ def test_quant_full_workload_sampled(name):
 
 
 # ------------------------------------------------------------------ QKV + RoPE with an FP8 K/V cache
-def _check_kv_fp8(out, ref, what):
-    Q, Kq, Vq, ks, vs = out
-    assert_bf16_close(host(Q), ref["q"], f"{what}: Q")
-    hd = 128
-    for codes, scale, r_codes, r_scale, exact, nm in ((Kq, ks, ref["kq"], ref["ks"], ref["kv"][:, :Kq.shape[1]], "K"),
-                                                      (Vq, vs, ref["vq"], ref["vs"], ref["kv"][:, Kq.shape[1]:], "V")):
-        c, s = codes.cpu().numpy(), scale.cpu().numpy().astype(np.float64)
-        assert_fp8_close(c, s, r_codes, r_scale, f"{what}: {nm}")
-        heads = np.arange(c.shape[1]) // hd
-        deq = oracle.e4m3_decode(c) * s[:, heads]
-        bound = 2.0 ** -4 * np.abs(exact) + 2.0 ** -10 * s[:, heads] + 1e-5 * np.abs(exact).max()
-        assert np.all(np.abs(deq - exact) <= bound), f"{what}: {nm} dequantised outside the E4M3 half-step"
-
-
 @pytest.mark.parametrize("pairing", [True, False])
 @pytest.mark.parametrize("H,Hkv", [(4, 2), (2, 2)])
 def test_qkv_fp8kv_small(pairing, H, Hkv):
