@@ -8,7 +8,8 @@ import torch
 import gemm_epilogue_tcgen05_gb300 as fl
 import oracle
 import synthetic as syn
-from parity_utils import assert_bf16_close, assert_fp8_close, assert_quant_close, dev_bf16, f64, host
+from parity_utils import (assert_bf16_close, assert_fp8_close, assert_quant_close, dev_bf16, f64, host,
+                          ordered_e4m3, ordered_nibble, unpack_nibbles)
 
 pytestmark = pytest.mark.gpu
 
@@ -128,3 +129,31 @@ def test_every_entry_point_accepts_empty_problems():
     assert st == [fl.FL_OK] * len(st), st
     torch.cuda.synchronize()
     assert torch.all(sentinel == 7)
+
+
+def test_nvfp4_scale_saturates_and_underflows_like_the_oracle():
+    """NVFP4's block scale is itself an E4M3 byte, e4m3(max / 6).  Inverse smoothing factors from
+    1e-7 to 1e7 across the 16-column blocks push it through both ends of E4M3: a block whose
+    max / 6 rounds to 0 gets scale 0 and zero codes, and a block whose max / 6 exceeds 448 gets the
+    largest scale and codes saturated at +-6.  Scale codes and value codes against the oracle."""
+    M, N, K = 48, 512, 128
+    X = _draw((M, K), syn.STREAM_X, seed=12)
+    W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=12)
+    nb = N // 16
+    inv = np.repeat((10.0 ** (-7.0 + 14.0 * np.arange(nb) / (nb - 1))).astype(np.float32), 16)
+    Yq, S = fl.fused_linear_quant(dev_bf16(X), dev_bf16(W), None, 2, inv_smooth=torch.from_numpy(inv).cuda())
+    Yq, S = Yq.cpu().numpy(), S.cpu().numpy()
+    q_ref, s_ref, _ = oracle.linear_quant(f64(X), f64(W), None, 2, inv_smooth=inv.astype(np.float64))
+    s_ref = s_ref.astype(np.uint8)
+    assert (s_ref == 0).sum() >= 4 * M and (s_ref == 0x7E).sum() >= 4 * M, "both ends of E4M3 are reached"
+    ds = np.abs(ordered_e4m3(S) - ordered_e4m3(s_ref))
+    assert ds.max() <= 1 and np.mean(ds != 0) < 0.02, "scale codes"
+    assert np.array_equal(S == 0, s_ref == 0) and np.array_equal(S == 0x7E, s_ref == 0x7E), "saturated / zero scales"
+    codes, ref = unpack_nibbles(Yq, N), unpack_nibbles(q_ref, N)
+    blk = np.arange(N) // 16
+    assert not codes[(S == 0)[:, blk]].any(), "a zero scale gives zero codes"
+    sat = (S == 0x7E)[:, blk]
+    assert np.mean((codes[sat] & 7) == 7) > 0.5, "saturated blocks hold mostly +-6"
+    d = np.abs(ordered_nibble(codes, 2) - ordered_nibble(ref, 2))
+    same = (ds == 0)[:, blk]
+    assert d[same].max(initial=0) <= 1 and np.mean(d != 0) < 0.02, "value codes"
