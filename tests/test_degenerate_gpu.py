@@ -1,6 +1,7 @@
-"""Degenerate inputs the method defines, on the GPU, through the C ABI, against the fp64 oracle:
-rows, heads and blocks whose maximum is zero (scale 0 and zero codes), K = 0 (the Linear output is
-the bias alone), and empty problems (M = 0 or N = 0) for every entry point (nothing is written)."""
+"""Degenerate inputs and range edges the method defines, on the GPU, through the C ABI, against the
+fp64 oracle: rows, heads and blocks whose maximum is zero (scale 0 and zero codes), K = 0 (the Linear
+output is the bias alone), empty problems (M = 0 or N = 0) for every entry point (nothing is
+written), NVFP4 block scales at both ends of E4M3, and RoPE at the largest accepted positions."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,7 @@ import gemm_epilogue_tcgen05_gb300 as fl
 import oracle
 import synthetic as syn
 from parity_utils import (assert_bf16_close, assert_fp8_close, assert_quant_close, dev_bf16, f64, host,
-                          ordered_e4m3, ordered_nibble, unpack_nibbles)
+                          check_kv_fp8, ordered_e4m3, ordered_nibble, qkv_ref, unpack_nibbles)
 
 pytestmark = pytest.mark.gpu
 
@@ -157,3 +158,27 @@ def test_nvfp4_scale_saturates_and_underflows_like_the_oracle():
     d = np.abs(ordered_nibble(codes, 2) - ordered_nibble(ref, 2))
     same = (ds == 0)[:, blk]
     assert d[same].max(initial=0) <= 1 and np.mean(d != 0) < 0.02, "value codes"
+
+
+@pytest.mark.parametrize("M,decode", [(300, False), (24, True), (24, False)])
+def test_rope_at_the_top_of_the_position_range(M, decode):
+    """Positions just below 2^24, the largest the entry points accept, where the rotation angle of the
+    lowest pair reaches 1.7e7 rad and its reduction decides the result: QKV + RoPE and its FP8 K/V
+    form (prefill, the decode kernels, and the GEMM kernel on the decode shape) against the oracle."""
+    fl.set_linear_decode(decode)
+    try:
+        H, Hkv, D, K = 4, 2, 128, 256
+        X = _draw((M, K), syn.STREAM_X, seed=13)
+        pos = ((1 << 24) - 1 - np.random.default_rng(13).integers(0, 4096, size=M)).astype(np.int32)
+        pos[0] = (1 << 24) - 1
+        Wq = _draw((3 * H * D, K), syn.STREAM_W, K ** -0.5, seed=13)
+        q, k, v = fl.fused_qkv_rope(dev_bf16(X), dev_bf16(Wq), None, n_heads=H, head_dim=D,
+                                    positions=torch.from_numpy(pos).cuda())
+        assert_bf16_close(host(torch.cat([q, k, v], 1)), qkv_ref(X, Wq, None, H, D, pos), f"qkv top positions M={M}")
+        W8 = _draw(((H + 2 * Hkv) * D, K), syn.STREAM_W, K ** -0.5, seed=14)
+        out = fl.fused_qkv_rope_fp8kv(dev_bf16(X), dev_bf16(W8), None, n_heads=H, n_kv_heads=Hkv, head_dim=D,
+                                      positions=torch.from_numpy(pos).cuda())
+        check_kv_fp8(out, oracle.qkv_rope_kv_fp8(f64(X), f64(W8), None, H, Hkv, D, 1e4, pos),
+                     f"qkv fp8 kv top positions M={M}")
+    finally:
+        fl.set_linear_decode(True)
