@@ -279,15 +279,11 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   } else {
     fv[0] = flags[0];
   }
-  int all = 1;
-#pragma unroll
-  for (int j = 0; j < C; ++j) all &= fv[j] != 0 ? 1 : 0;
   // QKV: section (0 Q, 1 K, 2 V) of the tile (a tile is one head of one section) and its first column
   const int sec = !kQkv ? 0 : (f * 128 < p.n_out ? 0 : (f * 128 < p.n_out + p.kv_width ? 1 : 2));
   const int col_base = !kQkv ? f * kOut : f * 128 - (sec == 0 ? 0 : (sec == 1 ? p.n_out : p.n_out + p.kv_width));
   const int width = !kQkv || sec == 0 ? p.n_out : p.kv_width;
   const bool fp8 = KIND == LD_QKV_FP8KV && sec > 0;  // the same for every CTA of the cluster
-  const bool ok = all != 0;
   // The C partials of item `it` (token t, features j..j+7 of the tile) from every rank's P, in
   // flight at once (SwiGLU: the gate rows j.., and the up rows 64 + j..).
   constexpr int kCu = kSwiglu ? C : 1;
@@ -315,8 +311,13 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   // 32 x 12288 x 4096 is slower split, 21.0 against 19.4, and 19.3 against 19.0 with the loads
   // of both its items ahead of the epilogue.)
   constexpr bool kSplitB = kTokSplit && C > 1;
+  // The partials are loaded together with the flags, not after them: reading a peer's P is safe
+  // whatever its flag says (the values are used only when every flag is set), and the tail loses
+  // one distributed-shared-memory round trip (measured, 3 alternating runs on one box: FP8 K/V
+  // 32 x 6144 x 4096 interleaved 12.88 -> 12.73 us, one launch 20.15 -> 19.80 us, back to back
+  // unchanged at 12.2 us; QKV 32 x 12288 x 4096 back to back 18.40 -> 18.26 us).
   if constexpr (kSplitB) {
-    if (ti >= 0 && ok) {
+    if (ti >= 0) {
 #pragma unroll
       for (int it = 0; it < kIpt; ++it) {
         const int item = ti + 128 * it;
@@ -327,7 +328,15 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
     }
     __syncwarp();
     cluster_arrive_release();
+  } else if (ti >= 0) {
+    int t, gl;
+    item_tg(ti, t, gl);
+    if (item_has(ti, t, gl)) load_item(0, t, (g0 + gl) * 8);  // the first item's; the others in the loop
   }
+  int all = 1;
+#pragma unroll
+  for (int j = 0; j < C; ++j) all &= fv[j] != 0 ? 1 : 0;
+  const bool ok = all != 0;
 
   // Sums in rank order, epilogue, stores.
   float y[kIpt][8];
@@ -342,7 +351,9 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[it][e] = 0.f;
       if (has && ok) {
-        if constexpr (!kSplitB) load_item(it, t, j);
+        if constexpr (!kSplitB) {
+          if (it > 0) load_item(it, t, j);
+        }
         float s[8], s2[8];
         float4 a = xa[it][0], b = xb[it][0], u = make_float4(0.f, 0.f, 0.f, 0.f), v = u;
         if constexpr (kSwiglu) {
