@@ -305,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   // barrier's first half then says this CTA has read everything it needs from its peers' P (the
   // loads have returned before the release), and its second half, before the CTA leaves, keeps
   // its own P alive until every peer has read it, with the epilogue and the stores in between.
-  // The other kinds load each item's partials just before its epilogue and keep the whole barrier
-  // at the end.  (Measured, 20 back-to-back calls, 5 alternating runs on one box: FP8 K/V
+  // The other kinds load their first item's partials with the flags and each later item's just
+  // before its epilogue, and keep the whole barrier at the end.  (Measured, 20 back-to-back calls, 5 alternating runs on one box: FP8 K/V
   // 32 x 6144 x 4096 12.06 us against 12.60 with the feature split and one barrier more; QKV
   // 32 x 12288 x 4096 is slower split, 21.0 against 19.4, and 19.3 against 19.0 with the loads
   // of both its items ahead of the epilogue.)
