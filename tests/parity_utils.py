@@ -6,6 +6,7 @@ block-scaled codes: see ``assert_quant_close``)."""
 import numpy as np
 import torch
 
+import oracle
 import synthetic as syn
 
 BF16_ATOL, BF16_RTOL = 2e-2, 1e-2
@@ -158,7 +159,6 @@ def rms_case(M: int, N: int, K: int, bias: bool, seed: int = 0):
 
 def qkv_ref(X, Wq, bq, H, D, pos, theta=10000.0):
     """The oracle's QKV + RoPE output [Q | K | V] for bf16 host operands."""
-    import oracle
     return oracle.qkv_rope(f64(X), f64(Wq), None if bq is None else f64(bq), H, D, theta, pos)
 
 
@@ -172,7 +172,6 @@ def assert_loss_close(got, ref, what):
 def check_kv_fp8(out, ref, what):
     """Q in bf16, and the K and V codes and scales of the FP8 cache form, against the oracle; the
     dequantised K and V also within half an E4M3 step of the exact values."""
-    import oracle
     Q, Kq, Vq, ks, vs = out
     assert_bf16_close(host(Q), ref["q"], f"{what}: Q")
     hd = 128
