@@ -14,7 +14,8 @@
  *     never frees or retains them.  Except where stated, bf16 means IEEE
  *     bfloat16 stored as 16-bit words.
  *   - Calls are asynchronous: they validate the arguments on the host, enqueue
- *     one kernel on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     their work on `stream` (a cudaStream_t; NULL = legacy default stream:
+ *     normally one kernel; the exceptions are stated with each call) and
  *     return.  Device-side failures (a bounded wait that ran out) are recorded
  *     in the status record at the start of the call's workspace (calls that take
  *     one: fl_check_device_status(workspace, stream)) or else in a device-wide
@@ -24,8 +25,10 @@
  *     element size must be a multiple of 16 bytes.
  *   - M, N or K equal to 0 is allowed; M == 0 or N == 0 enqueues nothing, and
  *     K == 0 treats X W^T as zero.
- *   - Return value: an fl_status code (FL_OK = 0).  No partial work is
- *     enqueued when a call returns an error.
+ *   - Return value: an fl_status code (FL_OK = 0).  A call rejected by its
+ *     checks (every code but FL_ERR_CUDA) enqueues nothing.  FL_ERR_CUDA after
+ *     a call's first launch (a decode call that runs as several launches, the
+ *     host-buffer pipeline) can leave the launches before it enqueued.
  *
  * Page citations name the page title and its section:
  *   "Triton 算子融合: Linear 与 Attention" (aiqz.cc, triton-operator-fusion-linear-attention)
@@ -71,7 +74,8 @@ enum { FL_GELU_ERF = 0, FL_GELU_TANH = 1 };
  * TF32 products per term, hi*hi + hi*lo + lo*hi with x = hi + lo split exactly, fp32
  * accumulate: within ~2^-21 of each product, where one TF32 product would miss fp32 accuracy).
  * mode: FL_GELU_ERF or FL_GELU_TANH.  Y must not alias X, W or b.
- * bf16 with M <= 32 runs the decode kernel (fl_set_linear_decode, fl_linear_decode_shape).
+ * bf16 with M <= 32 runs the decode kernel (fl_set_linear_decode): one launch, or several
+ * when its W-row tiles do not all fit on the GPU at once (fl_linear_decode_shape reports which).
  */
 FL_API int fused_linear_gelu(const void* X, const void* W, const void* b, void* Y,
                       int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldy,
@@ -152,10 +156,12 @@ FL_API int fused_swiglu(const void* X, const void* Wgate, const void* Wup,
  * reset the counters they keep there before they return, so the same workspace
  * serves later calls on the same stream without clearing; after FL_ERR_TIMEOUT
  * it must be zero-filled again.  Calls that may run concurrently must not share
- * a workspace.  M <= 32 with K > 0 runs the split-K decode kernel (one CTA per
- * SM, each streaming an equal share of W); larger M runs the persistent
- * prefill kernel.  Both keep every CTA resident at once (the prefill kernel
- * launches cooperatively) and fail with FL_ERR_CUDA if that is impossible.
+ * a workspace.  M <= 32 with K > 0 runs a split-K decode kernel: one thread-block
+ * cluster per 128-feature tile, its CTAs each streaming an equal share of K, when
+ * every cluster fits on the GPU at once, else one CTA per SM each streaming an equal
+ * share of all of W; larger M runs the persistent prefill kernel.  All keep every
+ * CTA resident at once (the prefill kernel launches cooperatively) and fail with
+ * FL_ERR_CUDA if that is impossible.
  * N must not exceed 256 * (number of SMs) on the prefill path.
  */
 FL_API int fused_linear_residual_rmsnorm_fp8(const void* X, const void* W, const void* b,
