@@ -343,7 +343,7 @@ class Case:
             self.flops = 2.0 * w.M * w.N * w.K
         self.bytes = algorithmic_bytes(w)
         # decode shapes (32 tokens): the weight stream bounds them
-        self.hbm_bound = w.M <= 32 and w.kind in ("rmsnorm_fp8", "gelu_tanh", "qkv_rope", "qkv_fp8kv", "swiglu")
+        self.hbm_bound = w.M <= 32 and w.kind in ("rmsnorm_fp8", "gelu_tanh", "qkv_rope", "qkv_fp8kv", "swiglu", "quant")
 
     def run(self, stream=None, d=None, out=None, ws=None):
         """One call; `d`, `out` and `ws` replace the case's own operands, outputs and workspace."""
@@ -840,7 +840,7 @@ def main():
         for name in ("qkv_rope_8192x12288x4096", "qkv_fp8kv_8192x6144x4096", "swiglu_8192x14336x4096", "rmsnorm_fp8_prefill_8192x4096x14336",
                      "rmsnorm_fp8_decode_32x4096x14336", "gelu_decode_32x16384x4096", "qkv_decode_32x12288x4096",
                      "qkv_fp8kv_decode_32x6144x4096", "swiglu_decode_32x14336x4096",
-                     "rms_chain_8192x4096x4096_to_14336",
+                     "quant_fp8_1x128_decode_32x16384x4096", "rms_chain_8192x4096x4096_to_14336",
                      "lm_head_ce_8192x32768x4096", "gelu_bwd_8192x16384x4096", "swiglu_bwd_8192x14336x4096",
                      "quant_fp8_1x128_8192x16384x4096",
                      "quant_int4_g32_8192x16384x4096", "quant_nvfp4_g16_8192x16384x4096",

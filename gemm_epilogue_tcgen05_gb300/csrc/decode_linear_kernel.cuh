@@ -21,13 +21,17 @@
 //           so the maximum is a shuffle inside the CTA and needs no exchange between the CTAs);
 //   SwiGLU: 64 gate rows and the 64 up rows of the same 64 output features (two TMA boxes), so the
 //           gate and up values of a feature sit in the same tile.
+//   block-scaled write-back: 128 output features, finished like the FP8 K/V form by whole tokens,
+//           so every block of 128, 32 or 16 columns of a token lies inside one CTA.
 // Every CTA passes both cluster barriers whatever happens (errors only skip work).
 #pragma once
 #include "gemm_kernel.cuh"
 
 namespace fl {
 
-enum LinearDecodeKind : int { LD_GELU_TANH = 0, LD_GELU_ERF = 1, LD_SWIGLU = 2, LD_QKV_ROPE = 3, LD_QKV_FP8KV = 4 };
+enum LinearDecodeKind : int {
+  LD_GELU_TANH = 0, LD_GELU_ERF = 1, LD_SWIGLU = 2, LD_QKV_ROPE = 3, LD_QKV_FP8KV = 4, LD_QUANT = 5
+};
 
 constexpr int kLdTokens = 32;                   // MMA N: the tokens
 constexpr int kLdStages = 10;
@@ -58,6 +62,12 @@ struct alignas(128) LinearDecodeParams {
   long long ldkv;
   float* kv_scale[2];          // FP8 K/V form: K and V scales [M][lds], one per head
   long long lds;
+  uint8_t* qout;               // block-scaled form: codes [M, n_out] (FP8) or [M, n_out / 2] (4-bit), row pitch ldq
+  long long ldq;
+  void* qscale;                // its scales [M][qlds]: fp32 (FP8, INT4) or E4M3 bytes (NVFP4)
+  long long qlds;
+  const float* smooth;         // its optional inverse smoothing factors [n_out]
+  int qfmt;                    // QF_FP8_1X128, QF_INT4_G32 or QF_NVFP4_G16
   const int* positions;        // QKV: token positions [M], or null for m % seq_len
   int seq_len;
   double log2_theta;
@@ -87,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   constexpr int kGmax = (kG + C - 1) / C;     // groups per CTA, at most
   constexpr int kP2 = ld_pow2_at_least(kGmax);  // lanes per token: a power of two for the butterflies
   // FP8 K/V form: (token, group) items of this rank's tokens, a token's 16 groups in 16 lanes
-  constexpr bool kTokSplit = KIND == LD_QKV_FP8KV;
+  constexpr bool kTokSplit = KIND == LD_QKV_FP8KV || KIND == LD_QUANT;
   constexpr int kTokMax = (32 + C - 1) / C;   // tokens per CTA, at most
   constexpr int kItems = kTokSplit ? kTokMax * kG : 32 * kP2;  // (token, group slot) items
   constexpr int kIpt = (kItems + 127) / 128;  // items per epilogue thread
@@ -394,6 +404,87 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
           }
         }
       }
+      if constexpr (KIND == LD_QUANT) {
+        // Block-scaled write-back ("GEMM Epilogue 完全拆解", §仿射量化与尾声的五步): y times the optional
+        // inverse smoothing factor (step 3), then per block of 128 (FP8), 32 (INT4) or 16 (NVFP4)
+        // columns the maximum, the scale and the codes, with the arithmetic of the GEMM kernel's
+        // epilogue.  A token's 16 groups of 8 features sit in 16 consecutive lanes, so a block's
+        // maximum is a butterfly over its 16, 4 or 2 lanes (lanes without an item hold zeros).
+        const int col = col_base + j;
+        if (p.smooth != nullptr) {
+          float sm[8];
+          if (col + 8 <= width) {  // 32-byte aligned: smooth is 16-byte aligned, col % 8 == 0
+            const float4 s0 = *reinterpret_cast<const float4*>(p.smooth + col);
+            const float4 s1 = *reinterpret_cast<const float4*>(p.smooth + col + 4);
+            sm[0] = s0.x; sm[1] = s0.y; sm[2] = s0.z; sm[3] = s0.w;
+            sm[4] = s1.x; sm[5] = s1.y; sm[6] = s1.z; sm[7] = s1.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sm[e] = col + e < width ? p.smooth[col + e] : 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[it][e] *= sm[e];
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[it][e]));
+        const int lanes = p.qfmt == QF_FP8_1X128 ? 16 : (p.qfmt == QF_INT4_G32 ? 4 : 2);  // the same in every lane
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+          if (o < lanes) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const bool wr = has && ok && t < p.M && col < width;
+        uint8_t* qrow = p.qout + static_cast<size_t>(wr ? t : 0) * p.ldq;
+        if (p.qfmt == QF_FP8_1X128) {
+          const float qs = amax > 0.f ? 448.f / amax : 0.f;
+          uint32_t w[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k)  // + 0: a zero block codes as +0
+            w[k] = f32x2_to_e4m3x2(fmaf(y[it][4 * k], qs, 0.f), fmaf(y[it][4 * k + 1], qs, 0.f)) |
+                   (f32x2_to_e4m3x2(fmaf(y[it][4 * k + 2], qs, 0.f), fmaf(y[it][4 * k + 3], qs, 0.f)) << 16);
+          if (wr) {
+            if (gl == 0) static_cast<float*>(p.qscale)[static_cast<size_t>(t) * p.qlds + col / 128] = amax * (1.f / 448.f);
+            if (col + 8 <= width) {  // 8-byte aligned: ldq % 16 == 0, col % 8 == 0
+              *reinterpret_cast<uint2*>(qrow + col) = make_uint2(w[0], w[1]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (col + e < width) qrow[col + e] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+            }
+          }
+        } else {
+          uint32_t word = 0, sc = 0;
+          if (p.qfmt == QF_INT4_G32) {
+            const float inv = amax > 0.f ? 7.f / amax : 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              int qv = __float2int_rn(y[it][e] * inv);  // round half to even
+              qv = max(-7, min(7, qv));
+              word |= (static_cast<uint32_t>(qv) & 15u) << (4 * e);
+            }
+          } else {
+            const float s = round_to_e4m3(amax * (1.f / 6.f), sc);
+            const float inv = s > 0.f ? 1.f / s : 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)  // + 0 as above
+              word |= f32x2_to_e2m1x2(fmaf(y[it][2 * e], inv, 0.f), fmaf(y[it][2 * e + 1], inv, 0.f)) << (8 * e);
+          }
+          if (wr) {
+            if (p.qfmt == QF_INT4_G32) {
+              if ((gl & 3) == 0) static_cast<float*>(p.qscale)[static_cast<size_t>(t) * p.qlds + col / 32] = amax * (1.f / 7.f);
+            } else if ((gl & 1) == 0) {
+              static_cast<uint8_t*>(p.qscale)[static_cast<size_t>(t) * p.qlds + col / 16] = static_cast<uint8_t>(sc);
+            }
+            uint8_t* dst = qrow + col / 2;  // two codes per byte, column 2i in the low nibble of byte i
+            if (col + 8 <= width) {  // 4-byte aligned: ldq % 16 == 0, col % 8 == 0
+              *reinterpret_cast<uint32_t*>(dst) = word;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (col + 2 * i < width) dst[i] = static_cast<uint8_t>(word >> (8 * i));
+            }
+          }
+        }
+      }
       if (fp8) {
         // the head's max |y| of token t: a butterfly over the token's kG lanes, which hold all 128
         // features of the head (lanes without an item hold zeros); then scale and codes
@@ -423,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
           }
         }
       }
-      if (!fp8 && has && ok) {
+      if (KIND != LD_QUANT && !fp8 && has && ok) {
         const int col = col_base + j;
         __nv_bfloat16* out = p.out[sec];
         if (t < p.M && col < width) {

@@ -61,8 +61,9 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Process-wide switch for the two-CTA (cta_group::2) mainloop: 1 = use it when
 // M spans at least two 128-row blocks (default), 0 = always one CTA per tile.
 int cta_pairing_mode();
-int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU and QKV + RoPE (both forms) run the decode kernels
-// Decode-shaped (M <= 32) GELU, SwiGLU and QKV + RoPE (k_linear_decode_*.cu).  Returns FL_OK, an
+int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU, QKV + RoPE (both forms) and the block-scaled
+                           // write-back run the decode kernels
+// Decode-shaped (M <= 32) GELU, SwiGLU, QKV + RoPE and block-scaled write-back (k_linear_decode_*.cu).  Returns FL_OK, an
 // error, or kDecodeNotTaken when the call should run on the GEMM kernel instead.
 constexpr int kDecodeNotTaken = -2;
 int linear_decode_gelu(const void* X, const void* W, const void* b, void* Y, int M, int N, int K, int64_t ldx,
@@ -81,6 +82,11 @@ void linear_decode_plan_qkv(int num_f, int num_kb, const DeviceInfo& di, int* cl
                             int* launches);
 void linear_decode_plan_qkv_fp8kv(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
                                   int* launches);
+void linear_decode_plan_quant(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                              int* launches);
+int linear_decode_quant(const void* X, const void* W, const void* b, const float* inv_smooth, void* Yq, void* scales,
+                        int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldq, int64_t lds, int fmt,
+                        const DeviceInfo& di, cudaStream_t s);
 int linear_decode_qkv_fp8kv(const void* X, const void* Wqkv, const void* bqkv, void* Q, void* Kq, void* Vq,
                             float* k_scale, float* v_scale, const int32_t* positions, int M, int K, int d_model,
                             int kv_width, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldq, int64_t ldkv,

@@ -25,6 +25,10 @@ extern "C" int fused_linear_quant(const void* X, const void* W, const void* b, c
   DeviceInfo di;
   int st = current_device(&di);
   if (st != FL_OK) return st;
+  // a few tokens: the swap-AB decode kernel streams W instead of padding a 256-row tile
+  st = linear_decode_quant(X, W, b, inv_smooth, Yq, scales, M, N, K, ldx, ldw, ldq, lds, fmt, di,
+                           static_cast<cudaStream_t>(stream));
+  if (st != kDecodeNotTaken) return st;
   auto setup = [&](int cg, GemmParams& p) -> bool {
     init_params(p, M, N, K, 256, cg);
     if (K > 0 &&

@@ -263,7 +263,9 @@ FL_API size_t fl_cross_entropy_workspace_bytes(int M, int V);
  *     stored as E4M3 bytes [M][lds] = e4m3(max / 6), the values divided by that stored
  *     scale.  N must be even.
  * X [M,K] bf16, W [N,K] bf16, b [N] bf16 (nullable); ldq in bytes (multiple of 16),
- * lds in scale elements (>= number of blocks per row). */
+ * lds in scale elements (>= number of blocks per row).
+ * M <= 32 runs the decode kernel (fl_set_linear_decode), tiles of 128 output features
+ * finished by whole tokens, so every block of a token is inside one CTA. */
 enum { FL_QUANT_FP8_1X128 = 0, FL_QUANT_INT4_G32 = 1, FL_QUANT_NVFP4_G16 = 2 };
 FL_API int fused_linear_quant(const void* X, const void* W, const void* b, const float* inv_smooth,
                               void* Yq, void* scales, int M, int N, int K, int64_t ldx, int64_t ldw,
@@ -373,7 +375,8 @@ FL_API void fl_set_descriptor_cache(int enable);
 FL_API void fl_descriptor_cache_stats(unsigned long long* hits, unsigned long long* misses);
 
 /* Decode-shaped calls: with 1 (the default) fused_linear_gelu (bf16), fused_swiglu,
- * fused_qkv_rope and fused_qkv_rope_fp8kv with M <= 32 rows run a swap-AB kernel that streams W once (tiles of W rows
+ * fused_qkv_rope, fused_qkv_rope_fp8kv and fused_linear_quant with M <= 32 rows run a swap-AB
+ * kernel that streams W once (tiles of W rows
  * on the tensor cores' M side, the tokens on N, split-K across a thread-block cluster; tiles of
  * 128 output features, SwiGLU 64; more tiles than fit at once, at two CTAs per SM, in several
  * launches); with 0 they run on the prefill GEMM kernel.  Results agree within rounding (the
@@ -383,14 +386,15 @@ FL_API void fl_set_linear_decode(int enable);
 
 /* The launches a decode-shaped call would make on the current device, without making them.
  * kind: FL_DECODE_GELU (fused_linear_gelu, N output features), FL_DECODE_SWIGLU (fused_swiglu,
- * N = d_ff), FL_DECODE_QKV (fused_qkv_rope, N = 3 * n_heads * head_dim) or FL_DECODE_QKV_FP8KV
- * (fused_qkv_rope_fp8kv, N = (n_heads + 2 * n_kv_heads) * head_dim).  On FL_OK: *cluster = CTAs
+ * N = d_ff), FL_DECODE_QKV (fused_qkv_rope, N = 3 * n_heads * head_dim), FL_DECODE_QKV_FP8KV
+ * (fused_qkv_rope_fp8kv, N = (n_heads + 2 * n_kv_heads) * head_dim) or FL_DECODE_QUANT
+ * (fused_linear_quant, N output features).  On FL_OK: *cluster = CTAs
  * per W-row tile (0 when the call runs on the GEMM kernel instead: M outside 1..32, the decode
  * path off, or no shape fits), *ctas_per_sm = 1 or 2 (the kernel variant with 10 or 5 stages),
  * *launches = consecutive launches of equal tile shares (more tiles than fit at once).
  * Takes fl_set_max_ctas and fl_set_linear_decode into account.  FL_ERR_INVALID_ARG for a null
  * output pointer, a negative size or an unknown kind. */
-enum { FL_DECODE_GELU = 0, FL_DECODE_SWIGLU = 1, FL_DECODE_QKV = 2, FL_DECODE_QKV_FP8KV = 3 };
+enum { FL_DECODE_GELU = 0, FL_DECODE_SWIGLU = 1, FL_DECODE_QKV = 2, FL_DECODE_QKV_FP8KV = 3, FL_DECODE_QUANT = 4 };
 FL_API int fl_linear_decode_shape(int kind, int M, int N, int K, int* cluster, int* ctas_per_sm, int* launches);
 
 /* Static text for a status code. */

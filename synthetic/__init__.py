@@ -283,6 +283,9 @@ WORKLOADS = {
                                               seq_len=2048),
     "swiglu_decode_32x14336x4096": Workload("swiglu_decode_32x14336x4096", "swiglu", 32, 14336, 4096,
                                             has_bias=False),
+    # decode shape of the block-scaled up projection (FP8 activations for a low-precision consumer)
+    "quant_fp8_1x128_decode_32x16384x4096": Workload("quant_fp8_1x128_decode_32x16384x4096", "quant", 32, 16384,
+                                                     4096, quant="fp8_1x128"),
 }
 
 

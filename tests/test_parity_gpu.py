@@ -785,6 +785,36 @@ def test_quant_smoothing_small(fmt, pairing, M, N, K):
     _check_quant(fmt, Yq, S, X, W, b, f"smoothed quant fmt {fmt} {M}x{N}x{K}", inv_smooth=inv)
 
 
+@pytest.mark.parametrize("decode", [True, False])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K,smooth", [(32, 4096, 1024, False), (7, 1000, 4096, True), (1, 16384, 256, True),
+                                          (20, 6144, 2048, False), (3, 384, 8192, True)])
+def test_quant_decode_shapes(decode, fmt, M, N, K, smooth):
+    """Decode shapes of the block-scaled write-back (tiles of 128 features finished by whole tokens, on
+    every launch shape these sizes pick: clusters of 4 at two CTAs per SM, clusters of 8, one CTA per
+    tile at two per SM for 128 tiles; N = 1000 and 384 end inside a tile), with and without the
+    smoothing factor, and the GEMM kernel on the same shapes with the decode path off; an all-zero
+    token gets scale 0 and zero codes."""
+    fl.set_linear_decode(decode)
+    try:
+        X = _draw((M, K), syn.STREAM_X, seed=M + 3)
+        W = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=M + 3)
+        b = _draw((N,), syn.STREAM_B, 0.5, seed=M + 3) if not smooth else None
+        if M > 2:
+            X[M // 2] = 0
+        inv = syn.draw_inv_smooth(M, N) if smooth else None
+        plan = fl.linear_decode_shape(fl.DECODE_QUANT, M, N, K)
+        assert (plan[0] > 0) == decode, plan
+        Yq, S = fl.fused_linear_quant(dev_bf16(X), dev_bf16(W), None if b is None else dev_bf16(b), fmt,
+                                      inv_smooth=None if inv is None else torch.from_numpy(inv).cuda())
+        _check_quant(fmt, Yq, S, X, W, b, f"quant decode={decode} fmt {fmt} {M}x{N}x{K} smooth {smooth} plan {plan}",
+                     inv_smooth=inv)
+        if M > 2 and b is None:
+            assert torch.count_nonzero(Yq[M // 2]) == 0 and torch.count_nonzero(S[M // 2]) == 0
+    finally:
+        fl.set_linear_decode(True)
+
+
 def test_quant_smoothing_of_ones_is_bit_identical():
     M, N, K = 257, 1024, 136
     X = dev_bf16(_draw((M, K), syn.STREAM_X))
@@ -809,7 +839,8 @@ def test_quant_rejects_odd_n_for_4bit_and_bad_format():
 
 
 @pytest.mark.parametrize("name", ["quant_fp8_1x128_8192x16384x4096", "quant_int4_g32_8192x16384x4096",
-                                  "quant_nvfp4_g16_8192x16384x4096", "quant_fp8_1x128_smooth_8192x16384x4096"])
+                                  "quant_nvfp4_g16_8192x16384x4096", "quant_fp8_1x128_smooth_8192x16384x4096",
+                                  "quant_fp8_1x128_decode_32x16384x4096"])
 def test_quant_full_workload_sampled(name):
     w = syn.WORKLOADS[name]
     fmt = {"fp8_1x128": 0, "int4_g32": 1, "nvfp4_g16": 2}[w.quant]
@@ -817,7 +848,7 @@ def test_quant_full_workload_sampled(name):
     inv = ops.get("inv_smooth")
     Yq, S = fl.fused_linear_quant(dev_bf16(ops["X"]), dev_bf16(ops["W"]), dev_bf16(ops["b"]), fmt,
                                   inv_smooth=None if inv is None else torch.from_numpy(inv).cuda())
-    rows = sample_rows(w.M)
+    rows = sample_rows(w.M) if w.M > 32 else np.arange(w.M)  # the decode shape: every output
     _check_quant(fmt, Yq[rows], S[rows], ops["X"][rows], ops["W"], ops["b"], name, inv_smooth=inv)
 
 
