@@ -593,12 +593,13 @@ def set_cta_pairing(enable: bool) -> None:
 
 
 DECODE_GELU, DECODE_SWIGLU, DECODE_QKV, DECODE_QKV_FP8KV, DECODE_QUANT = 0, 1, 2, 3, 4
+DECODE_RESID_GAMMA, DECODE_ROWSCALE = 5, 6
 
 
 def linear_decode_shape(kind: int, M: int, N: int, K: int) -> tuple[int, int, int]:
     """(CTAs per W-row tile, CTAs per SM, launches) that a decode-shaped call would use on the current
     device; (0, 0, 0) when it would run on the GEMM kernel.  N: the rows of W (SwiGLU: d_ff; QKV:
-    3 * d_model; QKV + FP8 K/V: (n_heads + 2 * n_kv_heads) * head_dim; block-scaled: N)."""
+    3 * d_model; QKV + FP8 K/V: (n_heads + 2 * n_kv_heads) * head_dim; block-scaled and the chain: N)."""
     out = [ctypes.c_int(0) for _ in range(3)]
     _check("fl_linear_decode_shape", load().fl_linear_decode_shape(kind, M, N, K, *(ctypes.byref(o) for o in out)))
     return tuple(o.value for o in out)
@@ -606,6 +607,6 @@ def linear_decode_shape(kind: int, M: int, N: int, K: int) -> tuple[int, int, in
 
 def set_linear_decode(enable: bool) -> None:
     """Decode kernels for M <= 32 calls of fused_linear_gelu (bf16), fused_swiglu, fused_qkv_rope,
-    fused_qkv_rope_fp8kv and fused_linear_quant on (default) or off (the prefill GEMM kernel then
-    takes them)."""
+    fused_qkv_rope_fp8kv, fused_linear_quant and both chain steps on (default) or off (the prefill
+    GEMM kernel then takes them)."""
     load().fl_set_linear_decode(1 if enable else 0)

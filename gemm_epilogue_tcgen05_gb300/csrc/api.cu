@@ -242,7 +242,7 @@ int fl_linear_decode_shape(int kind, int M, int N, int K, int* cluster, int* cta
   using namespace fl;
   if (cluster == nullptr || ctas_per_sm == nullptr || launches == nullptr) return FL_ERR_INVALID_ARG;
   *cluster = *ctas_per_sm = *launches = 0;
-  if (M < 0 || N < 0 || K < 0 || kind < FL_DECODE_GELU || kind > FL_DECODE_QUANT) return FL_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || kind < FL_DECODE_GELU || kind > FL_DECODE_ROWSCALE) return FL_ERR_INVALID_ARG;
   if (linear_decode_mode() == 0 || M == 0 || M > 32 || N == 0 || K == 0) return FL_OK;  // not a decode call
   DeviceInfo di;
   const int st = current_device(&di);
@@ -255,7 +255,11 @@ int fl_linear_decode_shape(int kind, int M, int N, int K, int* cluster, int* cta
     case FL_DECODE_QKV_FP8KV:
       linear_decode_plan_qkv_fp8kv(cdiv(N, 128), num_kb, di, cluster, ctas_per_sm, launches);
       break;
-    default: linear_decode_plan_quant(cdiv(N, 128), num_kb, di, cluster, ctas_per_sm, launches); break;
+    case FL_DECODE_QUANT: linear_decode_plan_quant(cdiv(N, 128), num_kb, di, cluster, ctas_per_sm, launches); break;
+    case FL_DECODE_RESID_GAMMA:
+      linear_decode_plan_resgamma(cdiv(N, 128), num_kb, di, cluster, ctas_per_sm, launches);
+      break;
+    default: linear_decode_plan_rowscale(cdiv(N, 128), num_kb, di, cluster, ctas_per_sm, launches); break;
   }
   return FL_OK;
 }

@@ -23,6 +23,9 @@
 //           gate and up values of a feature sit in the same tile.
 //   block-scaled write-back: 128 output features, finished like the FP8 K/V form by whole tokens,
 //           so every block of 128, 32 or 16 columns of a token lies inside one CTA.
+//   the deferred-scale chain: 128 output features; step 1 (h1 = XW^T + b + Z, h2 = h1 * gamma and
+//           each token's sum of h1^2) is finished by whole tokens, step 2 (r * (H2 W1^T) + b1) by
+//           features like GELU.
 // Every CTA passes both cluster barriers whatever happens (errors only skip work).
 #pragma once
 #include "gemm_kernel.cuh"
@@ -30,7 +33,9 @@
 namespace fl {
 
 enum LinearDecodeKind : int {
-  LD_GELU_TANH = 0, LD_GELU_ERF = 1, LD_SWIGLU = 2, LD_QKV_ROPE = 3, LD_QKV_FP8KV = 4, LD_QUANT = 5
+  LD_GELU_TANH = 0, LD_GELU_ERF = 1, LD_SWIGLU = 2, LD_QKV_ROPE = 3, LD_QKV_FP8KV = 4, LD_QUANT = 5,
+  LD_RESGAMMA = 6,  // step 1 of the deferred-scale chain: h1 = XW^T + b + Z, h1 * gamma, sums of h1^2
+  LD_ROWSCALE = 7   // step 2: y = r * (H2 W1^T) + b1 with r merged from the step-1 sums
 };
 
 constexpr int kLdTokens = 32;                   // MMA N: the tokens
@@ -68,6 +73,13 @@ struct alignas(128) LinearDecodeParams {
   long long qlds;
   const float* smooth;         // its optional inverse smoothing factors [n_out]
   int qfmt;                    // QF_FP8_1X128, QF_INT4_G32 or QF_NVFP4_G16
+  // the deferred-scale chain (out[0] = H2 or Y, out[1] = H1 or null, both with row pitch ldo)
+  const __nv_bfloat16* resid;  // step 1: Z [M, n_out], row pitch ldz
+  long long ldz;
+  const __nv_bfloat16* gamma;  // step 1: gamma [n_out]
+  float* partials;             // [n_partials][M] sums of h1^2 per 256 columns: step 1 adds, step 2 reads
+  int n_partials, n_norm;      // step 2: entries per row and the normalised width
+  float eps;
   const int* positions;        // QKV: token positions [M], or null for m % seq_len
   int seq_len;
   double log2_theta;
@@ -97,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   constexpr int kGmax = (kG + C - 1) / C;     // groups per CTA, at most
   constexpr int kP2 = ld_pow2_at_least(kGmax);  // lanes per token: a power of two for the butterflies
   // FP8 K/V form: (token, group) items of this rank's tokens, a token's 16 groups in 16 lanes
-  constexpr bool kTokSplit = KIND == LD_QKV_FP8KV || KIND == LD_QUANT;
+  constexpr bool kTokSplit = KIND == LD_QKV_FP8KV || KIND == LD_QUANT || KIND == LD_RESGAMMA;
   constexpr int kTokMax = (32 + C - 1) / C;   // tokens per CTA, at most
   constexpr int kItems = kTokSplit ? kTokMax * kG : 32 * kP2;  // (token, group slot) items
   constexpr int kIpt = (kItems + 127) / 128;  // items per epilogue thread
@@ -187,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
   // item < kItems, the token inside this CTA's range, a feature group inside its share; the same
   // across a warp's lanes of one token (kG and kP2 are powers of two dividing 32)
   auto item_has = [&](int item, int t, int gl) { return item < kItems && t < tk1 && gl < ng; };
-  float bs[kIpt][8], b2s[kIpt][8];
+  float bs[kIpt][8], b2s[kIpt][8];  // bias (and SwiGLU's up bias, or the chain's residual)
+  float gs[kIpt][8], rr[kIpt];      // the chain: gamma (step 1), the token's row scale (step 2)
 
   // ---------------------------------------------------------------- phase 1: stream W, partial tile
   if (warp == 0) {
@@ -258,6 +271,20 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
       if (kSwiglu) {
         load_bf16x4(p.bias2, n, b2l, *reinterpret_cast<float(*)[4]>(b2s[it]));
         load_bf16x4(p.bias2, n + 4, b2l, *reinterpret_cast<float(*)[4]>(b2s[it] + 4));
+      }
+      if constexpr (KIND == LD_RESGAMMA) {  // the residual row and gamma of this item
+        const bool zin = in && t < p.M;
+        const __nv_bfloat16* zr = p.resid + static_cast<size_t>(zin ? t : 0) * p.ldz;
+        load_bf16x4(zr, n, zin ? p.n_out : 0, *reinterpret_cast<float(*)[4]>(b2s[it]));
+        load_bf16x4(zr, n + 4, zin ? p.n_out : 0, *reinterpret_cast<float(*)[4]>(b2s[it] + 4));
+        load_bf16x4(p.gamma, n, in ? p.n_out : 0, *reinterpret_cast<float(*)[4]>(gs[it]));
+        load_bf16x4(p.gamma, n + 4, in ? p.n_out : 0, *reinterpret_cast<float(*)[4]>(gs[it] + 4));
+      }
+      if constexpr (KIND == LD_ROWSCALE) {  // r of the item's token, from the step-1 sums (in order)
+        float ssum = 0.f;
+        if (in && t < p.M)
+          for (int q = 0; q < p.n_partials; ++q) ssum += __ldg(p.partials + static_cast<size_t>(q) * p.M + t);
+        rr[it] = rsqrtf(ssum / static_cast<float>(p.n_norm) + p.eps);
       }
     }
     // TMEM lane quarter q = W rows 32 q .. 32 q + 31 of the tile; each thread one row, 32 tokens.
@@ -350,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
 
   // Sums in rank order, epilogue, stores.
   float y[kIpt][8];
+  float h1v[kIpt][8];  // the chain's step 1: h1 itself
   if (ti >= 0) {
 #pragma unroll
     for (int it = 0; it < kIpt; ++it) {
@@ -359,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
       const bool has = item_has(item, t, gl);
       const int j = (g0 + (gl < ng ? gl : 0)) * 8;  // first output feature within the tile
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[it][e] = 0.f;
+      for (int e = 0; e < 8; ++e) y[it][e] = h1v[it][e] = 0.f;
       if (has && ok) {
         if constexpr (!kSplitB) {
           if (it > 0) load_item(it, t, j);
@@ -387,6 +415,11 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
           if (KIND == LD_GELU_TANH) y[it][e] = gelu_tanh_f(h);
           else if (KIND == LD_GELU_ERF) y[it][e] = gelu_erf_f(h);
           else if (KIND == LD_SWIGLU) y[it][e] = silu_f(h) * (s2[e] + b2s[it][e]);
+          else if (KIND == LD_ROWSCALE) y[it][e] = fmaf(rr[it], s[e], bs[it][e]);  // r (H2 W1^T) + b1
+          else if (KIND == LD_RESGAMMA) {
+            h1v[it][e] = s[e] + (bs[it][e] + b2s[it][e]);  // h1 = X W^T + (b + z), as the GEMM epilogue
+            y[it][e] = gs[it][e] * h1v[it][e];            // h2 = gamma (.) h1 feeds step 2 unscaled
+          }
           else y[it][e] = h;
         }
         if (kQkv && sec < 2) {
@@ -401,6 +434,35 @@ __global__ void __launch_bounds__(kThreads, S == kLdStages ? 1 : 2)
             const float x0 = y[it][e], x1 = y[it][e + 1];
             y[it][e] = x0 * cs - x1 * sn;
             y[it][e + 1] = x0 * sn + x1 * cs;
+          }
+        }
+      }
+      if constexpr (KIND == LD_RESGAMMA) {
+        // the tile's sum of h1^2 for token t: this item's 8 values, then a butterfly over the token's
+        // 16 lanes (lanes without an item hold zeros); the two 128-feature tiles of a 256-column entry
+        // both add to it, and the host has zeroed it, so 0 + a + b gives the same bits in either order
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(h1v[it][e], h1v[it][e], ss);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const int col = col_base + j;
+        if (has && ok && t < p.M) {
+          if (gl == 0) atomicAdd(p.partials + static_cast<size_t>(f >> 1) * p.M + t, ss);
+          if (p.out[1] != nullptr && col < width) {  // h1 itself, the residual stream
+            __nv_bfloat16* dst = p.out[1] + static_cast<size_t>(t) * p.ldo + col;
+            if (col + 8 <= width) {  // 16-byte aligned: ldo % 8 == 0, col % 8 == 0
+              uint4 w;
+              w.x = pack_bf16x2(h1v[it][0], h1v[it][1]);
+              w.y = pack_bf16x2(h1v[it][2], h1v[it][3]);
+              w.z = pack_bf16x2(h1v[it][4], h1v[it][5]);
+              w.w = pack_bf16x2(h1v[it][6], h1v[it][7]);
+              *reinterpret_cast<uint4*>(dst) = w;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (col + e < width) dst[e] = __float2bfloat16_rn(h1v[it][e]);
+            }
           }
         }
       }

@@ -61,8 +61,8 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Process-wide switch for the two-CTA (cta_group::2) mainloop: 1 = use it when
 // M spans at least two 128-row blocks (default), 0 = always one CTA per tile.
 int cta_pairing_mode();
-int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU, QKV + RoPE (both forms) and the block-scaled
-                           // write-back run the decode kernels
+int linear_decode_mode();  // 1: M <= 32 calls of GELU, SwiGLU, QKV + RoPE (both forms), the block-scaled
+                           // write-back and both chain steps run the decode kernels
 // Decode-shaped (M <= 32) GELU, SwiGLU, QKV + RoPE and block-scaled write-back (k_linear_decode_*.cu).  Returns FL_OK, an
 // error, or kDecodeNotTaken when the call should run on the GEMM kernel instead.
 constexpr int kDecodeNotTaken = -2;
@@ -87,6 +87,16 @@ void linear_decode_plan_quant(int num_f, int num_kb, const DeviceInfo& di, int* 
 int linear_decode_quant(const void* X, const void* W, const void* b, const float* inv_smooth, void* Yq, void* scales,
                         int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldq, int64_t lds, int fmt,
                         const DeviceInfo& di, cudaStream_t s);
+int linear_decode_resgamma(const void* X, const void* W, const void* b, const void* Z, const void* gamma, void* H2,
+                           void* H1, float* rms_partials, int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldz,
+                           int64_t ldh, const DeviceInfo& di, cudaStream_t s);
+int linear_decode_rowscale(const void* H2, const void* W1, const void* b1, const float* rms_partials, int n_norm,
+                           float eps, void* Y, int M, int N, int K, int64_t ldh, int64_t ldw, int64_t ldy,
+                           const DeviceInfo& di, cudaStream_t s);
+void linear_decode_plan_resgamma(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                                 int* launches);
+void linear_decode_plan_rowscale(int num_f, int num_kb, const DeviceInfo& di, int* cluster, int* ctas_per_sm,
+                                 int* launches);
 int linear_decode_qkv_fp8kv(const void* X, const void* Wqkv, const void* bqkv, void* Q, void* Kq, void* Vq,
                             float* k_scale, float* v_scale, const int32_t* positions, int M, int K, int d_model,
                             int kv_width, int seq_len, float theta, int64_t ldx, int64_t ldw, int64_t ldq, int64_t ldkv,

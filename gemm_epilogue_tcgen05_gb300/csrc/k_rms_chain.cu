@@ -27,6 +27,11 @@ extern "C" int fused_linear_residual_gamma(const void* X, const void* W, const v
   DeviceInfo di;
   int st = current_device(&di);
   if (st != FL_OK) return st;
+  // a few tokens: the swap-AB decode kernel streams W instead of padding a 256-row tile (it adds the
+  // sums of two 128-feature tiles per 256-column entry, after zeroing the entries on the stream)
+  st = linear_decode_resgamma(X, W, b, Z, gamma, H2, H1, rms_partials, M, N, K, ldx, ldw, ldz, ldh, di,
+                              static_cast<cudaStream_t>(stream));
+  if (st != kDecodeNotTaken) return st;
   auto setup = [&](int cg, GemmParams& p) -> bool {
     init_params(p, M, N, K, 256, cg);
     if (K > 0 &&
@@ -66,6 +71,9 @@ extern "C" int fused_linear_rms_rowscale(const void* H2, const void* W1, const v
   DeviceInfo di;
   int st = current_device(&di);
   if (st != FL_OK) return st;
+  st = linear_decode_rowscale(H2, W1, b1, rms_partials, n_norm, eps, Y, M, N, K, ldh, ldw, ldy, di,
+                              static_cast<cudaStream_t>(stream));
+  if (st != kDecodeNotTaken) return st;
   auto setup = [&](int cg, GemmParams& p) -> bool {
     init_params(p, M, N, K, 256, cg);
     if (K > 0 &&

@@ -213,7 +213,11 @@ FL_API int fused_linear_residual_rmsnorm_fp8_noalloc(const void* X, const void* 
  * r[m] = 1 / sqrt((sum_j rms_partials[j][m]) / n_norm + eps), the partials merged in a
  * fixed order inside the epilogue (no separate reduction launch).  H2 [M,K] with
  * K = n_norm normally, W1 [N,K], b1 [N] (nullable), Y [M,N] bf16.  Run step 2 on the
- * same stream after step 1 (or after an event) so the partials are complete. */
+ * same stream after step 1 (or after an event) so the partials are complete.
+ * M <= 32 runs both steps on the decode kernel (fl_set_linear_decode): tiles of 128 output
+ * features; step 1 then enqueues a memset of its rms_partials before the kernel, which adds the
+ * sums of the two 128-feature halves of every 256-column entry onto zero (the same bits in
+ * either order). */
 FL_API int fused_linear_residual_gamma(const void* X, const void* W, const void* b, const void* Z,
                                        const void* gamma, void* H2, void* H1, float* rms_partials,
                                        int M, int N, int K, int64_t ldx, int64_t ldw, int64_t ldz,
@@ -375,8 +379,8 @@ FL_API void fl_set_descriptor_cache(int enable);
 FL_API void fl_descriptor_cache_stats(unsigned long long* hits, unsigned long long* misses);
 
 /* Decode-shaped calls: with 1 (the default) fused_linear_gelu (bf16), fused_swiglu,
- * fused_qkv_rope, fused_qkv_rope_fp8kv and fused_linear_quant with M <= 32 rows run a swap-AB
- * kernel that streams W once (tiles of W rows
+ * fused_qkv_rope, fused_qkv_rope_fp8kv, fused_linear_quant and both steps of the deferred-scale
+ * chain with M <= 32 rows run a swap-AB kernel that streams W once (tiles of W rows
  * on the tensor cores' M side, the tokens on N, split-K across a thread-block cluster; tiles of
  * 128 output features, SwiGLU 64; more tiles than fit at once, at two CTAs per SM, in several
  * launches); with 0 they run on the prefill GEMM kernel.  Results agree within rounding (the
@@ -387,14 +391,16 @@ FL_API void fl_set_linear_decode(int enable);
 /* The launches a decode-shaped call would make on the current device, without making them.
  * kind: FL_DECODE_GELU (fused_linear_gelu, N output features), FL_DECODE_SWIGLU (fused_swiglu,
  * N = d_ff), FL_DECODE_QKV (fused_qkv_rope, N = 3 * n_heads * head_dim), FL_DECODE_QKV_FP8KV
- * (fused_qkv_rope_fp8kv, N = (n_heads + 2 * n_kv_heads) * head_dim) or FL_DECODE_QUANT
- * (fused_linear_quant, N output features).  On FL_OK: *cluster = CTAs
+ * (fused_qkv_rope_fp8kv, N = (n_heads + 2 * n_kv_heads) * head_dim), FL_DECODE_QUANT
+ * (fused_linear_quant, N output features), FL_DECODE_RESID_GAMMA (fused_linear_residual_gamma) or
+ * FL_DECODE_ROWSCALE (fused_linear_rms_rowscale), N output features.  On FL_OK: *cluster = CTAs
  * per W-row tile (0 when the call runs on the GEMM kernel instead: M outside 1..32, the decode
  * path off, or no shape fits), *ctas_per_sm = 1 or 2 (the kernel variant with 10 or 5 stages),
  * *launches = consecutive launches of equal tile shares (more tiles than fit at once).
  * Takes fl_set_max_ctas and fl_set_linear_decode into account.  FL_ERR_INVALID_ARG for a null
  * output pointer, a negative size or an unknown kind. */
-enum { FL_DECODE_GELU = 0, FL_DECODE_SWIGLU = 1, FL_DECODE_QKV = 2, FL_DECODE_QKV_FP8KV = 3, FL_DECODE_QUANT = 4 };
+enum { FL_DECODE_GELU = 0, FL_DECODE_SWIGLU = 1, FL_DECODE_QKV = 2, FL_DECODE_QKV_FP8KV = 3, FL_DECODE_QUANT = 4,
+       FL_DECODE_RESID_GAMMA = 5, FL_DECODE_ROWSCALE = 6 };
 FL_API int fl_linear_decode_shape(int kind, int M, int N, int K, int* cluster, int* ctas_per_sm, int* launches);
 
 /* Static text for a status code. */

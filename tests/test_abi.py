@@ -146,7 +146,7 @@ def test_decode_shape_query_on_host(lib):
     out = [ctypes.c_int(7) for _ in range(3)]
     refs = [ctypes.byref(o) for o in out]
     # unknown kind, negative size, null output: rejected before the device is touched
-    assert lib.fl_linear_decode_shape(5, 8, 4096, 4096, *refs) == fl.FL_ERR_INVALID_ARG
+    assert lib.fl_linear_decode_shape(7, 8, 4096, 4096, *refs) == fl.FL_ERR_INVALID_ARG
     assert lib.fl_linear_decode_shape(-1, 8, 4096, 4096, *refs) == fl.FL_ERR_INVALID_ARG
     assert lib.fl_linear_decode_shape(fl.DECODE_GELU, -1, 4096, 4096, *refs) == fl.FL_ERR_INVALID_ARG
     assert lib.fl_linear_decode_shape(fl.DECODE_GELU, 8, 4096, 4096, None, refs[1], refs[2]) == fl.FL_ERR_INVALID_ARG
@@ -158,6 +158,8 @@ def test_decode_shape_query_on_host(lib):
         assert [o.value for o in out] == [0, 0, 0]
     assert fl.linear_decode_shape(fl.DECODE_QKV, 64, 12288, 4096) == (0, 0, 0)
     assert fl.linear_decode_shape(fl.DECODE_QUANT, 64, 16384, 4096) == (0, 0, 0)
+    assert fl.linear_decode_shape(fl.DECODE_RESID_GAMMA, 64, 4096, 4096) == (0, 0, 0)
+    assert fl.linear_decode_shape(fl.DECODE_ROWSCALE, 64, 14336, 4096) == (0, 0, 0)
 
 
 def test_workspace_status_check_and_diagnostic_switches_on_host(lib):

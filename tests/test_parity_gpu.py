@@ -689,6 +689,47 @@ def test_rms_chain_small(pairing):
     assert_bf16_close(host(Y), y_ref, "y = RMSNorm(h1) W1 + b1")
 
 
+@pytest.mark.parametrize("decode", [True, False])
+@pytest.mark.parametrize("M,N,K,N2,store_h1,bias", [(32, 4096, 4096, 1024, True, False), (7, 384, 2048, 640, False, True),
+                                                    (1, 1000, 512, 264, True, True), (3, 2048, 8192, 4096, True, False),
+                                                    (20, 6144, 1024, 2048, False, False)])
+def test_rms_chain_decode_shapes(decode, M, N, K, N2, store_h1, bias):
+    """Decode shapes of both chain steps (step 1 finished by whole tokens, its 256-column sums of h1^2
+    added from two 128-feature tiles onto zeroed entries; step 2 by features; N = 384 leaves the last
+    entry one tile, N = 1000 ends inside a tile), and the GEMM kernel on the same shapes with the decode
+    path off; two calls give the same bits."""
+    fl.set_linear_decode(decode)
+    try:
+        X = _draw((M, K), syn.STREAM_X, seed=M + 5)
+        W0 = _draw((N, K), syn.STREAM_W, K ** -0.5, seed=M + 5)
+        b0 = _draw((N,), syn.STREAM_B, 0.02, seed=M + 5) if bias else None
+        Z = _draw((M, N), syn.STREAM_Z, seed=M + 5)
+        g = _draw((N,), syn.STREAM_GAMMA, 0.1, 1.0, seed=M + 5)
+        W1 = _draw((N2, N), syn.STREAM_W2, N ** -0.5, seed=M + 5)
+        for kind, n_out, k_in in ((fl.DECODE_RESID_GAMMA, N, K), (fl.DECODE_ROWSCALE, N2, N)):
+            plan = fl.linear_decode_shape(kind, M, n_out, k_in)
+            assert (plan[0] > 0) == decode, (kind, plan)
+        outs = []
+        for _ in range(2):
+            H2, H1, part = fl.fused_linear_residual_gamma(dev_bf16(X), dev_bf16(W0), None if b0 is None else dev_bf16(b0),
+                                                          dev_bf16(Z), dev_bf16(g), store_h1=store_h1)
+            Y = fl.fused_linear_rms_rowscale(H2, dev_bf16(W1), None, part, N, 1e-6)
+            outs.append([t.clone() for t in (H2, part, Y) + ((H1,) if store_h1 else ())])
+        for a, c in zip(*outs):
+            assert torch.equal(a, c), "two calls differ"
+        y_ref, h1_ref = oracle.residual_rmsnorm_linear(f64(X), f64(W0), None if b0 is None else f64(b0), f64(Z), f64(g),
+                                                       1e-6, f64(W1), None)
+        what = f"chain decode={decode} {M}x{N}x{K} -> {N2}"
+        if store_h1:
+            assert_bf16_close(host(H1), h1_ref, what + ": h1")
+        assert_bf16_close(host(H2), h1_ref * f64(g), what + ": h2")
+        tiles = np.stack([np.sum(h1_ref[:, j * 256:(j + 1) * 256] ** 2, axis=1) for j in range(-(-N // 256))])
+        assert np.allclose(part.cpu().numpy(), tiles, rtol=1e-4, atol=1e-3), what + ": per-tile sums of squares"
+        assert_bf16_close(host(Y), y_ref, what + ": y")
+    finally:
+        fl.set_linear_decode(True)
+
+
 def test_rms_chain_full_workload_sampled():
     w = syn.WORKLOADS["rms_chain_8192x4096x4096_to_14336"]
     ops = syn.make_operands(w)
